@@ -1,0 +1,92 @@
+"""Pins for oracle/layout.py: inverses, padding values, fold decisions, -0 count."""
+import numpy as np
+import pytest
+
+from oracle import layout as L
+
+
+def rand_bytes(rng, shape):
+    return rng.integers(0, 256, size=shape, dtype=np.uint8)
+
+
+def test_e4m3_block_codes_roundtrip_and_padding():
+    rng = np.random.default_rng(0)
+    E, N, K = 2, 64, 2080
+    w = rand_bytes(rng, (E, N, K))
+    codes = rng.integers(118, 133, size=(E, N // 32, K // 32), dtype=np.uint8)
+    p = L.pack_e4m3(w, codes)
+    assert p["mode"] == "block" and p["Kp"] == 2176
+    assert p["wq"].shape == (E, N, 2176) and np.all(p["wq"][:, :, K:] == 0)
+    assert p["codes"].shape == (E, 2, 68) and np.all(p["codes"][:, :, 65:] == 128)
+    w2, row = L.unpack_e4m3(p)
+    assert np.array_equal(w2, w)
+    assert np.array_equal(row, np.repeat(codes, 32, axis=1))
+    # SF atoms hold the per-row codes; padded K blocks 128, padded rows 127
+    back = L.sf_atoms_inverse(p["sf"], N, 68)
+    assert np.array_equal(back[:, :, :65], row) and np.all(back[:, :, 65:] == 128)
+    assert p["sf"].shape == (E, 1, 17, 512)
+    assert np.all(p["sf"][:, 0, :, (100 % 32) * 16 + (100 // 32) * 4] == 127)  # row 100 >= N
+
+
+def test_sf_atom_byte_position_by_hand():
+    # row n = 37 (m = 37: m % 32 = 5, m // 32 = 1), K block j = 6 (kt 1, kb 2)
+    codes = np.full((1, 128, 8), 120, dtype=np.uint8)
+    codes[0, 37, 6] = 7
+    atoms = L.sf_atoms(codes, 256)
+    assert atoms.shape == (1, 1, 2, 512)
+    assert atoms[0, 0, 1, 5 * 16 + 1 * 4 + 2] == 7
+    assert np.count_nonzero(atoms != 120) == 1
+
+
+def test_fold_decisions():
+    rng = np.random.default_rng(1)
+    E, N, K = 1, 96, 256
+    w = rand_bytes(rng, (E, N, K))
+    block = rng.integers(118, 133, size=(E, N // 32, K // 32), dtype=np.uint8)
+    row = np.repeat(block, 32, axis=1)
+    p = L.pack_e4m3(w, row)                           # rows agree: folds
+    assert p["mode"] == "block" and np.array_equal(p["codes"][:, :, :8], block)
+    assert L.pack_e4m3(w, row, fold=False)["mode"] == "row"
+    bad = row.copy()
+    bad[0, 40, 3] ^= 1                                # one row disagrees
+    assert L.pack_e4m3(w, bad)["mode"] == "row"
+    with pytest.raises(L.PackError) as ei:
+        L.pack_e4m3(w, bad, require_block=True)
+    assert ei.value.code == L.MX_ERR_NOT_BLOCK32
+    # N not a multiple of 32 cannot fold
+    p = L.pack_e4m3(w[:, :40], bad[:, :40])
+    assert p["mode"] == "row"
+    with pytest.raises(L.PackError) as ei:
+        L.pack_e4m3(w, np.full_like(row, 255))
+    assert ei.value.code == L.MX_ERR_SCALE
+
+
+def test_e2m1_word_transpose_by_positions():
+    w = np.arange(64, dtype=np.uint8).reshape(1, 1, 64) & 0x77   # no -0 nibbles
+    codes = np.full((1, 1, 4), 127, dtype=np.uint8)
+    p = L.pack_e2m1(w, codes)
+    out = p["wq"][0, 0]
+    for pos in range(64):
+        wd, b, i = pos // 16, (pos // 4) % 4, pos % 4
+        assert out[pos] == w[0, 0, 16 * b + 4 * wd + i]
+
+
+def test_e2m1_roundtrip_padding_and_negative_zero_count():
+    rng = np.random.default_rng(2)
+    E, N, K = 3, 48, 2080
+    w = rand_bytes(rng, (E, N, K // 2))
+    codes = rng.integers(122, 131, size=(E, N, K // 32), dtype=np.uint8)
+    p = L.pack_e2m1(w, codes)
+    count = 0
+    for byte in w.reshape(-1).tolist():
+        count += (byte & 0xF) == 8
+        count += (byte >> 4) == 8
+    assert p["neg_zero_count"] == count
+    back, c2 = L.unpack_e2m1(p)
+    assert np.array_equal(back, L.drop_negative_zero(w))
+    assert np.array_equal(c2, codes)
+    assert np.all(p["codes"][:, :, K // 32:] == 128)
+    assert not np.any((p["wq"] & 0x0F) == 0x08) and not np.any((p["wq"] & 0xF0) == 0x80)
+    # the padded tail (past K/2 bytes, before the transpose) is zero
+    untransposed = L._word_transpose(p["wq"])
+    assert np.all(untransposed[:, :, K // 2:] == 0)
