@@ -1,0 +1,429 @@
+"""Benchmark of the MX quantized linear on one or more GB300s (replicas).
+
+Headline workload: the MXFP8 decode linear N=7168, K=2048 with 32x32-block E8M0
+scales, bf16 activations quantized inside each call; one step = one call at each
+of M = 1, 4, 16, 32 tokens.  value = algorithmic bytes of the step (weight bytes
++ codes + bf16 x + bf16 out, unpadded K) / device time of the step, summed over
+ranks (each rank runs its own replica; there is no data-path collective).
+
+Weights rotate over enough packed copies (> 4x L2) that every call streams its
+weight from HBM.  Steps are CUDA-graph replays queued behind a short device
+sleep, timed with CUDA events on the launching stream.
+
+Also reported: the roofline of the dominant call (event-timed graph of
+back-to-back M=32 calls over the rotated copies), the block-scaled prefill GEMM
+M=4096 N=K=7168 in TFLOP/s, the MXFP4 MoE gate/up (E=64, T=64, top-8) in GB/s,
+the oracle timed on the host cores (cpu_baseline), and an end-to-end figure
+through the Python API with pinned host copies each step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "MX linear HBM GB/s at M<=32 and block-scaled TFLOPS at M=4096 (1 GB300)"
+N_DEC, K_DEC, MS = 7168, 2048, (1, 4, 16, 32)
+WORKLOAD = "MXFP8 decode linear N=7168 K=2048, 32x32 E8M0 blocks (codes 118..132), bf16 x N(0,1) quantized per token in the call, M in {1,4,16,32}"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+def linear_bytes(M, N, K, block=True):
+    codes = (N // 32) * (K // 32) if block else N * (K // 32)
+    return N * K + codes + 2 * M * K + 2 * M * N
+
+
+def moe_bytes(D, N, K, T, topk):
+    return D * N * (K // 2 + K // 32) + 2 * T * K + 2 * T * topk * N + 4 * T * topk
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------- clocks
+
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clocks_setting"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.lines = [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                bits = int(parts[2], 16)
+            except Exception:
+                continue
+            for b, name in REASON_BITS.items():
+                if bits & b and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- our arm
+
+def run_ours(args, ws, rank, local):
+    import mxfp4_quantized_linear_gb300 as mx
+    from mxfp4_quantized_linear_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = mx.load_library()
+    _ = lib
+    stream = torch.cuda.Stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    # ---- weights: one packed copy per rotation slot, > 4x L2 in total
+    c = inputs.decode_linear(K=K_DEC, Ms=MS, N=N_DEC)
+    wdev, cdev = c["w"].to(dev), c["codes"].to(dev)
+    per_copy = mx.mx_pack_size("e4m3", 1, N_DEC, K_DEC)
+    ncopies = max(8, -(-4 * l2 // per_copy))
+    ncopies = -(-ncopies // len(MS)) * len(MS)
+    with torch.cuda.stream(stream):
+        packed = [mx.mx_pack_weights(wdev, cdev, "e4m3") for _ in range(ncopies)]
+    xs = {M: c["xs"][M].to(dev) for M in MS}
+    outs = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16, device=dev) for M in MS}
+    wsz = max(mx.mxfp8_linear_workspace_size(M, packed[0]) for M in MS)
+    work = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
+    step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
+    kernels_per_step = sum(1 if M <= 8 else 2 for M in MS)
+
+    def call(M, w):
+        mx.mxfp8_linear(xs[M], w, out=outs[M], workspace=work)
+
+    # ---- one graph per step slot: the 4 calls on 4 different weight copies
+    nslots = ncopies // len(MS)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for M in MS:  # warm up (PDL / cluster launch set-up) before capture
+            call(M, packed[0])
+        torch.cuda.synchronize()
+        for s in range(nslots):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i, M in enumerate(MS):
+                    call(M, packed[s * len(MS) + i])
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    def steps(n, start=0):
+        for s in range(n):
+            graphs[(start + s) % nslots].replay()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        steps(args.warmup)
+    torch.cuda.synchronize()
+    # ---- timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e6))  # keep the queue ahead of the device
+            e0.record(stream)
+            steps(args.steps, start=args.warmup)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---- roofline of the dominant call: back-to-back M=32 calls over the rotated copies
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    reps = 4
+    gdom = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(gdom, stream=stream):
+            for w in packed:
+                call(32, w)
+        gdom.replay()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(1e6))
+        e0.record(stream)
+        for _ in range(reps):
+            gdom.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    call_ms = e0.elapsed_time(e1) / (reps * ncopies)
+    call_bytes = linear_bytes(32, N_DEC, K_DEC, True)
+    achieved = call_bytes / (call_ms * 1e-3) / 1e9
+    per_m = {}
+    for M in MS:
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gm, stream=stream):
+                for w in packed:
+                    call(M, w)
+            gm.replay()
+            torch.cuda.synchronize()
+            torch.cuda._sleep(int(1e6))
+            e0.record(stream)
+            gm.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / ncopies
+        per_m[str(M)] = {"us_per_call": round(t * 1e3, 3),
+                         "GB/s": round(linear_bytes(M, N_DEC, K_DEC, True) / (t * 1e-3) / 1e9, 1)}
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "kernel": "mxfp8_linear M=32 (quantize + split-K GEMV, PDL-overlapped)",
+                "peak_source": f"{peak_kind} HBM copy bandwidth", "per_call": per_m}
+
+    result = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+              "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+              "data": "synthetic",
+              "config": {"workload": WORKLOAD, "N": N_DEC, "K": K_DEC, "Ms": list(MS),
+                         "l2": f"weights rotated over {ncopies} packed copies "
+                               f"({ncopies * per_copy / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)",
+                         "parallelism": f"replicas x{ws}"},
+              "roofline": roofline, "gpu_launches": kernels_per_step * args.steps,
+              "clocks": clk.summary()}
+    if rank == 0 and not args.no_extras:
+        result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
+        result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
+        result["e2e"] = bench_e2e(mx, packed, dev, stream, args)
+    del graphs, gdom
+    return result
+
+
+def bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind):
+    c = inputs.prefill_gemm()
+    x = c["x"].to(dev)
+    wd, cd = c["w"].to(dev), c["codes"].to(dev)
+    with torch.cuda.stream(stream):
+        ws = [mx.mx_pack_weights(wd, cd, "e4m3") for _ in range(4)]
+        out = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(mx.mxfp8_linear_workspace_size(4096, ws[0]), dtype=torch.uint8, device=dev)
+        for w in ws:
+            mx.mxfp8_linear(x, w, out=out, workspace=work)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 8
+        e0.record(stream)
+        for r in range(reps):
+            mx.mxfp8_linear(x, ws[r % 4], out=out, workspace=work)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = 2.0 * 4096 * 7168 * 7168
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "MXFP8 prefill GEMM M=4096 N=7168 K=7168, x quantized in the call",
+            "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+            "note": f"fraction of the {peak_kind} bf16 dense peak x2 (8-bit nominal ratio): "
+                    f"{tf / (2 * bf16_peak):.4f}"}
+
+
+def bench_moe(mx, inputs, dev, stream, hbm_peak):
+    m = inputs.moe_gate_up()
+    with torch.cuda.stream(stream):
+        p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+        x, ids = m["x"].to(dev), m["ids"].to(dev)
+        out = torch.empty((64, 8, 4096), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(64, 8, 64), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        e0.record(stream)
+        for _ in range(reps):
+            mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    D = int(torch.unique(m["ids"]).numel())
+    b = moe_bytes(D, 4096, 4096, 64, 8)
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"workload": "MXFP4 A16W4 MoE gate/up E=64 N=4096 K=4096 T=64 top-8 (weights 0.5 GB > L2)",
+            "ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
+            "experts_touched": D}
+
+
+def bench_e2e(mx, packed, dev, stream, args):
+    """The step through the public API: pinned host x -> device, call, out -> pinned host."""
+    c_host = {M: torch.randn((M, K_DEC), generator=torch.Generator().manual_seed(M)).to(torch.bfloat16).pin_memory()
+              for M in MS}
+    o_host = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16).pin_memory() for M in MS}
+    x_dev = {M: torch.empty((M, K_DEC), dtype=torch.bfloat16, device=dev) for M in MS}
+    work = torch.empty(max(mx.mxfp8_linear_workspace_size(M, packed[0]) for M in MS), dtype=torch.uint8, device=dev)
+    n = max(20, min(args.steps, 500))
+    h2d = sum(c_host[M].numel() * 2 for M in MS)
+    d2h = sum(o_host[M].numel() * 2 for M in MS)
+
+    def one(s):
+        for i, M in enumerate(MS):
+            x_dev[M].copy_(c_host[M], non_blocking=True)
+            out = mx.mxfp8_linear(x_dev[M], packed[(s * len(MS) + i) % len(packed)], workspace=work)
+            o_host[M].copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    with torch.cuda.stream(stream):
+        for s in range(5):
+            one(s)
+        t0 = time.perf_counter()
+        for s in range(n):
+            one(s)
+        t1 = time.perf_counter()
+    step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
+    sec = (t1 - t0) / n
+    return {"value": round(step_bytes / sec / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 4), "steps": n}
+
+
+# ------------------------------------------------------------- oracle (CPU)
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_step(c):
+    """One step of the workload on the oracle: the four calls, fp64."""
+    from oracle.linear import mxfp8_linear as ref_linear
+    from tests.helpers import bf16_np  # noqa: F401  (same exact bf16 -> fp64 conversion)
+    w = c["w"].numpy()
+    codes = c["codes"].numpy()
+    for M in MS:
+        x = c["xs"][M].float().numpy().astype(np.float64)
+        ref_linear(x, w, codes)
+
+
+def cpu_baseline(steps=1):
+    from mxfp4_quantized_linear_gb300 import inputs
+    c = inputs.decode_linear(K=K_DEC, Ms=MS, N=N_DEC)
+    oracle_step(c)  # warm caches / imports
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(c)
+    sec = (time.perf_counter() - t0) / steps
+    step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
+    return {"value": round(step_bytes / sec / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
+            "kind": "oracle", "sample": f"{steps} full step(s) of the workload (M=1,4,16,32), "
+                                        f"{sec:.3f} s per step, numpy fp64 decode + matmul"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    from mxfp4_quantized_linear_gb300 import inputs
+    c = inputs.decode_linear(K=K_DEC, Ms=MS, N=N_DEC)
+    for _ in range(args.warmup):
+        oracle_step(c)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(c)
+    sec = (time.perf_counter() - t0) / args.steps
+    step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
+    v = step_bytes / sec / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "N": N_DEC, "K": K_DEC, "Ms": list(MS)},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{args.steps} full steps of the workload on the CPU oracle"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the GEMM / MoE / e2e / CPU figures")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_env()
+    if ws > 1 and args.impl == "ours":
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res = run_ours(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and not args.no_extras:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) microscaled (OCP MX) quantized linear.
+ *
+ * Weights are OCP e4m3 (MXFP8) bytes or packed e2m1 (MXFP4, fp4x2, low nibble
+ * first) with one E8M0 power-of-two scale code per 32-element K block; code c
+ * stands for 2^(c - 127).  Sources, cited by page title and section:
+ *
+ *   weights942  = vllm.models.deepseek_v41.amd.mono.weights942
+ *   rocm_native = vllm.model_executor.kernels.linear.mxfp8.rocm_native
+ *   a16w4       = vllm.models.minimax_m3.amd.specialized_decode.mono.a16w4
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned,
+ *     row-major and dense.  The library allocates no memory.  bf16 tensors are
+ *     passed as void*.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work and return; only mx_pack_weights and mx_check_device_errors
+ *     synchronise the stream.
+ *   - The return value is an MX_* status.  On failure nothing was enqueued and
+ *     mx_last_error() returns a message (per host thread).  Conditions only the
+ *     device can see (bad expert ids) are written to a caller-provided device
+ *     int (`dev_status`) instead; no kernel ever traps.
+ *   - All calls require the current device to be an sm_103 GPU.
+ */
+#ifndef MX_GB300_H
+#define MX_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+enum {
+  MX_OK = 0,
+  MX_ERR_SHAPE = 1,        /* a size is out of range or inconsistent          */
+  MX_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned                 */
+  MX_ERR_ARG = 3,          /* NULL pointer, unknown format / mode / flag       */
+  MX_ERR_NOT_BLOCK32 = 4,  /* 32x32 block codes required, rows disagree       */
+  MX_ERR_SCALE = 5,        /* an E8M0 weight code is 255 (NaN)                */
+  MX_ERR_WORKSPACE = 6,    /* workspace missing or smaller than required      */
+  MX_ERR_EXPERT_ID = 7,    /* (device status) an expert id outside [-1, E)     */
+  MX_ERR_CUDA = 8,         /* a CUDA runtime call failed                      */
+  MX_ERR_UNSUPPORTED = 9,  /* device is not sm_103, or a size beyond a limit  */
+  MX_ERR_TIMEOUT = 10      /* (device flag) a bounded wait inside a kernel ran out */
+};
+
+enum { MX_FMT_E4M3 = 0, MX_FMT_E2M1 = 1 };
+enum { MX_SCALE_BLOCK32X32 = 0, MX_SCALE_ROW1X32 = 1 };
+
+/* mx_pack_weights flags */
+#define MX_PACK_FOLD 1u          /* fold [N, K/32] row codes into [N/32, K/32] blocks when
+                                    every 32 rows agree (rocm_native, _as_block32_scale)   */
+#define MX_PACK_REQUIRE_BLOCK 2u /* fail with MX_ERR_NOT_BLOCK32 when they do not
+                                    (weights942, linear_copy)                              */
+
+/* mxfp8_linear flags */
+#define MX_LINEAR_NO_FUSED_QUANT 1u /* always quantize x in a separate launch (the pages'
+                                       kill switch of the fused quant, rocm_native,
+                                       apply_weights)                                     */
+
+/* Largest token count the GEMV path serves; larger M runs the block-scaled GEMM. */
+#define MX_GEMV_MAX_M 32
+/* Largest expert count mx_route_experts / mxfp4_moe_linear accept. */
+#define MX_MAX_EXPERTS 512
+
+/*
+ * A packed weight, filled by mx_pack_weights.  All pointers are device
+ * pointers into the caller's pack buffer; the struct itself is plain host
+ * memory the caller keeps and passes back by pointer.
+ *
+ * E4M3 (dense MXFP8), K padded to Kp = roundup(K, 128) with zero bytes and
+ * code 128 (weights942, dense_copy):
+ *   bytes  [E, N, Kp]          row-major e4m3
+ *   codes  [E, N/32, Kp/32]    (scale_mode BLOCK32X32) or [E, N, Kp/32] (ROW1X32)
+ *   sf     [E, ceil(N/128), Kp/128, 512]  per-row codes in 512-byte atoms: row
+ *          n = 128 rt + m and K block j = 4 kt + kb at byte
+ *          (m % 32) * 16 + (m / 32) * 4 + kb of atom (rt, kt); 127 past N.
+ * E2M1 (MXFP4 experts):
+ *   bytes  [E, N, Kp/2]  each 64-byte chunk of a row (4 K blocks x 4 words of
+ *          4 bytes) stored word-transposed: word w of block b at word 4 w + b;
+ *          -0 nibbles rewritten to +0 (weights942, fp4_drop_negative_zero_)
+ *   codes  [E, N, Kp/32] per-row codes
+ *   sf     NULL
+ */
+typedef struct mx_packed_weight {
+  int32_t fmt;         /* MX_FMT_*                                 */
+  int32_t scale_mode;  /* MX_SCALE_*                               */
+  int32_t E, N, K, Kp; /* experts, rows, logical K, padded K       */
+  uint8_t* bytes;
+  uint8_t* codes;
+  uint8_t* sf;
+  int64_t neg_zero_count; /* -0 nibbles rewritten (E2M1), else 0   */
+} mx_packed_weight;
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* mx_last_error(void);
+
+/*
+ * Reads and clears the library's device error flags on the current device
+ * (synchronises the device).  Returns MX_OK, or MX_ERR_TIMEOUT when a bounded
+ * in-kernel wait gave up since the last check.
+ */
+int mx_check_device_errors(void);
+
+/* ------------------------------------------------------------------ packing */
+
+/* Bytes the pack buffer needs for a weight of this format and shape
+ * (0 if the shape is invalid). */
+size_t mx_pack_size(int fmt, int E, int N, int K);
+
+/*
+ * Load-time repack of MX weights into the layout above (one device pass).
+ *   bytes       E4M3: [E, N, K] e4m3;  E2M1: [E, N, K/2] fp4x2, low nibble first
+ *               (weights942, moe_copies: w13 [E, 2Np, K/2])
+ *   codes       [E, codes_rows, K/32] E8M0, codes_rows = N (1x32 rows) or
+ *               N/32 (32x32 blocks, weights942 dense_copy: [N/32, K/32])
+ *   flags       MX_PACK_* (E4M3 only; E2M1 always keeps per-row codes)
+ *   dst/dst_bytes  caller buffer of at least mx_pack_size() bytes, 256-byte aligned
+ *   out         filled on success
+ * Requirements: K % 32 == 0, N >= 1, E >= 1; codes_rows = N/32 needs N % 32 == 0.
+ * Errors: MX_ERR_SCALE if a code is 255; MX_ERR_NOT_BLOCK32 if REQUIRE_BLOCK and
+ * the rows of some 32-row group disagree.  The call synchronises `stream` (it
+ * returns the fold decision and the -0 count, as the pages' host functions do).
+ */
+int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, int N,
+                    int K, int codes_rows, unsigned flags, void* dst, size_t dst_bytes,
+                    mx_packed_weight* out, void* stream);
+
+/* ------------------------------------------------------------- activations */
+
+/*
+ * Per-token MXFP8 quantization of a bf16 activation (rocm_native,
+ * _quant_mxfp8_tile): per row and 32-wide K block, amax = max(max|x|, 2^-126),
+ * code = clamp(ceil(log2(amax / 448)) + 127, 0, 254), q = e4m3_rne(x * 2^(127 - code)).
+ * A block holding NaN or inf gets code 255 and bytes 0x7F.
+ *   x [M, K] bf16;  q [M, K] e4m3;  codes [M, K/32] E8M0, row-major
+ *   (rocm_native, input_quant_key).  K % 32 == 0; M == 0 is a no-op.
+ */
+int mx_quantize_act(const void* x, int M, int K, uint8_t* q, uint8_t* codes, void* stream);
+
+/*
+ * Dequantize MX weights to bf16: out = bf16_rne(value(byte) * 2^(code - 127))
+ * (weights942, ocp_from_dequant; rocm_native names it dequant_mxfp8_to_bf16).
+ *   bytes  E4M3: [N, K];  E2M1: [N, K/2] fp4x2, low nibble first (unpacked order)
+ *   codes  BLOCK32X32: [N/32, K/32]  or  ROW1X32: [N, K/32]
+ *   out    [N, K] bf16.   Code 255 gives NaN.
+ */
+int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode, int N,
+               int K, void* out, void* stream);
+
+/* ------------------------------------------------------------- MXFP8 linear */
+
+/* Workspace bytes mxfp8_linear needs for M tokens on weight w (0 = none). */
+size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
+
+/*
+ * out = x @ w^T (+ bias) with the bf16 activation MXFP8-quantized per token
+ * inside the call (rocm_native, apply_weights / _launch):
+ *   y[m, n] = sum_b 2^(cw[n,b]-127) 2^(cx[m,b]-127) sum_{k in b} W[n,k] xq[m,k]
+ * accumulated in fp32, bias added in fp32, rounded once to bf16.
+ *   x     [M, K] bf16           w     packed E4M3 weight with E == 1
+ *   bias  [N] bf16 or NULL      out   [M, N] bf16
+ *   workspace  device scratch of mxfp8_linear_workspace_size(M, w) bytes
+ * M <= MX_GEMV_MAX_M runs the split-K decode GEMV (quantization fused for
+ * small M), larger M the block-scaled GEMM.  Results do not depend on M.
+ */
+int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
+                 unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ MXFP4 MoE */
+
+/*
+ * Token -> expert grouping (the plainest reading of routed experts; the pages
+ * show no router).  Pairs p = t * topk + j are grouped by id in increasing p.
+ *   topk_ids [T, topk] int32; ids of -1 are skipped; ids outside [-1, E) are
+ *            skipped and set *dev_status = MX_ERR_EXPERT_ID (else it is set to 0)
+ *   counts [E], offsets [E + 1], pairs [T * topk] (first offsets[E] valid),
+ *   active [E] (experts with a pair, ascending; first *n_active valid),
+ *   n_active [1]: all int32 device outputs.   E <= MX_MAX_EXPERTS.
+ */
+int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* counts,
+                     int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
+                     int* dev_status, void* stream);
+
+/* Workspace bytes mxfp4_moe_linear needs. */
+size_t mxfp4_moe_workspace_size(int T, int topk, int E);
+
+/*
+ * Routed A16W4 expert GEMM (a16w4 module text, dequant / step_mfma): for every
+ * pair (t, j) with e = topk_ids[t, j] in [0, E),
+ *   out[t, j, n] = sum_k bf16(e2m1(W_e[n,k]) * 2^(c_e[n,k/32] - 127)) * x[t, k]
+ * in fp32, rounded to bf16; pairs with an invalid id get zeros.
+ *   x [T, K] bf16; topk_ids [T, topk] int32; w packed E2M1 weight [E, N, K];
+ *   out [T, topk, N] bf16; workspace of mxfp4_moe_workspace_size bytes;
+ *   dev_status as in mx_route_experts.
+ */
+int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk,
+                     const mx_packed_weight* w, void* out, void* workspace,
+                     size_t workspace_bytes, int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MX_GB300_H */

@@ -1,0 +1,387 @@
+// C ABI of the library (include/mx.h): argument checks, workspace carving and
+// dispatch to the kernels.  No call allocates memory; only mx_pack_weights and
+// mx_check_device_errors synchronise.
+
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+namespace {
+thread_local char g_msg[512] = {0};
+
+constexpr size_t kAlign = 256;
+constexpr int kFusedQuantMaxM = 8;  // quantize x inside the GEMV up to this many tokens
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int padded_k(int K) { return (K + 127) / 128 * 128; }
+
+struct DevCache {
+  bool valid;
+  DeviceInfo info;
+};
+DevCache g_dev[64];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int check_device() {
+  DeviceInfo di;
+  const int rc = current_device_info(&di);
+  if (rc != MX_OK) return rc;
+  if (di.cc_major != 10 || di.cc_minor != 3)
+    return set_error(MX_ERR_UNSUPPORTED, "device compute capability %d.%d is not sm_103", di.cc_major,
+                     di.cc_minor);
+  return MX_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return set_error(MX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Packed-buffer regions: [header 256 B][bytes][codes][sf]
+struct PackRegions {
+  size_t bytes_off, codes_off, sf_off, total;
+};
+
+PackRegions pack_regions(int fmt, int E, int N, int K) {
+  PackRegions r;
+  const int Kp = padded_k(K);
+  const size_t nbytes = static_cast<size_t>(E) * N * (fmt == MX_FMT_E4M3 ? Kp : Kp / 2);
+  const size_t ncodes = static_cast<size_t>(E) * N * (Kp / 32);  // row mode is the larger
+  const size_t nsf = fmt == MX_FMT_E4M3 ? static_cast<size_t>(E) * ((N + 127) / 128) * (Kp / 128) * 512 : 0;
+  r.bytes_off = kAlign;
+  r.codes_off = r.bytes_off + align_up(nbytes, kAlign);
+  r.sf_off = r.codes_off + align_up(ncodes, kAlign);
+  r.total = r.sf_off + align_up(nsf, kAlign);
+  return r;
+}
+
+struct LinearWs {
+  size_t xq_off, codes_off, total;
+};
+
+LinearWs linear_ws(int M, int Kp) {
+  LinearWs r;
+  const size_t Mp = M <= MX_GEMV_MAX_M ? static_cast<size_t>(M) : (static_cast<size_t>(M) + 127) / 128 * 128;
+  r.xq_off = 0;
+  r.codes_off = align_up(Mp * Kp, kAlign);
+  r.total = r.codes_off + align_up(Mp * (Kp / 32), kAlign);
+  return r;
+}
+
+struct MoeWs {
+  size_t counts, offsets, pairs, active, n_active, status, total;
+};
+
+MoeWs moe_ws(int T, int topk, int E) {
+  MoeWs r;
+  const size_t P = static_cast<size_t>(T) * topk;
+  size_t o = 0;
+  r.counts = o;   o += align_up(4 * static_cast<size_t>(E), 16);
+  r.offsets = o;  o += align_up(4 * (static_cast<size_t>(E) + 1), 16);
+  r.pairs = o;    o += align_up(4 * (P ? P : 1), 16);
+  r.active = o;   o += align_up(4 * static_cast<size_t>(E), 16);
+  r.n_active = o; o += 16;
+  r.status = o;   o += 16;
+  r.total = o;
+  return r;
+}
+
+}  // namespace
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int current_device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(MX_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_dev[dev].valid) {
+    DeviceInfo di = {};
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "device attribute");
+    di.sm_count = v;
+    cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    di.max_smem_optin = static_cast<size_t>(v);
+    g_dev[dev].info = di;
+    g_dev[dev].valid = true;
+  }
+  *out = g_dev[dev].info;
+  return MX_OK;
+}
+
+int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                         uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                         uint32_t box1, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return set_error(MX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(MX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return MX_OK;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" {
+
+const char* mx_last_error(void) { return g_msg; }
+
+int mx_check_device_errors(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  const unsigned int flags = take_error_flags_gemv();
+  if (flags & 0x80000000u) return set_error(MX_ERR_CUDA, "could not read the device error flags");
+  if (flags & 1u) return set_error(MX_ERR_TIMEOUT, "a bounded wait inside a kernel timed out");
+  return MX_OK;
+}
+
+size_t mx_pack_size(int fmt, int E, int N, int K) {
+  if ((fmt != MX_FMT_E4M3 && fmt != MX_FMT_E2M1) || E < 1 || N < 1 || K < 32 || K % 32) return 0;
+  return pack_regions(fmt, E, N, K).total;
+}
+
+int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, int N, int K,
+                    int codes_rows, unsigned flags, void* dst, size_t dst_bytes,
+                    mx_packed_weight* out, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (fmt != MX_FMT_E4M3 && fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "unknown format %d", fmt);
+  if (!bytes || !codes || !dst || !out) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (E < 1 || N < 1 || K < 32 || K % 32)
+    return set_error(MX_ERR_SHAPE, "E=%d N=%d K=%d: need E, N >= 1 and K a positive multiple of 32", E, N, K);
+  const bool rows_given = codes_rows == N;
+  const bool blocks_given = !rows_given && N % 32 == 0 && codes_rows == N / 32;
+  if (!rows_given && !blocks_given)
+    return set_error(MX_ERR_SHAPE, "codes_rows=%d must be N=%d or N/32", codes_rows, N);
+  if (flags & ~(MX_PACK_FOLD | MX_PACK_REQUIRE_BLOCK)) return set_error(MX_ERR_ARG, "unknown pack flags");
+  if (!aligned16(bytes) || (reinterpret_cast<uintptr_t>(dst) % kAlign))
+    return set_error(MX_ERR_ALIGN, "weight bytes need 16-byte and dst 256-byte alignment");
+  const PackRegions R = pack_regions(fmt, E, N, K);
+  if (dst_bytes < R.total) return set_error(MX_ERR_SHAPE, "dst holds %zu bytes, needs %zu", dst_bytes, R.total);
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+
+  uint8_t* base = static_cast<uint8_t*>(dst);
+  unsigned int* status = reinterpret_cast<unsigned int*>(base);
+  unsigned long long* negz = reinterpret_cast<unsigned long long*>(base + 8);
+  const int Kp = padded_k(K);
+  const int KB = K / 32;
+  const bool want_fold = fmt == MX_FMT_E4M3 && rows_given && N % 32 == 0 &&
+                         (flags & (MX_PACK_FOLD | MX_PACK_REQUIRE_BLOCK));
+  cudaError_t e = cudaMemsetAsync(base, 0, kAlign, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pack: memset");
+  if ((e = launch_pack_check_codes(codes, E, codes_rows, KB, want_fold, status, stream)) != cudaSuccess)
+    return cuda_fail(e, "pack: check codes");
+  unsigned int st = 0;
+  if ((e = cudaMemcpyAsync(&st, status, sizeof(st), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e, "pack: read status");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "pack: synchronize");
+  if (st & 1u) return set_error(MX_ERR_SCALE, "an E8M0 weight code is 255 (NaN)");
+
+  mx_packed_weight w = {};
+  w.fmt = fmt;
+  w.E = E;
+  w.N = N;
+  w.K = K;
+  w.Kp = Kp;
+  w.bytes = base + R.bytes_off;
+  w.codes = base + R.codes_off;
+  w.sf = fmt == MX_FMT_E4M3 ? base + R.sf_off : nullptr;
+  if (fmt == MX_FMT_E4M3) {
+    bool block;
+    if (blocks_given) {
+      block = true;
+    } else if (want_fold && !(st & 2u)) {
+      block = true;
+    } else {
+      if (flags & MX_PACK_REQUIRE_BLOCK)
+        return set_error(MX_ERR_NOT_BLOCK32, "row scales [%d, %d] are not 32 x 32 blocks", N, KB);
+      block = false;
+    }
+    w.scale_mode = block ? MX_SCALE_BLOCK32X32 : MX_SCALE_ROW1X32;
+    if ((e = launch_pack_e4m3(bytes, codes, E, N, K, Kp, codes_rows, block, w.bytes, w.codes, w.sf, stream)) !=
+        cudaSuccess)
+      return cuda_fail(e, "pack e4m3");
+  } else {
+    w.scale_mode = MX_SCALE_ROW1X32;
+    if ((e = launch_pack_e2m1(bytes, codes, E, N, K, Kp, codes_rows, w.bytes, w.codes, negz, stream)) !=
+        cudaSuccess)
+      return cuda_fail(e, "pack e2m1");
+  }
+  unsigned long long nz = 0;
+  if ((e = cudaMemcpyAsync(&nz, negz, sizeof(nz), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e, "pack: read -0 count");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "pack: synchronize");
+  w.neg_zero_count = static_cast<int64_t>(nz);
+  *out = w;
+  return MX_OK;
+}
+
+int mx_quantize_act(const void* x, int M, int K, uint8_t* q, uint8_t* codes, void* stream) {
+  if (M < 0 || K < 32 || K % 32) return set_error(MX_ERR_SHAPE, "M=%d K=%d: K must be a positive multiple of 32", M, K);
+  if (M == 0) return MX_OK;
+  if (!x || !q || !codes) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(q)) return set_error(MX_ERR_ALIGN, "x and q need 16-byte alignment");
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  cudaError_t e = launch_quant_act(x, M, K, K, q, K, codes, K / 32, 128, nullptr, false,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MX_OK : cuda_fail(e, "quantize launch");
+}
+
+int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode, int N, int K,
+               void* out, void* stream) {
+  if (fmt != MX_FMT_E4M3 && fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "unknown format %d", fmt);
+  if (scale_mode != MX_SCALE_BLOCK32X32 && scale_mode != MX_SCALE_ROW1X32)
+    return set_error(MX_ERR_ARG, "unknown scale mode %d", scale_mode);
+  if (N < 0 || K < 32 || K % 32) return set_error(MX_ERR_SHAPE, "N=%d K=%d", N, K);
+  if (scale_mode == MX_SCALE_BLOCK32X32 && N % 32) return set_error(MX_ERR_SHAPE, "32x32 blocks need N %% 32 == 0");
+  if (N == 0) return MX_OK;
+  if (!bytes || !codes || !out) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(bytes) || !aligned16(out)) return set_error(MX_ERR_ALIGN, "bytes and out need 16-byte alignment");
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  cudaError_t e = launch_dequant(bytes, codes, fmt, scale_mode, N, K, out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MX_OK : cuda_fail(e, "dequant launch");
+}
+
+size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w) {
+  if (!w || M <= 0) return 0;
+  return linear_ws(M, w->Kp).total;
+}
+
+int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
+                 unsigned flags, void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!w) return set_error(MX_ERR_ARG, "NULL weight");
+  if (w->fmt != MX_FMT_E4M3 || w->E != 1) return set_error(MX_ERR_ARG, "mxfp8_linear needs a dense E4M3 weight");
+  if (M < 0) return set_error(MX_ERR_SHAPE, "M=%d", M);
+  if (M == 0) return MX_OK;
+  if (!x || !out) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(out) || (bias && !aligned16(bias)))
+    return set_error(MX_ERR_ALIGN, "x, out and bias need 16-byte alignment");
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  const int force_splits = static_cast<int>((flags >> 8) & 0xfu);
+  const bool no_fuse = (flags & MX_LINEAR_NO_FUSED_QUANT) != 0;
+  const int Kp = w->Kp;
+  const LinearWs L = linear_ws(M, Kp);
+
+  auto run_chunk = [&](const void* xc, int Mc, void* oc) -> int {
+    GemvArgs a = {};
+    a.w = w;
+    a.x = xc;
+    a.bias = bias;
+    a.out = oc;
+    a.M = Mc;
+    a.force_splits = force_splits;
+    if (Mc <= kFusedQuantMaxM && !no_fuse) {
+      a.fused = true;
+      return launch_gemv(a, stream);
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.xq = ws + L.xq_off;
+    a.xcodes = ws + L.codes_off;
+    cudaError_t e = launch_quant_act(xc, Mc, w->K, Kp, ws + L.xq_off, Kp, ws + L.codes_off, Kp / 32, 127,
+                                     nullptr, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    a.fused = false;
+    a.pdl = true;
+    return launch_gemv(a, stream);
+  };
+
+  const bool needs_ws = M > kFusedQuantMaxM || no_fuse;
+  if (needs_ws && (!workspace || workspace_bytes < L.total))
+    return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, L.total);
+  if (needs_ws && !aligned16(workspace)) return set_error(MX_ERR_ALIGN, "workspace needs 16-byte alignment");
+  const size_t xrow = static_cast<size_t>(w->K) * 2, orow = static_cast<size_t>(w->N) * 2;
+  for (int m0 = 0; m0 < M; m0 += MX_GEMV_MAX_M) {
+    const int Mc = (M - m0) < MX_GEMV_MAX_M ? (M - m0) : MX_GEMV_MAX_M;
+    rc = run_chunk(static_cast<const uint8_t*>(x) + m0 * xrow, Mc, static_cast<uint8_t*>(out) + m0 * orow);
+    if (rc != MX_OK) return rc;
+  }
+  return MX_OK;
+}
+
+int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* counts,
+                     int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
+                     int* dev_status, void* stream) {
+  if (T < 0 || topk < 1 || E < 1) return set_error(MX_ERR_SHAPE, "T=%d topk=%d E=%d", T, topk, E);
+  if (E > MX_MAX_EXPERTS) return set_error(MX_ERR_UNSUPPORTED, "E=%d exceeds %d", E, MX_MAX_EXPERTS);
+  if ((T > 0 && !topk_ids) || !counts || !offsets || !pairs || !active || !n_active)
+    return set_error(MX_ERR_ARG, "NULL pointer");
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  cudaError_t e = launch_route(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, dev_status,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MX_OK : cuda_fail(e, "route launch");
+}
+
+size_t mxfp4_moe_workspace_size(int T, int topk, int E) {
+  if (T < 0 || topk < 1 || E < 1) return 0;
+  return moe_ws(T, topk, E).total;
+}
+
+int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, const mx_packed_weight* w,
+                     void* out, void* workspace, size_t workspace_bytes, int* dev_status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!w) return set_error(MX_ERR_ARG, "NULL weight");
+  if (w->fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "mxfp4_moe_linear needs an E2M1 weight");
+  if (T < 0 || topk < 1) return set_error(MX_ERR_SHAPE, "T=%d topk=%d", T, topk);
+  if (w->E > MX_MAX_EXPERTS) return set_error(MX_ERR_UNSUPPORTED, "E=%d exceeds %d", w->E, MX_MAX_EXPERTS);
+  if (T == 0) return MX_OK;
+  if (!x || !topk_ids || !out || !workspace) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(out) || !aligned16(workspace))
+    return set_error(MX_ERR_ALIGN, "x, out and workspace need 16-byte alignment");
+  const MoeWs R = moe_ws(T, topk, w->E);
+  if (workspace_bytes < R.total) return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, R.total);
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + R.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + R.offsets);
+  int32_t* pairs = reinterpret_cast<int32_t*>(ws + R.pairs);
+  int32_t* active = reinterpret_cast<int32_t*>(ws + R.active);
+  int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.n_active);
+  int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.status);
+  cudaError_t e = launch_route(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "route launch");
+  if ((e = launch_zero_invalid_pairs(topk_ids, T, topk, w->E, w->N, out, stream)) != cudaSuccess)
+    return cuda_fail(e, "zero launch");
+  return launch_moe(x, T, topk, w, offsets, pairs, active, n_active, out, stream);
+}
+
+}  // extern "C"

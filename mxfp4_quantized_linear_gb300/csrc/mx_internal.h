@@ -1,0 +1,76 @@
+// Host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mx.h"
+
+namespace mx {
+
+// Set the thread's last-error message; returns `code`.
+int set_error(int code, const char* fmt, ...);
+
+// Device properties of the current device (cached per device).
+struct DeviceInfo {
+  int sm_count;
+  int cc_major, cc_minor;
+  size_t max_smem_optin;
+};
+int current_device_info(DeviceInfo* out);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                         uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                         uint32_t box1, CUtensorMapSwizzle swizzle);
+
+// ---- quantize / dequant (quant.cu)
+// x [M, K] bf16 -> q [M, ldq] (columns K..Kout zero), codes [M, ldc] (blocks past
+// K get pad_code); optional sf atoms [ceil(M/128), Kout/128, 512].  When
+// `pdl_trigger` the kernel lets a programmatic dependent launch start at once.
+cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, int ldq,
+                             uint8_t* codes, int ldc, uint8_t pad_code, uint8_t* sf,
+                             bool pdl_trigger, cudaStream_t stream);
+cudaError_t launch_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode,
+                           int N, int K, void* out, cudaStream_t stream);
+
+// ---- pack (pack.cu)
+cudaError_t launch_pack_check_codes(const uint8_t* codes, int E, int rows, int KB, bool check_fold,
+                                    unsigned int* status, cudaStream_t stream);
+cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
+                             int Kp, int codes_rows, bool block_out, uint8_t* wq,
+                             uint8_t* codes_out, uint8_t* sf, cudaStream_t stream);
+cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
+                             int Kp, int codes_rows, uint8_t* wq, uint8_t* codes_out,
+                             unsigned long long* negz, cudaStream_t stream);
+
+// ---- decode GEMV (gemv.cu)
+struct GemvArgs {
+  const mx_packed_weight* w;
+  const void* x;         // bf16 [M, K]
+  const uint8_t* xq;     // [M, Kp] e4m3 (unfused path)
+  const uint8_t* xcodes; // [M, Kp/32] (unfused path)
+  const void* bias;      // bf16 [N] or NULL
+  void* out;             // bf16 [M, N]
+  int M;
+  bool fused;
+  bool pdl;              // launched right after the quant kernel with PDL
+  int force_splits;      // 0 = heuristic
+};
+int launch_gemv(const GemvArgs& a, cudaStream_t stream);
+unsigned int take_error_flags_gemv();
+int gemv_splits(int N, int Kp, int M, int force_splits);
+
+// ---- routing + MoE (moe.cu)
+cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
+                         int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
+                         int* dev_status, cudaStream_t stream);
+int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const int32_t* offsets,
+               const int32_t* pairs, const int32_t* active, const int32_t* n_active, void* out,
+               cudaStream_t stream);
+cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E, int N, void* out,
+                                      cudaStream_t stream);
+
+}  // namespace mx

@@ -1,0 +1,148 @@
+// K-QUANT (per-token MXFP8 activation quantizer) and K-DEQ (MX dequant to bf16).
+//
+// Quantizer: rocm_native (vllm.model_executor.kernels.linear.mxfp8.rocm_native),
+// _quant_mxfp8_tile.  Dequant: weights942, ocp_from_dequant (w = e4m3 value x
+// 2^(code - 127)) and a16w4, dequant (fp4x2, low nibble first).
+//
+// Both are HBM-bound elementwise passes: each thread moves 16 bytes of bf16,
+// four lanes form one 32-element MX block.
+
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+namespace {
+
+// One thread = 8 consecutive elements of a row; 4 lanes = one MX block.
+// Grid-stride over 8-element groups of the [M, Kout] output (Kout >= K,
+// multiple of 32).  All lanes of a warp run the same trip count, so the
+// 4-lane shuffles inside mx_quant_block8 always see a full warp.
+__global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
+                                                        int M, int K, int Kout,
+                                                        uint8_t* __restrict__ q, int ldq,
+                                                        uint8_t* __restrict__ codes, int ldc,
+                                                        uint8_t pad_code, uint8_t* __restrict__ sf,
+                                                        int pdl_trigger) {
+  if (pdl_trigger) pdl_launch_dependents();
+  const int groups_per_row = Kout >> 3;
+  const long long total = static_cast<long long>(M) * groups_per_row;
+  const int lane = threadIdx.x & 31;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       base < total; base += stride) {
+    const long long g = base + lane;
+    const bool inside = g < total;
+    const int row = inside ? static_cast<int>(g / groups_per_row) : 0;
+    const int k = inside ? static_cast<int>(g % groups_per_row) * 8 : 0;
+    const bool valid = inside && k < K;
+    float v[8];
+    if (valid) {
+      const uint4 u = *reinterpret_cast<const uint4*>(x + static_cast<long long>(row) * K + k);
+      bf16x8_to_f32(u, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    const QuantBlock8 b = mx_quant_block8(v);
+    if (!inside) continue;
+    uint2 out = valid ? make_uint2(b.lo, b.hi) : make_uint2(0u, 0u);
+    *reinterpret_cast<uint2*>(q + static_cast<long long>(row) * ldq + k) = out;
+    if ((k & 31) == 0) {
+      const uint8_t c = valid ? static_cast<uint8_t>(b.code) : pad_code;
+      if (codes) codes[static_cast<long long>(row) * ldc + (k >> 5)] = c;
+      if (sf) {
+        // 512-byte atom (row tile, 128-K tile): row m, block kb at (m%32)*16 + (m/32)*4 + kb
+        const int j = k >> 5;
+        const int m = row & 127;
+        const long long atom = static_cast<long long>(row >> 7) * (Kout >> 7) + (j >> 2);
+        sf[atom * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = c;
+      }
+    }
+  }
+}
+
+// Dequant: one thread = 8 consecutive output elements of a row.
+template <int kFmt>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ bytes,
+                                                      const uint8_t* __restrict__ codes,
+                                                      int block_scale, int N, int K,
+                                                      __nv_bfloat16* __restrict__ out) {
+  const int groups_per_row = K >> 3;
+  const long long total = static_cast<long long>(N) * groups_per_row;
+  const int KB = K >> 5;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(g / groups_per_row);
+    const int k = static_cast<int>(g % groups_per_row) * 8;
+    const int crow = block_scale ? (n >> 5) : n;
+    const float s = e8m0_to_f32(codes[static_cast<long long>(crow) * KB + (k >> 5)]);
+    float v[8];
+    if (kFmt == MX_FMT_E4M3) {
+      const uint2 u = *reinterpret_cast<const uint2*>(bytes + static_cast<long long>(n) * K + k);
+      const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1))));
+        const float2 f = __half22float2(h);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+      }
+    } else {
+      const uint32_t w =
+          *reinterpret_cast<const uint32_t*>(bytes + static_cast<long long>(n) * (K >> 1) + (k >> 1));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(e2m1x2_to_f16x2((w >> (8 * i)) & 0xffu));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i] * s, v[2 * i + 1] * s);
+      o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(out + static_cast<long long>(n) * K + k) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int grid_for(long long threads, int block) {
+  long long g = (threads + block - 1) / block;
+  DeviceInfo di;
+  const int cap = (current_device_info(&di) == MX_OK) ? di.sm_count * 16 : 2048;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, int ldq,
+                             uint8_t* codes, int ldc, uint8_t pad_code, uint8_t* sf,
+                             bool pdl_trigger, cudaStream_t stream) {
+  const long long groups = static_cast<long long>(M) * (Kout / 8);
+  const int block = 256;
+  const int grid = grid_for(groups, block);
+  quant_act_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), M, K, Kout,
+                                               q, ldq, codes, ldc, pad_code, sf,
+                                               pdl_trigger ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode,
+                           int N, int K, void* out, cudaStream_t stream) {
+  const long long groups = static_cast<long long>(N) * (K / 8);
+  const int block = 256;
+  const int grid = grid_for(groups, block);
+  const int blk = scale_mode == MX_SCALE_BLOCK32X32 ? 1 : 0;
+  if (fmt == MX_FMT_E4M3)
+    dequant_kernel<MX_FMT_E4M3><<<grid, block, 0, stream>>>(bytes, codes, blk, N, K,
+                                                             static_cast<__nv_bfloat16*>(out));
+  else
+    dequant_kernel<MX_FMT_E2M1><<<grid, block, 0, stream>>>(bytes, codes, blk, N, K,
+                                                             static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace mx

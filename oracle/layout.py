@@ -27,7 +27,10 @@ Packed E4M3 weight (dense MXFP8), E experts of [N, K]:
 Packed E2M1 weight (MXFP4 experts), E experts of [N, K]:
   wq     [E, N, Kp/2]   in every 64-byte chunk of a row (4 K blocks of 16 bytes,
          each 4 words of 4 bytes) word w of block b moves to word position
-         4 w + b, i.e. a 4x4 transpose of 4-byte words; -0 nibbles are +0
+         4 w + b, i.e. a 4x4 transpose of 4-byte words; inside every word the
+         element at nibble e (0..7, low nibble of byte 0 first) moves to nibble
+         slot e // 2 + 4 (e % 2), so elements 2i and 2i+1 sit at bits 4i and
+         16 + 4i; -0 nibbles are +0
   codes  [E, N, Kp/32]  per-row codes (32x32 block codes are expanded), 128
          past K
 
@@ -168,6 +171,26 @@ def _word_transpose(row_bytes: np.ndarray) -> np.ndarray:
     return np.swapaxes(v, -3, -2).reshape(*lead, L).copy()  # [chunk, w, b, byte]
 
 
+def _nibble_slot_shuffle(row_bytes: np.ndarray, inverse: bool = False) -> np.ndarray:
+    """Inside every 4-byte word, element nibble e -> slot e // 2 + 4 (e % 2)
+    (or back, with ``inverse``).  Nibble n of a word is bits 4n..4n+3, i.e. the
+    low nibble of byte n // 2 for even n."""
+    *lead, L = row_bytes.shape
+    words = row_bytes.reshape(*lead, L // 4, 4)
+    nib = np.empty(words.shape[:-1] + (8,), dtype=np.uint8)
+    nib[..., 0::2] = words & 0x0F
+    nib[..., 1::2] = words >> 4
+    out = np.empty_like(nib)
+    for e in range(8):
+        slot = e // 2 + 4 * (e % 2)
+        if inverse:
+            out[..., e] = nib[..., slot]
+        else:
+            out[..., slot] = nib[..., e]
+    packed = (out[..., 0::2] | (out[..., 1::2] << 4)).astype(np.uint8)
+    return packed.reshape(*lead, L)
+
+
 def count_negative_zero(w) -> int:
     w = np.asarray(w, dtype=np.uint8)
     return int(np.count_nonzero((w & 0x0F) == 0x08) + np.count_nonzero((w & 0xF0) == 0x80))
@@ -206,12 +229,14 @@ def pack_e2m1(w, codes) -> dict:
     padded = np.zeros((E, N, Kp // 2), dtype=np.uint8)
     padded[:, :, :KH] = clean
     return {"fmt": "e2m1", "mode": "row", "E": E, "N": N, "K": K, "Kp": Kp,
-            "wq": _word_transpose(padded), "codes": _pad_codes(row, Kp // 32),
+            "wq": _nibble_slot_shuffle(_word_transpose(padded)),
+            "codes": _pad_codes(row, Kp // 32),
             "neg_zero_count": negz}
 
 
 def unpack_e2m1(p: dict) -> tuple:
     """Inverse of pack_e2m1 (up to -0 -> +0): (bytes [E, N, K/2], codes [E, N, K/32])."""
     K = p["K"]
-    back = _word_transpose(p["wq"])  # the 4x4 word transpose is its own inverse
+    # the 4x4 word transpose is its own inverse
+    back = _word_transpose(_nibble_slot_shuffle(p["wq"], inverse=True))
     return back[:, :, : K // 2].copy(), p["codes"][:, :, : K // 32].copy()

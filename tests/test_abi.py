@@ -1,0 +1,59 @@
+"""The C ABI library builds, loads, and exports every entry point include/mx.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.helpers import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mx.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mx\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mx_quantize_act", "mx_dequant", "mxfp8_linear", "mxfp4_moe_linear", "mx_pack_weights"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ensure_built()
+    from mxfp4_quantized_linear_gb300 import binding
+    names = declared_functions()
+    assert set(binding.EXPORTED) == set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_host_side_argument_checks_without_gpu():
+    lib = ensure_built()
+    from mxfp4_quantized_linear_gb300 import binding as b
+    assert lib.mx_pack_size(b.MX_FMT_E4M3, 1, 7168, 2080) == 256 + 7168 * 2176 + 7168 * 68 + 56 * 17 * 512
+    assert lib.mx_pack_size(b.MX_FMT_E4M3, 1, 64, 33) == 0
+    assert lib.mx_pack_size(7, 1, 64, 64) == 0
+    assert lib.mx_quantize_act(None, 4, 33, None, None, None) == b.MX_ERR_SHAPE
+    assert b"multiple of 32" in lib.mx_last_error()
+    assert lib.mx_quantize_act(None, 0, 64, None, None, None) == b.MX_OK     # M == 0: no-op
+    assert lib.mx_quantize_act(None, 2, 64, None, None, None) == b.MX_ERR_ARG
+    assert lib.mx_dequant(None, None, 9, 0, 32, 64, None, None) == b.MX_ERR_ARG
+    assert lib.mx_dequant(None, None, 0, 0, 33, 64, None, None) == b.MX_ERR_SHAPE
+    assert lib.mx_route_experts(None, 4, 2, 4096, None, None, None, None, None, None, None) == b.MX_ERR_UNSUPPORTED
+    assert lib.mxfp8_linear(None, 1, None, None, None, 0, None, 0, None) == b.MX_ERR_ARG
+    w = b.MxPackedWeightC(fmt=b.MX_FMT_E2M1, E=1, N=64, K=64, Kp=128)
+    assert lib.mxfp8_linear(None, 1, ctypes.byref(w), None, None, 0, None, 0, None) == b.MX_ERR_ARG
+    bad = ctypes.c_void_p(0x1001)  # misaligned (never dereferenced: rejected first)
+    assert lib.mx_quantize_act(bad, 2, 64, bad, bad, None) == b.MX_ERR_ALIGN
+    assert lib.mxfp4_moe_workspace_size(4, 2, 8) > 0
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    from mxfp4_quantized_linear_gb300 import binding
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,136 @@
+"""mxfp8_linear (quantize + split-K GEMV / large-M path) on the GPU against the
+oracle: normalised max error <= 1e-2 (see tests/helpers.TOL), plus bitwise
+batch invariance and fused / unfused agreement."""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_quantized_linear_gb300 as mx
+from mxfp4_quantized_linear_gb300 import inputs
+from oracle.linear import mxfp8_linear as ref_linear, normalized_error
+from tests.helpers import TOL, bf16_np, cuda_device, ensure_built, u8
+
+pytestmark = pytest.mark.gpu
+
+
+def pack(w, c, flags=mx.MX_PACK_FOLD):
+    dev = cuda_device()
+    ensure_built()
+    return mx.mx_pack_weights(w.to(dev), c.to(dev), "e4m3", flags)
+
+
+def gpu_linear(p, x, bias=None, flags=0):
+    dev = cuda_device()
+    y = mx.mxfp8_linear(x.to(dev), p, None if bias is None else bias.to(dev), flags=flags)
+    torch.cuda.synchronize()
+    return y
+
+
+def row_codes(codes: np.ndarray, N: int) -> np.ndarray:
+    return np.repeat(codes, 32, axis=0)[:N] if codes.shape[0] != N else codes
+
+
+def check(p, w, c, x, bias=None, rows=None, flags=0, tol=TOL):
+    y = gpu_linear(p, x, bias, flags).float().cpu().numpy()
+    wn, cn = u8(w), row_codes(u8(c), w.shape[0])
+    if rows is not None:
+        wn, cn, y = wn[rows], cn[rows], y[:, rows]
+    ref = ref_linear(bf16_np(x), wn, cn, None if bias is None else bf16_np(bias)[rows if rows is not None else slice(None)])
+    err = normalized_error(y, ref["y"], ref["A"], ref["B"])
+    assert err <= tol, err
+    return err
+
+
+def test_gemv_small_m1_row_codes():
+    c = inputs.gemv_small()
+    p = pack(c["w"], c["codes"])
+    assert p.scale_mode == mx.MX_SCALE_ROW1X32
+    for M in (1, 2, 4):
+        check(p, c["w"], c["codes"], inputs.bf16_normal((M, c["K"]), inputs.generator(M)))
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 32])
+def test_ragged_rows_and_k(M):
+    g = inputs.generator(100 + M)
+    w = inputs.e4m3_bytes((96, 2080), g)
+    c = inputs.e8m0_codes((3, 65), 118, 132, g)
+    check(pack(w, c), w, c, inputs.bf16_normal((M, 2080), g))
+
+
+def test_row_mode_small_n_short_k_with_bias():
+    g = inputs.generator(7)
+    w = inputs.e4m3_bytes((40, 96), g)
+    c = inputs.e8m0_codes((40, 3), 120, 130, g)
+    b = inputs.bf16_normal((40,), g)
+    p = pack(w, c)
+    for M in (1, 5, 12):
+        check(p, w, c, inputs.bf16_normal((M, 96), g), bias=b)
+
+
+@pytest.mark.parametrize("K", [2048, 2080])
+def test_decode_linear_full_size(K):
+    c = inputs.decode_linear(K=K)
+    p = pack(c["w"], c["codes"])
+    assert p.scale_mode == mx.MX_SCALE_BLOCK32X32
+    for M, x in c["xs"].items():
+        check(p, c["w"], c["codes"], x)
+
+
+def test_large_m_path():
+    g = inputs.generator(9)
+    w = inputs.e4m3_bytes((192, 512), g)
+    c = inputs.e8m0_codes((6, 16), 118, 132, g)
+    p = pack(w, c)
+    for M in (33, 64, 130):
+        check(p, w, c, inputs.bf16_normal((M, 512), g))
+
+
+def test_batch_invariance_and_fused_equals_unfused():
+    c = inputs.decode_linear(K=2080, Ms=(32,), seed=3)
+    p = pack(c["w"], c["codes"])
+    x = c["xs"][32]
+    y32 = gpu_linear(p, x).cpu()
+    for m in (0, 7, 31):
+        y1 = gpu_linear(p, x[m:m + 1]).cpu()
+        assert torch.equal(y1[0].view(torch.int16), y32[m].view(torch.int16)), m
+    y4 = gpu_linear(p, x[:4]).cpu()
+    y4u = gpu_linear(p, x[:4], flags=mx.MX_LINEAR_NO_FUSED_QUANT).cpu()
+    assert torch.equal(y4.view(torch.int16), y4u.view(torch.int16))
+    assert torch.equal(y4.view(torch.int16), y32[:4].view(torch.int16))
+
+
+@pytest.mark.parametrize("N,K", [(24576, 1536), (7168, 8192)])
+def test_layer_sweep_linears_sampled_rows(N, K):
+    g = inputs.generator(N + K)
+    w = inputs.e4m3_bytes((N, K), g)
+    c = inputs.e8m0_codes((N // 32, K // 32), 118, 132, g)
+    p = pack(w, c)
+    rows = np.sort(np.random.default_rng(1).choice(N, size=256, replace=False))
+    for M in (1, 8, 32, 64):
+        check(p, w, c, inputs.bf16_normal((M, K), g), rows=rows)
+
+
+def test_prefill_full_size_sampled():
+    c = inputs.prefill_gemm()
+    p = pack(c["w"], c["codes"])
+    y = gpu_linear(p, c["x"]).float().cpu().numpy()
+    rng = np.random.default_rng(2)
+    ms = np.sort(rng.choice(4096, size=24, replace=False))
+    ns = np.sort(rng.choice(7168, size=48, replace=False))
+    wn = u8(c["w"])[ns]
+    cn = row_codes(u8(c["codes"]), 7168)[ns]
+    ref = ref_linear(bf16_np(c["x"][ms]), wn, cn)
+    err = normalized_error(y[np.ix_(ms, ns)], ref["y"], ref["A"], ref["B"])
+    assert err <= TOL, err
+
+
+def test_workspace_too_small_is_an_error():
+    g = inputs.generator(4)
+    w = inputs.e4m3_bytes((64, 256), g)
+    c = inputs.e8m0_codes((2, 8), 120, 130, g)
+    p = pack(w, c)
+    dev = cuda_device()
+    x = inputs.bf16_normal((20, 256), g).to(dev)
+    with pytest.raises(mx.MxError) as ei:
+        mx.mxfp8_linear(x, p, workspace=torch.empty(16, dtype=torch.uint8, device=dev))
+    assert ei.value.code == mx.binding.MX_ERR_WORKSPACE

@@ -1,0 +1,114 @@
+"""K-ROUTE (bit-exact) and the routed A16W4 expert GEMM (normalised error) on the
+GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_quantized_linear_gb300 as mx
+from mxfp4_quantized_linear_gb300 import inputs
+from oracle.linear import normalized_error
+from oracle.moe import MX_ERR_EXPERT_ID, dequant_experts_bf16, moe_linear, route
+from oracle.formats import bf16_rne_bits, bf16_value
+from oracle.linear import dequant_values
+from tests.helpers import TOL, bf16_np, cuda_device, ensure_built, u8
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_route(ids, E):
+    dev = cuda_device()
+    ensure_built()
+    r = mx.mx_route_experts(ids.to(dev), E)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in r.items()}
+
+
+@pytest.mark.parametrize("T,topk,E", [(37, 5, 11), (64, 8, 64), (256, 8, 256), (1, 8, 256), (300, 4, 512)])
+def test_route_bit_exact(T, topk, E):
+    rng = np.random.default_rng(T * E)
+    ids = rng.integers(-1, E, size=(T, topk)).astype(np.int32)
+    if T > 2:
+        ids[1, 0] = E + 3
+        ids[2, 1] = -9
+    r = gpu_route(torch.tensor(ids), E)
+    ref = route(ids, E)
+    assert np.array_equal(r["counts"], ref["counts"])
+    assert np.array_equal(r["offsets"], ref["offsets"])
+    n = int(ref["offsets"][-1])
+    assert np.array_equal(r["pairs"][:n], ref["pairs"])
+    na = int(r["n_active"][0])
+    assert na == len(ref["active"]) and np.array_equal(r["active"][:na], ref["active"])
+    assert int(r["status"][0]) == ref["status"]
+
+
+def test_route_empty():
+    r = gpu_route(torch.zeros((0, 4), dtype=torch.int32), 8)
+    assert int(r["n_active"][0]) == 0 and np.all(r["offsets"] == 0) and np.all(r["counts"] == 0)
+
+
+def gpu_moe(m, ids=None, status=None):
+    dev = cuda_device()
+    ensure_built()
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    ids = m["ids"] if ids is None else ids
+    y = mx.mxfp4_moe_linear(m["x"].to(dev), ids.to(dev), p, dev_status=status)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy()
+
+
+def check_moe(m, ids=None):
+    ids = m["ids"] if ids is None else ids
+    dev = cuda_device()
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    y = gpu_moe(m, ids, status)
+    xv = bf16_np(m["x"])
+    W = dequant_experts_bf16(u8(m["w"]), u8(m["codes"]))
+    ref = moe_linear(xv, u8(ids), u8(m["w"]), u8(m["codes"]), wdeq=W)
+    idn = u8(ids)
+    E = m["E"]
+    for t in range(idn.shape[0]):
+        for j in range(idn.shape[1]):
+            e = int(idn[t, j])
+            if 0 <= e < E:
+                err = normalized_error(y[t, j][None], ref[t, j][None], xv[t][None], W[e])
+                assert err <= TOL, (t, j, err)
+            else:
+                assert np.all(y[t, j] == 0)
+    return int(status.item())
+
+
+def test_moe_small_with_invalid_ids():
+    m = inputs.moe_gate_up(E=8, N=256, K=512, T=13, topk=3, seed=1)
+    ids = m["ids"].clone()
+    ids[4, 1] = -1
+    assert check_moe(m, ids) == 0
+    ids[6, 2] = 99
+    assert check_moe(m, ids) == MX_ERR_EXPERT_ID
+
+
+def test_moe_ragged_rows_and_k():
+    m = inputs.moe_gate_up(E=5, N=136, K=2080, T=9, topk=2, seed=2)
+    assert check_moe(m) == 0
+
+
+def test_moe_many_tokens_one_expert():
+    m = inputs.moe_gate_up(E=3, N=128, K=256, T=40, topk=1, seed=3)
+    ids = torch.zeros((40, 1), dtype=torch.int32)
+    ids[::5] = 2
+    assert check_moe(m, ids) == 0
+
+
+def test_moe_gate_up_full_size_sampled():
+    m = inputs.moe_gate_up()
+    y = gpu_moe(m)
+    rng = np.random.default_rng(4)
+    wb, cb, ids = u8(m["w"]), u8(m["codes"]), u8(m["ids"])
+    xv = bf16_np(m["x"])
+    for _ in range(48):
+        t, j = int(rng.integers(0, 64)), int(rng.integers(0, 8))
+        ns = np.sort(rng.choice(4096, size=64, replace=False))
+        e = int(ids[t, j])
+        Wd = bf16_value(bf16_rne_bits(dequant_values(wb[e, ns], cb[e, ns], "e2m1", len(ns), 4096)))
+        ref = Wd @ xv[t]
+        err = normalized_error(y[t, j, ns][None], ref[None], xv[t][None], Wd)
+        assert err <= TOL, (t, j, err)

@@ -61,14 +61,19 @@ def test_fold_decisions():
     assert ei.value.code == L.MX_ERR_SCALE
 
 
-def test_e2m1_word_transpose_by_positions():
-    w = np.arange(64, dtype=np.uint8).reshape(1, 1, 64) & 0x77   # no -0 nibbles
+def test_e2m1_word_transpose_and_nibble_slots_by_positions():
+    rng = np.random.default_rng(9)
+    w = (rng.integers(0, 256, size=(1, 1, 64)) & 0x77).astype(np.uint8)   # no -0 nibbles
     codes = np.full((1, 1, 4), 127, dtype=np.uint8)
-    p = L.pack_e2m1(w, codes)
-    out = p["wq"][0, 0]
-    for pos in range(64):
-        wd, b, i = pos // 16, (pos // 4) % 4, pos % 4
-        assert out[pos] == w[0, 0, 16 * b + 4 * wd + i]
+    out = L.pack_e2m1(w, codes)["wq"][0, 0]
+    outword = [int.from_bytes(bytes(out[4 * i: 4 * i + 4]), "little") for i in range(16)]
+    for o in range(16):                      # output word o = 4 w + b
+        wd, b = o // 4, o % 4
+        src = w[0, 0, 16 * b + 4 * wd: 16 * b + 4 * wd + 4]
+        for e in range(8):                   # element e of the source word
+            nib = (int(src[e // 2]) >> (4 * (e % 2))) & 0xF
+            slot = e // 2 + 4 * (e % 2)
+            assert (outword[o] >> (4 * slot)) & 0xF == nib
 
 
 def test_e2m1_roundtrip_padding_and_negative_zero_count():
@@ -88,5 +93,5 @@ def test_e2m1_roundtrip_padding_and_negative_zero_count():
     assert np.all(p["codes"][:, :, K // 32:] == 128)
     assert not np.any((p["wq"] & 0x0F) == 0x08) and not np.any((p["wq"] & 0xF0) == 0x80)
     # the padded tail (past K/2 bytes, before the transpose) is zero
-    untransposed = L._word_transpose(p["wq"])
+    untransposed = L._word_transpose(L._nibble_slot_shuffle(p["wq"], inverse=True))
     assert np.all(untransposed[:, :, K // 2:] == 0)
