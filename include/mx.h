@@ -170,6 +170,31 @@ size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
 int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
                  unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Scratch-free decode linear.  The source pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory or pass a
+ * workspace -- engines that plan all device memory before serving and forbid
+ * allocation on the request path, and plugin / callback code that receives
+ * only its input and output buffers from a framework owning the allocator.
+ *
+ * Computes exactly what mxfp8_linear computes for M <= MX_GEMV_MAX_M (the
+ * activation is quantized in a separate launch), but keeps the quantized
+ * activation and its codes in a fixed library-owned device array of
+ * MX_NOALLOC_SCRATCH_BYTES, present on every GPU that loads the library until
+ * the process exits.  It calls no allocator.
+ *   - Limits: 1 <= M <= MX_GEMV_MAX_M and M*Kp + M*Kp/32 (+ 256-byte alignment)
+ *     <= MX_NOALLOC_SCRATCH_BYTES (e.g. M = 32 up to K = 31744); otherwise
+ *     MX_ERR_UNSUPPORTED with a message.  M == 0 is a no-op.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array: calls that overlap on the GPU (e.g. on two
+ *     streams at once) race and must be serialised by the caller.  Each call
+ *     writes every scratch byte it reads, so stale contents are harmless.
+ */
+#define MX_NOALLOC_SCRATCH_BYTES (1u << 20)
+int mxfp8_linear_noalloc(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
+                         void* stream);
+
 /* ------------------------------------------------------------------ MXFP4 MoE */
 
 /*

@@ -25,7 +25,8 @@ MX_MAX_EXPERTS = 512
 
 EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_weights",
             "mx_quantize_act", "mx_dequant", "mxfp8_linear_workspace_size", "mxfp8_linear",
-            "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear")
+            "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear",
+            "mxfp8_linear_noalloc")
 
 
 class MxError(RuntimeError):
@@ -72,6 +73,7 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mx_route_experts": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "mxfp4_moe_workspace_size": (sz, [i32, i32, i32]),
         "mxfp4_moe_linear": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
+        "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -214,6 +216,24 @@ def mxfp8_linear(x: torch.Tensor, w: PackedWeight, bias: torch.Tensor = None, ou
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(load_library().mxfp8_linear(_ptr(x), M, ctypes.byref(w.desc), _ptr(bias), _ptr(out), flags,
                                        _ptr(workspace), ws_bytes, _stream()))
+    return out
+
+
+def mxfp8_linear_noalloc(x: torch.Tensor, w: PackedWeight, bias: torch.Tensor = None,
+                         out: torch.Tensor = None) -> torch.Tensor:
+    """mxfp8_linear for M <= 32 without a workspace: the library keeps the
+    quantized activation in its own fixed device array, for callers that may
+    not allocate (see include/mx.h).  Pass ``out`` to avoid the allocation this
+    Python wrapper would otherwise make for the result."""
+    _need(x, torch.bfloat16, "x")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias")
+    _check(load_library().mxfp8_linear_noalloc(_ptr(x), M, ctypes.byref(w.desc), _ptr(bias), _ptr(out),
+                                               _stream()))
     return out
 
 
