@@ -81,7 +81,10 @@ enum { MX_SCALE_BLOCK32X32 = 0, MX_SCALE_ROW1X32 = 1 };
  * E2M1 (MXFP4 experts):
  *   bytes  [E, N, Kp/2]  each 64-byte chunk of a row (4 K blocks x 4 words of
  *          4 bytes) stored word-transposed: word w of block b at word 4 w + b;
- *          -0 nibbles rewritten to +0 (weights942, fp4_drop_negative_zero_)
+ *          inside each word, element e (nibble e, low nibble of byte 0 first)
+ *          at nibble slot e / 2 + 4 (e % 2), so elements 2i and 2i+1 sit at
+ *          bits 4i and 16 + 4i; -0 nibbles rewritten to +0
+ *          (weights942, fp4_drop_negative_zero_)
  *   codes  [E, N, Kp/32] per-row codes
  *   sf     NULL
  */

@@ -163,7 +163,7 @@ const char* mx_last_error(void) { return g_msg; }
 int mx_check_device_errors(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  const unsigned int flags = take_error_flags_gemv();
+  const unsigned int flags = take_error_flags_gemv() | take_error_flags_gemm();
   if (flags & 0x80000000u) return set_error(MX_ERR_CUDA, "could not read the device error flags");
   if (flags & 1u) return set_error(MX_ERR_TIMEOUT, "a bounded wait inside a kernel timed out");
   return MX_OK;
@@ -295,7 +295,10 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     return set_error(MX_ERR_ALIGN, "x, out and bias need 16-byte alignment");
   int rc = check_device();
   if (rc != MX_OK) return rc;
+  // tuning overrides (not part of the documented flags): bits 8..11 force the
+  // split count, bit 12 forces the fused quantizer at any M <= 32
   const int force_splits = static_cast<int>((flags >> 8) & 0xfu);
+  const bool force_fuse = (flags & (1u << 12)) != 0;
   const bool no_fuse = (flags & MX_LINEAR_NO_FUSED_QUANT) != 0;
   const int Kp = w->Kp;
   const LinearWs L = linear_ws(M, Kp);
@@ -308,7 +311,7 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     a.out = oc;
     a.M = Mc;
     a.force_splits = force_splits;
-    if (Mc <= kFusedQuantMaxM && !no_fuse) {
+    if ((Mc <= kFusedQuantMaxM || force_fuse) && !no_fuse) {
       a.fused = true;
       return launch_gemv(a, stream);
     }
@@ -323,10 +326,27 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     return launch_gemv(a, stream);
   };
 
-  const bool needs_ws = M > kFusedQuantMaxM || no_fuse;
+  const bool needs_ws = (M > kFusedQuantMaxM && !force_fuse) || no_fuse || M > MX_GEMV_MAX_M;
   if (needs_ws && (!workspace || workspace_bytes < L.total))
     return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, L.total);
   if (needs_ws && !aligned16(workspace)) return set_error(MX_ERR_ALIGN, "workspace needs 16-byte alignment");
+  const bool force_gemv = (flags & (1u << 13)) != 0;  // tuning: chunked GEMV for M > 32
+  if (M > MX_GEMV_MAX_M && !force_gemv) {
+    // block-scaled GEMM: quantize into [Mp, Kp] + activation scale atoms, then tcgen05
+    const int Mp = (M + 127) / 128 * 128;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = launch_quant_act(x, M, w->K, Kp, ws + L.xq_off, Kp, nullptr, 0, 127, ws + L.codes_off,
+                                     false, stream, Mp);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    GemmArgs g = {};
+    g.w = w;
+    g.xq = ws + L.xq_off;
+    g.sfa = ws + L.codes_off;
+    g.bias = bias;
+    g.out = out;
+    g.M = M;
+    return launch_gemm(g, stream);
+  }
   const size_t xrow = static_cast<size_t>(w->K) * 2, orow = static_cast<size_t>(w->N) * 2;
   for (int m0 = 0; m0 < M; m0 += MX_GEMV_MAX_M) {
     const int Mc = (M - m0) < MX_GEMV_MAX_M ? (M - m0) : MX_GEMV_MAX_M;

@@ -1,0 +1,308 @@
+// K-GEMM: block-scaled MXFP8 GEMM for large M on the 5th-generation tensor cores.
+//
+// out[m, n] = sum_k xq[m, k] W[n, k] 2^(cx[m, k/32] - 127) 2^(cw[n, k/32] - 127)
+// (rocm_native = vllm.model_executor.kernels.linear.mxfp8.rocm_native, _launch:
+// out = x @ w.T, x MXFP8-quantized per token, weight 32x32 block scales expanded
+// per row at pack time).  The page's gfx950 path tiles M=4096 prefill with
+// 128x128x256 dot_scaled tiles (_select_cfg); here the scales are applied by the
+// tensor core itself: `tcgen05.mma ... kind::mxf8f6f4.block_scale.scale_vec::1X`
+// with one E8M0 code per row per 32-wide K block held in tensor memory.
+//
+// CTA = 6 warps, one CTA per SM, persistent over 128 x 256 output tiles:
+//   warp 0 (lane 0)  TMA producer: per 128-byte K step, A 128x128 and B 256x128
+//                    boxes (128B swizzle) plus the 512-byte scale-factor atoms of
+//                    A (1) and B (2), all completing on one mbarrier;
+//   warp 1 (lane 0)  MMA issuer: copies the step's scale factors into tensor
+//                    memory (tcgen05.cp .32x128b.warpx4) and issues 4 MMAs of
+//                    K = 32 (scale-factor id k picks byte k of each code word),
+//                    accumulating 128 x 256 f32 in tensor memory; tcgen05.commit
+//                    frees the smem stage and, after the last step, signals the
+//                    epilogue;
+//   warps 2..5       epilogue: tcgen05.ld 32 lanes x 32 columns at a time, bias
+//                    in f32, bf16 round, store; then release the accumulator.
+// Every mbarrier wait is bounded; on a timeout the CTA flags the error, stops
+// issuing, and still frees its tensor memory.
+
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+namespace {
+
+constexpr int BM = 128, BN = 256, BKB = 128;      // tile rows, tile cols, K bytes a step
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kABytes = BM * BKB;                  // 16 KB
+constexpr int kBBytes = BN * BKB;                  // 32 KB
+constexpr int kSfaBytes = 512, kSfbBytes = 1024;
+constexpr int kStageBytes = 51200;                 // A | B | SFA | SFB, rounded to 1024
+constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;                    // 256 f32 columns
+constexpr uint32_t kSfCol = 256;                   // + 16 columns a stage: SFA 4, SFB 8
+constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+
+struct GemmParams {
+  const uint8_t* sfa;         // activation scale atoms [Mp/128][KT][512]
+  const uint8_t* sfb;         // weight scale atoms [ceil(N/128)][KT][512]
+  const __nv_bfloat16* bias;  // [N] or null
+  __nv_bfloat16* out;         // [M, N]
+  int M, N, KT, RTb, m_tiles, n_tiles;
+};
+
+// K-major operand in 128B-swizzled 8-row x 128-byte atoms, atoms 1024 bytes apart.
+MX_DEV uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3fffu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Scale-factor source for tcgen05.cp .32x128b: 32 rows x 16 bytes, no swizzle,
+// 8-row core matrices 128 bytes apart.
+MX_DEV uint64_t sf_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3fffu) | (static_cast<uint64_t>(128 >> 4) << 32) |
+         (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: A, B e4m3 (format 0),
+// both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24;
+// the scale-factor ids (bits 4-5 for B, 29-30 for A) are added per MMA.
+constexpr uint32_t kIdesc = (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+MX_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+MX_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+MX_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MX_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+MX_DEV void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+MX_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+MX_DEV void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                        uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+MX_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive f32 columns of tensor memory -> 32 registers a lane.
+MX_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                                                           const __grid_constant__ CUtensorMap bmap,
+                                                           const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = p.m_tiles * p.n_tiles;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    tma_prefetch_desc(&amap);
+    tma_prefetch_desc(&bmap);
+    const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      const int rb0 = min(2 * nt, p.RTb - 1), rb1 = min(2 * nt + 1, p.RTb - 1);
+      for (int kt = 0; kt < p.KT; ++kt) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u)) { *abort_flag = 1u; break; }
+        uint8_t* st = smem + stage * kStageBytes;
+        mbar_arrive_expect_tx(&full[stage], kTxBytes);
+        tma_load_2d(st, &amap, &full[stage], kt * BKB, mt * BM, pol_a);
+        tma_load_2d(st + kABytes, &bmap, &full[stage], kt * BKB, nt * BN, pol_b);
+        bulk_load(st + kABytes + kBBytes, p.sfa + (static_cast<long long>(mt) * p.KT + kt) * 512, 512, &full[stage]);
+        bulk_load(st + kABytes + kBBytes + kSfaBytes, p.sfb + (static_cast<long long>(rb0) * p.KT + kt) * 512, 512,
+                  &full[stage]);
+        bulk_load(st + kABytes + kBBytes + kSfaBytes + 512, p.sfb + (static_cast<long long>(rb1) * p.KT + kt) * 512,
+                  512, &full[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+      if (!mbar_wait(acc_empty, acc_phase ^ 1u)) { *abort_flag = 1u; break; }
+      tc_fence_after();
+      for (int kt = 0; kt < p.KT; ++kt) {
+        if (!mbar_wait(&full[stage], phase)) { *abort_flag = 1u; break; }
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + stage * kStageBytes);
+        const uint32_t sf_col = tmem + kSfCol + stage * 16;
+        tc_cp_sf(sf_col, sf_desc(st + kABytes + kBBytes));
+        tc_cp_sf(sf_col + 4, sf_desc(st + kABytes + kBBytes + kSfaBytes));
+        tc_cp_sf(sf_col + 8, sf_desc(st + kABytes + kBBytes + kSfaBytes + 512));
+        const uint64_t adesc = sw128_desc(st);
+        const uint64_t bdesc = sw128_desc(st + kABytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t idesc = kIdesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+          // +32 bytes along K inside the swizzle atom = +2 in the start-address field
+          tc_mma_mxf8(tmem + kAccCol, adesc + 2 * k, bdesc + 2 * k, idesc, sf_col, sf_col + 4,
+                      (kt | k) != 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      tc_commit(acc_full);
+      acc_phase ^= 1u;
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      if (!mbar_wait(acc_full, acc_phase)) { *abort_flag = 1u; break; }
+      tc_fence_after();
+      const int row = mt * BM + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + c * 32, r);
+        const int n0 = nt * BN + c * 32;
+        if (row < p.M && n0 < p.N) {
+          __nv_bfloat16* dst = p.out + static_cast<long long>(row) * p.N + n0;
+          if (n0 + 32 <= p.N && (p.N & 7) == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                float a = __uint_as_float(r[j + 2 * h]), b = __uint_as_float(r[j + 2 * h + 1]);
+                if (p.bias) {
+                  a += __bfloat162float(p.bias[n0 + j + 2 * h]);
+                  b += __bfloat162float(p.bias[n0 + j + 2 * h + 1]);
+                }
+                const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+                pk[h] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              *reinterpret_cast<uint4*>(dst + j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (n0 + j < p.N) {
+                float a = __uint_as_float(r[j]);
+                if (p.bias) a += __bfloat162float(p.bias[n0 + j]);
+                dst[j] = __float2bfloat16_rn(a);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+unsigned int take_error_flags_gemm() { return take_tu_error_flags(); }
+
+int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
+  const mx_packed_weight* w = a.w;
+  DeviceInfo di;
+  if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
+  GemmParams p = {};
+  p.sfa = a.sfa;
+  p.sfb = w->sf;
+  p.bias = static_cast<const __nv_bfloat16*>(a.bias);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.M = a.M;
+  p.N = w->N;
+  p.KT = w->Kp / BKB;
+  p.RTb = (w->N + 127) / 128;
+  p.m_tiles = (a.M + BM - 1) / BM;
+  p.n_tiles = (w->N + BN - 1) / BN;
+  const int Mp = p.m_tiles * BM;
+  CUtensorMap amap, bmap;
+  int rc = encode_tensor_map_2d(&amap, a.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, Mp, w->Kp, BKB, BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != MX_OK) return rc;
+  rc = encode_tensor_map_2d(&bmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, BKB, BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != MX_OK) return rc;
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
+  const int ntiles = p.m_tiles * p.n_tiles;
+  const int grid = ntiles < di.sm_count ? ntiles : di.sm_count;
+  gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(amap, bmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+  return MX_OK;
+}
+
+}  // namespace mx

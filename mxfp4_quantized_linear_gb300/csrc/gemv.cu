@@ -273,7 +273,12 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const __grid_constant
     const uint32_t off = static_cast<uint32_t>((t * kRedPitch + r) * 4);
     float v = 0.0f;
     if (S > 1) {
-      for (int s = 0; s < S; ++s) v += ld_shared_cluster_f32(map_shared_rank(red_addr + off, s));
+      float part[8];
+#pragma unroll
+      for (int s = 0; s < 8; ++s)  // issue every rank's load before summing
+        part[s] = s < S ? ld_shared_cluster_f32(map_shared_rank(red_addr + off, s)) : 0.0f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) v += part[s];  // fixed rank order
     } else {
       v = red[t * kRedPitch + r];
     }
@@ -334,12 +339,13 @@ int gemv_splits(int N, int Kp, int M, int force_splits) {
   if (force_splits > 0) {
     S = force_splits;
   } else {
+    // smallest split giving ~2.5 CTAs per SM, so the whole grid is resident in
+    // one wave and every warp's TMA boxes are in flight from the start
     DeviceInfo di;
     const int sms = current_device_info(&di) == MX_OK ? di.sm_count : 148;
     const int tiles = (N + kRowsPerCta - 1) / kRowsPerCta;
-    const int want = 3 * sms;
     S = 1;
-    while (S < 8 && tiles * S < want) S *= 2;
+    while (S < 8 && 2 * tiles * S < 5 * sms) S *= 2;
   }
   const int ntok = MX_GEMV_MAX_M;
   while (S < 8 && ntok * ((nsteps + S - 1) / S) * kStepBytes > 96 * 1024) S *= 2;

@@ -147,9 +147,11 @@ MX_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// Not volatile: independent loads may be issued back to back.  Ordering against
+// the peers' writes comes from the cluster barrier that precedes every use.
 MX_DEV float ld_shared_cluster_f32(uint32_t addr) {
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
 }
 

@@ -30,9 +30,10 @@ int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
 // x [M, K] bf16 -> q [M, ldq] (columns K..Kout zero), codes [M, ldc] (blocks past
 // K get pad_code); optional sf atoms [ceil(M/128), Kout/128, 512].  When
 // `pdl_trigger` the kernel lets a programmatic dependent launch start at once.
+// `M_out` (>= M, default M) rows are written; rows M..M_out-1 quantize zeros.
 cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, int ldq,
                              uint8_t* codes, int ldc, uint8_t pad_code, uint8_t* sf,
-                             bool pdl_trigger, cudaStream_t stream);
+                             bool pdl_trigger, cudaStream_t stream, int M_out = -1);
 cudaError_t launch_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode,
                            int N, int K, void* out, cudaStream_t stream);
 
@@ -62,6 +63,18 @@ struct GemvArgs {
 int launch_gemv(const GemvArgs& a, cudaStream_t stream);
 unsigned int take_error_flags_gemv();
 int gemv_splits(int N, int Kp, int M, int force_splits);
+
+// ---- block-scaled GEMM (gemm.cu)
+struct GemmArgs {
+  const mx_packed_weight* w;
+  const uint8_t* xq;    // [roundup(M,128), Kp] e4m3
+  const uint8_t* sfa;   // [roundup(M,128)/128, Kp/128, 512] activation scale atoms
+  const void* bias;     // bf16 [N] or NULL
+  void* out;            // bf16 [M, N]
+  int M;
+};
+int launch_gemm(const GemmArgs& a, cudaStream_t stream);
+unsigned int take_error_flags_gemm();
 
 // ---- routing + MoE (moe.cu)
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,

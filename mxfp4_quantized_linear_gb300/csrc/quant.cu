@@ -23,10 +23,10 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
                                                         uint8_t* __restrict__ q, int ldq,
                                                         uint8_t* __restrict__ codes, int ldc,
                                                         uint8_t pad_code, uint8_t* __restrict__ sf,
-                                                        int pdl_trigger) {
+                                                        int pdl_trigger, int M_out) {
   if (pdl_trigger) pdl_launch_dependents();
   const int groups_per_row = Kout >> 3;
-  const long long total = static_cast<long long>(M) * groups_per_row;
+  const long long total = static_cast<long long>(M_out) * groups_per_row;
   const int lane = threadIdx.x & 31;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
     const bool inside = g < total;
     const int row = inside ? static_cast<int>(g / groups_per_row) : 0;
     const int k = inside ? static_cast<int>(g % groups_per_row) * 8 : 0;
-    const bool valid = inside && k < K;
+    const bool valid = inside && row < M && k < K;
     float v[8];
     if (valid) {
       const uint4 u = *reinterpret_cast<const uint4*>(x + static_cast<long long>(row) * K + k);
@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
     uint2 out = valid ? make_uint2(b.lo, b.hi) : make_uint2(0u, 0u);
     *reinterpret_cast<uint2*>(q + static_cast<long long>(row) * ldq + k) = out;
     if ((k & 31) == 0) {
-      const uint8_t c = valid ? static_cast<uint8_t>(b.code) : pad_code;
+      // blocks past K get pad_code; rows past M are quantized zeros (code 0)
+      const uint8_t c = valid ? static_cast<uint8_t>(b.code) : (k < K ? 0 : pad_code);
       if (codes) codes[static_cast<long long>(row) * ldc + (k >> 5)] = c;
       if (sf) {
         // 512-byte atom (row tile, 128-K tile): row m, block kb at (m%32)*16 + (m/32)*4 + kb
@@ -120,13 +121,14 @@ int grid_for(long long threads, int block) {
 
 cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, int ldq,
                              uint8_t* codes, int ldc, uint8_t pad_code, uint8_t* sf,
-                             bool pdl_trigger, cudaStream_t stream) {
-  const long long groups = static_cast<long long>(M) * (Kout / 8);
+                             bool pdl_trigger, cudaStream_t stream, int M_out) {
+  if (M_out < M) M_out = M;
+  const long long groups = static_cast<long long>(M_out) * (Kout / 8);
   const int block = 256;
   const int grid = grid_for(groups, block);
   quant_act_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), M, K, Kout,
                                                q, ldq, codes, ldc, pad_code, sf,
-                                               pdl_trigger ? 1 : 0);
+                                               pdl_trigger ? 1 : 0, M_out);
   return cudaGetLastError();
 }
 
