@@ -57,9 +57,12 @@ enum { MX_SCALE_BLOCK32X32 = 0, MX_SCALE_ROW1X32 = 1 };
                                     (weights942, linear_copy)                              */
 
 /* mxfp8_linear flags */
-#define MX_LINEAR_NO_FUSED_QUANT 1u /* always quantize x in a separate launch (the pages'
-                                       kill switch of the fused quant, rocm_native,
-                                       apply_weights)                                     */
+#define MX_LINEAR_NO_FUSED_QUANT 1u /* cluster GEMV: always quantize x in a separate launch
+                                       (the pages' kill switch of the fused quant,
+                                       rocm_native, apply_weights)                         */
+#define MX_LINEAR_CLUSTER_GEMV (1u << 14) /* M <= 32: run the CUDA-core-scaled mma.sync GEMV
+                                       with cluster split-K (fused quant for M <= 8)
+                                       instead of the tensor-core GEMV                      */
 
 /* Largest token count the GEMV path serves; larger M runs the block-scaled GEMM. */
 #define MX_GEMV_MAX_M 32
@@ -156,7 +159,9 @@ int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mo
 
 /* ------------------------------------------------------------- MXFP8 linear */
 
-/* Workspace bytes mxfp8_linear needs for M tokens on weight w (0 = none). */
+/* Workspace bytes mxfp8_linear needs for M tokens on weight w: the size of the
+ * quantized activation and its codes (used by the GEMM for M > 32 and by the
+ * MX_LINEAR_CLUSTER_GEMV path; the default decode GEMV uses none of it). */
 size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
 
 /*
@@ -167,8 +172,9 @@ size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
  *   x     [M, K] bf16           w     packed E4M3 weight with E == 1
  *   bias  [N] bf16 or NULL      out   [M, N] bf16
  *   workspace  device scratch of mxfp8_linear_workspace_size(M, w) bytes
- * M <= MX_GEMV_MAX_M runs the split-K decode GEMV (quantization fused for
- * small M), larger M the block-scaled GEMM.  Results do not depend on M.
+ * M <= MX_GEMV_MAX_M runs the persistent split-K decode GEMV on the tensor
+ * cores (block scales applied by tcgen05), larger M the block-scaled GEMM.
+ * Within the decode range a token's result does not depend on M.
  */
 int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
                  unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
@@ -180,8 +186,8 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
  * allocation on the request path, and plugin / callback code that receives
  * only its input and output buffers from a framework owning the allocator.
  *
- * Computes exactly what mxfp8_linear computes for M <= MX_GEMV_MAX_M (the
- * activation is quantized in a separate launch), but keeps the quantized
+ * Computes exactly what mxfp8_linear computes for M <= MX_GEMV_MAX_M with
+ * flags MX_LINEAR_CLUSTER_GEMV | MX_LINEAR_NO_FUSED_QUANT, but keeps the quantized
  * activation and its codes in a fixed library-owned device array of
  * MX_NOALLOC_SCRATCH_BYTES, present on every GPU that loads the library until
  * the process exits.  It calls no allocator.

@@ -20,6 +20,7 @@ MX_FMT_E4M3, MX_FMT_E2M1 = 0, 1
 MX_SCALE_BLOCK32X32, MX_SCALE_ROW1X32 = 0, 1
 MX_PACK_FOLD, MX_PACK_REQUIRE_BLOCK = 1, 2
 MX_LINEAR_NO_FUSED_QUANT = 1
+MX_LINEAR_CLUSTER_GEMV = 1 << 14
 MX_GEMV_MAX_M = 32
 MX_MAX_EXPERTS = 512
 

@@ -69,6 +69,9 @@ struct LinearWs {
   size_t xq_off, codes_off, total;
 };
 
+// Workspace of the cluster GEMV (M <= 32) and of the GEMM (M > 32): quantized
+// activation [Mp, Kp] then its codes / scale atoms.  The tensor-core GEMV
+// (M <= 32, the default) quantizes in shared memory and needs none.
 LinearWs linear_ws(int M, int Kp) {
   LinearWs r;
   const size_t Mp = M <= MX_GEMV_MAX_M ? static_cast<size_t>(M) : (static_cast<size_t>(M) + 127) / 128 * 128;
@@ -163,7 +166,7 @@ const char* mx_last_error(void) { return g_msg; }
 int mx_check_device_errors(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  const unsigned int flags = take_error_flags_gemv() | take_error_flags_gemm();
+  const unsigned int flags = take_error_flags_gemv() | take_error_flags_gemm() | take_error_flags_gemv_tc();
   if (flags & 0x80000000u) return set_error(MX_ERR_CUDA, "could not read the device error flags");
   if (flags & 1u) return set_error(MX_ERR_TIMEOUT, "a bounded wait inside a kernel timed out");
   return MX_OK;
@@ -295,11 +298,12 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     return set_error(MX_ERR_ALIGN, "x, out and bias need 16-byte alignment");
   int rc = check_device();
   if (rc != MX_OK) return rc;
-  // tuning overrides (not part of the documented flags): bits 8..11 force the
-  // split count, bit 12 forces the fused quantizer at any M <= 32
+  // tuning overrides of the cluster GEMV (not part of the documented flags):
+  // bits 8..11 force its split count, bit 12 forces its fused quantizer
   const int force_splits = static_cast<int>((flags >> 8) & 0xfu);
   const bool force_fuse = (flags & (1u << 12)) != 0;
   const bool no_fuse = (flags & MX_LINEAR_NO_FUSED_QUANT) != 0;
+  const bool legacy = (flags & MX_LINEAR_CLUSTER_GEMV) != 0;
   const int Kp = w->Kp;
   const LinearWs L = linear_ws(M, Kp);
 
@@ -326,6 +330,16 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     return launch_gemv(a, stream);
   };
 
+  if (M <= MX_GEMV_MAX_M && !legacy) {
+    TcGemvArgs g = {};
+    g.w = w;
+    g.x = x;
+    g.bias = bias;
+    g.out = out;
+    g.M = M;
+    g.force_splits = force_splits;
+    return launch_gemv_tc(g, stream);
+  }
   const bool needs_ws = (M > kFusedQuantMaxM && !force_fuse) || no_fuse || M > MX_GEMV_MAX_M;
   if (needs_ws && (!workspace || workspace_bytes < L.total))
     return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, L.total);
@@ -336,7 +350,7 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     const int Mp = (M + 127) / 128 * 128;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaError_t e = launch_quant_act(x, M, w->K, Kp, ws + L.xq_off, Kp, nullptr, 0, 127, ws + L.codes_off,
-                                     false, stream, Mp);
+                                     true, stream, Mp);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     GemmArgs g = {};
     g.w = w;

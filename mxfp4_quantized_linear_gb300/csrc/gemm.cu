@@ -25,6 +25,7 @@
 
 #include "mx_common.cuh"
 #include "mx_internal.h"
+#include "tc_common.cuh"
 
 namespace mx {
 namespace {
@@ -50,80 +51,7 @@ struct GemmParams {
   int M, N, KT, RTb, m_tiles, n_tiles;
 };
 
-// K-major operand in 128B-swizzled 8-row x 128-byte atoms, atoms 1024 bytes apart.
-MX_DEV uint64_t sw128_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3fffu) | (static_cast<uint64_t>(1) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-         (static_cast<uint64_t>(2) << 61);
-}
-
-// Scale-factor source for tcgen05.cp .32x128b: 32 rows x 16 bytes, no swizzle,
-// 8-row core matrices 128 bytes apart.
-MX_DEV uint64_t sf_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3fffu) | (static_cast<uint64_t>(128 >> 4) << 32) |
-         (static_cast<uint64_t>(1) << 46);
-}
-
-// Instruction descriptor, kind::mxf8f6f4 block-scaled: A, B e4m3 (format 0),
-// both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24;
-// the scale-factor ids (bits 4-5 for B, 29-30 for A) are added per MMA.
-constexpr uint32_t kIdesc = (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
-
-MX_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-MX_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-MX_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-MX_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-MX_DEV void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
-MX_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-MX_DEV void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
-                        uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
-}
-
-MX_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-// 32 lanes x 32 consecutive f32 columns of tensor memory -> 32 registers a lane.
-MX_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
+constexpr uint32_t kIdesc = mxf8_idesc(BM, BN);
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap,
                                                            const __grid_constant__ CUtensorMap bmap,
@@ -138,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -161,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tma_prefetch_desc(&amap);
     tma_prefetch_desc(&bmap);
     const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_last();
+    pdl_wait_prior_grid();  // the quantized activation is complete and visible
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
@@ -299,8 +229,17 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
   const int ntiles = p.m_tiles * p.n_tiles;
   const int grid = ntiles < di.sm_count ? ntiles : di.sm_count;
-  gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(amap, bmap, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_kernel, amap, bmap, p);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
   return MX_OK;
 }

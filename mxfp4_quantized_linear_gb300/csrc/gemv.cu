@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const __grid_constant
   const int ksb = ks >> 5;          // this slice's MX blocks
   const int wrow0 = row0 + warp * kRowsPerWarp;
 
+  pdl_launch_dependents();  // the next kernel may start streaming its own weights
   // ---- 1. start streaming this warp's weight rows (independent of earlier kernels)
   uint64_t* wbar = bars + warp * kStages;
   uint8_t* wst = wbuf + warp * kStages * kBoxBytes;
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const __grid_constant
 
   // ---- 3. activation slice -> shared (e4m3 bytes, swizzled) + f32 block scales
   const int k0 = st0 * kStepBytes;
+  pdl_wait_prior_grid();  // x (and the quantizer's output) complete and visible
   if (kFused) {
     // quantize x[0..M) x [k0, k0 + ks) here: 8 elements a lane, 4 lanes a block
     const int gpr = ks >> 3;               // 8-element groups per token
@@ -157,7 +159,6 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const __grid_constant
       }
     }
   } else {
-    pdl_wait_prior_grid();  // the quantizer's output is complete and visible
     const int cpr = ks >> 4;  // 16-byte chunks per token
     for (int i = threadIdx.x; i < NTOK * cpr; i += blockDim.x) {
       const int t = i / cpr, c = i % cpr;
@@ -309,11 +310,10 @@ int launch_one(const CUtensorMap& map, const GemvParams& p, int smem, bool pdl, 
   attrs[na].val.clusterDim.y = 1;
   attrs[na].val.clusterDim.z = 1;
   ++na;
-  if (pdl) {
-    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
+  (void)pdl;  // always a programmatic dependent: it waits before reading x
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   cfg.attrs = attrs;
   cfg.numAttrs = na;
   e = cudaLaunchKernelEx(&cfg, kern, map, p);

@@ -117,8 +117,9 @@ constexpr int kMoeWarps = 8;
 constexpr int kMoeRows = kMoeWarps * 16;  // 128 weight rows a CTA
 constexpr int kMoeTok = 16;               // tokens a chunk (two n8 tiles)
 constexpr int kMoeStepK = 128;            // K elements a step (64 bytes a row)
+constexpr int kChunkK = 256;              // K elements of activation a ring slot (2 steps)
+constexpr int kChunkBytes = kMoeTok * kChunkK * 2;  // 8 KB
 constexpr int kPF = 4;                    // steps of weight words in flight a lane
-constexpr int kMoeRedPitch = kMoeRows + 4;
 
 struct MoeParams {
   const __nv_bfloat16* x;  // [T, K]
@@ -129,7 +130,7 @@ struct MoeParams {
   const int32_t* active;
   const int32_t* n_active;
   __nv_bfloat16* out;      // [T * topk, N]
-  int topk, N, K, Kp, nsteps, splits, ks_max;
+  int topk, N, K, Kp, nsteps;
 };
 
 // e2m1 x 8 (nibble slots (i, i+4) = elements (2i, 2i+1)) -> 4 bf16 pairs, exact.
@@ -145,159 +146,159 @@ MX_DEV void e2m1x8_to_bf16x8(uint32_t w, uint32_t (&r)[4]) {
   }
 }
 
-// 16-byte chunk c of token row tk in the activation slice; the XOR by (tk & 1) * 4
-// keeps the 8 lanes of a quarter warp (2 tokens x 4 chunks) on distinct banks.
-MX_DEV int xs_chunk(int tk, int c) { return c ^ ((tk & 1) << 2); }
+// 16-byte chunk c (0..31) of token row tk in an activation ring slot; the XOR by
+// (tk & 1) * 4 keeps the 8 lanes of a quarter warp (2 tokens x 4 chunks) on
+// distinct banks.
+MX_DEV int xs_off(int tk, int c) { return tk * (kChunkK * 2) + ((c ^ ((tk & 1) << 2)) << 4); }
 
-__global__ void __launch_bounds__(kMoeWarps * 32) moe_kernel(const MoeParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t* xs = smem;  // [kMoeTok][ks_max] bf16
-  float* red = reinterpret_cast<float*>(smem + kMoeTok * p.ks_max * 2);
-  int* tok_pair = reinterpret_cast<int*>(red + kMoeTok * kMoeRedPitch);
+MX_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+MX_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+MX_DEV void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-  const int a = blockIdx.z;
-  if (a >= *p.n_active) return;  // same for every CTA of the cluster
+// One step of one warp: 16 weight rows x 128 K against up to 16 tokens.
+MX_DEV void moe_step(float (&acc)[2][4], const uint4& wa4, const uint4& wc4, uint32_t ca, uint32_t cc,
+                     uint32_t xs_base, int s_in_chunk, int g, int tq) {
+  const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
+  const uint32_t wc[4] = {wc4.x, wc4.y, wc4.z, wc4.w};
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t ra[4], rc[4];
+    e2m1x8_to_bf16x8(wa[b], ra);
+    e2m1x8_to_bf16x8(wc[b], rc);
+    const float s0 = e8m0_to_f32((ca >> (8 * b)) & 0xffu);
+    const float s1 = e8m0_to_f32((cc >> (8 * b)) & 0xffu);
+    const int c = s_in_chunk * 16 + b * 4 + tq;  // 16-byte chunk: K = 8c .. 8c + 7 of the slot
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int tk = h * 8 + g;
+      uint4 xv;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
+                   : "r"(xs_base + xs_off(tk, c)));
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      mma_bf16_16816(d, ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
+      mma_bf16_16816(d, ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
+      acc[h][0] = fmaf(d[0], s0, acc[h][0]);
+      acc[h][1] = fmaf(d[1], s0, acc[h][1]);
+      acc[h][2] = fmaf(d[2], s1, acc[h][2]);
+      acc[h][3] = fmaf(d[3], s1, acc[h][3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMoeWarps * 32, 1) moe_kernel(const MoeParams p) {
+  __shared__ __align__(128) uint8_t xs[2][kChunkBytes];
+  __shared__ int tok_src[kMoeTok];   // token row of x, or -1
+  __shared__ int tok_pair[kMoeTok];  // output row (pair index), or -1
+
+  const int a = blockIdx.y;
+  if (a >= *p.n_active) return;
   const int e = p.active[a];
   const int o0 = p.offsets[e];
   const int cnt = p.offsets[e + 1] - o0;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
-  const int split = p.splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int base_steps = p.nsteps / p.splits, rem = p.nsteps % p.splits;
-  const int st0 = split * base_steps + (split < rem ? split : rem);
-  const int ns = base_steps + (split < rem ? 1 : 0);
-  const int ks = ns * kMoeStepK;      // slice K elements
-  const int kxb = ks * 2;             // slice bytes of one token row
-  const int row0 = blockIdx.y * kMoeRows;
+  const int row0 = blockIdx.x * kMoeRows;
   const int rg = row0 + warp * 16 + g;  // rows rg and rg + 8
   const int KHp = p.Kp >> 1, KBp = p.Kp >> 5;
   const bool v0 = rg < p.N, v1 = rg + 8 < p.N;
   const long long erow = static_cast<long long>(e) * p.N;
-  const uint8_t* w0 = p.wq + (erow + (v0 ? rg : 0)) * KHp + st0 * 64 + tq * 16;
-  const uint8_t* w1 = p.wq + (erow + (v1 ? rg + 8 : 0)) * KHp + st0 * 64 + tq * 16;
-  const uint8_t* c0p = p.codes + (erow + (v0 ? rg : 0)) * KBp + st0 * 4;
-  const uint8_t* c1p = p.codes + (erow + (v1 ? rg + 8 : 0)) * KBp + st0 * 4;
-  const uint32_t xs_base = smem_u32(xs);
+  const uint8_t* w0 = p.wq + (erow + (v0 ? rg : 0)) * KHp + tq * 16;
+  const uint8_t* w1 = p.wq + (erow + (v1 ? rg + 8 : 0)) * KHp + tq * 16;
+  const uint8_t* c0p = p.codes + (erow + (v0 ? rg : 0)) * KBp;
+  const uint8_t* c1p = p.codes + (erow + (v1 ? rg + 8 : 0)) * KBp;
+  const int ns = p.nsteps;
+  const int nchunks = (ns + 1) >> 1;
 
   for (int ch = 0; ch < cnt; ch += kMoeTok) {
-    // ---- stage the chunk's token rows of the K slice (bf16, swizzled 16-byte chunks)
-    if (threadIdx.x < kMoeTok)
-      tok_pair[threadIdx.x] = (ch + static_cast<int>(threadIdx.x) < cnt) ? p.pairs[o0 + ch + threadIdx.x] : -1;
-    __syncthreads();
-    const int cpt = ks >> 3;  // 16-byte chunks a token row
-    for (int i = threadIdx.x; i < kMoeTok * cpt; i += blockDim.x) {
-      const int tk = i / cpt, c = i % cpt;
-      const int pr = tok_pair[tk];
-      const int k = st0 * kMoeStepK + c * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (pr >= 0 && k < p.K)
-        v = *reinterpret_cast<const uint4*>(p.x + static_cast<long long>(pr / p.topk) * p.K + k);
-      *reinterpret_cast<uint4*>(xs + tk * kxb + xs_chunk(tk, c) * 16) = v;
+    // ---- 1. weights of the first kPF steps: independent of the activations
+    uint4 wb0[kPF], wb1[kPF];
+    uint32_t cb0[kPF], cb1[kPF];
+#pragma unroll
+    for (int q = 0; q < kPF; ++q) {
+      const bool in = q < ns;
+      wb0[q] = (in && v0) ? ld_nc_v4(w0 + q * 64) : make_uint4(0u, 0u, 0u, 0u);
+      wb1[q] = (in && v1) ? ld_nc_v4(w1 + q * 64) : make_uint4(0u, 0u, 0u, 0u);
+      cb0[q] = in ? *reinterpret_cast<const uint32_t*>(c0p + q * 4) : 0x7f7f7f7fu;
+      cb1[q] = in ? *reinterpret_cast<const uint32_t*>(c1p + q * 4) : 0x7f7f7f7fu;
+    }
+    // ---- 2. the chunk's tokens, and the first two activation slots
+    if (threadIdx.x < kMoeTok) {
+      const int pr = (ch + static_cast<int>(threadIdx.x) < cnt) ? p.pairs[o0 + ch + threadIdx.x] : -1;
+      tok_pair[threadIdx.x] = pr;
+      tok_src[threadIdx.x] = pr >= 0 ? pr / p.topk : -1;
     }
     __syncthreads();
+    auto load_slot = [&](int c, int buf) {
+      const uint32_t dst = smem_u32(xs[buf]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int idx = threadIdx.x + j * kMoeWarps * 32;  // 512 chunks of 16 bytes
+        const int tk = idx >> 5, cc = idx & 31;
+        const int src = tok_src[tk];
+        const int k = c * kChunkK + cc * 8;
+        const bool ok = src >= 0 && k < p.K && c < nchunks;
+        const __nv_bfloat16* sp = ok ? p.x + static_cast<long long>(src) * p.K + k : p.x;
+        cp_async16(dst + xs_off(tk, cc), sp, ok);
+      }
+      cp_async_commit();
+    };
+    load_slot(0, 0);
+    load_slot(1, 1);
 
-    // ---- K loop: 16 rows a warp, two n8 token tiles
+    // ---- 3. K loop: two slots (four steps) an iteration so register slots stay static
     float acc[2][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[h][i] = 0.0f;
-    uint4 wb0[kPF], wb1[kPF];
-    uint32_t cb0[kPF], cb1[kPF];
+    for (int c0 = 0; c0 < nchunks; c0 += 2) {
 #pragma unroll
-    for (int q = 0; q < kPF; ++q) {
-      if (q < ns) {
-        wb0[q] = v0 ? ld_nc_v4(w0 + q * 64) : make_uint4(0u, 0u, 0u, 0u);
-        wb1[q] = v1 ? ld_nc_v4(w1 + q * 64) : make_uint4(0u, 0u, 0u, 0u);
-        cb0[q] = *reinterpret_cast<const uint32_t*>(c0p + q * 4);
-        cb1[q] = *reinterpret_cast<const uint32_t*>(c1p + q * 4);
-      }
-    }
-    for (int i0 = 0; i0 < ns; i0 += kPF) {
+      for (int cs = 0; cs < 2; ++cs) {
+        const int c = c0 + cs;
+        if (c < nchunks) {
+          cp_async_wait1();
+          __syncthreads();
+          const uint32_t xs_base = smem_u32(xs[cs]);
 #pragma unroll
-      for (int q = 0; q < kPF; ++q) {
-        const int i = i0 + q;
-        if (i < ns) {
-          const uint32_t wa[4] = {wb0[q].x, wb0[q].y, wb0[q].z, wb0[q].w};
-          const uint32_t wc[4] = {wb1[q].x, wb1[q].y, wb1[q].z, wb1[q].w};
-          const uint32_t ca = cb0[q], cc = cb1[q];
-          if (i + kPF < ns) {  // refill this slot with step i + kPF
-            wb0[q] = v0 ? ld_nc_v4(w0 + (i + kPF) * 64) : make_uint4(0u, 0u, 0u, 0u);
-            wb1[q] = v1 ? ld_nc_v4(w1 + (i + kPF) * 64) : make_uint4(0u, 0u, 0u, 0u);
-            cb0[q] = *reinterpret_cast<const uint32_t*>(c0p + (i + kPF) * 4);
-            cb1[q] = *reinterpret_cast<const uint32_t*>(c1p + (i + kPF) * 4);
-          }
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            uint32_t ra[4], rc[4];
-            e2m1x8_to_bf16x8(wa[b], ra);
-            e2m1x8_to_bf16x8(wc[b], rc);
-            const float s0 = e8m0_to_f32((ca >> (8 * b)) & 0xffu);
-            const float s1 = e8m0_to_f32((cc >> (8 * b)) & 0xffu);
-            const int c = i * 16 + b * 4 + tq;  // 16-byte chunk: logical k = 8c .. 8c + 7
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int tk = h * 8 + g;
-              uint4 xv;
-              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
-                           : "r"(xs_base + tk * kxb + xs_chunk(tk, c) * 16));
-              float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-              mma_bf16_16816(d, ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
-              mma_bf16_16816(d, ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
-              acc[h][0] = fmaf(d[0], s0, acc[h][0]);
-              acc[h][1] = fmaf(d[1], s0, acc[h][1]);
-              acc[h][2] = fmaf(d[2], s1, acc[h][2]);
-              acc[h][3] = fmaf(d[3], s1, acc[h][3]);
+          for (int s = 0; s < 2; ++s) {
+            const int q = cs * 2 + s;  // register slot (static)
+            const int i = c * 2 + s;   // step
+            if (i < ns) {
+              const uint4 wa = wb0[q], wc = wb1[q];
+              const uint32_t ca = cb0[q], cc = cb1[q];
+              if (i + kPF < ns) {
+                wb0[q] = v0 ? ld_nc_v4(w0 + (i + kPF) * 64) : make_uint4(0u, 0u, 0u, 0u);
+                wb1[q] = v1 ? ld_nc_v4(w1 + (i + kPF) * 64) : make_uint4(0u, 0u, 0u, 0u);
+                cb0[q] = *reinterpret_cast<const uint32_t*>(c0p + (i + kPF) * 4);
+                cb1[q] = *reinterpret_cast<const uint32_t*>(c1p + (i + kPF) * 4);
+              }
+              moe_step(acc, wa, wc, ca, cc, xs_base, s, g, tq);
             }
           }
+          __syncthreads();  // every warp is done with this slot
+          load_slot(c + 2, cs);
         }
       }
     }
 
-    // ---- partial tile [token][row], fixed-order cluster reduction, bf16 store
+    // ---- 4. store: out[pair, row] (pairs with no token stay untouched)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t0 = h * 8 + 2 * tq;
-      const int r = warp * 16 + g;
-      red[t0 * kMoeRedPitch + r] = acc[h][0];
-      red[(t0 + 1) * kMoeRedPitch + r] = acc[h][1];
-      red[t0 * kMoeRedPitch + r + 8] = acc[h][2];
-      red[(t0 + 1) * kMoeRedPitch + r + 8] = acc[h][3];
+      const int pa = tok_pair[t0], pb = tok_pair[t0 + 1];
+      if (pa >= 0 && v0) p.out[static_cast<long long>(pa) * p.N + rg] = __float2bfloat16_rn(acc[h][0]);
+      if (pb >= 0 && v0) p.out[static_cast<long long>(pb) * p.N + rg] = __float2bfloat16_rn(acc[h][1]);
+      if (pa >= 0 && v1) p.out[static_cast<long long>(pa) * p.N + rg + 8] = __float2bfloat16_rn(acc[h][2]);
+      if (pb >= 0 && v1) p.out[static_cast<long long>(pb) * p.N + rg + 8] = __float2bfloat16_rn(acc[h][3]);
     }
-    const int S = p.splits;
-    if (S > 1) cluster_sync(); else __syncthreads();
-    const int rows_per = kMoeRows / S;
-    const int r_begin = split * rows_per;
-    const int nt = (cnt - ch) < kMoeTok ? (cnt - ch) : kMoeTok;
-    const uint32_t red_addr = smem_u32(red);
-    for (int idx = threadIdx.x; idx < nt * rows_per; idx += blockDim.x) {
-      const int t = idx / rows_per;
-      const int r = r_begin + idx % rows_per;
-      const int n = row0 + r;
-      if (n >= p.N) continue;
-      const uint32_t off = static_cast<uint32_t>((t * kMoeRedPitch + r) * 4);
-      float v = 0.0f;
-      if (S > 1) {
-        for (int s = 0; s < S; ++s) v += ld_shared_cluster_f32(map_shared_rank(red_addr + off, s));
-      } else {
-        v = red[t * kMoeRedPitch + r];
-      }
-      p.out[static_cast<long long>(tok_pair[t]) * p.N + n] = __float2bfloat16_rn(v);
-    }
-    if (S > 1) cluster_sync(); else __syncthreads();
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();  // tok_* and the ring are reused by the next chunk of tokens
   }
-}
-
-int moe_splits(int Kp, int N, int zmax, int sms) {
-  const int nsteps = Kp / kMoeStepK;
-  int S = 1;
-  while (S < 8 && ((nsteps + S - 1) / S) * kMoeStepK * 2 * kMoeTok > 64 * 1024) S *= 2;
-  const long long tiles = static_cast<long long>((N + kMoeRows - 1) / kMoeRows) * zmax;
-  while (S < 8 && tiles * S < 2LL * sms && (nsteps + 2 * S - 1) / (2 * S) >= kPF) S *= 2;
-  while (S > 1 && S > nsteps) S >>= 1;
-  return S;
 }
 
 }  // namespace
@@ -325,8 +326,6 @@ cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E
 int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const int32_t* offsets,
                const int32_t* pairs, const int32_t* active, const int32_t* n_active, void* out,
                cudaStream_t stream) {
-  DeviceInfo di;
-  if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
   MoeParams p = {};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.wq = w->bytes;
@@ -343,26 +342,9 @@ int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const 
   p.nsteps = w->Kp / kMoeStepK;
   const long long P = static_cast<long long>(T) * topk;
   const int zmax = static_cast<int>(P < w->E ? P : w->E);
-  p.splits = moe_splits(w->Kp, w->N, zmax, di.sm_count);
-  p.ks_max = ((p.nsteps + p.splits - 1) / p.splits) * kMoeStepK;
-  const int smem = kMoeTok * p.ks_max * 2 + kMoeTok * kMoeRedPitch * 4 + kMoeTok * 4;
-  if (static_cast<size_t>(smem) > di.max_smem_optin)
-    return set_error(MX_ERR_UNSUPPORTED, "moe: K = %d needs %d bytes of shared memory", w->K, smem);
-  cudaError_t e = cudaFuncSetAttribute(moe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe: smem attribute: %s", cudaGetErrorString(e));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.splits, (w->N + kMoeRows - 1) / kMoeRows, zmax);
-  cfg.blockDim = dim3(kMoeWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = p.splits;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, moe_kernel, p);
+  dim3 grid((w->N + kMoeRows - 1) / kMoeRows, zmax, 1);
+  moe_kernel<<<grid, kMoeWarps * 32, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;
 }

@@ -147,6 +147,11 @@ MX_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// Store to the shared memory of another CTA of the cluster (address from map_shared_rank).
+MX_DEV void st_shared_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Not volatile: independent loads may be issued back to back.  Ordering against
 // the peers' writes comes from the cluster barrier that precedes every use.
 MX_DEV float ld_shared_cluster_f32(uint32_t addr) {

@@ -31,9 +31,11 @@ int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
 // K get pad_code); optional sf atoms [ceil(M/128), Kout/128, 512].  When
 // `pdl_trigger` the kernel lets a programmatic dependent launch start at once.
 // `M_out` (>= M, default M) rows are written; rows M..M_out-1 quantize zeros.
+// `zero` / `nzero`: ints the kernel also sets to 0 (split-K arrival counters).
 cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, int ldq,
                              uint8_t* codes, int ldc, uint8_t pad_code, uint8_t* sf,
-                             bool pdl_trigger, cudaStream_t stream, int M_out = -1);
+                             bool pdl_trigger, cudaStream_t stream, int M_out = -1,
+                             int* zero = nullptr, int nzero = 0);
 cudaError_t launch_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode,
                            int N, int K, void* out, cudaStream_t stream);
 
@@ -63,6 +65,19 @@ struct GemvArgs {
 int launch_gemv(const GemvArgs& a, cudaStream_t stream);
 unsigned int take_error_flags_gemv();
 int gemv_splits(int N, int Kp, int M, int force_splits);
+
+// ---- tensor-core decode GEMV (gemv_tc.cu): quantizes x itself, no workspace
+struct TcGemvArgs {
+  const mx_packed_weight* w;
+  const void* x;     // bf16 [M, K]
+  const void* bias;  // bf16 [N] or NULL
+  void* out;         // bf16 [M, N]
+  int M;             // 1..32
+  int force_splits;  // 0 = heuristic
+};
+int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream);
+int gemv_tc_splits(int N, int Kp, int sms, int force);
+unsigned int take_error_flags_gemv_tc();
 
 // ---- block-scaled GEMM (gemm.cu)
 struct GemmArgs {

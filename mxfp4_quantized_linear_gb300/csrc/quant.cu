@@ -23,8 +23,15 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
                                                         uint8_t* __restrict__ q, int ldq,
                                                         uint8_t* __restrict__ codes, int ldc,
                                                         uint8_t pad_code, uint8_t* __restrict__ sf,
-                                                        int pdl_trigger, int M_out) {
-  if (pdl_trigger) pdl_launch_dependents();
+                                                        int pdl_trigger, int M_out, int* zero,
+                                                        int nzero) {
+  if (pdl_trigger) {
+    // launched as a programmatic dependent: let the next kernel start, but
+    // touch x and the outputs only once the previous kernel is complete
+    pdl_launch_dependents();
+    pdl_wait_prior_grid();
+  }
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
   const int groups_per_row = Kout >> 3;
   const long long total = static_cast<long long>(M_out) * groups_per_row;
   const int lane = threadIdx.x & 31;
@@ -121,15 +128,23 @@ int grid_for(long long threads, int block) {
 
 cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, int ldq,
                              uint8_t* codes, int ldc, uint8_t pad_code, uint8_t* sf,
-                             bool pdl_trigger, cudaStream_t stream, int M_out) {
+                             bool pdl_trigger, cudaStream_t stream, int M_out, int* zero,
+                             int nzero) {
   if (M_out < M) M_out = M;
   const long long groups = static_cast<long long>(M_out) * (Kout / 8);
   const int block = 256;
   const int grid = grid_for(groups, block);
-  quant_act_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), M, K, Kout,
-                                               q, ldq, codes, ldc, pad_code, sf,
-                                               pdl_trigger ? 1 : 0, M_out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl_trigger ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), M, K, Kout, q, ldq,
+                            codes, ldc, pad_code, sf, pdl_trigger ? 1 : 0, M_out, zero, nzero);
 }
 
 cudaError_t launch_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode,

@@ -124,13 +124,39 @@ def test_prefill_full_size_sampled():
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("M", [1, 5, 9, 32])
+def test_cluster_gemv_path(M):
+    """The mma.sync GEMV with cluster split-K (MX_LINEAR_CLUSTER_GEMV)."""
+    g = inputs.generator(300 + M)
+    w = inputs.e4m3_bytes((96, 2080), g)
+    c = inputs.e8m0_codes((3, 65), 118, 132, g)
+    p = pack(w, c)
+    x = inputs.bf16_normal((M, 2080), g)
+    check(p, w, c, x, flags=mx.MX_LINEAR_CLUSTER_GEMV)
+    check(p, w, c, x, flags=mx.MX_LINEAR_CLUSTER_GEMV | mx.MX_LINEAR_NO_FUSED_QUANT)
+    cr = inputs.e8m0_codes((96, 65), 118, 132, g)
+    check(pack(w, cr), w, cr, x, flags=mx.MX_LINEAR_CLUSTER_GEMV)
+
+
+def test_decode_linear_cluster_gemv_full_size():
+    c = inputs.decode_linear(K=2048, Ms=(1, 32), seed=4)
+    p = pack(c["w"], c["codes"])
+    for M, x in c["xs"].items():
+        check(p, c["w"], c["codes"], x, flags=mx.MX_LINEAR_CLUSTER_GEMV)
+
+
 def test_workspace_too_small_is_an_error():
     g = inputs.generator(4)
     w = inputs.e4m3_bytes((64, 256), g)
     c = inputs.e8m0_codes((2, 8), 120, 130, g)
     p = pack(w, c)
     dev = cuda_device()
-    x = inputs.bf16_normal((20, 256), g).to(dev)
+    x = inputs.bf16_normal((40, 256), g).to(dev)   # M > 32: the GEMM needs the workspace
     with pytest.raises(mx.MxError) as ei:
         mx.mxfp8_linear(x, p, workspace=torch.empty(16, dtype=torch.uint8, device=dev))
+    assert ei.value.code == mx.binding.MX_ERR_WORKSPACE
+    x = inputs.bf16_normal((20, 256), g).to(dev)   # so does the cluster GEMV past the fused range
+    with pytest.raises(mx.MxError) as ei:
+        mx.mxfp8_linear(x, p, flags=mx.MX_LINEAR_CLUSTER_GEMV,
+                        workspace=torch.empty(16, dtype=torch.uint8, device=dev))
     assert ei.value.code == mx.binding.MX_ERR_WORKSPACE

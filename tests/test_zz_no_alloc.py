@@ -26,7 +26,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     row_codes = np.repeat(u8(c["codes"]), 32, axis=0)
     for M in (32, 16):  # the second call reuses the array the first one filled
         x = c["xs"][M].to(dev)
-        want = mx.mxfp8_linear(x, p, flags=mx.MX_LINEAR_NO_FUSED_QUANT)
+        want = mx.mxfp8_linear(x, p, flags=mx.MX_LINEAR_CLUSTER_GEMV | mx.MX_LINEAR_NO_FUSED_QUANT)
         got = mx.mxfp8_linear_noalloc(x, p)
         torch.cuda.synchronize()
         ref = ref_linear(bf16_np(c["xs"][M]), u8(c["w"]), row_codes)
