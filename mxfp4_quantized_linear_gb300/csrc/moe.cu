@@ -116,14 +116,15 @@ __global__ void zero_invalid_pairs_kernel(const int32_t* __restrict__ ids, int P
 constexpr int kMoeWarps = 8;
 constexpr int kMoeRows = kMoeWarps * 16;  // 128 weight rows a CTA
 constexpr int kMoeTok = 16;               // tokens a chunk (two n8 tiles)
-constexpr int kMoeStepK = 128;            // K elements a step (64 bytes a row)
-constexpr int kChunkK = 256;              // K elements of activation a ring slot (2 steps)
-constexpr int kChunkBytes = kMoeTok * kChunkK * 2;  // 8 KB
-constexpr int kPF = 4;                    // steps of weight words in flight a lane
+constexpr int kStageSteps = 4;            // 128-wide K steps a ring stage (256 bytes a row)
+constexpr int kStageK = kStageSteps * 128;                   // 512 K elements
+constexpr int kWarpStageBytes = 16 * kStageSteps * 64;       // 4 KB: two 16x128-byte boxes
+constexpr int kRing = 2;                                     // stages a warp keeps in flight
+constexpr int kChunkBytes = kMoeTok * kStageK * 2;           // 16 KB of bf16 activations a stage
+constexpr int kMoeSmem = kMoeWarps * kRing * kWarpStageBytes + 2 * kChunkBytes + 1024;
 
 struct MoeParams {
   const __nv_bfloat16* x;  // [T, K]
-  const uint8_t* wq;       // [E, N, Kp/2]
   const uint8_t* codes;    // [E, N, Kp/32]
   const int32_t* offsets;
   const int32_t* pairs;
@@ -146,10 +147,10 @@ MX_DEV void e2m1x8_to_bf16x8(uint32_t w, uint32_t (&r)[4]) {
   }
 }
 
-// 16-byte chunk c (0..31) of token row tk in an activation ring slot; the XOR by
+// 16-byte chunk c (0..63) of token row tk in an activation stage; the XOR by
 // (tk & 1) * 4 keeps the 8 lanes of a quarter warp (2 tokens x 4 chunks) on
 // distinct banks.
-MX_DEV int xs_off(int tk, int c) { return tk * (kChunkK * 2) + ((c ^ ((tk & 1) << 2)) << 4); }
+MX_DEV int xs_off(int tk, int c) { return tk * (kStageK * 2) + ((c ^ ((tk & 1) << 2)) << 4); }
 
 MX_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
@@ -158,39 +159,19 @@ MX_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
 MX_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 MX_DEV void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// One step of one warp: 16 weight rows x 128 K against up to 16 tokens.
-MX_DEV void moe_step(float (&acc)[2][4], const uint4& wa4, const uint4& wc4, uint32_t ca, uint32_t cc,
-                     uint32_t xs_base, int s_in_chunk, int g, int tq) {
-  const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
-  const uint32_t wc[4] = {wc4.x, wc4.y, wc4.z, wc4.w};
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    uint32_t ra[4], rc[4];
-    e2m1x8_to_bf16x8(wa[b], ra);
-    e2m1x8_to_bf16x8(wc[b], rc);
-    const float s0 = e8m0_to_f32((ca >> (8 * b)) & 0xffu);
-    const float s1 = e8m0_to_f32((cc >> (8 * b)) & 0xffu);
-    const int c = s_in_chunk * 16 + b * 4 + tq;  // 16-byte chunk: K = 8c .. 8c + 7 of the slot
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int tk = h * 8 + g;
-      uint4 xv;
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
-                   : "r"(xs_base + xs_off(tk, c)));
-      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      mma_bf16_16816(d, ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
-      mma_bf16_16816(d, ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
-      acc[h][0] = fmaf(d[0], s0, acc[h][0]);
-      acc[h][1] = fmaf(d[1], s0, acc[h][1]);
-      acc[h][2] = fmaf(d[2], s1, acc[h][2]);
-      acc[h][3] = fmaf(d[3], s1, acc[h][3]);
-    }
-  }
+MX_DEV uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
-__global__ void __launch_bounds__(kMoeWarps * 32, 1) moe_kernel(const MoeParams p) {
-  __shared__ __align__(128) uint8_t xs[2][kChunkBytes];
+__global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                const MoeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wring = smem;                                              // [warp][kRing][4 KB]
+  uint8_t* xs = smem + kMoeWarps * kRing * kWarpStageBytes;           // [2][16 KB]
+  __shared__ uint64_t bars[kMoeWarps][kRing];
   __shared__ int tok_src[kMoeTok];   // token row of x, or -1
   __shared__ int tok_pair[kMoeTok];  // output row (pair index), or -1
 
@@ -203,90 +184,131 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 1) moe_kernel(const MoeParams 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int row0 = blockIdx.x * kMoeRows;
-  const int rg = row0 + warp * 16 + g;  // rows rg and rg + 8
-  const int KHp = p.Kp >> 1, KBp = p.Kp >> 5;
+  const int wrow = row0 + warp * 16;        // this warp's first row within the expert
+  const int rg = wrow + g;                   // rows rg and rg + 8
+  const int KBp = p.Kp >> 5;
   const bool v0 = rg < p.N, v1 = rg + 8 < p.N;
   const long long erow = static_cast<long long>(e) * p.N;
-  const uint8_t* w0 = p.wq + (erow + (v0 ? rg : 0)) * KHp + tq * 16;
-  const uint8_t* w1 = p.wq + (erow + (v1 ? rg + 8 : 0)) * KHp + tq * 16;
   const uint8_t* c0p = p.codes + (erow + (v0 ? rg : 0)) * KBp;
   const uint8_t* c1p = p.codes + (erow + (v1 ? rg + 8 : 0)) * KBp;
-  const int ns = p.nsteps;
-  const int nchunks = (ns + 1) >> 1;
+  const int nst = (p.nsteps + kStageSteps - 1) / kStageSteps;  // ring stages along K
+  uint8_t* myring = wring + warp * kRing * kWarpStageBytes;
+  uint64_t* mybar = bars[warp];
+  const int grow = static_cast<int>(erow) + wrow;               // row in the flattened [E*N] map
+  const uint64_t pol = policy_evict_first();
+  uint32_t uses = 0;  // parity of each ring slot's next completion
+
+  if (lane == 0) {
+    for (int s = 0; s < kRing; ++s) mbar_init(&mybar[s], 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  auto issue = [&](int st, int slot) {  // weights of ring stage st (4 steps, 16 rows)
+    uint8_t* dst = myring + slot * kWarpStageBytes;
+    mbar_arrive_expect_tx(&mybar[slot], kWarpStageBytes);
+    tma_load_2d(dst, &wmap, &mybar[slot], st * 256, grow, pol);
+    tma_load_2d(dst + 2048, &wmap, &mybar[slot], st * 256 + 128, grow, pol);
+  };
 
   for (int ch = 0; ch < cnt; ch += kMoeTok) {
-    // ---- 1. weights of the first kPF steps: independent of the activations
-    uint4 wb0[kPF], wb1[kPF];
-    uint32_t cb0[kPF], cb1[kPF];
-#pragma unroll
-    for (int q = 0; q < kPF; ++q) {
-      const bool in = q < ns;
-      wb0[q] = (in && v0) ? ld_nc_v4(w0 + q * 64) : make_uint4(0u, 0u, 0u, 0u);
-      wb1[q] = (in && v1) ? ld_nc_v4(w1 + q * 64) : make_uint4(0u, 0u, 0u, 0u);
-      cb0[q] = in ? *reinterpret_cast<const uint32_t*>(c0p + q * 4) : 0x7f7f7f7fu;
-      cb1[q] = in ? *reinterpret_cast<const uint32_t*>(c1p + q * 4) : 0x7f7f7f7fu;
-    }
-    // ---- 2. the chunk's tokens, and the first two activation slots
+    // ---- 1. weight stages 0..kRing-1 (independent of the tokens)
+    if (lane == 0)
+      for (int s = 0; s < kRing && s < nst; ++s) issue(s, s);
+    // ---- 2. the chunk's tokens and the first two activation stages
     if (threadIdx.x < kMoeTok) {
       const int pr = (ch + static_cast<int>(threadIdx.x) < cnt) ? p.pairs[o0 + ch + threadIdx.x] : -1;
       tok_pair[threadIdx.x] = pr;
       tok_src[threadIdx.x] = pr >= 0 ? pr / p.topk : -1;
     }
     __syncthreads();
-    auto load_slot = [&](int c, int buf) {
-      const uint32_t dst = smem_u32(xs[buf]);
+    auto load_x = [&](int st, int buf) {
+      const uint32_t dst = smem_u32(xs + buf * kChunkBytes);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int idx = threadIdx.x + j * kMoeWarps * 32;  // 512 chunks of 16 bytes
-        const int tk = idx >> 5, cc = idx & 31;
+      for (int j = 0; j < 4; ++j) {
+        const int idx = threadIdx.x + j * kMoeWarps * 32;  // 1024 chunks of 16 bytes
+        const int tk = idx >> 6, cc = idx & 63;
         const int src = tok_src[tk];
-        const int k = c * kChunkK + cc * 8;
-        const bool ok = src >= 0 && k < p.K && c < nchunks;
+        const int k = st * kStageK + cc * 8;
+        const bool ok = src >= 0 && k < p.K && st < nst;
         const __nv_bfloat16* sp = ok ? p.x + static_cast<long long>(src) * p.K + k : p.x;
         cp_async16(dst + xs_off(tk, cc), sp, ok);
       }
       cp_async_commit();
     };
-    load_slot(0, 0);
-    load_slot(1, 1);
+    load_x(0, 0);
+    load_x(1, 1);
+    uint4 cnext0, cnext1;  // codes of the next stage: 4 steps x 4 blocks, rows rg and rg + 8
+    auto load_codes = [&](int st, uint4& c0, uint4& c1) {
+      const uint32_t* a0 = reinterpret_cast<const uint32_t*>(c0p + st * 16);
+      const uint32_t* a1 = reinterpret_cast<const uint32_t*>(c1p + st * 16);
+      const int nsl = p.nsteps - st * kStageSteps;  // steps of this stage that exist
+      c0.x = a0[0]; c1.x = a1[0];
+      c0.y = nsl > 1 ? a0[1] : 0x7f7f7f7fu; c1.y = nsl > 1 ? a1[1] : 0x7f7f7f7fu;
+      c0.z = nsl > 2 ? a0[2] : 0x7f7f7f7fu; c1.z = nsl > 2 ? a1[2] : 0x7f7f7f7fu;
+      c0.w = nsl > 3 ? a0[3] : 0x7f7f7f7fu; c1.w = nsl > 3 ? a1[3] : 0x7f7f7f7fu;
+    };
+    load_codes(0, cnext0, cnext1);
 
-    // ---- 3. K loop: two slots (four steps) an iteration so register slots stay static
     float acc[2][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[h][i] = 0.0f;
-    for (int c0 = 0; c0 < nchunks; c0 += 2) {
+
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % kRing;
+      const uint4 cs0 = cnext0, cs1 = cnext1;
+      if (st + 1 < nst) load_codes(st + 1, cnext0, cnext1);
+      cp_async_wait1();
+      __syncthreads();  // activation stage st is in shared memory for every warp
+      mbar_wait(&mybar[slot], (uses >> slot) & 1u);
+      const uint32_t wbase = smem_u32(myring + slot * kWarpStageBytes);
+      const uint32_t xbase = smem_u32(xs + (st & 1) * kChunkBytes);
+      const uint32_t c0w[4] = {cs0.x, cs0.y, cs0.z, cs0.w};
+      const uint32_t c1w[4] = {cs1.x, cs1.y, cs1.z, cs1.w};
 #pragma unroll
-      for (int cs = 0; cs < 2; ++cs) {
-        const int c = c0 + cs;
-        if (c < nchunks) {
-          cp_async_wait1();
-          __syncthreads();
-          const uint32_t xs_base = smem_u32(xs[cs]);
+      for (int s = 0; s < kStageSteps; ++s) {
+        if (st * kStageSteps + s < p.nsteps) {
+          // this lane's 16 bytes (4 K blocks, word tq) of rows g and g + 8; box s / 2,
+          // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+          const int c = (s & 1) * 4 + tq;
+          const uint32_t box = wbase + (s >> 1) * 2048;
+          const uint4 wa4 = ld_shared_v4(box + g * 128 + ((c ^ g) << 4));
+          const uint4 wc4 = ld_shared_v4(box + (g + 8) * 128 + ((c ^ g) << 4));
+          const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
+          const uint32_t wc[4] = {wc4.x, wc4.y, wc4.z, wc4.w};
 #pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            const int q = cs * 2 + s;  // register slot (static)
-            const int i = c * 2 + s;   // step
-            if (i < ns) {
-              const uint4 wa = wb0[q], wc = wb1[q];
-              const uint32_t ca = cb0[q], cc = cb1[q];
-              if (i + kPF < ns) {
-                wb0[q] = v0 ? ld_nc_v4(w0 + (i + kPF) * 64) : make_uint4(0u, 0u, 0u, 0u);
-                wb1[q] = v1 ? ld_nc_v4(w1 + (i + kPF) * 64) : make_uint4(0u, 0u, 0u, 0u);
-                cb0[q] = *reinterpret_cast<const uint32_t*>(c0p + (i + kPF) * 4);
-                cb1[q] = *reinterpret_cast<const uint32_t*>(c1p + (i + kPF) * 4);
-              }
-              moe_step(acc, wa, wc, ca, cc, xs_base, s, g, tq);
+          for (int b = 0; b < 4; ++b) {
+            uint32_t ra[4], rc[4];
+            e2m1x8_to_bf16x8(wa[b], ra);
+            e2m1x8_to_bf16x8(wc[b], rc);
+            const float s0 = e8m0_to_f32((c0w[s] >> (8 * b)) & 0xffu);
+            const float s1 = e8m0_to_f32((c1w[s] >> (8 * b)) & 0xffu);
+            const int xc = s * 16 + b * 4 + tq;  // 16-byte activation chunk: K = 8 xc .. + 7
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int tk = h * 8 + g;
+              const uint4 xv = ld_shared_v4(xbase + xs_off(tk, xc));
+              float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              mma_bf16_16816(d, ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
+              mma_bf16_16816(d, ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
+              acc[h][0] = fmaf(d[0], s0, acc[h][0]);
+              acc[h][1] = fmaf(d[1], s0, acc[h][1]);
+              acc[h][2] = fmaf(d[2], s1, acc[h][2]);
+              acc[h][3] = fmaf(d[3], s1, acc[h][3]);
             }
           }
-          __syncthreads();  // every warp is done with this slot
-          load_slot(c + 2, cs);
         }
       }
+      uses ^= 1u << slot;
+      __syncwarp();
+      if (lane == 0 && st + kRing < nst) issue(st + kRing, slot);
+      __syncthreads();  // every warp is done with activation stage st
+      load_x(st + 2, st & 1);
     }
 
-    // ---- 4. store: out[pair, row] (pairs with no token stay untouched)
+    // ---- 3. store out[pair, row]
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t0 = h * 8 + 2 * tq;
@@ -297,7 +319,7 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 1) moe_kernel(const MoeParams 
       if (pb >= 0 && v1) p.out[static_cast<long long>(pb) * p.N + rg + 8] = __float2bfloat16_rn(acc[h][3]);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();  // tok_* and the ring are reused by the next chunk of tokens
+    __syncthreads();  // tok_* and the buffers are reused by the next chunk of tokens
   }
 }
 
@@ -328,7 +350,6 @@ int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const 
                cudaStream_t stream) {
   MoeParams p = {};
   p.x = static_cast<const __nv_bfloat16*>(x);
-  p.wq = w->bytes;
   p.codes = w->codes;
   p.offsets = offsets;
   p.pairs = pairs;
@@ -339,12 +360,19 @@ int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const 
   p.N = w->N;
   p.K = w->K;
   p.Kp = w->Kp;
-  p.nsteps = w->Kp / kMoeStepK;
+  p.nsteps = w->Kp / 128;
+  CUtensorMap wmap;
+  const int KHp = w->Kp / 2;
+  int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, KHp,
+                                static_cast<uint64_t>(w->E) * w->N, KHp, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != MX_OK) return rc;
+  cudaError_t e = cudaFuncSetAttribute(moe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoeSmem);
+  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe: smem attribute: %s", cudaGetErrorString(e));
   const long long P = static_cast<long long>(T) * topk;
   const int zmax = static_cast<int>(P < w->E ? P : w->E);
   dim3 grid((w->N + kMoeRows - 1) / kMoeRows, zmax, 1);
-  moe_kernel<<<grid, kMoeWarps * 32, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  moe_kernel<<<grid, kMoeWarps * 32, kMoeSmem, stream>>>(wmap, p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;
 }
