@@ -299,7 +299,8 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
   int rc = check_device();
   if (rc != MX_OK) return rc;
   // tuning overrides of the cluster GEMV (not part of the documented flags):
-  // bits 8..11 force its split count, bit 12 forces its fused quantizer
+  // bits 8..11 force its split count, bit 12 forces its fused quantizer;
+  // bits 16..18 force the tensor-core GEMV's weight ring depth
   const int force_splits = static_cast<int>((flags >> 8) & 0xfu);
   const bool force_fuse = (flags & (1u << 12)) != 0;
   const bool no_fuse = (flags & MX_LINEAR_NO_FUSED_QUANT) != 0;
@@ -338,6 +339,7 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     g.out = out;
     g.M = M;
     g.force_splits = force_splits;
+    g.force_ring = static_cast<int>((flags >> 16) & 0x7u);      // tuning: weight ring depth
     return launch_gemv_tc(g, stream);
   }
   const bool needs_ws = (M > kFusedQuantMaxM && !force_fuse) || no_fuse || M > MX_GEMV_MAX_M;

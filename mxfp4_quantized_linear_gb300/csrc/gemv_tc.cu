@@ -10,19 +10,20 @@
 //   * one 128-row weight tile and one K slice (the S CTAs of a cluster hold the
 //     S slices of a tile); the weight boxes (128 rows x 128 bytes, 128B swizzle)
 //     and their 512-byte scale atoms stream through a TMA ring from the first
-//     instruction, together with one TMA box of the bf16 activation slice per
-//     128-wide K step (rows >= M and columns >= K come back as zeros);
-//   * the four epilogue warps first quantize that slice (same block rule as the
+//     instruction, before the previous kernel on the stream has finished;
+//   * once it has, the four epilogue warps load the bf16 activation slice from
+//     L2 (columns >= K read as zeros) and quantize it (same block rule as the
 //     standalone quantizer) straight into the 128B-swizzled K-major layout the
 //     tensor core reads, plus the activation scale atom;
 //   * warp 1 issues, per K step, tcgen05.cp of both scale atoms into tensor
 //     memory and four tcgen05.mma kind::mxf8f6f4.block_scale (M = 128 weight
 //     rows, N = 32 token columns, K = 32): the block scales are applied by the
 //     tensor core, the f32 sums stay in tensor memory;
-//   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld), stages the
-//     partial in shared memory, and after one cluster barrier each CTA sums its
-//     128 / S rows over the S partials in rank order (DSMEM), adds the bias and
-//     stores bf16.
+//   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld) and, once every
+//     CTA of the cluster is done with its weight ring, pushes each row's partial
+//     into the ring of the CTA that owns the row (DSMEM); after one more cluster
+//     barrier each CTA sums its 128 / S rows over the S partials in rank order,
+//     adds the bias and stores bf16.
 // The split depends on (N, K) only, so a token's result does not depend on M.
 // Every mbarrier wait is bounded.
 
@@ -37,40 +38,52 @@ constexpr int kRows = 128;                // weight rows a tile (MMA M)
 constexpr int kTok = 32;                  // token columns (MMA N)
 constexpr int kStepB = 128;               // K bytes a step
 constexpr int kMaxRing = 6;               // weight ring depth
+constexpr int kXBatch = 8;                // activation loads in flight a thread
 constexpr int kMaxSteps = 8;              // K steps a CTA (slice)
 constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 quant + epilogue
 constexpr int kWBox = kRows * kStepB;     // 16 KB
 constexpr int kXq = kTok * kStepB;        // 4 KB quantized activation a step
-constexpr int kXbf = kTok * kStepB * 2;   // 8 KB bf16 activation a step
 constexpr uint32_t kTmemCols = 128;       // accumulator 32 + one (SFw 4 + SFx 4) slot a step
 constexpr uint32_t kIdesc = mxf8_idesc(kRows, kTok);
 
 struct TcGemvParams {
   const uint8_t* sfw;          // weight scale atoms [RT][KT][512]
+  const __nv_bfloat16* x;      // [M, K]
   const __nv_bfloat16* bias;   // [N] or null
   __nv_bfloat16* out;          // [M, N]
   int M, N, K, KT, splits, ring;
 };
 
 struct Layout {
-  int w, sfw, xq, sfx, xbf, recv, bars, total;
+  int w, sfw, xq, sfx, recv, bars, total;
 };
 
-__host__ __device__ inline Layout layout_for(int ring, int steps, int splits) {
+// Shared memory.  The receive buffer of the split-K partials (M token rows)
+// reuses the weight ring once every CTA of the cluster has finished its MMAs.
+__host__ __device__ inline Layout layout_for(int ring, int steps, int splits, int M) {
   Layout L;
+  const int ring_bytes = ring * kWBox;
+  const int recv_bytes = splits > 1 ? M * splits * ((kRows + splits - 1) / splits) * 4 : 0;
   L.w = 0;                                   // ring x 16 KB
-  L.xq = ring * kWBox;                       // steps x 4 KB, 1024-aligned
-  L.xbf = L.xq + steps * kXq;                // steps x 8 KB
-  L.sfw = L.xbf + steps * kXbf;              // ring x 512
+  L.recv = 0;                                // S partials of this CTA's ceil(128/S) rows, M tokens
+  L.xq = ((ring_bytes > recv_bytes ? ring_bytes : recv_bytes) + 1023) & ~1023;  // steps x 4 KB
+  L.sfw = L.xq + steps * kXq;                // ring x 512
   L.sfx = L.sfw + ring * 512;                // steps x 512
-  L.recv = L.sfx + steps * 512;              // S partials of this CTA's ceil(128/S) rows
-  L.bars = L.recv + (splits > 1 ? kTok * splits * ((kRows + splits - 1) / splits) * 4 : 0);
+  L.bars = L.sfx + steps * 512;
   L.total = L.bars + 256;
   return L;
 }
 
+// At most four CTAs per SM: four 128-column tensor-memory allocations fill
+// the 512 columns, so a fifth CTA would wait in tcgen05.alloc on CTAs that may
+// themselves wait on cluster peers.  Five CTAs of at least this much shared
+// memory (plus the 1 KB the system reserves a CTA) exceed the 228 KB of an SM.
+constexpr int kMinSmem = 48 * 1024;
+// Two weight stages a CTA: with three or four CTAs per SM that keeps 96-128 KB
+// of weight requests in flight on every SM.
+constexpr int kDefaultRing = 2;
+
 __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                              const __grid_constant__ CUtensorMap xmap,
                                                               const TcGemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -81,12 +94,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   const int st0 = split * base + (split < rem ? split : rem);
   const int ns = base + (split < rem ? 1 : 0);
   const int ring = p.ring;
-  const Layout L = layout_for(ring, (p.KT + p.splits - 1) / p.splits, p.splits);
+  const Layout L = layout_for(ring, (p.KT + p.splits - 1) / p.splits, p.splits, p.M);
   pdl_launch_dependents();  // the next kernel may start streaming its own weights
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* wempty = wfull + kMaxRing;
-  uint64_t* xfull = wempty + kMaxRing;   // bf16 activation boxes landed
-  uint64_t* xready = xfull + 1;          // quantized activation written (128 arrivals)
+  uint64_t* xready = wempty + kMaxRing;  // quantized activation written (128 arrivals)
   uint64_t* accfull = xready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -96,7 +108,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 1);
     }
-    mbar_init(xfull, 1);
     mbar_init(xready, 128);
     mbar_init(accfull, 1);
     *abort_flag = 0u;
@@ -112,21 +123,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     tma_prefetch_desc(&wmap);
-    tma_prefetch_desc(&xmap);
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-    // weights first: immutable, so they may stream while earlier kernels finish
+    const uint64_t pol_w = policy_evict_first();
+    // the weight is immutable: it streams while earlier kernels finish
     const int first = ns < ring ? ns : ring;
     for (int i = 0; i < first; ++i) {
       mbar_arrive_expect_tx(&wfull[i], kWBox + 512);
       tma_load_2d(smem + L.w + i * kWBox, &wmap, &wfull[i], (st0 + i) * kStepB, tile * kRows, pol_w);
       bulk_load(smem + L.sfw + i * 512, p.sfw + (static_cast<long long>(tile) * p.KT + st0 + i) * 512, 512, &wfull[i]);
     }
-    // the activation slice may be written by the previous kernel: wait for it,
-    // then one bf16 box of 128 columns x 32 rows a step
-    pdl_wait_prior_grid();
-    mbar_arrive_expect_tx(xfull, ns * kXbf);
-    for (int i = 0; i < ns; ++i)
-      tma_load_2d(smem + L.xbf + i * kXbf, &xmap, xfull, (st0 + i) * kStepB, 0, pol_x);
     for (int i = first; i < ns && !*abort_flag; ++i) {
       const int stage = i % ring;
       if (!mbar_wait(&wempty[stage], (static_cast<uint32_t>(i / ring) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
@@ -161,31 +165,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   } else if (warp >= 2) {
     // ------------------------------------------------------------ quantize the slice
     const int et = threadIdx.x - 64;  // 0..127
-    const bool have_x = mbar_wait(xfull, 0);
-    if (!have_x) *abort_flag = 1u;
-    // item = (step, token, 8-element group): 4 consecutive lanes hold one MX block.
-    // Only the M real token rows are quantized: rows >= M feed only output
-    // columns that are never stored (every column of the MMA is independent).
+    // the activation may be written by the previous kernel on the stream
+    pdl_wait_prior_grid();
+    // item = (step, token, 8-element group): 4 consecutive lanes hold one MX
+    // block.  Only the M real token rows are quantized: rows >= M feed only
+    // output columns that are never stored (every column of the MMA is
+    // independent).  kXBatch loads a thread are in flight at once.
     const int mrows = p.M;
     const int items = ns * mrows * 16;
-    for (int base_i = (et & ~31); base_i < items; base_i += 128) {
-      const int it = base_i + lane;
-      const bool inside = it < items;
-      const int step = it / (mrows * 16), t = (it / 16) % mrows, g8 = it % 16;
-      float v[8];
-      if (inside && have_x) {
-        const uint4 u = *reinterpret_cast<const uint4*>(smem + L.xbf + step * kXbf + t * (kStepB * 2) + g8 * 16);
-        bf16x8_to_f32(u, v);
-      } else {
+    for (int b0 = (et & ~31); b0 < items; b0 += 128 * kXBatch) {
+      uint4 u[kXBatch];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+      for (int j = 0; j < kXBatch; ++j) {
+        const int it = b0 + j * 128 + lane;
+        u[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (it < items) {
+          const int step = it / (mrows * 16), t = (it / 16) % mrows, g8 = it % 16;
+          const int col = (st0 + step) * kStepB + g8 * 8;
+          if (col < p.K) u[j] = __ldcg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.K + col));
+        }
       }
-      const QuantBlock8 qb = mx_quant_block8(v);
-      if (inside) {
-        const int c = g8 >> 1;  // 16-byte chunk of the 128-byte row, 128B swizzle
-        *reinterpret_cast<uint2*>(smem + L.xq + step * kXq + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) =
-            make_uint2(qb.lo, qb.hi);
-        if ((g8 & 3) == 0) smem[L.sfx + step * 512 + t * 16 + (g8 >> 2)] = static_cast<uint8_t>(qb.code);
+#pragma unroll
+      for (int j = 0; j < kXBatch; ++j) {
+        if (b0 + j * 128 >= items) break;  // warp-uniform
+        const int it = b0 + j * 128 + lane;
+        const int step = it / (mrows * 16), t = (it / 16) % mrows, g8 = it % 16;
+        float v[8];
+        bf16x8_to_f32(u[j], v);
+        const QuantBlock8 qb = mx_quant_block8(v);
+        if (it < items) {
+          const int c = g8 >> 1;  // 16-byte chunk of the 128-byte row, 128B swizzle
+          *reinterpret_cast<uint2*>(smem + L.xq + step * kXq + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) =
+              make_uint2(qb.lo, qb.hi);
+          if ((g8 & 3) == 0) smem[L.sfx + step * 512 + t * 16 + (g8 >> 2)] = static_cast<uint8_t>(qb.code);
+        }
       }
     }
     fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
@@ -196,7 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     const int S = p.splits;
     const int n = tile * kRows + r;
     uint32_t acc[32];
-    if (mbar_wait(accfull, 0)) {
+    const bool done = mbar_wait(accfull, 0);
+    // every MMA of this CTA has completed, so its weight ring is dead: peers
+    // may push partials over it
+    if (S > 1) cluster_arrive_release();
+    if (done) {
       tc_fence_after();
       tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16), acc);
     } else {
@@ -216,18 +233,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       // push this row's partial to the CTA that owns it: CTA o owns rows
       // [o * rows_per, (o + 1) * rows_per), recv[split][t][row - o * rows_per]
       const int rows_per = (kRows + S - 1) / S;
+      cluster_wait_acquire();  // every CTA of the cluster is done with its ring
       const int owner = r / rows_per;
       const uint32_t dst = map_shared_rank(smem_u32(smem + L.recv), static_cast<uint32_t>(owner));
       const int rr = r - owner * rows_per;
 #pragma unroll
       for (int t = 0; t < kTok; ++t)
         if (t < p.M)
-          st_shared_cluster_f32(dst + static_cast<uint32_t>(((split * kTok + t) * rows_per + rr) * 4),
+          st_shared_cluster_f32(dst + static_cast<uint32_t>(((split * p.M + t) * rows_per + rr) * 4),
                                 __uint_as_float(acc[t]));
     }
   }
 
   if (p.splits > 1) {
+    if (warp < 2) {
+      // the TMA and MMA warps take part in the buffer hand-over barrier too
+      cluster_arrive_release();
+      cluster_wait_acquire();
+    }
     // every partial has landed in its owner's receive buffer; sum in rank order
     cluster_sync();
     const int S = p.splits;
@@ -239,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       const int n = tile * kRows + row;
       if (row >= kRows || n >= p.N) continue;
       float v = 0.0f;
-      for (int s = 0; s < S; ++s) v += recv[(s * kTok + t) * rows_per + rr];
+      for (int s = 0; s < S; ++s) v += recv[(s * p.M + t) * rows_per + rr];
       if (p.bias) v += __bfloat162float(p.bias[n]);
       p.out[static_cast<long long>(t) * p.N + n] = __float2bfloat16_rn(v);
     }
@@ -274,6 +297,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
   TcGemvParams p = {};
   p.sfw = w->sf;
+  p.x = static_cast<const __nv_bfloat16*>(a.x);
   p.bias = static_cast<const __nv_bfloat16*>(a.bias);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.M = a.M;
@@ -284,17 +308,16 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   if (p.splits < 1 || p.splits > 8) return set_error(MX_ERR_ARG, "gemv: split count %d outside 1..8", p.splits);
   if (p.splits > 8) return set_error(MX_ERR_UNSUPPORTED, "gemv: K = %d is too long for the decode GEMV", w->K);
   const int steps = (p.KT + p.splits - 1) / p.splits;
-  p.ring = steps < kMaxRing ? steps : kMaxRing;
-  const Layout L = layout_for(p.ring, steps, p.splits);
-  const int smem = L.total + 1024;
+  const int ring_max = a.force_ring > 0 ? (a.force_ring < kMaxRing ? a.force_ring : kMaxRing) : kDefaultRing;
+  p.ring = steps < ring_max ? steps : ring_max;
+  const Layout L = layout_for(p.ring, steps, p.splits, a.M);
+  const int smem = (L.total + 1024 > kMinSmem) ? L.total + 1024 : kMinSmem;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)
     return set_error(MX_ERR_UNSUPPORTED, "gemv: %d K steps a CTA (%d bytes of shared memory) is too many", steps, smem);
-  CUtensorMap wmap, xmap;
-  int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, kStepB, kRows,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc != MX_OK) return rc;
-  rc = encode_tensor_map_2d(&xmap, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w->K, a.M, static_cast<uint64_t>(w->K) * 2,
-                            kStepB, kTok, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (reinterpret_cast<uintptr_t>(a.x) % 16 != 0) return set_error(MX_ERR_ALIGN, "gemv: x needs 16-byte alignment");
+  CUtensorMap wmap;
+  const int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, kStepB,
+                                      kRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != MX_OK) return rc;
   cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemv_tc: smem attribute: %s", cudaGetErrorString(e));
@@ -312,7 +335,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, gemv_tc_kernel, wmap, xmap, p);
+  e = cudaLaunchKernelEx(&cfg, gemv_tc_kernel, wmap, p);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemv_tc launch: %s", cudaGetErrorString(e));
   return MX_OK;
 }

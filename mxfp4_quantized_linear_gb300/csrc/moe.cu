@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_con
       c0.w = nsl > 3 ? a0[3] : 0x7f7f7f7fu; c1.w = nsl > 3 ? a1[3] : 0x7f7f7f7fu;
     };
     load_codes(0, cnext0, cnext1);
+    // a chunk of at most 8 tokens needs only the first n8 tile of the MMA
+    const int ntile = (cnt - ch) > 8 ? 2 : 1;
 
     float acc[2][4];
 #pragma unroll
@@ -288,6 +290,7 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_con
             const int xc = s * 16 + b * 4 + tq;  // 16-byte activation chunk: K = 8 xc .. + 7
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+              if (h >= ntile) break;  // block-uniform
               const int tk = h * 8 + g;
               const uint4 xv = ld_shared_v4(xbase + xs_off(tk, xc));
               float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};

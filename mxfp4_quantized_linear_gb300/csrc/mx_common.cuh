@@ -140,6 +140,12 @@ MX_DEV void cluster_sync() {
                    : "memory");
 }
 
+// The two halves of a cluster barrier, for threads that reach them at
+// different points of divergent code (no .aligned).  Every thread of every CTA
+// of the cluster arrives once per phase before any of them may pass the wait.
+MX_DEV void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+MX_DEV void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
 // Shared-memory address of the same variable in CTA `rank` of the cluster.
 MX_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;

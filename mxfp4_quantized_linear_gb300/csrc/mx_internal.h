@@ -74,6 +74,7 @@ struct TcGemvArgs {
   void* out;         // bf16 [M, N]
   int M;             // 1..32
   int force_splits;  // 0 = heuristic
+  int force_ring;    // 0 = default weight ring depth
 };
 int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream);
 int gemv_tc_splits(int N, int Kp, int sms, int force);
