@@ -49,6 +49,30 @@ def moe_bytes(D, N, K, T, topk):
     return D * N * (K // 2 + K // 32) + 2 * T * K + 2 * T * topk * N + 4 * T * topk
 
 
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemv_tc_kernel_decode_7168x2048.md")
+GEMV_SOURCE = os.path.join(ROOT, "mxfp4_quantized_linear_gb300", "csrc", "gemv_tc.cu")
+
+
+def profiled_traffic():
+    """DRAM bytes (read + write) a gemv_tc_kernel launch of the step moved, averaged
+    over the 4 launches of a step, from the committed ncu summary; None when the
+    kernel source has changed since that capture."""
+    import hashlib
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+        want = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    sha = traffic = None
+    for line in text.splitlines():
+        line = line.replace("`", "").strip()
+        if line.startswith("source sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        elif line.startswith("traffic_bytes_per_launch:"):
+            traffic = int(line.split(":", 1)[1].strip())
+    return traffic if sha == want else None
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -144,7 +168,7 @@ def run_ours(args, ws, rank, local):
     wsz = max(mx.mxfp8_linear_workspace_size(M, packed[0]) for M in MS)
     work = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
     step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
-    kernels_per_step = sum(1 if M <= 8 else 2 for M in MS)
+    kernels_per_step = len(MS)  # one gemv_tc_kernel launch a call (M <= 32)
 
     def call(M, w):
         mx.mxfp8_linear(xs[M], w, out=outs[M], workspace=work)
@@ -195,25 +219,13 @@ def run_ours(args, ws, rank, local):
     ms_step = ms_total / args.steps
     value = ws * step_bytes / (ms_step * 1e-3) / 1e9
 
-    # ---- roofline of the dominant call: back-to-back M=32 calls over the rotated copies
+    # ---- roofline of the dominant (and only) kernel of the step, gemv_tc_kernel:
+    # algorithmic bytes of a launch (averaged over its 4 launches a step) over
+    # its average launch duration in the timed region, on this rank
     hbm_peak, bf16_peak, peak_kind = peaks()
-    reps = 4
-    gdom = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(gdom, stream=stream):
-            for w in packed:
-                call(32, w)
-        gdom.replay()
-        torch.cuda.synchronize()
-        torch.cuda._sleep(int(1e6))
-        e0.record(stream)
-        for _ in range(reps):
-            gdom.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    call_ms = e0.elapsed_time(e1) / (reps * ncopies)
-    call_bytes = linear_bytes(32, N_DEC, K_DEC, True)
-    achieved = call_bytes / (call_ms * 1e-3) / 1e9
+    launch_ms = ms_step / kernels_per_step
+    achieved = (step_bytes / kernels_per_step) / (launch_ms * 1e-3) / 1e9
+    # context: each M alone, back-to-back over the rotated copies
     per_m = {}
     for M in MS:
         gm = torch.cuda.CUDAGraph()
@@ -232,8 +244,10 @@ def run_ours(args, ws, rank, local):
         per_m[str(M)] = {"us_per_call": round(t * 1e3, 3),
                          "GB/s": round(linear_bytes(M, N_DEC, K_DEC, True) / (t * 1e-3) / 1e9, 1)}
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                "kernel": "mxfp8_linear M=32 (quantize + split-K GEMV, PDL-overlapped)",
+                "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic(),
+                "kernel": "gemv_tc_kernel (in-kernel activation quant + tcgen05 split-K GEMV), "
+                          f"{kernels_per_step} launches a step, {step_bytes // kernels_per_step} "
+                          "algorithmic bytes a launch on average",
                 "peak_source": f"{peak_kind} HBM copy bandwidth", "per_call": per_m}
 
     result = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
@@ -250,7 +264,7 @@ def run_ours(args, ws, rank, local):
         result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
         result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
         result["e2e"] = bench_e2e(mx, packed, dev, stream, args)
-    del graphs, gdom
+    del graphs
     return result
 
 
