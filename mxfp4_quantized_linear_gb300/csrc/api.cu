@@ -125,6 +125,11 @@ int current_device_info(DeviceInfo* out) {
     cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     di.max_smem_optin = static_cast<size_t>(v);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    di.smem_per_sm = static_cast<size_t>(v);
+    v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    di.smem_reserved_per_block = static_cast<size_t>(v);
     g_dev[dev].info = di;
     g_dev[dev].valid = true;
   }

@@ -19,11 +19,13 @@
 //     memory and four tcgen05.mma kind::mxf8f6f4.block_scale (M = 128 weight
 //     rows, N = 32 token columns, K = 32): the block scales are applied by the
 //     tensor core, the f32 sums stay in tensor memory;
-//   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld) and, once every
-//     CTA of the cluster is done with its weight ring, pushes each row's partial
-//     into the ring of the CTA that owns the row (DSMEM); after one more cluster
-//     barrier each CTA sums its 128 / S rows over the S partials in rank order,
-//     adds the bias and stores bf16.
+//   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld) and pushes each
+//     row's partial to the CTA of the cluster that owns the row (st.async into
+//     its receive buffer, completing on its mbarrier); each CTA waits for the
+//     S partials of its 128 / S rows, sums them in rank order, adds the bias
+//     and stores bf16.  The receive buffer has its own shared memory when four
+//     CTAs per SM still fit, else it reuses the weight ring once every CTA of
+//     the cluster has finished its MMAs (one cluster barrier).
 // The split depends on (N, K) only, so a token's result does not depend on M.
 // Every mbarrier wait is bounded.
 
@@ -44,7 +46,8 @@ constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 
 constexpr int kWBox = kRows * kStepB;     // 16 KB
 constexpr int kXq = kTok * kStepB;        // 4 KB quantized activation a step
 constexpr uint32_t kTmemCols = 128;       // accumulator 32 + one (SFw 4 + SFx 4) slot a step
-constexpr uint32_t kIdesc = mxf8_idesc(kRows, kTok);
+constexpr uint32_t kIdesc32 = mxf8_idesc(kRows, 32);  // 17..32 tokens
+constexpr uint32_t kIdesc16 = mxf8_idesc(kRows, 16);  // 1..16 tokens: half the tensor work
 
 struct TcGemvParams {
   const uint8_t* sfw;          // weight scale atoms [RT][KT][512]
@@ -52,24 +55,37 @@ struct TcGemvParams {
   const __nv_bfloat16* bias;   // [N] or null
   __nv_bfloat16* out;          // [M, N]
   int M, N, K, KT, splits, ring;
+  int own_recv;                // 1: the receive buffer has its own shared memory
 };
 
 struct Layout {
   int w, sfw, xq, sfx, recv, bars, total;
 };
 
-// Shared memory.  The receive buffer of the split-K partials (M token rows)
-// reuses the weight ring once every CTA of the cluster has finished its MMAs.
-__host__ __device__ inline Layout layout_for(int ring, int steps, int splits, int M) {
+// Shared memory.  The receive buffer of the split-K partials holds, for each
+// of the S slices and each of this CTA's ceil(128 / S) rows, recv_stride(M)
+// floats: M rounded up to 4, plus 4 when that is a multiple of 8, so that the
+// 16-byte reads of consecutive rows fall in distinct banks.  It either has its
+// own region or reuses the weight ring.
+__host__ __device__ inline int recv_stride(int M) {
+  const int m4 = (M + 3) & ~3;
+  return (m4 & 7) == 0 ? m4 + 4 : m4;
+}
+
+__host__ __device__ inline int recv_bytes_for(int splits, int M) {
+  return splits > 1 ? splits * ((kRows + splits - 1) / splits) * recv_stride(M) * 4 : 0;
+}
+
+__host__ __device__ inline Layout layout_for(int ring, int steps, int splits, int M, bool own_recv) {
   Layout L;
   const int ring_bytes = ring * kWBox;
-  const int recv_bytes = splits > 1 ? M * splits * ((kRows + splits - 1) / splits) * 4 : 0;
+  const int recv_bytes = recv_bytes_for(splits, M);
   L.w = 0;                                   // ring x 16 KB
-  L.recv = 0;                                // S partials of this CTA's ceil(128/S) rows, M tokens
-  L.xq = ((ring_bytes > recv_bytes ? ring_bytes : recv_bytes) + 1023) & ~1023;  // steps x 4 KB
+  L.xq = own_recv ? ring_bytes : ((ring_bytes > recv_bytes ? ring_bytes : recv_bytes) + 1023) & ~1023;
   L.sfw = L.xq + steps * kXq;                // ring x 512
   L.sfx = L.sfw + ring * 512;                // steps x 512
-  L.bars = L.sfx + steps * 512;
+  L.recv = own_recv ? L.sfx + steps * 512 : 0;
+  L.bars = own_recv ? L.recv + recv_bytes : L.sfx + steps * 512;
   L.total = L.bars + 256;
   return L;
 }
@@ -83,7 +99,7 @@ constexpr int kMinSmem = 48 * 1024;
 // of weight requests in flight on every SM.
 constexpr int kDefaultRing = 2;
 
-__global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const TcGemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -94,13 +110,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   const int st0 = split * base + (split < rem ? split : rem);
   const int ns = base + (split < rem ? 1 : 0);
   const int ring = p.ring;
-  const Layout L = layout_for(ring, (p.KT + p.splits - 1) / p.splits, p.splits, p.M);
+  const Layout L = layout_for(ring, (p.KT + p.splits - 1) / p.splits, p.splits, p.M, p.own_recv != 0);
+  const int S = p.splits;
+  const int rows_per = (kRows + S - 1) / S;        // rows each CTA of the cluster owns
+  const int Mp = recv_stride(p.M);                 // receive-buffer floats a (slice, row)
+  const int own_lo = split * rows_per;
+  const int own_hi = own_lo + rows_per < kRows ? own_lo + rows_per : kRows;
+  const int own_rows = own_hi > own_lo ? own_hi - own_lo : 0;
   pdl_launch_dependents();  // the next kernel may start streaming its own weights
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* wempty = wfull + kMaxRing;
   uint64_t* xready = wempty + kMaxRing;  // quantized activation written (128 arrivals)
   uint64_t* accfull = xready + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
+  uint64_t* redbar = accfull + 1;        // this CTA's rows: all S partials received
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(redbar + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   if (threadIdx.x == 0) {
@@ -110,15 +133,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     }
     mbar_init(xready, 128);
     mbar_init(accfull, 1);
+    mbar_init(redbar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     fence_proxy_async_smem();
+    // armed now; completes once the S partials of the owned rows have landed
+    if (S > 1) mbar_arrive_expect_tx(redbar, static_cast<uint32_t>(S * own_rows * ((p.M + 3) / 4) * 16));
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // with its own receive buffer a CTA may be pushed to as soon as its
+  // barriers exist: the cluster barrier's arrive goes here, its wait just
+  // before the first push (off the critical path)
+  if (S > 1 && p.own_recv) cluster_arrive_release();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -141,25 +171,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    bool ok = mbar_wait(xready, 0);
-    if (!ok) *abort_flag = 1u;
+    // a scale-factor slot per step (SFw in its first 4 columns, SFx in the
+    // next 4): no step overwrites columns an earlier, possibly still running
+    // MMA reads.  The weight scales of the stages already in flight go to
+    // tensor memory before the activation is ready.
+    bool ok = true;
+    const int pre = ns < ring ? ns : ring;
+    const uint32_t idesc_n = p.M <= 16 ? kIdesc16 : kIdesc32;
+    for (int i = 0; i < pre && ok; ++i) {
+      if (!mbar_wait(&wfull[i], 0u)) { *abort_flag = 1u; ok = false; break; }
+      tc_fence_after();
+      tc_cp_sf(tmem + kTok + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
+    }
+    if (ok && !mbar_wait(xready, 0)) { *abort_flag = 1u; ok = false; }
+    tc_fence_after();
     for (int i = 0; i < ns && ok; ++i) {
       const int stage = i % ring;
-      if (!mbar_wait(&wfull[stage], static_cast<uint32_t>(i / ring) & 1u)) { *abort_flag = 1u; ok = false; break; }
-      tc_fence_after();
-      // a scale-factor slot per step: no step overwrites columns an earlier,
-      // possibly still running MMA reads
       const uint32_t sf = tmem + kTok + static_cast<uint32_t>(i * 8);
-      tc_cp_sf(sf, sf_desc(smem_u32(smem + L.sfw + stage * 512)));
+      if (i >= pre) {
+        if (!mbar_wait(&wfull[stage], static_cast<uint32_t>(i / ring) & 1u)) { *abort_flag = 1u; ok = false; break; }
+        tc_fence_after();
+        tc_cp_sf(sf, sf_desc(smem_u32(smem + L.sfw + stage * 512)));
+      }
       tc_cp_sf(sf + 4, sf_desc(smem_u32(smem + L.sfx + i * 512)));
       const uint64_t adesc = sw128_desc(smem_u32(smem + L.w + stage * kWBox));
       const uint64_t bdesc = sw128_desc(smem_u32(smem + L.xq + i * kXq));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t idesc = kIdesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+        const uint32_t idesc = idesc_n | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
         tc_mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sf, sf + 4, (i | k) != 0 ? 1u : 0u);
       }
-      tc_commit(&wempty[stage]);
+      if (i + ring < ns) tc_commit(&wempty[stage]);  // the producer refills this stage
     }
     tc_commit(accfull);
   } else if (warp >= 2) {
@@ -171,8 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     // block.  Only the M real token rows are quantized: rows >= M feed only
     // output columns that are never stored (every column of the MMA is
     // independent).  kXBatch loads a thread are in flight at once.
+    // item it: row it / 16 of the slice = (step, token), 8-element group it % 16;
+    // row / M by a multiply-shift, exact for rows < 2^16 / M (rows <= 8 x 32)
     const int mrows = p.M;
     const int items = ns * mrows * 16;
+    const int mmul = (65536 + mrows - 1) / mrows;
     for (int b0 = (et & ~31); b0 < items; b0 += 128 * kXBatch) {
       uint4 u[kXBatch];
 #pragma unroll
@@ -180,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         const int it = b0 + j * 128 + lane;
         u[j] = make_uint4(0u, 0u, 0u, 0u);
         if (it < items) {
-          const int step = it / (mrows * 16), t = (it / 16) % mrows, g8 = it % 16;
+          const int row = it >> 4, step = (row * mmul) >> 16, t = row - step * mrows, g8 = it & 15;
           const int col = (st0 + step) * kStepB + g8 * 8;
           if (col < p.K) u[j] = __ldcg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.K + col));
         }
@@ -189,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       for (int j = 0; j < kXBatch; ++j) {
         if (b0 + j * 128 >= items) break;  // warp-uniform
         const int it = b0 + j * 128 + lane;
-        const int step = it / (mrows * 16), t = (it / 16) % mrows, g8 = it % 16;
+        const int row = it >> 4, step = (row * mmul) >> 16, t = row - step * mrows, g8 = it & 15;
         float v[8];
         bf16x8_to_f32(u[j], v);
         const QuantBlock8 qb = mx_quant_block8(v);
@@ -206,13 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
 
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, r = q * 32 + lane;
-    const int S = p.splits;
     const int n = tile * kRows + r;
     uint32_t acc[32];
     const bool done = mbar_wait(accfull, 0);
     // every MMA of this CTA has completed, so its weight ring is dead: peers
     // may push partials over it
-    if (S > 1) cluster_arrive_release();
+    if (S > 1 && !p.own_recv) cluster_arrive_release();
     if (done) {
       tc_fence_after();
       tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16), acc);
@@ -231,40 +275,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       }
     } else {
       // push this row's partial to the CTA that owns it: CTA o owns rows
-      // [o * rows_per, (o + 1) * rows_per), recv[split][t][row - o * rows_per]
-      const int rows_per = (kRows + S - 1) / S;
-      cluster_wait_acquire();  // every CTA of the cluster is done with its ring
+      // [o * rows_per, (o + 1) * rows_per); recv[slice][row - o * rows_per][t]
+      cluster_wait_acquire();  // the owner's barrier (and, if shared, buffer) is ready
       const int owner = r / rows_per;
-      const uint32_t dst = map_shared_rank(smem_u32(smem + L.recv), static_cast<uint32_t>(owner));
       const int rr = r - owner * rows_per;
+      const uint32_t dst = map_shared_rank(smem_u32(smem + L.recv), static_cast<uint32_t>(owner)) +
+                           static_cast<uint32_t>((split * rows_per + rr) * Mp * 4);
+      const uint32_t bar = map_shared_rank(smem_u32(redbar), static_cast<uint32_t>(owner));
 #pragma unroll
-      for (int t = 0; t < kTok; ++t)
+      for (int t = 0; t < kTok; t += 4)
         if (t < p.M)
-          st_shared_cluster_f32(dst + static_cast<uint32_t>(((split * p.M + t) * rows_per + rr) * 4),
-                                __uint_as_float(acc[t]));
+          st_async_v4_f32(dst + static_cast<uint32_t>(t * 4), __uint_as_float(acc[t]), __uint_as_float(acc[t + 1]),
+                          __uint_as_float(acc[t + 2]), __uint_as_float(acc[t + 3]), bar);
     }
   }
 
-  if (p.splits > 1) {
+  if (S > 1) {
     if (warp < 2) {
-      // the TMA and MMA warps take part in the buffer hand-over barrier too
-      cluster_arrive_release();
+      // the TMA and MMA warps take part in the cluster barrier too
+      if (!p.own_recv) cluster_arrive_release();
       cluster_wait_acquire();
     }
-    // every partial has landed in its owner's receive buffer; sum in rank order
-    cluster_sync();
-    const int S = p.splits;
-    const int rows_per = (kRows + S - 1) / S;
+    // the S partials of this CTA's rows have landed; sum them in rank order
+    if (!mbar_wait_cluster(redbar, 0)) *abort_flag = 1u;
+    // item = (4-token group, owned row): consecutive threads take consecutive
+    // rows, so each 16-byte read hits its own banks and the stores of a token
+    // are contiguous
     const float* recv = reinterpret_cast<const float*>(smem + L.recv);
-    for (int idx = threadIdx.x; idx < p.M * rows_per; idx += kThreads) {
-      const int t = idx / rows_per, rr = idx % rows_per;
-      const int row = split * rows_per + rr;
-      const int n = tile * kRows + row;
-      if (row >= kRows || n >= p.N) continue;
-      float v = 0.0f;
-      for (int s = 0; s < S; ++s) v += recv[(s * p.M + t) * rows_per + rr];
-      if (p.bias) v += __bfloat162float(p.bias[n]);
-      p.out[static_cast<long long>(t) * p.N + n] = __float2bfloat16_rn(v);
+    const int groups = (p.M + 3) / 4;
+    for (int idx = threadIdx.x; idx < own_rows * groups; idx += kThreads) {
+      const int g4 = idx / own_rows, rr = idx % own_rows;
+      const int n = tile * kRows + own_lo + rr;
+      if (n >= p.N) continue;
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int s = 0; s < S; ++s) {
+        const float4 u = *reinterpret_cast<const float4*>(recv + (s * rows_per + rr) * Mp + 4 * g4);
+        v.x += u.x;
+        v.y += u.y;
+        v.z += u.z;
+        v.w += u.w;
+      }
+      const float b = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int t = 4 * g4 + j;
+        if (t < p.M) p.out[static_cast<long long>(t) * p.N + n] = __float2bfloat16_rn(vv[j] + b);
+      }
     }
   }
   __syncthreads();
@@ -310,7 +367,10 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   const int steps = (p.KT + p.splits - 1) / p.splits;
   const int ring_max = a.force_ring > 0 ? (a.force_ring < kMaxRing ? a.force_ring : kMaxRing) : kDefaultRing;
   p.ring = steps < ring_max ? steps : ring_max;
-  const Layout L = layout_for(p.ring, steps, p.splits, a.M);
+  // its own receive buffer when four CTAs per SM still fit
+  const int four_per_sm = static_cast<int>(di.smem_per_sm / 4) - static_cast<int>(di.smem_reserved_per_block);
+  p.own_recv = p.splits > 1 && layout_for(p.ring, steps, p.splits, a.M, true).total + 1024 <= four_per_sm ? 1 : 0;
+  const Layout L = layout_for(p.ring, steps, p.splits, a.M, p.own_recv != 0);
   const int smem = (L.total + 1024 > kMinSmem) ? L.total + 1024 : kMinSmem;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)
     return set_error(MX_ERR_UNSUPPORTED, "gemv: %d K steps a CTA (%d bytes of shared memory) is too many", steps, smem);

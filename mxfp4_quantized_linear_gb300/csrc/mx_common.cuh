@@ -74,6 +74,20 @@ MX_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with cluster-scope acquire: the waiting thread sees every write
+// that peers of the cluster completed on this barrier (st.async complete_tx).
+MX_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs, sets the device timeout flag and returns false.
 MX_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
@@ -81,6 +95,19 @@ MX_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+      flag_timeout();
+      return false;
+    }
+  }
+}
+
+// mbar_wait with cluster-scope acquire (bounded the same way).
+MX_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
       flag_timeout();
       return false;
@@ -151,6 +178,16 @@ MX_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// Four floats into the shared memory of a CTA of the cluster (addresses from
+// map_shared_rank, 16-byte aligned); their 16 bytes complete on that CTA's
+// mbarrier `bar` (complete_tx), which orders them for its waiting threads.
+MX_DEV void st_async_v4_f32(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+               : "memory");
 }
 
 // Store to the shared memory of another CTA of the cluster (address from map_shared_rank).

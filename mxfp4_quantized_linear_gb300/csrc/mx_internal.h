@@ -18,6 +18,8 @@ struct DeviceInfo {
   int sm_count;
   int cc_major, cc_minor;
   size_t max_smem_optin;
+  size_t smem_per_sm;              // shared memory of one SM
+  size_t smem_reserved_per_block;  // shared memory the system reserves for each CTA
 };
 int current_device_info(DeviceInfo* out);
 
