@@ -143,15 +143,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const __grid_constant
       const int q8 = inside ? u % gpr : 0;
       const int k = k0 + q8 * 8;
       const bool valid = inside && t < p.M && k < p.K;
-      float v[8];
-      if (valid) {
-        const uint4 xu = *reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.K + k);
-        bf16x8_to_f32(xu, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-      }
-      const QuantBlock8 b = mx_quant_block8(v);
+      const uint4 xu = valid ? *reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.K + k)
+                             : make_uint4(0u, 0u, 0u, 0u);
+      const QuantBlock8 b = mx_quant_bf16x8(xu);
       if (inside) {
         const uint2 qv = valid ? make_uint2(b.lo, b.hi) : make_uint2(0u, 0u);
         *reinterpret_cast<uint2*>(xbuf + xchunk(t, q8 >> 1, ks) + (q8 & 1) * 8) = qv;

@@ -235,9 +235,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
         if (b0 + j * 128 >= items) break;  // warp-uniform
         const int it = b0 + j * 128 + lane;
         const int row = it >> 4, step = (row * mmul) >> 16, t = row - step * mrows, g8 = it & 15;
-        float v[8];
-        bf16x8_to_f32(u[j], v);
-        const QuantBlock8 qb = mx_quant_block8(v);
+        const QuantBlock8 qb = mx_quant_bf16x8(u[j]);
         if (it < items) {
           const int c = g8 >> 1;  // 16-byte chunk of the 128-byte row, 128B swizzle
           *reinterpret_cast<uint2*>(smem + L.xq + step * kXq + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) =

@@ -301,31 +301,38 @@ MX_DEV uint32_t mx_block_code(float amax) {
   return static_cast<uint32_t>(c < 0 ? 0 : (c > 254 ? 254 : c));
 }
 
-// v[0..7]: this lane's 8 consecutive elements of the block.
-MX_DEV QuantBlock8 mx_quant_block8(const float (&v)[8]) {
-  float amax = 0.0f;
-  bool bad = false;
+MX_DEV void bf16x8_to_f32(const uint4& u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a = fabsf(v[i]);
-    bad |= !(a <= 3.40282347e38f);  // NaN or inf
-    amax = fmaxf(amax, a);
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  uint32_t b = bad ? 1u : 0u;
-  b |= __shfl_xor_sync(0xffffffffu, b, 1);
-  b |= __shfl_xor_sync(0xffffffffu, b, 2);
+}
+
+// u: this lane's 8 consecutive bf16 elements of the block (element 0 in the
+// low half of u.x); 4 consecutive lanes hold the 32 elements of one block.
+// The block maximum is taken on the bf16 bit patterns with the sign cleared:
+// for finite values their unsigned order is the order of the magnitudes, inf
+// is 0x7f80 and every NaN lies above it.
+MX_DEV QuantBlock8 mx_quant_bf16x8(const uint4& u) {
+  const uint32_t m2 = __vmaxu2(__vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu),
+                               __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu));
+  uint32_t m = max(m2 & 0xffffu, m2 >> 16);
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
   QuantBlock8 r;
-  if (b) {
+  if (m >= 0x7f80u) {  // NaN or inf in the block
     r.lo = r.hi = 0x7f7f7f7fu;
     r.code = 255u;
     return r;
   }
-  const uint32_t code = mx_block_code(amax);
+  const uint32_t code = mx_block_code(__uint_as_float(m << 16));
   // 2^(127 - code): exponent field 254 - code; 0 -> the subnormal 2^-127
   const uint32_t ef = 254u - code;
   const float rescale = ef ? __uint_as_float(ef << 23) : __uint_as_float(0x00400000u);
+  float v[8];
+  bf16x8_to_f32(u, v);
   const uint32_t p0 = f32x2_to_e4m3x2(v[0] * rescale, v[1] * rescale);
   const uint32_t p1 = f32x2_to_e4m3x2(v[2] * rescale, v[3] * rescale);
   const uint32_t p2 = f32x2_to_e4m3x2(v[4] * rescale, v[5] * rescale);
@@ -334,15 +341,6 @@ MX_DEV QuantBlock8 mx_quant_block8(const float (&v)[8]) {
   r.hi = p2 | (p3 << 16);
   r.code = code;
   return r;
-}
-
-MX_DEV void bf16x8_to_f32(const uint4& u, float (&v)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
 }
 
 }  // namespace mx

@@ -17,7 +17,7 @@ namespace {
 // One thread = 8 consecutive elements of a row; 4 lanes = one MX block.
 // Grid-stride over 8-element groups of the [M, Kout] output (Kout >= K,
 // multiple of 32).  All lanes of a warp run the same trip count, so the
-// 4-lane shuffles inside mx_quant_block8 always see a full warp.
+// 4-lane shuffles inside mx_quant_bf16x8 always see a full warp.
 __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
                                                         int M, int K, int Kout,
                                                         uint8_t* __restrict__ q, int ldq,
@@ -43,15 +43,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
     const int row = inside ? static_cast<int>(g / groups_per_row) : 0;
     const int k = inside ? static_cast<int>(g % groups_per_row) * 8 : 0;
     const bool valid = inside && row < M && k < K;
-    float v[8];
-    if (valid) {
-      const uint4 u = *reinterpret_cast<const uint4*>(x + static_cast<long long>(row) * K + k);
-      bf16x8_to_f32(u, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    }
-    const QuantBlock8 b = mx_quant_block8(v);
+    const uint4 u = valid ? *reinterpret_cast<const uint4*>(x + static_cast<long long>(row) * K + k)
+                          : make_uint4(0u, 0u, 0u, 0u);
+    const QuantBlock8 b = mx_quant_bf16x8(u);
     if (!inside) continue;
     uint2 out = valid ? make_uint2(b.lo, b.hi) : make_uint2(0u, 0u);
     *reinterpret_cast<uint2*>(q + static_cast<long long>(row) * ldq + k) = out;
