@@ -3,10 +3,10 @@
 // A16W4 product (a16w4 = vllm.models.minimax_m3.amd.specialized_decode.mono.a16w4,
 // module text, dequant, step_mfma): MXFP4 weights are dequantized to bf16 in
 // registers and multiplied by the bf16 token activations on tensor cores with
-// f32 accumulation.  Here every e2m1 nibble becomes its exact bf16 value, one
-// m16n8k16 bf16 MMA pair covers a 32-wide K block from zero, and the block's
-// E8M0 factor 2^(c - 127) multiplies that f32 partial (exact up to f32 rounding
-// of the product; the pages fold the factor into the bf16 operand instead).
+// f32 accumulation.  Here, as on the page, every e2m1 nibble becomes the bf16
+// value of the dequantized weight e2m1 x 2^(c - 127) (exact: a power-of-two
+// multiply of an exact bf16), and the m16n8k16 bf16 MMAs accumulate the whole
+// K extent straight into the f32 accumulators.
 //
 // The packed weight stores, per 64-byte chunk of a row, word w of K block b at
 // word 4 w + b, and inside each word the element pair (2i, 2i+1) at nibble slots
@@ -14,7 +14,8 @@
 // blocks with one 16-byte load (the "16 bytes a lane" lesson of weights942,
 // fp4_lane_major / fp4_tile_major), and each bf16 pair is
 //   ((w >> 4i) & 0x000F000F) * (2^6 + 2^12) & 0x81C081C0   (sign -> bit 15,
-// exponent/mantissa -> bits 6..8, i.e. the value times 2^-126), times 2^126.
+// exponent/mantissa -> bits 6..8, i.e. the value times 2^-126), times 2^126,
+// times the block's 2^(c - 127).
 //
 // Routing is the plainest reading of "routed experts" (the pages show no
 // router): pairs grouped by expert id, stable in (token, slot) order.
@@ -134,15 +135,25 @@ struct MoeParams {
   int topk, N, K, Kp, nsteps;
 };
 
-// e2m1 x 8 (nibble slots (i, i+4) = elements (2i, 2i+1)) -> 4 bf16 pairs, exact.
-MX_DEV void e2m1x8_to_bf16x8(uint32_t w, uint32_t (&r)[4]) {
+// E8M0 code c of one block -> bf16x2 {2^(c-127), 2^(c-127)}: exponent field c
+// in both halves; code 0 -> the bf16 subnormal 2^-127 (0x0040).  Weight codes
+// are never 255 (the packer rejects them).
+MX_DEV uint32_t e8m0_to_bf16x2(uint32_t c) { return __vmaxu2(c * 0x00800080u, 0x00400040u); }
+
+// e2m1 x 8 (nibble slots (i, i+4) = elements (2i, 2i+1)) -> 4 bf16 pairs of the
+// dequantized weight e2m1 x 2^(c-127), exact (a16w4, dequant: fp4 with its
+// E8M0 scale to bf16).  The sign and the 3 exponent/mantissa bits land in a
+// bf16 whose value is the e2m1 value x 2^-126 (e2m1 subnormals map onto bf16
+// subnormals); two power-of-two multiplies give the scaled value.
+MX_DEV void e2m1x8_to_bf16x8_scaled(uint32_t w, uint32_t scale2, uint32_t (&r)[4]) {
   const __nv_bfloat162 two126 = __halves2bfloat162(__ushort_as_bfloat16(0x7e80),
                                                    __ushort_as_bfloat16(0x7e80));
+  const __nv_bfloat162 sc = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t u = (w >> (4 * i)) & 0x000f000fu;
     const uint32_t v = (u * 0x1040u) & 0x81c081c0u;
-    const __nv_bfloat162 b = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), two126);
+    const __nv_bfloat162 b = __hmul2(__hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), two126), sc);
     r[i] = *reinterpret_cast<const uint32_t*>(&b);
   }
 }
@@ -283,23 +294,17 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_con
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
             uint32_t ra[4], rc[4];
-            e2m1x8_to_bf16x8(wa[b], ra);
-            e2m1x8_to_bf16x8(wc[b], rc);
-            const float s0 = e8m0_to_f32((c0w[s] >> (8 * b)) & 0xffu);
-            const float s1 = e8m0_to_f32((c1w[s] >> (8 * b)) & 0xffu);
+            e2m1x8_to_bf16x8_scaled(wa[b], e8m0_to_bf16x2((c0w[s] >> (8 * b)) & 0xffu), ra);
+            e2m1x8_to_bf16x8_scaled(wc[b], e8m0_to_bf16x2((c1w[s] >> (8 * b)) & 0xffu), rc);
             const int xc = s * 16 + b * 4 + tq;  // 16-byte activation chunk: K = 8 xc .. + 7
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (h >= ntile) break;  // block-uniform
               const int tk = h * 8 + g;
               const uint4 xv = ld_shared_v4(xbase + xs_off(tk, xc));
-              float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-              mma_bf16_16816(d, ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
-              mma_bf16_16816(d, ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
-              acc[h][0] = fmaf(d[0], s0, acc[h][0]);
-              acc[h][1] = fmaf(d[1], s0, acc[h][1]);
-              acc[h][2] = fmaf(d[2], s1, acc[h][2]);
-              acc[h][3] = fmaf(d[3], s1, acc[h][3]);
+              // the weights carry their block scale: accumulate straight into acc
+              mma_bf16_16816(acc[h], ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
+              mma_bf16_16816(acc[h], ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
             }
           }
         }
