@@ -8,7 +8,7 @@
 // tensor core itself: `tcgen05.mma ... kind::mxf8f6f4.block_scale.scale_vec::1X`
 // with one E8M0 code per row per 32-wide K block held in tensor memory.
 //
-// CTA = 6 warps, one CTA per SM, persistent over 128 x 256 output tiles:
+// CTA = 10 warps, one CTA per SM, persistent over 128 x 256 output tiles:
 //   warp 0 (lane 0)  TMA producer: per 128-byte K step, A 128x128 and B 256x128
 //                    boxes (128B swizzle) plus the 512-byte scale-factor atoms of
 //                    A (1) and B (2), all completing on one mbarrier;
@@ -18,8 +18,11 @@
 //                    accumulating 128 x 256 f32 in tensor memory; tcgen05.commit
 //                    frees the smem stage and, after the last step, signals the
 //                    epilogue;
-//   warps 2..5       epilogue: tcgen05.ld 32 lanes x 32 columns at a time, bias
-//                    in f32, bf16 round, store; then release the accumulator.
+//   warps 2..9       epilogue, two warps per tensor-memory lane quarter, 128
+//                    columns each: tcgen05.ld of the warp's 32 rows x 128
+//                    columns into registers, release of the accumulator (the
+//                    next tile's MMAs start), then bias in f32, bf16 round and
+//                    store from registers, overlapping those MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA flags the error, stops
 // issuing, and still frees its tensor memory.
 
@@ -32,7 +35,8 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BKB = 128;      // tile rows, tile cols, K bytes a step
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr int kABytes = BM * BKB;                  // 16 KB
 constexpr int kBBytes = BN * BKB;                  // 32 KB
 constexpr int kSfaBytes = 512, kSfbBytes = 1024;
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, kEpiWarps);
     *abort_flag = 0u;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -142,52 +146,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    const int q = warp & 3;              // tensor-memory lane quarter this warp may access
+    const int half = (warp - 2) >> 2;    // columns [128 half, 128 half + 128)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
       if (!mbar_wait(acc_full, acc_phase)) { *abort_flag = 1u; break; }
       tc_fence_after();
-      const int row = mt * BM + q * 32 + lane;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + c * 32, r);
-        const int n0 = nt * BN + c * 32;
-        if (row < p.M && n0 < p.N) {
-          __nv_bfloat16* dst = p.out + static_cast<long long>(row) * p.N + n0;
-          if (n0 + 32 <= p.N && (p.N & 7) == 0) {
+      uint32_t r[128];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * 128;
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                float a = __uint_as_float(r[j + 2 * h]), b = __uint_as_float(r[j + 2 * h + 1]);
-                if (p.bias) {
-                  a += __bfloat162float(p.bias[n0 + j + 2 * h]);
-                  b += __bfloat162float(p.bias[n0 + j + 2 * h + 1]);
-                }
-                const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-                pk[h] = *reinterpret_cast<const uint32_t*>(&v);
-              }
-              *reinterpret_cast<uint4*>(dst + j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (n0 + j < p.N) {
-                float a = __uint_as_float(r[j]);
-                if (p.bias) a += __bfloat162float(p.bias[n0 + j]);
-                dst[j] = __float2bfloat16_rn(a);
-              }
-            }
-          }
-        }
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld32_async(taddr + c * 32, r + 32 * c);
+      tmem_wait_ld();
+      // the accumulator is in registers: the next tile's MMAs may overwrite it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
       acc_phase ^= 1u;
+      const int row = mt * BM + q * 32 + lane;
+      const int nb = nt * BN + half * 128;
+      if (row < p.M) {
+        __nv_bfloat16* dst = p.out + static_cast<long long>(row) * p.N + nb;
+        if (nb + 128 <= p.N && (p.N & 7) == 0) {
+#pragma unroll
+          for (int j = 0; j < 128; j += 8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              float a = __uint_as_float(r[j + 2 * h]), b = __uint_as_float(r[j + 2 * h + 1]);
+              if (p.bias) {
+                a += __bfloat162float(p.bias[nb + j + 2 * h]);
+                b += __bfloat162float(p.bias[nb + j + 2 * h + 1]);
+              }
+              const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+              pk[h] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            *reinterpret_cast<uint4*>(dst + j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) {
+            if (nb + j < p.N) {
+              float a = __uint_as_float(r[j]);
+              if (p.bias) a += __bfloat162float(p.bias[nb + j]);
+              dst[j] = __float2bfloat16_rn(a);
+            }
+          }
+        }
+      }
     }
   }
   tc_fence_before();
