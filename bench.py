@@ -173,7 +173,10 @@ def run_ours(args, ws, rank, local):
     def call(M, w):
         mx.mxfp8_linear(xs[M], w, out=outs[M], workspace=work)
 
-    # ---- one graph per step slot: the 4 calls on 4 different weight copies
+    # ---- graphs of whole steps (4 calls on 4 different weight copies each):
+    # one graph runs all nslots steps of the rotation back to back (calls of
+    # consecutive steps overlap through programmatic dependent launch), and
+    # one graph per slot covers a remainder
     nslots = ncopies // len(MS)
     graphs = []
     with torch.cuda.stream(stream):
@@ -186,11 +189,24 @@ def run_ours(args, ws, rank, local):
                 for i, M in enumerate(MS):
                     call(M, packed[s * len(MS) + i])
             graphs.append(g)
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all, stream=stream):
+            for s in range(nslots):
+                for i, M in enumerate(MS):
+                    call(M, packed[s * len(MS) + i])
     torch.cuda.synchronize()
 
     def steps(n, start=0):
-        for s in range(n):
+        s = 0
+        while s < n and (start + s) % nslots != 0:
             graphs[(start + s) % nslots].replay()
+            s += 1
+        while n - s >= nslots:
+            g_all.replay()
+            s += nslots
+        while s < n:
+            graphs[(start + s) % nslots].replay()
+            s += 1
 
     def barrier():
         if ws > 1:
@@ -264,7 +280,7 @@ def run_ours(args, ws, rank, local):
         result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
         result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
         result["e2e"] = bench_e2e(mx, packed, dev, stream, args)
-    del graphs
+    del graphs, g_all
     return result
 
 
@@ -322,34 +338,131 @@ def bench_moe(mx, inputs, dev, stream, hbm_peak):
 
 
 def bench_e2e(mx, packed, dev, stream, args):
-    """The step through the public API: pinned host x -> device, call, out -> pinned host."""
-    c_host = {M: torch.randn((M, K_DEC), generator=torch.Generator().manual_seed(M)).to(torch.bfloat16).pin_memory()
-              for M in MS}
-    o_host = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16).pin_memory() for M in MS}
-    x_dev = {M: torch.empty((M, K_DEC), dtype=torch.bfloat16, device=dev) for M in MS}
-    work = torch.empty(max(mx.mxfp8_linear_workspace_size(M, packed[0]) for M in MS), dtype=torch.uint8, device=dev)
+    """The step through the public API: pinned host x -> device, the 4 calls, out ->
+    pinned host, one stream synchronize a step.  ``value``: plain eager calls; ``graph``: the same
+    step (copies included) captured once in a CUDA graph and replayed each step, the
+    way a decode loop drives it."""
+    # one pinned buffer holds the 4 inputs (and one the 4 outputs): a step moves
+    # them with one host->device and one device->host copy
+    rows = sum(MS)
+    in_host = torch.randn((rows, K_DEC), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).pin_memory()
+    out_host = torch.empty((rows, N_DEC), dtype=torch.bfloat16).pin_memory()
+    in_dev = torch.empty((rows, K_DEC), dtype=torch.bfloat16, device=dev)
+    out_dev = torch.empty((rows, N_DEC), dtype=torch.bfloat16, device=dev)
+    offs = [sum(MS[:i]) for i in range(len(MS))]
+    x_dev = {M: in_dev[o:o + M] for o, M in zip(offs, MS)}
+    o_dev = {M: out_dev[o:o + M] for o, M in zip(offs, MS)}
+    work = torch.empty(max(mx.mxfp8_linear_workspace_size(M, packed[0]) for M in MS) + 256, dtype=torch.uint8,
+                       device=dev)
     n = max(20, min(args.steps, 500))
-    h2d = sum(c_host[M].numel() * 2 for M in MS)
-    d2h = sum(o_host[M].numel() * 2 for M in MS)
+    h2d = in_host.numel() * 2
+    d2h = out_host.numel() * 2
+    nslots = len(packed) // len(MS)
 
-    def one(s):
+    def enqueue(s):
+        in_dev.copy_(in_host, non_blocking=True)
         for i, M in enumerate(MS):
-            x_dev[M].copy_(c_host[M], non_blocking=True)
-            out = mx.mxfp8_linear(x_dev[M], packed[(s * len(MS) + i) % len(packed)], workspace=work)
-            o_host[M].copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+            mx.mxfp8_linear(x_dev[M], packed[(s % nslots) * len(MS) + i], out=o_dev[M], workspace=work)
+        out_host.copy_(out_dev, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for s in range(5):
-            one(s)
+            enqueue(s)
+            stream.synchronize()
         t0 = time.perf_counter()
         for s in range(n):
-            one(s)
+            enqueue(s)
+            stream.synchronize()
         t1 = time.perf_counter()
+        graphs = []
+        for s in range(nslots):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                enqueue(s)
+            graphs.append(g)
+        for s in range(5):
+            graphs[s % nslots].replay()
+            stream.synchronize()
+        t2 = time.perf_counter()
+        for s in range(n):
+            graphs[s % nslots].replay()
+            stream.synchronize()
+        t3 = time.perf_counter()
+    del graphs
     step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
-    sec = (t1 - t0) / n
+    sec, sec_g = (t1 - t0) / n, (t3 - t2) / n
     return {"value": round(step_bytes / sec / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 4), "steps": n}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(sec * 1e3, 4), "steps": n,
+            "graph": {"value": round(step_bytes / sec_g / 1e9, 1), "unit": "GB/s",
+                      "ms_per_step": round(sec_g * 1e3, 4)}}
+
+
+def bench_sweep(mx, inputs, dev, stream, hbm_peak, bf16_peak):
+    """The shape sweep: MXFP8 linears N=24576 K=1536 and N=7168 K=8192 at M = 1..256
+    (M <= 32 on the decode GEMV, larger M on the block-scaled GEMM), and the MXFP4 MoE
+    E=256 N=4096 K=7168 top-8 at T = 1..256.  Weights rotate over > 4x L2 of copies
+    (one 3.8 GB expert tensor already is); per-call time = graph time / calls."""
+    Ms = (1, 2, 4, 8, 16, 32, 64, 128, 256)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    lines = []
+
+    def timed(fn, calls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(calls):
+                    fn(i)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            times = []
+            for _ in range(5):
+                torch.cuda._sleep(int(1e6))
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) / calls)
+        return statistics.median(times)
+
+    for (N, K) in ((24576, 1536), (7168, 8192)):
+        c = inputs.decode_linear(K=K, Ms=Ms, N=N)
+        wd, cd = c["w"].to(dev), c["codes"].to(dev)
+        per_copy = mx.mx_pack_size("e4m3", 1, N, K)
+        ncopies = max(4, -(-4 * l2 // per_copy))
+        with torch.cuda.stream(stream):
+            packed = [mx.mx_pack_weights(wd, cd, "e4m3") for _ in range(ncopies)]
+        work = torch.empty(max(256, mx.mxfp8_linear_workspace_size(max(Ms), packed[0])), dtype=torch.uint8,
+                           device=dev)
+        for M in Ms:
+            x = c["xs"][M].to(dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ms = timed(lambda i=0: mx.mxfp8_linear(x, packed[i % ncopies], out=out, workspace=work), 2 * ncopies)
+            b = linear_bytes(M, N, K, True)
+            fl = 2.0 * M * N * K
+            lines.append({"sweep": "mxfp8_linear", "N": N, "K": K, "M": M, "us": round(ms * 1e3, 3),
+                          "GB/s": round(b / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1)})
+        del packed, work
+    E, N, K, topk = 256, 4096, 7168, 8
+    m = inputs.moe_gate_up(E=E, N=N, K=K, T=max(Ms), topk=topk, device=dev)
+    with torch.cuda.stream(stream):
+        p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
+    del m["w"], m["codes"]
+    for T in Ms:
+        x = m["x"][:T].contiguous()
+        ids = m["ids"][:T].contiguous()
+        out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E), dtype=torch.uint8, device=dev)
+        ms = timed(lambda i=0: mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work), 4)
+        D = int(torch.unique(ids).numel())
+        b = moe_bytes(D, N, K, T, topk)
+        lines.append({"sweep": "mxfp4_moe_linear", "E": E, "N": N, "K": K, "T": T, "topk": topk,
+                      "experts_touched": D, "us": round(ms * 1e3, 3), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)})
+    return lines
 
 
 # ------------------------------------------------------------- oracle (CPU)
@@ -420,6 +533,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the GEMM / MoE / e2e / CPU figures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print one JSON line per shape of the linear / MoE sweep instead of the step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()
@@ -429,6 +544,16 @@ def main():
         res = run_reference(args, ws, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+    if args.sweep:
+        if rank == 0:
+            import mxfp4_quantized_linear_gb300 as mx
+            from mxfp4_quantized_linear_gb300 import inputs
+            dev = torch.device("cuda", local)
+            torch.cuda.set_device(dev)
+            hbm_peak, bf16_peak, _ = peaks()
+            for line in bench_sweep(mx, inputs, dev, torch.cuda.Stream(dev), hbm_peak, bf16_peak):
+                print(json.dumps(line), flush=True)
         return
     res = run_ours(args, ws, rank, local)
     if rank == 0:

@@ -90,7 +90,12 @@ def _check(rc: int):
         raise MxError(rc, load_library().mx_last_error().decode())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream():
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
@@ -211,9 +216,10 @@ def mxfp8_linear(x: torch.Tensor, w: PackedWeight, bias: torch.Tensor = None, ou
     _need(out, torch.bfloat16, "out")
     if bias is not None:
         _need(bias, torch.bfloat16, "bias")
-    need = mxfp8_linear_workspace_size(M, w)
-    if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if workspace is None:  # the library reports a too-small workspace itself
+        need = mxfp8_linear_workspace_size(M, w)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(load_library().mxfp8_linear(_ptr(x), M, ctypes.byref(w.desc), _ptr(bias), _ptr(out), flags,
                                        _ptr(workspace), ws_bytes, _stream()))

@@ -121,6 +121,7 @@ int current_device_info(DeviceInfo* out) {
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "device attribute");
     di.sm_count = v;
+    di.device = dev;
     cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -134,6 +135,17 @@ int current_device_info(DeviceInfo* out) {
     g_dev[dev].valid = true;
   }
   *out = g_dev[dev].info;
+  return MX_OK;
+}
+
+int raise_smem_limit(const void* func, int bytes, const DeviceInfo& di, int* cache) {
+  int* slot = cache + di.device;
+  if (__atomic_load_n(slot, __ATOMIC_ACQUIRE) >= bytes) return MX_OK;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "shared memory attribute");
+  int cur = __atomic_load_n(slot, __ATOMIC_ACQUIRE);
+  while (cur < bytes && !__atomic_compare_exchange_n(slot, &cur, bytes, false, __ATOMIC_ACQ_REL, __ATOMIC_ACQUIRE)) {
+  }
   return MX_OK;
 }
 

@@ -231,8 +231,10 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   rc = encode_tensor_map_2d(&bmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, BKB, BN,
                             CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != MX_OK) return rc;
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
+  static int smem_set[64];
+  if (raise_smem_limit(reinterpret_cast<const void*>(gemm_kernel), kSmemBytes, di, smem_set) != MX_OK)
+    return MX_ERR_CUDA;
+  cudaError_t e;
   const int ntiles = p.m_tiles * p.n_tiles;
   const int grid = ntiles < di.sm_count ? ntiles : di.sm_count;
   cudaLaunchConfig_t cfg = {};

@@ -377,8 +377,9 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   const int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, kStepB,
                                       kRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != MX_OK) return rc;
-  cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemv_tc: smem attribute: %s", cudaGetErrorString(e));
+  static int smem_set[64];
+  if (raise_smem_limit(reinterpret_cast<const void*>(gemv_tc_kernel), smem, di, smem_set) != MX_OK) return MX_ERR_CUDA;
+  cudaError_t e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, (w->N + kRows - 1) / kRows, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

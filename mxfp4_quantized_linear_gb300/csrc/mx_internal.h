@@ -15,6 +15,7 @@ int set_error(int code, const char* fmt, ...);
 
 // Device properties of the current device (cached per device).
 struct DeviceInfo {
+  int device;  // ordinal of the current device
   int sm_count;
   int cc_major, cc_minor;
   size_t max_smem_optin;
@@ -22,6 +23,11 @@ struct DeviceInfo {
   size_t smem_reserved_per_block;  // shared memory the system reserves for each CTA
 };
 int current_device_info(DeviceInfo* out);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `func` on the current
+// device only when `bytes` exceeds what an earlier call set there (`cache`:
+// one slot per device ordinal, owned by the caller's translation unit).
+int raise_smem_limit(const void* func, int bytes, const DeviceInfo& di, int* cache);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,

@@ -14,38 +14,42 @@ Recipes (seed 0 unless stated, draws in the order listed):
   packer rewrites -0 to +0)
 * top-k expert ids: per token the first ``topk`` entries of a random
   permutation of the E experts (distinct experts)
+
+A generator made for a CUDA device draws there (same recipes, another
+stream of numbers): the benchmark uses that for the multi-GB expert sweep,
+whose inputs never go to the oracle.
 """
 import torch
 
 
-def generator(seed: int = 0) -> torch.Generator:
-    g = torch.Generator()
+def generator(seed: int = 0, device=None) -> torch.Generator:
+    g = torch.Generator() if device is None else torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
 
 def e4m3_bytes(shape, g: torch.Generator) -> torch.Tensor:
-    r = torch.randint(0, 254, tuple(shape), generator=g, dtype=torch.int32)
+    r = torch.randint(0, 254, tuple(shape), generator=g, dtype=torch.int32, device=g.device)
     r = r + (r >= 0x7F).to(torch.int32)          # skip 0x7F; 0xFF is never reached
     return r.to(torch.uint8)
 
 
 def e8m0_codes(shape, lo: int, hi: int, g: torch.Generator) -> torch.Tensor:
-    return torch.randint(lo, hi + 1, tuple(shape), generator=g, dtype=torch.int32).to(torch.uint8)
+    return torch.randint(lo, hi + 1, tuple(shape), generator=g, dtype=torch.int32, device=g.device).to(torch.uint8)
 
 
 def bf16_normal(shape, g: torch.Generator) -> torch.Tensor:
-    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32, device=g.device).to(torch.bfloat16)
 
 
 def fp4x2_bytes(shape, g: torch.Generator) -> torch.Tensor:
-    return torch.randint(0, 256, tuple(shape), generator=g, dtype=torch.int32).to(torch.uint8)
+    return torch.randint(0, 256, tuple(shape), generator=g, dtype=torch.int32, device=g.device).to(torch.uint8)
 
 
 def topk_ids(T: int, E: int, topk: int, g: torch.Generator) -> torch.Tensor:
-    out = torch.empty((T, topk), dtype=torch.int32)
+    out = torch.empty((T, topk), dtype=torch.int32, device=g.device)
     for t in range(T):
-        out[t] = torch.randperm(E, generator=g)[:topk].to(torch.int32)
+        out[t] = torch.randperm(E, generator=g, device=g.device)[:topk].to(torch.int32)
     return out
 
 
@@ -72,9 +76,9 @@ def decode_linear(K: int = 2048, Ms=(1, 4, 16, 32), N: int = 7168, seed: int = 0
 
 
 def moe_gate_up(E: int = 64, N: int = 4096, K: int = 4096, T: int = 64, topk: int = 8,
-                code_lo: int = 122, code_hi: int = 130, seed: int = 0) -> dict:
+                code_lo: int = 122, code_hi: int = 130, seed: int = 0, device=None) -> dict:
     """MXFP4 A16W4 MoE gate/up: w13 [E, N, K/2], per-row codes, T tokens top-k."""
-    g = generator(seed)
+    g = generator(seed, device)
     w = fp4x2_bytes((E, N, K // 2), g)
     codes = e8m0_codes((E, N, K // 32), code_lo, code_hi, g)
     x = bf16_normal((T, K), g)
