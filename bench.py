@@ -89,6 +89,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The slowest rank's time: every rank's timed region ends at the same
+    barrier, so the job took the maximum."""
+    if ws <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ws: int, bytes_per_rank_step: int, ms_step: float) -> float:
+    """Whole-job GB/s: every rank streams its own replica's bytes each step
+    (weak scaling: the work per GPU is fixed as the GPU count grows)."""
+    return ws * bytes_per_rank_step / (ms_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------- clocks
 
 REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -227,13 +243,9 @@ def run_ours(args, ws, rank, local):
             e1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     ms_step = ms_total / args.steps
-    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_throughput(ws, step_bytes, ms_step)
 
     # ---- roofline of the dominant (and only) kernel of the step, gemv_tc_kernel:
     # algorithmic bytes of a launch (averaged over its 4 launches a step) over

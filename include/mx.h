@@ -172,9 +172,15 @@ size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
  *   x     [M, K] bf16           w     packed E4M3 weight with E == 1
  *   bias  [N] bf16 or NULL      out   [M, N] bf16
  *   workspace  device scratch of mxfp8_linear_workspace_size(M, w) bytes
- * M <= MX_GEMV_MAX_M runs the persistent split-K decode GEMV on the tensor
- * cores (block scales applied by tcgen05), larger M the block-scaled GEMM.
- * Within the decode range a token's result does not depend on M.
+ * M <= MX_GEMV_MAX_M runs the split-K decode GEMV on the tensor cores (block
+ * scales applied by tcgen05, activation quantized inside the kernel), larger M
+ * the block-scaled GEMM.  Within the decode range a token's result does not
+ * depend on M.
+ * The kernels start streaming w's buffers before the previous kernel on the
+ * stream has finished (programmatic dependent launch): w must not be written
+ * by the kernel launched just before on the same stream (mx_pack_weights
+ * returns only once its writes are complete).  x, bias and out are ordered
+ * with earlier work as usual.
  */
 int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
                  unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
