@@ -33,6 +33,13 @@ Packed E2M1 weight (MXFP4 experts), E experts of [N, K]:
          16 + 4i; -0 nibbles are +0
   codes  [E, N, Kp/32]  per-row codes (32x32 block codes are expanded), 128
          past K
+  gate / up experts (w13 [E, 2 I, K/2], gate rows then up rows, weights942
+  ``moe_copies``) can be packed with their halves interleaved in 8-row groups:
+  packed row 16 q + i holds gate row 8 q + i for i < 8 and up row
+  8 q + i - 8 for i >= 8 (codes alike), so the 16 rows of one MMA fragment
+  hold the gate and up rows of the same 8 intermediate indices.  (The page's
+  gfx942 copy interleaves single rows, 2 i and 2 i + 1, for its own MFMA
+  fragment.)
 
 Pinned by tests/test_oracle_layout.py: unpack(pack(w)) == w, the padding
 values, the fold / refuse decisions on agreeing and disagreeing rows, and the
@@ -205,9 +212,20 @@ def drop_negative_zero(w) -> np.ndarray:
     return np.where(hi, w & 0x0F, w).astype(np.uint8)
 
 
-def pack_e2m1(w, codes) -> dict:
+def gate_up_source_rows(N: int) -> np.ndarray:
+    """Packed row r -> source row of a gate-then-up [2 I = N] expert tensor
+    under the 8-row-group interleave (see module text)."""
+    if N % 16 != 0:
+        raise PackError(MX_ERR_SHAPE, "gate/up interleave needs 2 I a multiple of 16")
+    r = np.arange(N)
+    q, i = r // 16, r % 16
+    return np.where(i < 8, 8 * q + i, N // 2 + 8 * q + i - 8)
+
+
+def pack_e2m1(w, codes, gate_up: bool = False) -> dict:
     """MXFP4 experts: bytes [E, N, K/2] (fp4x2, low nibble first), codes
-    [E, N, K/32] or [E, N/32, K/32] -> packed dict (see module text)."""
+    [E, N, K/32] or [E, N/32, K/32] -> packed dict (see module text).
+    ``gate_up``: interleave the gate and up halves (see module text)."""
     w = np.asarray(w, dtype=np.uint8)
     codes = np.asarray(codes, dtype=np.uint8)
     E, N, KH = w.shape
@@ -223,6 +241,9 @@ def pack_e2m1(w, codes) -> dict:
         row = expand_block_codes(codes, N)
     else:
         raise PackError(MX_ERR_SHAPE, f"codes shape {codes.shape} does not fit w {w.shape}")
+    if gate_up:
+        src = gate_up_source_rows(N)
+        w, row = w[:, src], row[:, src]
     Kp = padded_k(K)
     negz = count_negative_zero(w)
     clean = drop_negative_zero(w)
@@ -231,12 +252,18 @@ def pack_e2m1(w, codes) -> dict:
     return {"fmt": "e2m1", "mode": "row", "E": E, "N": N, "K": K, "Kp": Kp,
             "wq": _nibble_slot_shuffle(_word_transpose(padded)),
             "codes": _pad_codes(row, Kp // 32),
-            "neg_zero_count": negz}
+            "neg_zero_count": negz, "gate_up": bool(gate_up)}
 
 
 def unpack_e2m1(p: dict) -> tuple:
     """Inverse of pack_e2m1 (up to -0 -> +0): (bytes [E, N, K/2], codes [E, N, K/32])."""
     K = p["K"]
     # the 4x4 word transpose is its own inverse
-    back = _word_transpose(_nibble_slot_shuffle(p["wq"], inverse=True))
-    return back[:, :, : K // 2].copy(), p["codes"][:, :, : K // 32].copy()
+    back = _word_transpose(_nibble_slot_shuffle(p["wq"], inverse=True))[:, :, : K // 2]
+    codes = p["codes"][:, :, : K // 32]
+    if p.get("gate_up"):
+        src = gate_up_source_rows(p["N"])
+        w, c = np.empty_like(back), np.empty_like(codes)
+        w[:, src], c[:, src] = back, codes
+        return w, c
+    return back.copy(), codes.copy()

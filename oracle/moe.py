@@ -17,10 +17,25 @@ within an expert; ids of -1 are skipped and their outputs are zero; any other
 id outside [0, E) is an error and is skipped the same way.  Routing weights
 are not applied (the gate/up GEMM output is per (token, slot)).
 
+The full routed expert (``moe_expert``) follows the tensors weights942
+``moe_copies`` describes: w13 [E, 2 I, K/2] with the I gate rows first, then
+the I up rows, and w2 [E, H, I/2].  Readings where the pages are silent:
+
+* the gated activation is SiLU-and-mul: act = silu(gate) * up, silu(v) =
+  v / (1 + e^-v);
+* act is rounded to bf16 before the down projection (the down GEMM is A16W4
+  too: bf16 activations times MXFP4 weights);
+* the routing weights scale each slot's down-projection row and the top-k
+  slots are summed: out[t] = sum_j weight[t, j] y2[t, j]; slots whose id is
+  not a valid expert contribute nothing.
+
 Pinned by tests/test_oracle_moe.py: E = 1 / top-1 reduces to a dense A16W4
 linear checked by exact rational brute force, invariance under permuting the
 tokens, -0 and +0 nibbles giving identical outputs (weights942,
-``fp4_drop_negative_zero_``), and routing against Python's stable sort.
+``fp4_drop_negative_zero_``), routing against Python's stable sort; silu
+against torch's CPU ``silu``; the full expert at E = 1 / top-1 against the
+same chain in torch CPU ops on a table-decoded weight; gate / up roles,
+slot permutation, linearity in the routing weights and skipped invalid slots.
 """
 import numpy as np
 
@@ -82,3 +97,40 @@ def moe_linear(x, topk_ids, w_bytes, codes, wdeq=None) -> np.ndarray:
             if 0 <= e < E:
                 y[t, j] = W[e] @ x[t]
     return y
+
+
+def silu(v) -> np.ndarray:
+    """SiLU in fp64: v / (1 + e^-v) (-> 0 for v -> -inf, -> v for v -> +inf)."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def moe_expert(x, topk_ids, topk_weights, w13_bytes, w13_codes, w2_bytes, w2_codes) -> dict:
+    """The routed expert MLP, fp64.
+
+    x [T, K] (bf16 values), topk_ids [T, topk], topk_weights [T, topk];
+    w13 bytes [E, 2 I, K/2] (gate rows 0..I-1, up rows I..2I-1) with per-row
+    codes [E, 2 I, K/32]; w2 bytes [E, H, I/2] with codes [E, H, I/32].
+
+    Returns dict(out [T, H], act [T, topk, I] (bf16 values), y13 [T, topk, 2I],
+    y2 [T, topk, H])."""
+    x = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    wts = np.asarray(topk_weights, dtype=np.float64)
+    T, topk = ids.shape
+    E, I2 = np.asarray(w13_bytes).shape[:2]
+    I = I2 // 2
+    H = np.asarray(w2_bytes).shape[1]
+    y13 = moe_linear(x, ids, w13_bytes, w13_codes)                 # [T, topk, 2I]
+    act = bf16_value(bf16_rne_bits(silu(y13[:, :, :I]) * y13[:, :, I:]))
+    W2 = dequant_experts_bf16(w2_bytes, w2_codes)                  # [E, H, I]
+    y2 = np.zeros((T, topk, H), dtype=np.float64)
+    out = np.zeros((T, H), dtype=np.float64)
+    for t in range(T):
+        for j in range(topk):
+            e = ids[t, j]
+            if 0 <= e < E:
+                y2[t, j] = W2[e] @ act[t, j]
+                out[t] += wts[t, j] * y2[t, j]
+    return {"out": out, "act": act, "y13": y13, "y2": y2}

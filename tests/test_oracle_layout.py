@@ -95,3 +95,22 @@ def test_e2m1_roundtrip_padding_and_negative_zero_count():
     # the padded tail (past K/2 bytes, before the transpose) is zero
     untransposed = L._word_transpose(L._nibble_slot_shuffle(p["wq"], inverse=True))
     assert np.all(untransposed[:, :, K // 2:] == 0)
+
+
+def test_gate_up_interleave_rows_and_inverse():
+    from oracle import layout as L
+    src = L.gate_up_source_rows(48)          # I = 24
+    assert src[:8].tolist() == list(range(8))            # gate rows 0..7
+    assert src[8:16].tolist() == list(range(24, 32))     # up rows 0..7
+    assert src[16:24].tolist() == list(range(8, 16))     # gate rows 8..15
+    assert sorted(src.tolist()) == list(range(48))
+    rng = np.random.default_rng(9)
+    w = rng.integers(0, 256, size=(2, 48, 80), dtype=np.uint8)
+    c = rng.integers(118, 133, size=(2, 48, 5), dtype=np.uint8)
+    p = L.pack_e2m1(w, c, gate_up=True)
+    plain = L.pack_e2m1(w[:, src], c[:, src])
+    assert np.array_equal(p["wq"], plain["wq"]) and np.array_equal(p["codes"], plain["codes"])
+    back, cb = L.unpack_e2m1(p)
+    assert np.array_equal(back, L.drop_negative_zero(w)) and np.array_equal(cb, c)
+    with pytest.raises(L.PackError):
+        L.pack_e2m1(w[:, :40], c[:, :40], gate_up=True)

@@ -79,3 +79,93 @@ def test_token_permutation_and_negative_zero():
     hi0 = (wneg & 0xF0) == 0
     wneg[hi0] |= 0x80
     assert np.array_equal(moe_linear(x, ids, wneg, codes), y)
+
+
+# ---------------------------------------------------------------- full expert
+
+def test_silu_matches_torch_cpu():
+    import torch
+    v = np.concatenate([np.linspace(-40, 40, 2001), [-700.0, -50.0, 0.0, 50.0, 700.0]])
+    from oracle.moe import silu
+    ref = torch.nn.functional.silu(torch.tensor(v, dtype=torch.float64)).numpy()
+    assert np.allclose(silu(v), ref, rtol=1e-15, atol=1e-300)
+    assert silu(np.array([0.0]))[0] == 0.0
+
+
+def _table_dequant(w, codes):
+    """[N, K/2] fp4x2 bytes + [N, K/32] codes -> fp64 [N, K] from the OCP table fixture."""
+    tab = e2m1_table()
+    N, KH = w.shape
+    out = np.empty((N, 2 * KH))
+    for n in range(N):
+        for k in range(2 * KH):
+            byte = int(w[n, k // 2])
+            nib = byte & 0xF if k % 2 == 0 else byte >> 4
+            out[n, k] = float(tab[nib]) * 2.0 ** (int(codes[n, k // 32]) - 127)
+    return out
+
+
+def _expert_case(seed, T=3, topk=2, E=3, I=32, K=64, H=48):
+    rng = np.random.default_rng(seed)
+    x = F.bf16_value(F.bf16_rne_bits(rng.standard_normal((T, K))))
+    ids = np.stack([rng.permutation(E)[:topk] for _ in range(T)]).astype(np.int32)
+    wts = rng.random((T, topk))
+    w13 = rng.integers(0, 256, size=(E, 2 * I, K // 2), dtype=np.uint8)
+    c13 = rng.integers(122, 131, size=(E, 2 * I, K // 32), dtype=np.uint8)
+    w2 = rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
+    c2 = rng.integers(122, 131, size=(E, H, I // 32), dtype=np.uint8)
+    return x, ids, wts, w13, c13, w2, c2
+
+
+def test_expert_single_expert_matches_torch_chain():
+    import torch
+    from oracle.moe import moe_expert
+    x, _, _, w13, c13, w2, c2 = _expert_case(2, E=1)
+    T, I = x.shape[0], w13.shape[1] // 2
+    ids = np.zeros((T, 1), dtype=np.int32)
+    wts = np.full((T, 1), 0.75)
+    r = moe_expert(x, ids, wts, w13, c13, w2, c2)
+    W13 = torch.tensor(_table_dequant(w13[0], c13[0]))
+    W2 = torch.tensor(_table_dequant(w2[0], c2[0]))
+    xt = torch.tensor(x)
+    g, u = xt @ W13[:I].T, xt @ W13[I:].T
+    act = torch.nn.functional.silu(g) * u
+    # bf16 rounding of act: compare within one bf16 ulp, then feed the oracle's
+    # rounded act to the down projection
+    # bf16 spacing at |act|, never below the subnormal spacing 2^-133
+    ulp = np.maximum(2.0 ** (np.floor(np.log2(np.maximum(np.abs(act.numpy()), 1e-300))) - 7), 2.0 ** -133)
+    assert np.all(np.abs(r["act"][:, 0] - act.numpy()) <= ulp)
+    out = 0.75 * (torch.tensor(r["act"][:, 0]) @ W2.T)
+    assert np.allclose(r["out"], out.numpy(), rtol=1e-12, atol=1e-12 * np.abs(out.numpy()).max())
+
+
+def test_expert_gate_and_up_roles():
+    from oracle.moe import moe_expert, silu
+    x, ids, wts, w13, c13, w2, c2 = _expert_case(3)
+    I = w13.shape[1] // 2
+    up0 = w13.copy()
+    up0[:, I:] = 0                          # up = 0 -> act = 0 -> out = 0
+    assert np.all(moe_expert(x, ids, wts, up0, c13, w2, c2)["out"] == 0.0)
+    gate0 = w13.copy()
+    gate0[:, :I] = 0                        # silu(0) = 0 -> act = 0
+    assert np.all(moe_expert(x, ids, wts, gate0, c13, w2, c2)["out"] == 0.0)
+    r = moe_expert(x, ids, wts, w13, c13, w2, c2)
+    g, u = r["y13"][:, :, :I], r["y13"][:, :, I:]
+    assert np.array_equal(r["act"], F.bf16_value(F.bf16_rne_bits(silu(g) * u)))
+
+
+def test_expert_slot_permutation_weights_and_invalid_ids():
+    from oracle.moe import moe_expert
+    x, ids, wts, w13, c13, w2, c2 = _expert_case(4, topk=3, E=4)
+    base = moe_expert(x, ids, wts, w13, c13, w2, c2)["out"]
+    perm = [2, 0, 1]
+    p = moe_expert(x, ids[:, perm], wts[:, perm], w13, c13, w2, c2)["out"]
+    assert np.allclose(p, base, rtol=1e-13, atol=1e-13 * np.abs(base).max())
+    d = moe_expert(x, ids, 2.0 * wts, w13, c13, w2, c2)["out"]
+    assert np.array_equal(d, 2.0 * base)    # power-of-two scaling is exact
+    ids_bad = ids.copy()
+    ids_bad[:, 1] = -1
+    wts0 = wts.copy()
+    wts0[:, 1] = 0.0
+    assert np.array_equal(moe_expert(x, ids_bad, wts, w13, c13, w2, c2)["out"],
+                          moe_expert(x, ids, wts0, w13, c13, w2, c2)["out"])
