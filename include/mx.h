@@ -55,6 +55,16 @@ enum { MX_SCALE_BLOCK32X32 = 0, MX_SCALE_ROW1X32 = 1 };
                                     every 32 rows agree (rocm_native, _as_block32_scale)   */
 #define MX_PACK_REQUIRE_BLOCK 2u /* fail with MX_ERR_NOT_BLOCK32 when they do not
                                     (weights942, linear_copy)                              */
+#define MX_PACK_GATE_UP 4u       /* E2M1 only: the weight is a gate / up expert tensor
+                                    [E, 2 I, K/2] with the I gate rows first, then the I up
+                                    rows (weights942, moe_copies); pack it with the halves
+                                    interleaved in 8-row groups (layout MX_LAYOUT_GATE_UP).
+                                    Needs N = 2 I a multiple of 16.                        */
+
+/* mx_packed_weight.layout */
+#define MX_LAYOUT_PLAIN 0
+#define MX_LAYOUT_GATE_UP 1      /* packed row 16 q + i = gate row 8 q + i (i < 8), else
+                                    up row 8 q + i - 8; codes alike                         */
 
 /* mxfp8_linear flags */
 #define MX_LINEAR_NO_FUSED_QUANT 1u /* cluster GEMV: always quantize x in a separate launch
@@ -99,6 +109,7 @@ typedef struct mx_packed_weight {
   uint8_t* codes;
   uint8_t* sf;
   int64_t neg_zero_count; /* -0 nibbles rewritten (E2M1), else 0   */
+  int32_t layout;         /* MX_LAYOUT_* (row order of the packed rows) */
 } mx_packed_weight;
 
 /* Message of the last failed call on this host thread ("" if none). */
@@ -123,7 +134,8 @@ size_t mx_pack_size(int fmt, int E, int N, int K);
  *               (weights942, moe_copies: w13 [E, 2Np, K/2])
  *   codes       [E, codes_rows, K/32] E8M0, codes_rows = N (1x32 rows) or
  *               N/32 (32x32 blocks, weights942 dense_copy: [N/32, K/32])
- *   flags       MX_PACK_* (E4M3 only; E2M1 always keeps per-row codes)
+ *   flags       MX_PACK_FOLD / MX_PACK_REQUIRE_BLOCK (E4M3; E2M1 always keeps
+ *               per-row codes), MX_PACK_GATE_UP (E2M1)
  *   dst/dst_bytes  caller buffer of at least mx_pack_size() bytes, 256-byte aligned
  *   out         filled on success
  * Requirements: K % 32 == 0, N >= 1, E >= 1; codes_rows = N/32 needs N % 32 == 0.
@@ -239,6 +251,32 @@ size_t mxfp4_moe_workspace_size(int T, int topk, int E);
  */
 int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk,
                      const mx_packed_weight* w, void* out, void* workspace,
+                     size_t workspace_bytes, int* dev_status, void* stream);
+
+/* Workspace bytes mxfp4_moe_expert needs (routing, the activation [T*topk, I]
+ * bf16 and the down projection [T*topk, H] f32). */
+size_t mxfp4_moe_expert_workspace_size(int T, int topk, int E, int I, int H);
+
+/*
+ * The routed expert MLP (A16W4 throughout), from the tensors weights942
+ * moe_copies describes -- w13 [E, 2 I, K/2] gate rows then up rows, w2
+ * [E, H, I/2]:
+ *   g, u   = w13_e[:I] x_t, w13_e[I:] x_t        (as mxfp4_moe_linear)
+ *   act    = bf16(silu(g) * u),  silu(v) = v / (1 + e^-v)   (f32, fused into
+ *            the gate/up kernel's epilogue)
+ *   y2     = w2_e act                              (f32, kept in the workspace)
+ *   out[t] = bf16(sum_j topk_weights[t, j] * y2[t, j])  in increasing j, f32;
+ *            slots whose id is not in [0, E) are skipped.
+ * The activation and the combine are not printed on the pages (SiLU-and-mul
+ * and a weighted sum over the top-k slots are the plain reading).
+ *   x [T, K] bf16; topk_ids [T, topk] int32; topk_weights [T, topk] f32;
+ *   w13 packed E2M1 with MX_PACK_GATE_UP (N = 2 I, K = x's K);
+ *   w2 packed E2M1 plain (E alike, N = H, K = I; H a multiple of 4);
+ *   out [T, H] bf16; workspace of mxfp4_moe_expert_workspace_size bytes
+ *   (16-byte aligned); dev_status as in mx_route_experts.
+ */
+int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_weights, int T, int topk,
+                     const mx_packed_weight* w13, const mx_packed_weight* w2, void* out, void* workspace,
                      size_t workspace_bytes, int* dev_status, void* stream);
 
 #ifdef __cplusplus

@@ -18,7 +18,8 @@ MX_ERR_SHAPE, MX_ERR_ALIGN, MX_ERR_ARG, MX_ERR_NOT_BLOCK32, MX_ERR_SCALE = 1, 2,
 MX_ERR_WORKSPACE, MX_ERR_EXPERT_ID, MX_ERR_CUDA, MX_ERR_UNSUPPORTED, MX_ERR_TIMEOUT = 6, 7, 8, 9, 10
 MX_FMT_E4M3, MX_FMT_E2M1 = 0, 1
 MX_SCALE_BLOCK32X32, MX_SCALE_ROW1X32 = 0, 1
-MX_PACK_FOLD, MX_PACK_REQUIRE_BLOCK = 1, 2
+MX_PACK_FOLD, MX_PACK_REQUIRE_BLOCK, MX_PACK_GATE_UP = 1, 2, 4
+MX_LAYOUT_PLAIN, MX_LAYOUT_GATE_UP = 0, 1
 MX_LINEAR_NO_FUSED_QUANT = 1
 MX_LINEAR_CLUSTER_GEMV = 1 << 14
 MX_GEMV_MAX_M = 32
@@ -27,7 +28,7 @@ MX_MAX_EXPERTS = 512
 EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_weights",
             "mx_quantize_act", "mx_dequant", "mxfp8_linear_workspace_size", "mxfp8_linear",
             "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear",
-            "mxfp8_linear_noalloc")
+            "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert")
 
 
 class MxError(RuntimeError):
@@ -40,7 +41,7 @@ class MxPackedWeightC(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("scale_mode", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("K", ctypes.c_int32), ("Kp", ctypes.c_int32),
                 ("bytes", ctypes.c_void_p), ("codes", ctypes.c_void_p), ("sf", ctypes.c_void_p),
-                ("neg_zero_count", ctypes.c_int64)]
+                ("neg_zero_count", ctypes.c_int64), ("layout", ctypes.c_int32)]
 
 
 _lib = None
@@ -75,6 +76,8 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp4_moe_workspace_size": (sz, [i32, i32, i32]),
         "mxfp4_moe_linear": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
+        "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "mxfp4_moe_expert": (i32, [vp, vp, vp, i32, i32, pw, pw, vp, vp, sz, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -278,6 +281,32 @@ def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, o
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(load_library().mxfp4_moe_linear(_ptr(x), _ptr(topk_ids), T, topk, ctypes.byref(w.desc), _ptr(out),
+                                           _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream()))
+    return out
+
+
+def mxfp4_moe_expert_workspace_size(T: int, topk: int, E: int, I: int, H: int) -> int:
+    return int(load_library().mxfp4_moe_expert_workspace_size(T, topk, E, I, H))
+
+
+def mxfp4_moe_expert(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, w13: PackedWeight,
+                     w2: PackedWeight, out: torch.Tensor = None, workspace: torch.Tensor = None,
+                     dev_status: torch.Tensor = None) -> torch.Tensor:
+    """The routed expert MLP: bf16 x [T, K], int32 topk_ids [T, topk], f32
+    topk_weights [T, topk], w13 packed with MX_PACK_GATE_UP, w2 [E, H, I] ->
+    bf16 [T, H] (see include/mx.h)."""
+    _need(x, torch.bfloat16, "x")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    T, topk = topk_ids.shape
+    if out is None:
+        out = torch.empty((T, w2.N), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        need = mxfp4_moe_expert_workspace_size(T, topk, w13.E, w13.N // 2, w2.N)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(load_library().mxfp4_moe_expert(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), T, topk,
+                                           ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(out),
                                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream()))
     return out
 

@@ -206,7 +206,11 @@ int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, 
   const bool blocks_given = !rows_given && N % 32 == 0 && codes_rows == N / 32;
   if (!rows_given && !blocks_given)
     return set_error(MX_ERR_SHAPE, "codes_rows=%d must be N=%d or N/32", codes_rows, N);
-  if (flags & ~(MX_PACK_FOLD | MX_PACK_REQUIRE_BLOCK)) return set_error(MX_ERR_ARG, "unknown pack flags");
+  if (flags & ~(MX_PACK_FOLD | MX_PACK_REQUIRE_BLOCK | MX_PACK_GATE_UP))
+    return set_error(MX_ERR_ARG, "unknown pack flags");
+  const bool gate_up = (flags & MX_PACK_GATE_UP) != 0;
+  if (gate_up && fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "MX_PACK_GATE_UP applies to E2M1 experts");
+  if (gate_up && N % 16 != 0) return set_error(MX_ERR_SHAPE, "MX_PACK_GATE_UP needs N = 2 I a multiple of 16");
   if (!aligned16(bytes) || (reinterpret_cast<uintptr_t>(dst) % kAlign))
     return set_error(MX_ERR_ALIGN, "weight bytes need 16-byte and dst 256-byte alignment");
   const PackRegions R = pack_regions(fmt, E, N, K);
@@ -257,7 +261,8 @@ int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, 
       return cuda_fail(e, "pack e4m3");
   } else {
     w.scale_mode = MX_SCALE_ROW1X32;
-    if ((e = launch_pack_e2m1(bytes, codes, E, N, K, Kp, codes_rows, w.bytes, w.codes, negz, stream)) !=
+    w.layout = gate_up ? MX_LAYOUT_GATE_UP : MX_LAYOUT_PLAIN;
+    if ((e = launch_pack_e2m1(bytes, codes, E, N, K, Kp, codes_rows, gate_up, w.bytes, w.codes, negz, stream)) !=
         cudaSuccess)
       return cuda_fail(e, "pack e2m1");
   }
@@ -434,7 +439,102 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, co
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   if ((e = launch_zero_invalid_pairs(topk_ids, T, topk, w->E, w->N, out, stream)) != cudaSuccess)
     return cuda_fail(e, "zero launch");
-  return launch_moe(x, T, topk, w, offsets, pairs, active, n_active, out, stream);
+  MoeLaunch a = {};
+  a.x = x;
+  a.T = T;
+  a.topk = topk;
+  a.w = w;
+  a.offsets = offsets;
+  a.pairs = pairs;
+  a.active = active;
+  a.n_active = n_active;
+  a.out_mode = 0;
+  a.out = out;
+  return launch_moe(a, stream);
+}
+
+// (internal: static inside the extern "C" block)
+struct ExpertWs {
+  MoeWs route;
+  size_t act, y2, total;
+};
+
+static ExpertWs expert_ws(int T, int topk, int E, int I, int H) {
+  ExpertWs r;
+  r.route = moe_ws(T, topk, E);
+  const size_t P = static_cast<size_t>(T) * topk;
+  r.act = align_up(r.route.total, 256);
+  r.y2 = align_up(r.act + P * static_cast<size_t>(I) * 2, 256);
+  r.total = r.y2 + P * static_cast<size_t>(H) * 4;
+  return r;
+}
+
+size_t mxfp4_moe_expert_workspace_size(int T, int topk, int E, int I, int H) {
+  if (T < 0 || topk < 1 || E < 1 || I < 1 || H < 1) return 0;
+  return expert_ws(T, topk, E, I, H).total;
+}
+
+int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_weights, int T, int topk,
+                     const mx_packed_weight* w13, const mx_packed_weight* w2, void* out, void* workspace,
+                     size_t workspace_bytes, int* dev_status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!w13 || !w2) return set_error(MX_ERR_ARG, "NULL weight");
+  if (w13->fmt != MX_FMT_E2M1 || w2->fmt != MX_FMT_E2M1)
+    return set_error(MX_ERR_ARG, "mxfp4_moe_expert needs E2M1 weights");
+  if (w13->layout != MX_LAYOUT_GATE_UP)
+    return set_error(MX_ERR_ARG, "w13 must be packed with MX_PACK_GATE_UP");
+  if (w2->layout != MX_LAYOUT_PLAIN) return set_error(MX_ERR_ARG, "w2 must be packed without MX_PACK_GATE_UP");
+  const int I = w13->N / 2, H = w2->N, E = w13->E;
+  if (w2->E != E || w2->K != I)
+    return set_error(MX_ERR_SHAPE, "w2 [E=%d, H=%d, K=%d] does not fit w13 [E=%d, 2I=%d]", w2->E, H, w2->K, E,
+                     w13->N);
+  if (H % 4 != 0) return set_error(MX_ERR_SHAPE, "H=%d must be a multiple of 4", H);
+  if (T < 0 || topk < 1) return set_error(MX_ERR_SHAPE, "T=%d topk=%d", T, topk);
+  if (E > MX_MAX_EXPERTS) return set_error(MX_ERR_UNSUPPORTED, "E=%d exceeds %d", E, MX_MAX_EXPERTS);
+  if (T == 0) return MX_OK;
+  if (!x || !topk_ids || !topk_weights || !out || !workspace) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(out) || !aligned16(workspace))
+    return set_error(MX_ERR_ALIGN, "x, out and workspace need 16-byte alignment");
+  const ExpertWs R = expert_ws(T, topk, E, I, H);
+  if (workspace_bytes < R.total)
+    return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, R.total);
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + R.route.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + R.route.offsets);
+  int32_t* pairs = reinterpret_cast<int32_t*>(ws + R.route.pairs);
+  int32_t* active = reinterpret_cast<int32_t*>(ws + R.route.active);
+  int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.route.n_active);
+  int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.route.status);
+  cudaError_t e = launch_route(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "route launch");
+  MoeLaunch a = {};
+  a.T = T;
+  a.topk = topk;
+  a.offsets = offsets;
+  a.pairs = pairs;
+  a.active = active;
+  a.n_active = n_active;
+  // gate / up with SiLU-and-mul fused: act [T * topk, I] bf16
+  a.x = x;
+  a.w = w13;
+  a.x_per_pair = 0;
+  a.out_mode = 1;
+  a.out = ws + R.act;
+  if ((rc = launch_moe(a, stream)) != MX_OK) return rc;
+  // down projection: one activation row a pair, f32 [T * topk, H]
+  a.x = ws + R.act;
+  a.w = w2;
+  a.x_per_pair = 1;
+  a.out_mode = 2;
+  a.out = nullptr;
+  a.out_f32 = ws + R.y2;
+  if ((rc = launch_moe(a, stream)) != MX_OK) return rc;
+  if ((e = launch_combine(reinterpret_cast<const float*>(ws + R.y2), topk_ids, topk_weights, T, topk, E, H, out,
+                          stream)) != cudaSuccess)
+    return cuda_fail(e, "combine launch");
+  return MX_OK;
 }
 
 }  // extern "C"

@@ -114,6 +114,37 @@ __global__ void zero_invalid_pairs_kernel(const int32_t* __restrict__ ids, int P
   for (int n = threadIdx.x & 31; n < N; n += 32) out[static_cast<long long>(p) * N + n] = z;
 }
 
+// out[t, h] = bf16(sum_j w[t, j] y2[t * topk + j, h]) over the slots j with a
+// valid expert id, in increasing j, in f32: one thread per 4 consecutive h.
+__global__ void combine_kernel(const float* __restrict__ y2, const int32_t* __restrict__ ids,
+                               const float* __restrict__ wts, int T, int topk, int E, int H,
+                               __nv_bfloat16* __restrict__ out) {
+  const int H4 = H >> 2;
+  const long long total = static_cast<long long>(T) * H4;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / H4), h = static_cast<int>(i % H4) * 4;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int j = 0; j < topk; ++j) {
+      const int e = ids[t * topk + j];
+      if (e < 0 || e >= E) continue;
+      const float w = wts[t * topk + j];
+      const float4 v = *reinterpret_cast<const float4*>(y2 + static_cast<long long>(t * topk + j) * H + h);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(out + static_cast<long long>(t) * H + h) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+}
+
+constexpr int kMoeOutBf16 = 0;    // out [pairs, N] bf16 (rows in gate-then-up order)
+constexpr int kMoeOutSwiglu = 1;  // out [pairs, N/2] bf16 = silu(gate) * up
+constexpr int kMoeOutF32 = 2;     // out_f32 [pairs, N] f32
+
 constexpr int kMoeWarps = 8;
 constexpr int kMoeRows = kMoeWarps * 16;  // 128 weight rows a CTA
 constexpr int kMoeTok = 16;               // tokens a chunk (two n8 tiles)
@@ -125,14 +156,18 @@ constexpr int kChunkBytes = kMoeTok * kStageK * 2;           // 16 KB of bf16 ac
 constexpr int kMoeSmem = kMoeWarps * kRing * kWarpStageBytes + 2 * kChunkBytes + 1024;
 
 struct MoeParams {
-  const __nv_bfloat16* x;  // [T, K]
+  const __nv_bfloat16* x;  // [T, K] (one row a token) or [T * topk, K] (one row a pair)
   const uint8_t* codes;    // [E, N, Kp/32]
   const int32_t* offsets;
   const int32_t* pairs;
   const int32_t* active;
   const int32_t* n_active;
-  __nv_bfloat16* out;      // [T * topk, N]
+  __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
+  float* out_f32;          // kMoeOutF32: [T * topk, N]
   int topk, N, K, Kp, nsteps;
+  int x_per_pair;          // 1: activation row = pair index (the down projection)
+  int gate_up;             // weight rows interleaved gate / up in 8-row groups
+  int out_mode;
 };
 
 // E8M0 code c of one block -> bf16x2 {2^(c-127), 2^(c-127)}: exponent field c
@@ -175,6 +210,14 @@ MX_DEV uint4 ld_shared_v4(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
+
+// Packed row r of a gate / up interleaved weight -> its row in gate-then-up order.
+MX_DEV int gate_up_row(int r, int N) {
+  const int q = r >> 4, i = r & 15;
+  return i < 8 ? 8 * q + i : (N >> 1) + 8 * q + i - 8;
+}
+
+MX_DEV float silu_f32(float v) { return v / (1.0f + expf(-v)); }
 
 __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                 const MoeParams p) {
@@ -230,7 +273,7 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_con
     if (threadIdx.x < kMoeTok) {
       const int pr = (ch + static_cast<int>(threadIdx.x) < cnt) ? p.pairs[o0 + ch + threadIdx.x] : -1;
       tok_pair[threadIdx.x] = pr;
-      tok_src[threadIdx.x] = pr >= 0 ? pr / p.topk : -1;
+      tok_src[threadIdx.x] = pr >= 0 ? (p.x_per_pair ? pr : pr / p.topk) : -1;
     }
     __syncthreads();
     auto load_x = [&](int st, int buf) {
@@ -316,15 +359,32 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_con
       load_x(st + 2, st & 1);
     }
 
-    // ---- 3. store out[pair, row]
+    // ---- 3. store the chunk's rows: acc[h][0..1] are row rg, [2..3] row rg + 8,
+    // columns (tokens) h * 8 + 2 tq and + 1
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t0 = h * 8 + 2 * tq;
       const int pa = tok_pair[t0], pb = tok_pair[t0 + 1];
-      if (pa >= 0 && v0) p.out[static_cast<long long>(pa) * p.N + rg] = __float2bfloat16_rn(acc[h][0]);
-      if (pb >= 0 && v0) p.out[static_cast<long long>(pb) * p.N + rg] = __float2bfloat16_rn(acc[h][1]);
-      if (pa >= 0 && v1) p.out[static_cast<long long>(pa) * p.N + rg + 8] = __float2bfloat16_rn(acc[h][2]);
-      if (pb >= 0 && v1) p.out[static_cast<long long>(pb) * p.N + rg + 8] = __float2bfloat16_rn(acc[h][3]);
+      if (p.out_mode == kMoeOutSwiglu) {
+        // rows rg (gate) and rg + 8 (up) are gate / up of intermediate index i
+        const int I = p.N >> 1, i = (wrow >> 1) + g;
+        if (pa >= 0 && v1)
+          p.out[static_cast<long long>(pa) * I + i] = __float2bfloat16_rn(silu_f32(acc[h][0]) * acc[h][2]);
+        if (pb >= 0 && v1)
+          p.out[static_cast<long long>(pb) * I + i] = __float2bfloat16_rn(silu_f32(acc[h][1]) * acc[h][3]);
+      } else if (p.out_mode == kMoeOutF32) {
+        if (pa >= 0 && v0) p.out_f32[static_cast<long long>(pa) * p.N + rg] = acc[h][0];
+        if (pb >= 0 && v0) p.out_f32[static_cast<long long>(pb) * p.N + rg] = acc[h][1];
+        if (pa >= 0 && v1) p.out_f32[static_cast<long long>(pa) * p.N + rg + 8] = acc[h][2];
+        if (pb >= 0 && v1) p.out_f32[static_cast<long long>(pb) * p.N + rg + 8] = acc[h][3];
+      } else {
+        const int n0 = p.gate_up ? gate_up_row(rg, p.N) : rg;
+        const int n1 = p.gate_up ? gate_up_row(rg + 8, p.N) : rg + 8;
+        if (pa >= 0 && v0) p.out[static_cast<long long>(pa) * p.N + n0] = __float2bfloat16_rn(acc[h][0]);
+        if (pb >= 0 && v0) p.out[static_cast<long long>(pb) * p.N + n0] = __float2bfloat16_rn(acc[h][1]);
+        if (pa >= 0 && v1) p.out[static_cast<long long>(pa) * p.N + n1] = __float2bfloat16_rn(acc[h][2]);
+        if (pb >= 0 && v1) p.out[static_cast<long long>(pb) * p.N + n1] = __float2bfloat16_rn(acc[h][3]);
+      }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();  // tok_* and the buffers are reused by the next chunk of tokens
@@ -353,10 +413,28 @@ cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E
   return cudaGetLastError();
 }
 
-int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const int32_t* offsets,
-               const int32_t* pairs, const int32_t* active, const int32_t* n_active, void* out,
-               cudaStream_t stream) {
+cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts, int T, int topk, int E, int H,
+                           void* out, cudaStream_t stream) {
+  const long long total = static_cast<long long>(T) * (H / 4);
+  combine_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(y2, ids, wts, T, topk, E, H,
+                                                             static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
+  const mx_packed_weight* w = a.w;
+  const void* x = a.x;
+  const int T = a.T, topk = a.topk;
   MoeParams p = {};
+  p.x_per_pair = a.x_per_pair;
+  p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
+  p.out_mode = a.out_mode;
+  p.out_f32 = static_cast<float*>(a.out_f32);
+  const int32_t* offsets = a.offsets;
+  const int32_t* pairs = a.pairs;
+  const int32_t* active = a.active;
+  const int32_t* n_active = a.n_active;
+  void* out = a.out;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.codes = w->codes;
   p.offsets = offsets;
@@ -369,13 +447,19 @@ int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const 
   p.K = w->K;
   p.Kp = w->Kp;
   p.nsteps = w->Kp / 128;
+  // a 128-byte weight box per row and step: rows of at least 128 packed bytes
+  if (w->Kp < 256) return set_error(MX_ERR_UNSUPPORTED, "MXFP4 experts need K > 128 (K = %d)", w->K);
   CUtensorMap wmap;
   const int KHp = w->Kp / 2;
   int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, KHp,
                                 static_cast<uint64_t>(w->E) * w->N, KHp, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != MX_OK) return rc;
-  cudaError_t e = cudaFuncSetAttribute(moe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoeSmem);
-  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe: smem attribute: %s", cudaGetErrorString(e));
+  DeviceInfo di;
+  if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
+  static int smem_set[64];
+  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel), kMoeSmem, di, smem_set) != MX_OK)
+    return MX_ERR_CUDA;
+  cudaError_t e;
   const long long P = static_cast<long long>(T) * topk;
   const int zmax = static_cast<int>(P < w->E ? P : w->E);
   dim3 grid((w->N + kMoeRows - 1) / kMoeRows, zmax, 1);

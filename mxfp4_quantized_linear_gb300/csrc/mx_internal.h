@@ -24,6 +24,13 @@ struct DeviceInfo {
 };
 int current_device_info(DeviceInfo* out);
 
+// Grid size for a grid-stride loop over `items` with `per_block` threads a block.
+inline int blocks_for(long long items, int per_block) {
+  long long g = (items + per_block - 1) / per_block;
+  if (g > 65535LL * 8) g = 65535LL * 8;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `func` on the current
 // device only when `bytes` exceeds what an earlier call set there (`cache`:
 // one slot per device ordinal, owned by the caller's translation unit).
@@ -54,7 +61,7 @@ cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, 
                              int Kp, int codes_rows, bool block_out, uint8_t* wq,
                              uint8_t* codes_out, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
-                             int Kp, int codes_rows, uint8_t* wq, uint8_t* codes_out,
+                             int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
                              unsigned long long* negz, cudaStream_t stream);
 
 // ---- decode GEMV (gemv.cu)
@@ -104,9 +111,19 @@ unsigned int take_error_flags_gemm();
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
                          int* dev_status, cudaStream_t stream);
-int launch_moe(const void* x, int T, int topk, const mx_packed_weight* w, const int32_t* offsets,
-               const int32_t* pairs, const int32_t* active, const int32_t* n_active, void* out,
-               cudaStream_t stream);
+struct MoeLaunch {
+  const void* x;               // bf16 [T, K] (x_per_pair = 0) or [T * topk, K] (x_per_pair = 1)
+  int T, topk;
+  const mx_packed_weight* w;
+  const int32_t *offsets, *pairs, *active, *n_active;  // routing (mx_route_experts)
+  int x_per_pair;
+  int out_mode;                // 0: out bf16 [pairs, N]; 1: out bf16 [pairs, N/2] = silu(gate) * up; 2: out_f32
+  void* out;
+  void* out_f32;               // f32 [pairs, N]
+};
+int launch_moe(const MoeLaunch& a, cudaStream_t stream);
+cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts, int T, int topk, int E, int H,
+                           void* out, cudaStream_t stream);
 cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E, int N, void* out,
                                       cudaStream_t stream);
 

@@ -21,10 +21,11 @@ namespace {
 constexpr uint8_t kPadCode = 128;
 constexpr uint8_t kPadRowCode = 127;
 
-int blocks_for(long long items, int per_block) {
-  long long g = (items + per_block - 1) / per_block;
-  if (g > 65535LL * 8) g = 65535LL * 8;
-  return g < 1 ? 1 : static_cast<int>(g);
+// Packed row r of a gate / up interleaved expert -> its source row (gate rows
+// first, then up rows): 8-row groups alternate gate and up.
+__device__ __forceinline__ int gate_up_src_row(int r, int N) {
+  const int q = r >> 4, i = r & 15;
+  return i < 8 ? 8 * q + i : (N >> 1) + 8 * q + i - 8;
 }
 
 // status bit 0: a code is 255; bit 1: some row differs from its 32-row group's first row.
@@ -72,7 +73,7 @@ __device__ __forceinline__ uint8_t src_row_code(const uint8_t* codes, int e, int
 
 // Compact codes: block mode [E, N/32, KBp] (first row of each group), row mode [E, N, KBp].
 __global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int E, int N, int KB, int KBp,
-                                  int codes_rows, int block_out, uint8_t* __restrict__ out) {
+                                  int codes_rows, int block_out, int gate_up, uint8_t* __restrict__ out) {
   const int orows = block_out ? (N >> 5) : N;
   const long long total = static_cast<long long>(E) * orows * KBp;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -81,7 +82,7 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int E, int 
     const long long er = i / KBp;
     const int r = static_cast<int>(er % orows);
     const int e = static_cast<int>(er / orows);
-    const int n = block_out ? (r << 5) : r;
+    const int n = block_out ? (r << 5) : (gate_up ? gate_up_src_row(r, N) : r);
     out[i] = j < KB ? src_row_code(codes, e, n, j, N, KB, codes_rows) : kPadCode;
   }
 }
@@ -137,8 +138,8 @@ __device__ __forceinline__ uint32_t nibble_slot_shuffle(uint32_t w) {
 
 // E2M1 bytes [E, N, K/2] -> [E, N, Kp/2]; per 64-byte chunk, output word 4 w + b
 // holds input word (block b, word w), nibble-shuffled.  One thread per output word.
-__global__ void pack_e2m1_bytes_kernel(const uint8_t* __restrict__ in, long long rows, int KH,
-                                       int KHp, uint8_t* __restrict__ out,
+__global__ void pack_e2m1_bytes_kernel(const uint8_t* __restrict__ in, long long rows, int N, int gate_up,
+                                       int KH, int KHp, uint8_t* __restrict__ out,
                                        unsigned long long* negz) {
   const int words = KHp >> 2;
   const long long total = rows * words;
@@ -146,6 +147,7 @@ __global__ void pack_e2m1_bytes_kernel(const uint8_t* __restrict__ in, long long
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long r = i / words;
+    const long long rs = gate_up ? (r / N) * N + gate_up_src_row(static_cast<int>(r % N), N) : r;
     const int o = static_cast<int>(i % words);  // output word index in the row
     const int chunk = o >> 4;
     const int ow = o & 15;
@@ -154,7 +156,7 @@ __global__ void pack_e2m1_bytes_kernel(const uint8_t* __restrict__ in, long long
     uint32_t v = 0u;
     if (src < KH)
       v = nibble_slot_shuffle(
-          drop_negative_zero_word(*reinterpret_cast<const uint32_t*>(in + r * KH + src), &count));
+          drop_negative_zero_word(*reinterpret_cast<const uint32_t*>(in + rs * KH + src), &count));
     *reinterpret_cast<uint32_t*>(out + r * KHp + o * 4) = v;
   }
   // warp-reduce the -0 count, one atomic a warp (integer: order-independent)
@@ -181,22 +183,22 @@ cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, 
   const int KB = K >> 5, KBp = Kp >> 5;
   const long long ncodes = static_cast<long long>(E) * (block_out ? N / 32 : N) * KBp;
   pack_codes_kernel<<<blocks_for(ncodes, 256), 256, 0, stream>>>(codes, E, N, KB, KBp, codes_rows,
-                                                                 block_out ? 1 : 0, codes_out);
+                                                                 block_out ? 1 : 0, 0, codes_out);
   const long long nsf = static_cast<long long>(E) * ((N + 127) / 128) * (Kp / 128) * 512;
   pack_sf_kernel<<<blocks_for(nsf, 256), 256, 0, stream>>>(codes, E, N, KB, Kp, codes_rows, sf);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
-                             int Kp, int codes_rows, uint8_t* wq, uint8_t* codes_out,
+                             int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
                              unsigned long long* negz, cudaStream_t stream) {
   const long long rows = static_cast<long long>(E) * N;
   pack_e2m1_bytes_kernel<<<blocks_for(rows * (Kp >> 3), 256), 256, 0, stream>>>(
-      bytes, rows, K >> 1, Kp >> 1, wq, negz);
+      bytes, rows, N, gate_up ? 1 : 0, K >> 1, Kp >> 1, wq, negz);
   const int KB = K >> 5, KBp = Kp >> 5;
   const long long ncodes = static_cast<long long>(E) * N * KBp;
   pack_codes_kernel<<<blocks_for(ncodes, 256), 256, 0, stream>>>(codes, E, N, KB, KBp, codes_rows,
-                                                                 0, codes_out);
+                                                                 0, gate_up ? 1 : 0, codes_out);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,24 @@ def moe_gate_up(E: int = 64, N: int = 4096, K: int = 4096, T: int = 64, topk: in
             "T": T, "topk": topk}
 
 
+def moe_expert(E: int = 64, I: int = 2048, H: int = 4096, T: int = 64, topk: int = 8,
+               code_lo: int = 122, code_hi: int = 130, seed: int = 0, device=None) -> dict:
+    """MXFP4 routed expert MLP: w13 [E, 2 I, H/2] (gate rows, then up rows) and
+    w2 [E, H, I/2] with per-row codes, x [T, H], top-k ids and routing weights
+    (uniform draws, each token's row divided by its sum)."""
+    g = generator(seed, device)
+    w13 = fp4x2_bytes((E, 2 * I, H // 2), g)
+    c13 = e8m0_codes((E, 2 * I, H // 32), code_lo, code_hi, g)
+    w2 = fp4x2_bytes((E, H, I // 2), g)
+    c2 = e8m0_codes((E, H, I // 32), code_lo, code_hi, g)
+    x = bf16_normal((T, H), g)
+    ids = topk_ids(T, E, topk, g)
+    u = torch.rand((T, topk), generator=g, dtype=torch.float32, device=g.device)
+    wts = u / u.sum(dim=1, keepdim=True)
+    return {"w13": w13, "c13": c13, "w2": w2, "c2": c2, "x": x, "ids": ids, "weights": wts,
+            "E": E, "I": I, "H": H, "T": T, "topk": topk}
+
+
 def prefill_gemm(M: int = 4096, N: int = 7168, K: int = 7168, seed: int = 0) -> dict:
     """MXFP8 prefill GEMM: bf16 x [M, K], e4m3 W [N, K], 32x32 codes 118..132."""
     g = generator(seed)

@@ -112,3 +112,118 @@ def test_moe_gate_up_full_size_sampled():
         ref = Wd @ xv[t]
         err = normalized_error(y[t, j, ns][None], ref[None], xv[t][None], Wd)
         assert err <= TOL, (t, j, err)
+
+
+# ---------------------------------------------------------------- full expert
+
+def test_moe_linear_on_gate_up_packing_is_identical():
+    """The interleaved packing only moves rows: every output of mxfp4_moe_linear
+    is bit-identical to the plain packing's."""
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_gate_up(E=6, N=192, K=1056, T=11, topk=3, seed=5)
+    x, ids = m["x"].to(dev), m["ids"].to(dev)
+    pp = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1", 0)
+    pg = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1", mx.MX_PACK_GATE_UP)
+    yp, yg = mx.mxfp4_moe_linear(x, ids, pp), mx.mxfp4_moe_linear(x, ids, pg)
+    torch.cuda.synchronize()
+    assert torch.equal(yp.view(torch.int16), yg.view(torch.int16))
+
+
+def expert_error(out, ref, t, h, x_unused=None):
+    """|out - out_ref| / sum_j |w_tj| ||W2[e_j, h]|| ||act_tj||: the normalised
+    error of the combine (Cauchy-Schwarz bound of each slot's term)."""
+    return abs(out - ref["out"][t, h]) / ref["den"][t, h] if ref["den"][t, h] > 0 else abs(out - ref["out"][t, h])
+
+
+def oracle_expert(m, ids=None):
+    from oracle.moe import moe_expert
+    ids = u8(m["ids"] if ids is None else ids)
+    r = moe_expert(bf16_np(m["x"]), ids, m["weights"].cpu().numpy().astype(np.float64), u8(m["w13"]),
+                   u8(m["c13"]), u8(m["w2"]), u8(m["c2"]))
+    W2 = dequant_experts_bf16(u8(m["w2"]), u8(m["c2"]))
+    T, topk = ids.shape
+    den = np.zeros_like(r["out"])
+    for t in range(T):
+        for j in range(topk):
+            e = int(ids[t, j])
+            if 0 <= e < m["E"]:
+                den[t] += abs(float(m["weights"][t, j])) * np.linalg.norm(W2[e], axis=1) * np.linalg.norm(r["act"][t, j])
+    r["den"] = den
+    return r
+
+
+def gpu_expert(m, ids=None, status=None):
+    dev = cuda_device()
+    ensure_built()
+    w13 = mx.mx_pack_weights(m["w13"].to(dev), m["c13"].to(dev), "e2m1", mx.MX_PACK_GATE_UP)
+    w2 = mx.mx_pack_weights(m["w2"].to(dev), m["c2"].to(dev), "e2m1", 0)
+    ids = m["ids"] if ids is None else ids
+    y = mx.mxfp4_moe_expert(m["x"].to(dev), ids.to(dev), m["weights"].to(dev), w13, w2, dev_status=status)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("E,I,H,T,topk", [(8, 160, 256, 13, 3), (5, 192, 160, 9, 2), (4, 256, 2080, 33, 4)])
+def test_expert_matches_oracle(E, I, H, T, topk):
+    m = inputs.moe_expert(E=E, I=I, H=H, T=T, topk=topk, seed=E + I)
+    ids = m["ids"].clone()
+    ids[T // 2, 0] = -1                  # a skipped slot
+    y = gpu_expert(m, ids)
+    ref = oracle_expert(m, ids)
+    err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
+    assert err <= TOL, err
+
+
+def test_expert_invalid_id_status():
+    dev = cuda_device()
+    m = inputs.moe_expert(E=4, I=160, H=256, T=5, topk=2, seed=1)
+    ids = m["ids"].clone()
+    ids[2, 1] = 77
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    y = gpu_expert(m, ids, status)
+    assert int(status.item()) == MX_ERR_EXPERT_ID
+    ref = oracle_expert(m, ids)
+    assert np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0)) <= TOL
+
+
+def test_expert_refuses_plain_w13():
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_expert(E=2, I=160, H=256, T=2, topk=1, seed=2)
+    w13 = mx.mx_pack_weights(m["w13"].to(dev), m["c13"].to(dev), "e2m1", 0)
+    w2 = mx.mx_pack_weights(m["w2"].to(dev), m["c2"].to(dev), "e2m1", 0)
+    with pytest.raises(mx.MxError):
+        mx.mxfp4_moe_expert(m["x"].to(dev), m["ids"].to(dev), m["weights"].to(dev), w13, w2)
+
+
+def test_expert_full_size_sampled_tokens():
+    """E=64, I=2048, H=4096, T=64, top-8 (the gate/up GEMM of the bench, then
+    SwiGLU, the down projection and the combine): two tokens checked in full."""
+    from oracle.moe import silu
+    m = inputs.moe_expert()
+    y = gpu_expert(m)
+    xv, ids, wts = bf16_np(m["x"]), u8(m["ids"]), m["weights"].numpy().astype(np.float64)
+    I = m["I"]
+    for t in (0, 37):
+        out = np.zeros(m["H"])
+        den = np.zeros(m["H"])
+        for j in range(m["topk"]):
+            e = int(ids[t, j])
+            W13 = bf16_value(bf16_rne_bits(dequant_values(u8(m["w13"][e]), u8(m["c13"][e]), "e2m1", 2 * I, m["H"])))
+            y13 = W13 @ xv[t]
+            act = bf16_value(bf16_rne_bits(silu(y13[:I]) * y13[I:]))
+            W2 = bf16_value(bf16_rne_bits(dequant_values(u8(m["w2"][e]), u8(m["c2"][e]), "e2m1", m["H"], I)))
+            out += wts[t, j] * (W2 @ act)
+            den += abs(wts[t, j]) * np.linalg.norm(W2, axis=1) * np.linalg.norm(act)
+        err = np.max(np.abs(y[t] - out) / den)
+        assert err <= TOL, (t, err)
+
+
+def test_moe_refuses_short_expert_rows():
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_gate_up(E=2, N=64, K=128, T=3, topk=1, seed=6)
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    with pytest.raises(mx.MxError):
+        mx.mxfp4_moe_linear(m["x"].to(dev), m["ids"].to(dev), p)

@@ -98,3 +98,28 @@ def test_e2m1_block_codes_expand():
 def test_e2m1_moe_full_size_sampled_experts():
     m = inputs.moe_gate_up(T=1)
     check_e2m1(m["w"], m["codes"], experts=[0, 17, 63])
+
+
+def test_e2m1_gate_up_interleave():
+    g = inputs.generator(6)
+    w = inputs.fp4x2_bytes((3, 96, 1040), g)          # 2 I = 96, ragged K = 2080
+    c = inputs.e8m0_codes((3, 96, 65), 122, 130, g)
+    p = gpu_pack(w, c, "e2m1", mx.MX_PACK_GATE_UP)
+    ref = L.pack_e2m1(u8(w), u8(c), gate_up=True)
+    assert p.desc.layout == mx.MX_LAYOUT_GATE_UP
+    assert np.array_equal(u8(p.bytes_tensor()), ref["wq"])
+    assert np.array_equal(u8(p.codes_tensor()), ref["codes"])
+    assert p.neg_zero_count == ref["neg_zero_count"]
+    plain = gpu_pack(w, c, "e2m1", 0)
+    assert plain.desc.layout == mx.MX_LAYOUT_PLAIN
+
+
+def test_gate_up_flag_refusals():
+    g = inputs.generator(7)
+    w = inputs.fp4x2_bytes((1, 40, 64), g)
+    c = inputs.e8m0_codes((1, 40, 4), 122, 130, g)
+    with pytest.raises(mx.MxError):
+        gpu_pack(w, c, "e2m1", mx.MX_PACK_GATE_UP)           # 2 I = 40 is not a multiple of 16
+    with pytest.raises(mx.MxError):
+        gpu_pack(inputs.e4m3_bytes((64, 128), g), inputs.e8m0_codes((2, 4), 120, 130, g), "e4m3",
+                 mx.MX_PACK_GATE_UP)                          # E4M3 weights have no gate / up form
