@@ -16,9 +16,14 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
   plus an optional bias added after the product (``apply_weights``).  The sum
   is taken by a float64 matrix product of the exactly dequantized operands.
 
+``mxfp8_linear_q`` is the same product on an activation given already
+quantized (rocm_native, apply_weights: QuantizedActivation, row-major
+[M, K/32] E8M0 scales); ``mxfp8_linear`` quantizes first, then calls it.
+
 Pinned by tests/test_oracle_linear.py: exact rational (Fraction) brute force on
-tiny shapes, the one-hot / all-ones special cases, and invariance under
-permuting 32-wide K chunks together with their code columns.
+tiny shapes (from bf16 activations and from arbitrary e4m3 bytes and codes),
+the one-hot / all-ones special cases, and invariance under permuting 32-wide K
+chunks together with their code columns.
 """
 import numpy as np
 
@@ -52,23 +57,37 @@ def dequant_bf16(w_bytes, codes, fmt: str, N: int, K: int) -> np.ndarray:
     return bf16_rne_bits(dequant_values(w_bytes, codes, fmt, N, K))
 
 
-def mxfp8_linear(x, w_bytes, w_codes, bias=None) -> dict:
-    """x: fp64 [M, K] (bf16 values); w_bytes [N, K] e4m3; w_codes block
-    [N/32, K/32] or row [N, K/32]; bias fp64 [N] or None.
+def mxfp8_linear_q(xq, xcodes, w_bytes, w_codes, bias=None) -> dict:
+    """The linear on an activation that arrives already MXFP8-quantized
+    (rocm_native, apply_weights: a QuantizedActivation with row-major
+    [M, K/32] E8M0 scales, input_quant_key): xq [M, K] e4m3 bytes, xcodes
+    [M, K/32]; weight and bias as in mxfp8_linear.
 
-    Returns dict(y=[M, N] fp64, xq, xcodes, A=[M, K] dequantized activation,
-    B=[N, K] dequantized weight)."""
-    x = np.asarray(x, dtype=np.float64)
-    M, K = x.shape
+    Returns dict(y=[M, N] fp64, A=[M, K] dequantized activation, B)."""
+    xq = np.asarray(xq, dtype=np.uint8)
+    M, K = xq.shape
     w_bytes = np.asarray(w_bytes, dtype=np.uint8)
     N = w_bytes.shape[0]
-    xq, xcodes = quantize_act(x)
     A = e4m3_decode(xq) * expand_codes(xcodes, M, K)
     B = dequant_values(w_bytes, w_codes, "e4m3", N, K)
     y = A @ B.T
     if bias is not None:
         y = y + np.asarray(bias, dtype=np.float64)[None, :]
-    return {"y": y, "xq": xq, "xcodes": xcodes, "A": A, "B": B}
+    return {"y": y, "A": A, "B": B}
+
+
+def mxfp8_linear(x, w_bytes, w_codes, bias=None) -> dict:
+    """x: fp64 [M, K] (bf16 values); w_bytes [N, K] e4m3; w_codes block
+    [N/32, K/32] or row [N, K/32]; bias fp64 [N] or None.  The activation is
+    quantized per token first, then multiplied as in mxfp8_linear_q.
+
+    Returns dict(y=[M, N] fp64, xq, xcodes, A=[M, K] dequantized activation,
+    B=[N, K] dequantized weight)."""
+    x = np.asarray(x, dtype=np.float64)
+    xq, xcodes = quantize_act(x)
+    r = mxfp8_linear_q(xq, xcodes, w_bytes, w_codes, bias)
+    r.update(xq=xq, xcodes=xcodes)
+    return r
 
 
 def normalized_error(y, y_ref, A, B) -> float:

@@ -147,3 +147,24 @@ def test_normalized_error_measure():
     y_ref = A @ B.T
     y = y_ref + np.array([[0.5, 1.0]])
     assert normalized_error(y, y_ref, A, B) == max(0.5 / 5.0, 1.0 / 10.0)
+
+
+def test_prequantized_linear_matches_rational_brute_force():
+    """Arbitrary e4m3 activation bytes (NaN codes excluded) and codes across the
+    E8M0 range, with row codes on the weight: exact rational sums."""
+    from oracle.linear import mxfp8_linear_q
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 5, 96
+    xq = rand_e4m3(rng, (M, K))
+    xc = rng.integers(100, 150, size=(M, K // 32)).astype(np.uint8)
+    w = rand_e4m3(rng, (N, K))
+    wc = rng.integers(110, 140, size=(N, K // 32)).astype(np.uint8)
+    y = mxfp8_linear_q(xq, xc, w, wc)["y"]
+    xv, wv = torch_e4m3(xq), torch_e4m3(w)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += (Fraction(xv[m, k]) * Fraction(2) ** (int(xc[m, k // 32]) - 127)
+                        * Fraction(wv[n, k]) * Fraction(2) ** (int(wc[n, k // 32]) - 127))
+            assert abs(float(acc) - y[m, n]) <= 1e-12 * max(1.0, abs(float(acc)))
