@@ -197,6 +197,27 @@ size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
 int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
                  unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes mxfp8_linear_q needs for M tokens on weight w (the
+ * activation's scale-factor atoms for the GEMM when M > MX_GEMV_MAX_M, else 0). */
+size_t mxfp8_linear_q_workspace_size(int M, const mx_packed_weight* w);
+
+/*
+ * mxfp8_linear on an activation that arrives already MXFP8-quantized
+ * (rocm_native, apply_weights / input_quant_key: a QuantizedActivation with
+ * row-major, not swizzled, [M, K/32] E8M0 scales):
+ *   y[m, n] = sum_b 2^(cw[n,b]-127) 2^(cx[m,b]-127) sum_{k in b} W[n,k] xq[m,k]
+ * accumulated in fp32, bias added in fp32, rounded once to bf16.
+ *   xq     [M, K] e4m3 bytes row-major (16-byte aligned)
+ *   xcodes [M, K/32] E8M0 codes row-major
+ *   w, bias, out as in mxfp8_linear; flags must be 0;
+ *   workspace of mxfp8_linear_q_workspace_size(M, w) bytes (16-byte aligned).
+ * Given (xq, xcodes) = mx_quantize_act(x), the result is bit-identical to
+ * mxfp8_linear(x).  M <= MX_GEMV_MAX_M runs the decode GEMV, larger M the GEMM
+ * reading xq in place.
+ */
+int mxfp8_linear_q(const uint8_t* xq, const uint8_t* xcodes, int M, const mx_packed_weight* w, const void* bias,
+                   void* out, unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Scratch-free decode linear.  The source pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory or pass a

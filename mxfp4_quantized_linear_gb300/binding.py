@@ -28,7 +28,8 @@ MX_MAX_EXPERTS = 512
 EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_weights",
             "mx_quantize_act", "mx_dequant", "mxfp8_linear_workspace_size", "mxfp8_linear",
             "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear",
-            "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert")
+            "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert",
+            "mxfp8_linear_q_workspace_size", "mxfp8_linear_q")
 
 
 class MxError(RuntimeError):
@@ -77,6 +78,8 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp4_moe_linear": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
         "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "mxfp8_linear_q_workspace_size": (sz, [i32, pw]),
+        "mxfp8_linear_q": (i32, [vp, vp, i32, pw, vp, vp, u, vp, sz, vp]),
         "mxfp4_moe_expert": (i32, [vp, vp, vp, i32, i32, pw, pw, vp, vp, sz, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -226,6 +229,28 @@ def mxfp8_linear(x: torch.Tensor, w: PackedWeight, bias: torch.Tensor = None, ou
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check(load_library().mxfp8_linear(_ptr(x), M, ctypes.byref(w.desc), _ptr(bias), _ptr(out), flags,
                                        _ptr(workspace), ws_bytes, _stream()))
+    return out
+
+
+def mxfp8_linear_q(xq: torch.Tensor, xcodes: torch.Tensor, w: PackedWeight, bias: torch.Tensor = None,
+                   out: torch.Tensor = None, workspace: torch.Tensor = None) -> torch.Tensor:
+    """Pre-quantized activation: e4m3 bytes xq uint8 [M, K] and row-major E8M0
+    codes uint8 [M, K/32] @ w^T (+ bias) -> bf16 [M, N]."""
+    _need(xq, torch.uint8, "xq")
+    _need(xcodes, torch.uint8, "xcodes")
+    M = xq.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=xq.device)
+    _need(out, torch.bfloat16, "out")
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias")
+    if workspace is None:
+        need = int(load_library().mxfp8_linear_q_workspace_size(M, ctypes.byref(w.desc)))
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=xq.device)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(load_library().mxfp8_linear_q(_ptr(xq), _ptr(xcodes), M, ctypes.byref(w.desc), _ptr(bias), _ptr(out), 0,
+                                         _ptr(workspace), ws_bytes, _stream()))
     return out
 
 

@@ -394,6 +394,54 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
   return MX_OK;
 }
 
+size_t mxfp8_linear_q_workspace_size(int M, const mx_packed_weight* w) {
+  if (!w || M <= MX_GEMV_MAX_M) return 0;
+  return static_cast<size_t>((M + 127) / 128) * (w->Kp / 128) * 512;
+}
+
+int mxfp8_linear_q(const uint8_t* xq, const uint8_t* xcodes, int M, const mx_packed_weight* w, const void* bias,
+                   void* out, unsigned flags, void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!w) return set_error(MX_ERR_ARG, "NULL weight");
+  if (w->fmt != MX_FMT_E4M3 || w->E != 1) return set_error(MX_ERR_ARG, "mxfp8_linear_q needs a dense E4M3 weight");
+  if (flags != 0) return set_error(MX_ERR_ARG, "mxfp8_linear_q takes no flags");
+  if (M < 0) return set_error(MX_ERR_SHAPE, "M=%d", M);
+  if (M == 0) return MX_OK;
+  if (!xq || !xcodes || !out) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(xq) || !aligned16(out) || (bias && !aligned16(bias)))
+    return set_error(MX_ERR_ALIGN, "xq, out and bias need 16-byte alignment");
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  if (M <= MX_GEMV_MAX_M) {
+    TcGemvArgs g = {};
+    g.w = w;
+    g.xq = xq;
+    g.xcodes = xcodes;
+    g.bias = bias;
+    g.out = out;
+    g.M = M;
+    return launch_gemv_tc(g, stream);
+  }
+  const size_t need = mxfp8_linear_q_workspace_size(M, w);
+  if (!workspace || workspace_bytes < need)
+    return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, need);
+  if (!aligned16(workspace)) return set_error(MX_ERR_ALIGN, "workspace needs 16-byte alignment");
+  uint8_t* sfa = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_act_sf_atoms(xcodes, M, w->K, w->Kp, sfa, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scale atoms launch");
+  GemmArgs g = {};
+  g.w = w;
+  g.xq = xq;          // [M, K]: rows past M and columns past K read as zeros
+  g.xq_rows = M;
+  g.xq_cols = w->K;
+  g.xq_ld = w->K;
+  g.sfa = sfa;
+  g.bias = bias;
+  g.out = out;
+  g.M = M;
+  return launch_gemm(g, stream);
+}
+
 int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* counts,
                      int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
                      int* dev_status, void* stream) {

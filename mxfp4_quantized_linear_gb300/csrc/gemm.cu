@@ -225,7 +225,9 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.n_tiles = (w->N + BN - 1) / BN;
   const int Mp = p.m_tiles * BM;
   CUtensorMap amap, bmap;
-  int rc = encode_tensor_map_2d(&amap, a.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, Mp, w->Kp, BKB, BM,
+  const uint64_t a_cols = a.xq_cols ? a.xq_cols : w->Kp, a_rows = a.xq_rows ? a.xq_rows : Mp;
+  const uint64_t a_ld = a.xq_ld ? a.xq_ld : w->Kp;
+  int rc = encode_tensor_map_2d(&amap, a.xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_cols, a_rows, a_ld, BKB, BM,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != MX_OK) return rc;
   rc = encode_tensor_map_2d(&bmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, BKB, BN,

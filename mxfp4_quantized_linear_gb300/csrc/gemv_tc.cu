@@ -52,6 +52,8 @@ constexpr uint32_t kIdesc16 = mxf8_idesc(kRows, 16);  // 1..16 tokens: half the 
 struct TcGemvParams {
   const uint8_t* sfw;          // weight scale atoms [RT][KT][512]
   const __nv_bfloat16* x;      // [M, K]
+  const uint8_t* xq;           // pre-quantized activation [M, K] e4m3, or null (quantize x here)
+  const uint8_t* xcodes;       // its E8M0 codes [M, K/32] row-major
   const __nv_bfloat16* bias;   // [N] or null
   __nv_bfloat16* out;          // [M, N]
   int M, N, K, KT, splits, ring;
@@ -218,7 +220,23 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
     const int mrows = p.M;
     const int items = ns * mrows * 16;
     const int mmul = (65536 + mrows - 1) / mrows;
-    for (int b0 = (et & ~31); b0 < items; b0 += 128 * kXBatch) {
+    if (p.xq != nullptr) {
+      // the activation arrives quantized: copy its bytes and codes into place
+      for (int it = et; it < items; it += 128) {
+        const int row = it >> 4, step = (row * mmul) >> 16, t = row - step * mrows, g8 = it & 15;
+        const int col = (st0 + step) * kStepB + g8 * 8;
+        uint2 v = make_uint2(0u, 0u);
+        uint8_t code = 0;
+        if (col < p.K) {
+          v = __ldcg(reinterpret_cast<const uint2*>(p.xq + static_cast<long long>(t) * p.K + col));
+          code = p.xcodes[static_cast<long long>(t) * (p.K >> 5) + (col >> 5)];
+        }
+        const int c = g8 >> 1;  // 16-byte chunk of the 128-byte row, 128B swizzle
+        *reinterpret_cast<uint2*>(smem + L.xq + step * kXq + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) = v;
+        if ((g8 & 3) == 0) smem[L.sfx + step * 512 + t * 16 + (g8 >> 2)] = code;
+      }
+    }
+    for (int b0 = (et & ~31); b0 < items && p.xq == nullptr; b0 += 128 * kXBatch) {
       uint4 u[kXBatch];
 #pragma unroll
       for (int j = 0; j < kXBatch; ++j) {
@@ -353,6 +371,8 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   TcGemvParams p = {};
   p.sfw = w->sf;
   p.x = static_cast<const __nv_bfloat16*>(a.x);
+  p.xq = a.xq;
+  p.xcodes = a.xcodes;
   p.bias = static_cast<const __nv_bfloat16*>(a.bias);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.M = a.M;
@@ -372,7 +392,8 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   const int smem = (L.total + 1024 > kMinSmem) ? L.total + 1024 : kMinSmem;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)
     return set_error(MX_ERR_UNSUPPORTED, "gemv: %d K steps a CTA (%d bytes of shared memory) is too many", steps, smem);
-  if (reinterpret_cast<uintptr_t>(a.x) % 16 != 0) return set_error(MX_ERR_ALIGN, "gemv: x needs 16-byte alignment");
+  if (reinterpret_cast<uintptr_t>(a.xq ? static_cast<const void*>(a.xq) : a.x) % 16 != 0)
+    return set_error(MX_ERR_ALIGN, "gemv: the activation needs 16-byte alignment");
   CUtensorMap wmap;
   const int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, kStepB,
                                       kRows, CU_TENSOR_MAP_SWIZZLE_128B);

@@ -60,6 +60,9 @@ cudaError_t launch_pack_check_codes(const uint8_t* codes, int E, int rows, int K
 cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
                              int Kp, int codes_rows, bool block_out, uint8_t* wq,
                              uint8_t* codes_out, uint8_t* sf, cudaStream_t stream);
+// Activation scale atoms [ceil(M/128), Kp/128, 512] from row-major codes [M, K/32]
+// (127 past M, 128 past K), the layout the GEMM's tensor-memory copy reads.
+cudaError_t launch_act_sf_atoms(const uint8_t* codes, int M, int K, int Kp, uint8_t* sf, cudaStream_t stream);
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
                              int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
                              unsigned long long* negz, cudaStream_t stream);
@@ -88,6 +91,8 @@ struct TcGemvArgs {
   const void* bias;  // bf16 [N] or NULL
   void* out;         // bf16 [M, N]
   int M;             // 1..32
+  const uint8_t* xq;      // pre-quantized activation [M, K] e4m3 (x unused), or NULL
+  const uint8_t* xcodes;  // its codes [M, K/32]
   int force_splits;  // 0 = heuristic
   int force_ring;    // 0 = default weight ring depth
 };
@@ -98,11 +103,13 @@ unsigned int take_error_flags_gemv_tc();
 // ---- block-scaled GEMM (gemm.cu)
 struct GemmArgs {
   const mx_packed_weight* w;
-  const uint8_t* xq;    // [roundup(M,128), Kp] e4m3
+  const uint8_t* xq;    // [xq_rows, xq_cols] e4m3, row stride xq_ld bytes; rows and columns
+                        // past the extent read as zeros (TMA fill)
   const uint8_t* sfa;   // [roundup(M,128)/128, Kp/128, 512] activation scale atoms
   const void* bias;     // bf16 [N] or NULL
   void* out;            // bf16 [M, N]
   int M;
+  int xq_rows, xq_cols, xq_ld;  // 0: the workspace layout [roundup(M,128), Kp]
 };
 int launch_gemm(const GemmArgs& a, cudaStream_t stream);
 unsigned int take_error_flags_gemm();

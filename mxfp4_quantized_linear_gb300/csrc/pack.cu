@@ -189,6 +189,12 @@ cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_act_sf_atoms(const uint8_t* codes, int M, int K, int Kp, uint8_t* sf, cudaStream_t stream) {
+  const long long total = static_cast<long long>((M + 127) >> 7) * (Kp >> 7) * 512;
+  pack_sf_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(codes, 1, M, K >> 5, Kp, M, sf);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
                              int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
                              unsigned long long* negz, cudaStream_t stream) {

@@ -160,3 +160,39 @@ def test_workspace_too_small_is_an_error():
         mx.mxfp8_linear(x, p, flags=mx.MX_LINEAR_CLUSTER_GEMV,
                         workspace=torch.empty(16, dtype=torch.uint8, device=dev))
     assert ei.value.code == mx.binding.MX_ERR_WORKSPACE
+
+
+# ------------------------------------------------ pre-quantized activation input
+
+@pytest.mark.parametrize("M,K", [(1, 2048), (5, 2080), (32, 2080), (40, 2080), (200, 1024)])
+def test_prequantized_equals_fused_quant_bitwise(M, K):
+    """mxfp8_linear_q on mx_quantize_act(x) is bit-identical to mxfp8_linear(x)
+    (decode GEMV for M <= 32, GEMM reading xq in place for larger M)."""
+    dev = cuda_device()
+    c = inputs.decode_linear(K=K, Ms=(M,), N=704)
+    p = pack(c["w"], c["codes"])
+    x = c["xs"][M].to(dev)
+    bias = inputs.bf16_normal((704,), inputs.generator(3)).to(dev)
+    xq, xc = mx.mx_quantize_act(x)
+    y1 = mx.mxfp8_linear(x, p, bias)
+    y2 = mx.mxfp8_linear_q(xq, xc, p, bias)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [3, 77])
+def test_prequantized_arbitrary_bytes_vs_oracle(M):
+    """Activation bytes and codes that no quantizer produced (every non-NaN e4m3
+    byte, codes 110..140) against the oracle's pre-quantized linear."""
+    from oracle.linear import mxfp8_linear_q as ref_q
+    dev = cuda_device()
+    g = inputs.generator(M)
+    N, K = 320, 1056
+    w = inputs.e4m3_bytes((N, K), g)
+    wc = inputs.e8m0_codes((N // 32, K // 32), 118, 132, g)
+    xq = inputs.e4m3_bytes((M, K), g)
+    xc = inputs.e8m0_codes((M, K // 32), 110, 140, g)
+    p = pack(w, wc)
+    y = mx.mxfp8_linear_q(xq.to(dev), xc.to(dev), p).float().cpu().numpy()
+    ref = ref_q(u8(xq), u8(xc), u8(w), row_codes(u8(wc), N))
+    assert normalized_error(y, ref["y"], ref["A"], ref["B"]) <= TOL
