@@ -27,7 +27,7 @@ chunks together with their code columns.
 """
 import numpy as np
 
-from .formats import bf16_rne_bits, e2m1_decode, e2m1_unpack, e4m3_decode, e8m0_decode
+from .formats import bf16_rne_bits, bf16_value, e2m1_decode, e2m1_unpack, e4m3_decode, e4m3_rne, e8m0_decode
 from .quant import quantize_act
 
 
@@ -50,6 +50,27 @@ def dequant_values(w_bytes, codes, fmt: str, N: int, K: int) -> np.ndarray:
     else:
         raise ValueError(fmt)
     return v * expand_codes(codes, N, K)
+
+
+def e4m3_from_dequant(w_bf16_values, codes) -> tuple:
+    """weights942, ocp_from_dequant: the OCP e4m3 bytes [N, K] behind a bf16
+    weight w = e4m3 value x 2^(code - 127) (codes [N/32, K/32] blocks or
+    [N, K/32] rows).  Each value is scaled by 2^(127 - code) and rounded to
+    e4m3 (nearest-even); it is given back exactly when that byte's dequant,
+    rounded to bf16, equals w (-0 and +0 compare equal, NaN never does).
+
+    Returns (bytes uint8 [N, K], number of values not given back)."""
+    w = np.asarray(w_bf16_values, dtype=np.float64)
+    N, K = w.shape
+    scale = expand_codes(codes, N, K)               # 2^(code - 127), fp64 (exact)
+    v = w / scale                                    # exact power-of-two scaling
+    finite = np.isfinite(v) & (np.abs(v) <= 448.0)
+    q = np.full((N, K), 0x7F, dtype=np.uint8)        # values outside e4m3 -> NaN byte
+    q[finite] = e4m3_rne(v[finite])
+    back = bf16_value(bf16_rne_bits(e4m3_decode(q) * scale))
+    with np.errstate(invalid="ignore"):
+        bad = ~(back == w)
+    return q, int(np.count_nonzero(bad))
 
 
 def dequant_bf16(w_bytes, codes, fmt: str, N: int, K: int) -> np.ndarray:

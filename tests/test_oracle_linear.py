@@ -168,3 +168,38 @@ def test_prequantized_linear_matches_rational_brute_force():
                 acc += (Fraction(xv[m, k]) * Fraction(2) ** (int(xc[m, k // 32]) - 127)
                         * Fraction(wv[n, k]) * Fraction(2) ** (int(wc[n, k // 32]) - 127))
             assert abs(float(acc) - y[m, n]) <= 1e-12 * max(1.0, abs(float(acc)))
+
+
+def test_e4m3_from_dequant_round_trip_and_refusals():
+    """weights942 ocp_from_dequant: every non-NaN e4m3 byte comes back from its
+    bf16 dequant at the codes where that dequant is exact (3..246); a value
+    moved by one bf16 ulp, or one between two e4m3 values, is refused."""
+    from oracle.linear import e4m3_from_dequant
+    b = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    for code in (3, 64, 118, 127, 132, 200, 246):
+        N = 32
+        w = np.tile(b[None, :224], (N, 1))                      # [32, 224]
+        codes = np.full((1, 7), code, dtype=np.uint8)           # 32x32 blocks
+        wv = F.bf16_value(dequant_bf16(w, codes, "e4m3", N, 224))
+        q, bad = e4m3_from_dequant(wv, codes)
+        assert bad == 0
+        assert np.array_equal(q, w)
+    rest = np.tile(b[None, 224:], (32, 1))                     # the last 30 bytes, row codes
+    rc = np.full((32, 1), 120, dtype=np.uint8)
+    wv = F.bf16_value(dequant_bf16(np.pad(rest, ((0, 0), (0, 2))), rc, "e4m3", 32, 32))
+    q, bad = e4m3_from_dequant(wv, rc)
+    assert bad == 0 and np.array_equal(q[:, :30], rest)
+    # refusals
+    codes = np.full((1, 1), 127, dtype=np.uint8)
+    w = np.ones((32, 32))
+    q, bad = e4m3_from_dequant(w, codes)
+    assert bad == 0 and np.all(q == 0x38)                      # 1.0 = 0x38
+    w[3, 4] = 1.0625                                           # between 1.0 and 1.125
+    w[7, 9] = F.bf16_value(np.array([0x3F81], dtype=np.uint16))[0]   # 1.0 + one bf16 ulp
+    w[8, 1] = 449.0                                            # beyond e4m3
+    w[9, 2] = np.nan
+    assert e4m3_from_dequant(w, codes)[1] == 4
+    w2 = np.ones((32, 32))
+    w2[0, 0] = -0.0                                            # -0 is e4m3 0x80
+    q, bad = e4m3_from_dequant(w2, codes)
+    assert bad == 0 and q[0, 0] == 0x80
