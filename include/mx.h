@@ -44,7 +44,9 @@ enum {
   MX_ERR_EXPERT_ID = 7,    /* (device status) an expert id outside [-1, E)     */
   MX_ERR_CUDA = 8,         /* a CUDA runtime call failed                      */
   MX_ERR_UNSUPPORTED = 9,  /* device is not sm_103, or a size beyond a limit  */
-  MX_ERR_TIMEOUT = 10      /* (device flag) a bounded wait inside a kernel ran out */
+  MX_ERR_TIMEOUT = 10,     /* (device flag) a bounded wait inside a kernel ran out */
+  MX_ERR_INEXACT = 11      /* a bf16 weight is not e4m3 x its scale (weights942,
+                              ocp_from_dequant refuses it)                      */
 };
 
 enum { MX_FMT_E4M3 = 0, MX_FMT_E2M1 = 1 };
@@ -158,6 +160,22 @@ int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, 
  *   (rocm_native, input_quant_key).  K % 32 == 0; M == 0 is a no-op.
  */
 int mx_quantize_act(const void* x, int M, int K, uint8_t* q, uint8_t* codes, void* stream);
+
+/*
+ * The OCP e4m3 bytes behind a bf16 weight that was dequantized at load
+ * (weights942, ocp_from_dequant: w = e4m3 value x 2^(code - 127)), so such a
+ * weight can be packed and served as MXFP8.  Each value is scaled by
+ * 2^(127 - code) and rounded to e4m3; the call refuses the weight unless every
+ * byte gives its value back (dequant rounded to bf16; -0 equals +0, NaN never).
+ *   w        [N, K] bf16 (16-byte aligned), K a multiple of 32
+ *   codes    [N/32, K/32] (scale_mode BLOCK32X32) or [N, K/32] (ROW1X32)
+ *   out      [N, K] e4m3 bytes (16-byte aligned)
+ *   scratch  8 bytes of device memory the call may overwrite
+ *   *mismatches  (host, may be NULL) the number of values not given back
+ * Returns MX_ERR_INEXACT when that number is not 0.  Synchronises the stream.
+ */
+int mx_e4m3_from_dequant(const void* w, const uint8_t* codes, int scale_mode, int N, int K, uint8_t* out,
+                         void* scratch, int64_t* mismatches, void* stream);
 
 /*
  * Dequantize MX weights to bf16: out = bf16_rne(value(byte) * 2^(code - 127))

@@ -16,6 +16,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "
 MX_OK = 0
 MX_ERR_SHAPE, MX_ERR_ALIGN, MX_ERR_ARG, MX_ERR_NOT_BLOCK32, MX_ERR_SCALE = 1, 2, 3, 4, 5
 MX_ERR_WORKSPACE, MX_ERR_EXPERT_ID, MX_ERR_CUDA, MX_ERR_UNSUPPORTED, MX_ERR_TIMEOUT = 6, 7, 8, 9, 10
+MX_ERR_INEXACT = 11
 MX_FMT_E4M3, MX_FMT_E2M1 = 0, 1
 MX_SCALE_BLOCK32X32, MX_SCALE_ROW1X32 = 0, 1
 MX_PACK_FOLD, MX_PACK_REQUIRE_BLOCK, MX_PACK_GATE_UP = 1, 2, 4
@@ -29,7 +30,7 @@ EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_
             "mx_quantize_act", "mx_dequant", "mxfp8_linear_workspace_size", "mxfp8_linear",
             "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear",
             "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert",
-            "mxfp8_linear_q_workspace_size", "mxfp8_linear_q")
+            "mxfp8_linear_q_workspace_size", "mxfp8_linear_q", "mx_e4m3_from_dequant")
 
 
 class MxError(RuntimeError):
@@ -79,6 +80,7 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
         "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "mxfp8_linear_q_workspace_size": (sz, [i32, pw]),
+        "mx_e4m3_from_dequant": (i32, [vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(ctypes.c_int64), vp]),
         "mxfp8_linear_q": (i32, [vp, vp, i32, pw, vp, vp, u, vp, sz, vp]),
         "mxfp4_moe_expert": (i32, [vp, vp, vp, i32, i32, pw, pw, vp, vp, sz, vp, vp]),
     }
@@ -193,6 +195,26 @@ def mx_quantize_act(x: torch.Tensor):
     c = torch.empty((M, K // 32), dtype=torch.uint8, device=x.device)
     _check(load_library().mx_quantize_act(_ptr(x), M, K, _ptr(q), _ptr(c), _stream()))
     return q, c
+
+
+def mx_e4m3_from_dequant(w: torch.Tensor, codes: torch.Tensor, scale_mode: int = MX_SCALE_BLOCK32X32,
+                         strict: bool = True):
+    """bf16 weight [N, K] dequantized as e4m3 x 2^(code - 127), codes [N/32, K/32]
+    (or [N, K/32] with MX_SCALE_ROW1X32) -> its e4m3 bytes uint8 [N, K]; raises
+    MxError(MX_ERR_INEXACT) when some value is not given back exactly.  With
+    ``strict=False`` returns (bytes, number of values not given back) instead."""
+    _need(w, torch.bfloat16, "w")
+    _need(codes, torch.uint8, "codes")
+    N, K = w.shape
+    out = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    scratch = torch.empty(1, dtype=torch.int64, device=w.device)
+    bad = ctypes.c_int64(0)
+    rc = load_library().mx_e4m3_from_dequant(_ptr(w), _ptr(codes), scale_mode, N, K, _ptr(out), _ptr(scratch),
+                                             ctypes.byref(bad), _stream())
+    if not strict and rc == MX_ERR_INEXACT:
+        return out, int(bad.value)
+    _check(rc)
+    return out if strict else (out, 0)
 
 
 def mx_dequant(w_bytes: torch.Tensor, codes: torch.Tensor, fmt="e4m3",

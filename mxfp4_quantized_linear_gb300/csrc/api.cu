@@ -287,6 +287,36 @@ int mx_quantize_act(const void* x, int M, int K, uint8_t* q, uint8_t* codes, voi
   return e == cudaSuccess ? MX_OK : cuda_fail(e, "quantize launch");
 }
 
+int mx_e4m3_from_dequant(const void* w, const uint8_t* codes, int scale_mode, int N, int K, uint8_t* out,
+                         void* scratch, int64_t* mismatches, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (mismatches) *mismatches = 0;
+  if (scale_mode != MX_SCALE_BLOCK32X32 && scale_mode != MX_SCALE_ROW1X32)
+    return set_error(MX_ERR_ARG, "unknown scale mode %d", scale_mode);
+  if (N < 0 || K < 32 || K % 32) return set_error(MX_ERR_SHAPE, "N=%d K=%d", N, K);
+  if (scale_mode == MX_SCALE_BLOCK32X32 && N % 32) return set_error(MX_ERR_SHAPE, "32x32 blocks need N %% 32 == 0");
+  if (N == 0) return MX_OK;
+  if (!w || !codes || !out || !scratch) return set_error(MX_ERR_ARG, "NULL pointer");
+  if (!aligned16(w) || !aligned16(out) || (reinterpret_cast<uintptr_t>(scratch) & 7u))
+    return set_error(MX_ERR_ALIGN, "w and out need 16-byte, scratch 8-byte alignment");
+  int rc = check_device();
+  if (rc != MX_OK) return rc;
+  unsigned long long* cnt = static_cast<unsigned long long*>(scratch);
+  cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(*cnt), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "from_dequant: memset");
+  if ((e = launch_from_dequant(w, codes, scale_mode == MX_SCALE_BLOCK32X32 ? 1 : 0, N, K, out, cnt, stream)) !=
+      cudaSuccess)
+    return cuda_fail(e, "from_dequant launch");
+  unsigned long long host = 0;
+  if ((e = cudaMemcpyAsync(&host, cnt, sizeof(host), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e, "from_dequant: read count");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "from_dequant: synchronize");
+  if (mismatches) *mismatches = static_cast<int64_t>(host);
+  if (host) return set_error(MX_ERR_INEXACT, "%llu of %lld values are not e4m3 x scale", host,
+                             static_cast<long long>(N) * K);
+  return MX_OK;
+}
+
 int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode, int N, int K,
                void* out, void* stream) {
   if (fmt != MX_FMT_E4M3 && fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "unknown format %d", fmt);

@@ -63,6 +63,8 @@ cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, 
 // Activation scale atoms [ceil(M/128), Kp/128, 512] from row-major codes [M, K/32]
 // (127 past M, 128 past K), the layout the GEMM's tensor-memory copy reads.
 cudaError_t launch_act_sf_atoms(const uint8_t* codes, int M, int K, int Kp, uint8_t* sf, cudaStream_t stream);
+cudaError_t launch_from_dequant(const void* w, const uint8_t* codes, int block_scale, int N, int K, uint8_t* out,
+                                unsigned long long* mismatches, cudaStream_t stream);
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
                              int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
                              unsigned long long* negz, cudaStream_t stream);

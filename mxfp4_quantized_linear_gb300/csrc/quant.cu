@@ -110,6 +110,56 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   }
 }
 
+// weights942, ocp_from_dequant: the e4m3 bytes behind a bf16 weight w = e4m3
+// value x 2^(code - 127).  One thread = 8 consecutive elements of a row: scale
+// by 2^(127 - code), round to e4m3 (nearest-even, saturating: a value beyond
+// 448 fails the check below anyway), and count the values whose byte does not
+// give w back (dequant rounded to bf16; -0 equals +0, a NaN never matches).
+__global__ void __launch_bounds__(256) from_dequant_kernel(const __nv_bfloat16* __restrict__ w,
+                                                           const uint8_t* __restrict__ codes,
+                                                           int block_scale, int N, int K,
+                                                           uint8_t* __restrict__ out,
+                                                           unsigned long long* mismatches) {
+  const int groups_per_row = K >> 3;
+  const long long total = static_cast<long long>(N) * groups_per_row;
+  const int KB = K >> 5;
+  unsigned int bad = 0;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(g / groups_per_row);
+    const int k = static_cast<int>(g % groups_per_row) * 8;
+    const uint32_t c = codes[static_cast<long long>(block_scale ? (n >> 5) : n) * KB + (k >> 5)];
+    const uint4 u = *reinterpret_cast<const uint4*>(w + static_cast<long long>(n) * K + k);
+    const uint32_t wb[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[2] = {0x7f7f7f7fu, 0x7f7f7f7fu};
+    if (c == 255u) {
+      bad += 8;  // a NaN scale gives nothing back
+    } else {
+      // 2^(127 - c) and 2^(c - 127) as f32: exponent fields 254 - c and c, 0 -> 2^-127
+      const float down = (c == 254u) ? __uint_as_float(0x00400000u) : __uint_as_float((254u - c) << 23);
+      const float up = (c == 0u) ? __uint_as_float(0x00400000u) : __uint_as_float(c << 23);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = wb[i] & 0xffffu, hi = wb[i] >> 16;
+        const uint32_t q = f32x2_to_e4m3x2(__uint_as_float(lo << 16) * down, __uint_as_float(hi << 16) * down);
+        const float2 f = __half22float2(e4m3x2_to_f16x2(static_cast<uint16_t>(q)));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * up, f.y * up);
+        const uint32_t bb = *reinterpret_cast<const uint32_t*>(&b);
+        const uint32_t blo = bb & 0xffffu, bhi = bb >> 16;
+        const bool ok_lo = ((blo == lo) || (((blo | lo) & 0x7fffu) == 0)) && (lo & 0x7fffu) <= 0x7f80u;
+        const bool ok_hi = ((bhi == hi) || (((bhi | hi) & 0x7fffu) == 0)) && (hi & 0x7fffu) <= 0x7f80u;
+        bad += (ok_lo ? 0u : 1u) + (ok_hi ? 0u : 1u);
+        // bytes 2i, 2i + 1 of the 8 outputs
+        const uint32_t shift = 16u * (i & 1);
+        o[i >> 1] = (o[i >> 1] & ~(0xffffu << shift)) | (q << shift);
+      }
+    }
+    *reinterpret_cast<uint2*>(out + static_cast<long long>(n) * K + k) = make_uint2(o[0], o[1]);
+  }
+  for (int off = 16; off > 0; off >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, off);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(mismatches, static_cast<unsigned long long>(bad));
+}
+
 int grid_for(long long threads, int block) {
   long long g = (threads + block - 1) / block;
   DeviceInfo di;
@@ -139,6 +189,15 @@ cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, 
   cfg.numAttrs = pdl_trigger ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), M, K, Kout, q, ldq,
                             codes, ldc, pad_code, sf, pdl_trigger ? 1 : 0, M_out, zero, nzero);
+}
+
+cudaError_t launch_from_dequant(const void* w, const uint8_t* codes, int block_scale, int N, int K, uint8_t* out,
+                                unsigned long long* mismatches, cudaStream_t stream) {
+  const long long groups = static_cast<long long>(N) * (K / 8);
+  const int grid = grid_for(groups, 256);
+  from_dequant_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(w), codes, block_scale, N, K, out,
+                                                mismatches);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mode,

@@ -113,3 +113,53 @@ def test_dequant_e2m1_every_nibble_and_code():
     c = np.repeat(np.array(codes_list, dtype=np.uint8)[:, None], 16, axis=1)
     got = gpu_dequant(torch.tensor(b), torch.tensor(c), "e2m1", mx.MX_SCALE_ROW1X32)
     compare_bf16_bits(got, dequant_bf16(b, c, "e2m1", len(codes_list), 512))
+
+
+# ------------------------------------------------ e4m3 bytes from a bf16 dequant
+
+def _bf16_tensor(bits: np.ndarray) -> torch.Tensor:
+    return torch.tensor(bits.astype(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("codes_lohi", [(118, 132), (3, 40), (200, 246)])
+def test_from_dequant_recovers_the_bytes(codes_lohi):
+    """weights942 ocp_from_dequant on the GPU: the bf16 dequant of random bytes
+    (the oracle's bits) gives every byte back, block and row codes alike."""
+    from oracle.linear import e4m3_from_dequant
+    dev = cuda_device()
+    ensure_built()
+    g = inputs.generator(codes_lohi[0])
+    b = inputs.e4m3_bytes((96, 2080), g)
+    cb = inputs.e8m0_codes((3, 65), *codes_lohi, g)
+    w = _bf16_tensor(dequant_bf16(u8(b), u8(cb), "e4m3", 96, 2080)).to(dev)
+    q = mx.mx_e4m3_from_dequant(w, cb.to(dev), mx.MX_SCALE_BLOCK32X32)
+    torch.cuda.synchronize()
+    assert np.array_equal(u8(q), u8(b))
+    cr = inputs.e8m0_codes((96, 65), *codes_lohi, g)
+    w = _bf16_tensor(dequant_bf16(u8(b), u8(cr), "e4m3", 96, 2080))
+    q = mx.mx_e4m3_from_dequant(w.to(dev), cr.to(dev), mx.MX_SCALE_ROW1X32)
+    assert np.array_equal(u8(q), u8(b))
+    assert e4m3_from_dequant(bf16_np(w), u8(cr))[1] == 0
+
+
+def test_from_dequant_refusals_count_like_the_oracle():
+    from oracle.linear import e4m3_from_dequant
+    dev = cuda_device()
+    ensure_built()
+    g = inputs.generator(12)
+    b = inputs.e4m3_bytes((64, 256), g)
+    cb = inputs.e8m0_codes((2, 8), 118, 132, g)
+    bits = dequant_bf16(u8(b), u8(cb), "e4m3", 64, 256).copy()
+    rng = np.random.default_rng(0)
+    idx = rng.choice(bits.size, size=37, replace=False)
+    flat = bits.reshape(-1)
+    flat[idx[:30]] ^= 0x0001                 # one bf16 ulp away (off the e4m3 grid, or +-0 -> subnormal)
+    flat[idx[30:33]] = 0x7FC0                # NaN
+    flat[idx[33:35]] = 0x7F80                # inf
+    flat[idx[35:]] = 0x7F00                  # 2^127: far beyond 448 x the block scale
+    w = _bf16_tensor(bits)
+    with pytest.raises(mx.MxError) as ei:
+        mx.mx_e4m3_from_dequant(w.to(dev), cb.to(dev))
+    assert ei.value.code == mx.binding.MX_ERR_INEXACT
+    _, bad = mx.mx_e4m3_from_dequant(w.to(dev), cb.to(dev), strict=False)
+    assert bad == e4m3_from_dequant(bf16_np(w), u8(cb))[1]
