@@ -291,6 +291,7 @@ def run_ours(args, ws, rank, local):
     if rank == 0 and not args.no_extras:
         result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
         result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
+        result["moe_expert"] = bench_expert(mx, inputs, dev, stream, hbm_peak)
         result["e2e"] = bench_e2e(mx, packed, dev, stream, args)
     del graphs, g_all
     return result
@@ -347,6 +348,43 @@ def bench_moe(mx, inputs, dev, stream, hbm_peak):
     return {"workload": "MXFP4 A16W4 MoE gate/up E=64 N=4096 K=4096 T=64 top-8 (weights 0.5 GB > L2)",
             "ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
             "experts_touched": D}
+
+
+def bench_expert(mx, inputs, dev, stream, hbm_peak):
+    """The full routed expert (gate/up + SiLU-and-mul, down projection, combine),
+    E=64 I=2048 H=4096 T=64 top-8, graph-replayed back to back."""
+    E, I, H, T, topk = 64, 2048, 4096, 64, 8
+    m = inputs.moe_expert(E=E, I=I, H=H, T=T, topk=topk)
+    reps = 10
+    with torch.cuda.stream(stream):
+        w13 = mx.mx_pack_weights(m["w13"].to(dev), m["c13"].to(dev), "e2m1", mx.MX_PACK_GATE_UP)
+        w2 = mx.mx_pack_weights(m["w2"].to(dev), m["c2"].to(dev), "e2m1", 0)
+        x, ids, wts = m["x"].to(dev), m["ids"].to(dev), m["weights"].to(dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(mx.mxfp4_moe_expert_workspace_size(T, topk, E, I, H), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            mx.mxfp4_moe_expert(x, ids, wts, w13, w2, out=out, workspace=work)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                mx.mxfp4_moe_expert(x, ids, wts, w13, w2, out=out, workspace=work)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(1e6))
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    D = int(torch.unique(m["ids"]).numel())
+    b = D * (2 * I * (H // 2 + H // 32) + H * (I // 2 + I // 32)) + 2 * T * H * 2 + 8 * T * topk
+    gbs = b / (ms * 1e-3) / 1e9
+    del g
+    return {"workload": "MXFP4 routed expert E=64 I=2048 H=4096 T=64 top-8: gate/up + SiLU-and-mul, "
+                        "down projection, top-k combine", "ms": round(ms, 4), "GB/s": round(gbs, 1),
+            "frac_hbm": round(gbs / hbm_peak, 4), "experts_touched": D}
 
 
 def bench_e2e(mx, packed, dev, stream, args):
