@@ -19,13 +19,15 @@
 //     memory and four tcgen05.mma kind::mxf8f6f4.block_scale (M = 128 weight
 //     rows, N = 32 token columns, K = 32): the block scales are applied by the
 //     tensor core, the f32 sums stay in tensor memory;
-//   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld) and pushes each
-//     row's partial to the CTA of the cluster that owns the row (st.async into
-//     its receive buffer, completing on its mbarrier); each CTA waits for the
-//     S partials of its 128 / S rows, sums them in rank order, adds the bias
-//     and stores bf16.  The receive buffer has its own shared memory when four
-//     CTAs per SM still fit, else it reuses the weight ring once every CTA of
-//     the cluster has finished its MMAs (one cluster barrier).
+//   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld) and sends each
+//     row's partial to the CTA of the cluster that owns the row, completing on
+//     that CTA's mbarrier: per-thread st.async for M <= 8 over more than two
+//     owners, else staged in the CTA's dead weight ring and sent with one bulk
+//     copy a owner; each CTA
+//     waits for the S partials of its 128 / S rows, sums them in rank order,
+//     adds the bias and stores bf16.  The receive buffer has its own shared
+//     memory when four CTAs per SM still fit, else it reuses the weight ring
+//     once every CTA of the cluster has finished its MMAs (one cluster barrier).
 // The split depends on (N, K) only, so a token's result does not depend on M.
 // Every mbarrier wait is bounded.
 
@@ -40,7 +42,8 @@ constexpr int kRows = 128;                // weight rows a tile (MMA M)
 constexpr int kTok = 32;                  // token columns (MMA N)
 constexpr int kStepB = 128;               // K bytes a step
 constexpr int kMaxRing = 6;               // weight ring depth
-constexpr int kXBatch = 8;                // activation loads in flight a thread
+constexpr int kXBlocks = 2;               // MX blocks (4 x 16-byte loads each) in flight a thread
+constexpr int kPushMaxM = 8;              // up to this M, partials go by per-thread st.async, above by bulk copy
 constexpr int kMaxSteps = 8;              // K steps a CTA (slice)
 constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 quant + epilogue
 constexpr int kWBox = kRows * kStepB;     // 16 KB
@@ -58,10 +61,11 @@ struct TcGemvParams {
   __nv_bfloat16* out;          // [M, N]
   int M, N, K, KT, splits, ring;
   int own_recv;                // 1: the receive buffer has its own shared memory
+  int bulk;                    // 1: partials go by bulk copy, 0: by per-thread st.async
 };
 
 struct Layout {
-  int w, sfw, xq, sfx, recv, bars, total;
+  int w, sfw, xq, sfx, recv, stage, bars, total;
 };
 
 // Shared memory.  The receive buffer of the split-K partials holds, for each
@@ -78,16 +82,32 @@ __host__ __device__ inline int recv_bytes_for(int splits, int M) {
   return splits > 1 ? splits * ((kRows + splits - 1) / splits) * recv_stride(M) * 4 : 0;
 }
 
+// The CTA's own 128 x M partial is staged (by owner, in the owners' receive
+// layout) in shared memory that is dead once its MMAs are done, then sent with
+// one bulk copy a owner.
 __host__ __device__ inline Layout layout_for(int ring, int steps, int splits, int M, bool own_recv) {
   Layout L;
   const int ring_bytes = ring * kWBox;
   const int recv_bytes = recv_bytes_for(splits, M);
+  const int stage_bytes = splits > 1 ? kRows * recv_stride(M) * 4 : 0;
   L.w = 0;                                   // ring x 16 KB
   L.xq = own_recv ? ring_bytes : ((ring_bytes > recv_bytes ? ring_bytes : recv_bytes) + 1023) & ~1023;
   L.sfw = L.xq + steps * kXq;                // ring x 512
   L.sfx = L.sfw + ring * 512;                // steps x 512
-  L.recv = own_recv ? L.sfx + steps * 512 : 0;
-  L.bars = own_recv ? L.recv + recv_bytes : L.sfx + steps * 512;
+  const int dead_end = L.sfx + steps * 512;  // ring, xq and scale atoms: dead after the MMAs
+  if (own_recv) {
+    L.recv = dead_end;
+    L.stage = 0;
+    L.bars = L.recv + recv_bytes;
+    if (stage_bytes > dead_end) {            // (never at the decode shapes) stage past recv
+      L.stage = L.bars;
+      L.bars += stage_bytes;
+    }
+  } else {
+    L.recv = 0;
+    L.stage = (recv_bytes + 15) & ~15;
+    L.bars = dead_end > L.stage + stage_bytes ? dead_end : L.stage + stage_bytes;
+  }
   L.total = L.bars + 256;
   return L;
 }
@@ -140,7 +160,9 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
     fence_mbar_init();
     fence_proxy_async_smem();
     // armed now; completes once the S partials of the owned rows have landed
-    if (S > 1) mbar_arrive_expect_tx(redbar, static_cast<uint32_t>(S * own_rows * ((p.M + 3) / 4) * 16));
+    // bulk copies move whole receive rows (Mp floats); per-thread pushes M rounded up to 4
+    if (S > 1)
+      mbar_arrive_expect_tx(redbar, static_cast<uint32_t>(S * own_rows * (p.bulk ? Mp : (p.M + 3) & ~3) * 4));
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -211,12 +233,10 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
     const int et = threadIdx.x - 64;  // 0..127
     // the activation may be written by the previous kernel on the stream
     pdl_wait_prior_grid();
-    // item = (step, token, 8-element group): 4 consecutive lanes hold one MX
-    // block.  Only the M real token rows are quantized: rows >= M feed only
-    // output columns that are never stored (every column of the MMA is
-    // independent).  kXBatch loads a thread are in flight at once.
-    // item it: row it / 16 of the slice = (step, token), 8-element group it % 16;
-    // row / M by a multiply-shift, exact for rows < 2^16 / M (rows <= 8 x 32)
+    // Only the M real token rows are quantized: rows >= M feed only output
+    // columns that are never stored (every column of the MMA is independent).
+    // row = (step, token) of the slice; row / M by a multiply-shift, exact for
+    // rows < 2^16 / M (rows <= 8 x 32)
     const int mrows = p.M;
     const int items = ns * mrows * 16;
     const int mmul = (65536 + mrows - 1) / mrows;
@@ -236,30 +256,39 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
         if ((g8 & 3) == 0) smem[L.sfx + step * 512 + t * 16 + (g8 >> 2)] = code;
       }
     }
-    for (int b0 = (et & ~31); b0 < items && p.xq == nullptr; b0 += 128 * kXBatch) {
-      uint4 u[kXBatch];
+    // bf16 activation: one whole 32-element MX block a thread (item = (step,
+    // token, block)), kXBlocks blocks in flight a thread
+    const int blocks = ns * mrows * 4;
+    for (int b0 = et; b0 < blocks && p.xq == nullptr; b0 += 128 * kXBlocks) {
+      uint4 u[kXBlocks][4];
 #pragma unroll
-      for (int j = 0; j < kXBatch; ++j) {
-        const int it = b0 + j * 128 + lane;
-        u[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (it < items) {
-          const int row = it >> 4, step = (row * mmul) >> 16, t = row - step * mrows, g8 = it & 15;
-          const int col = (st0 + step) * kStepB + g8 * 8;
-          if (col < p.K) u[j] = __ldcg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.K + col));
+      for (int j = 0; j < kXBlocks; ++j) {
+        const int ib = b0 + j * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) u[j][q] = make_uint4(0u, 0u, 0u, 0u);
+        if (ib < blocks) {
+          const int row = ib >> 2, step = (row * mmul) >> 16, t = row - step * mrows, kb = ib & 3;
+          const int col = (st0 + step) * kStepB + kb * 32;
+          if (col < p.K) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<long long>(t) * p.K + col);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) u[j][q] = __ldcg(src + q);
+          }
         }
       }
 #pragma unroll
-      for (int j = 0; j < kXBatch; ++j) {
-        if (b0 + j * 128 >= items) break;  // warp-uniform
-        const int it = b0 + j * 128 + lane;
-        const int row = it >> 4, step = (row * mmul) >> 16, t = row - step * mrows, g8 = it & 15;
-        const QuantBlock8 qb = mx_quant_bf16x8(u[j]);
-        if (it < items) {
-          const int c = g8 >> 1;  // 16-byte chunk of the 128-byte row, 128B swizzle
-          *reinterpret_cast<uint2*>(smem + L.xq + step * kXq + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) =
-              make_uint2(qb.lo, qb.hi);
-          if ((g8 & 3) == 0) smem[L.sfx + step * 512 + t * 16 + (g8 >> 2)] = static_cast<uint8_t>(qb.code);
-        }
+      for (int j = 0; j < kXBlocks; ++j) {
+        const int ib = b0 + j * 128;
+        if (ib >= blocks) break;
+        const int row = ib >> 2, step = (row * mmul) >> 16, t = row - step * mrows, kb = ib & 3;
+        uint4 q8[2];
+        const uint32_t code = mx_quant_bf16x32(u[j], q8);
+        // the block's 32 bytes are 16-byte chunks 2 kb and 2 kb + 1 of the
+        // 128-byte row, 128B swizzle
+        uint8_t* rowp = smem + L.xq + step * kXq + t * kStepB;
+        *reinterpret_cast<uint4*>(rowp + (((2 * kb) ^ (t & 7)) << 4)) = q8[0];
+        *reinterpret_cast<uint4*>(rowp + (((2 * kb + 1) ^ (t & 7)) << 4)) = q8[1];
+        smem[L.sfx + step * 512 + t * 16 + kb] = static_cast<uint8_t>(code);
       }
     }
     fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
@@ -289,10 +318,10 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
         for (int t = 0; t < kTok; ++t)
           if (t < p.M) p.out[static_cast<long long>(t) * p.N + n] = __float2bfloat16_rn(__uint_as_float(acc[t]) + b);
       }
-    } else {
-      // push this row's partial to the CTA that owns it: CTA o owns rows
-      // [o * rows_per, (o + 1) * rows_per); recv[slice][row - o * rows_per][t]
-      cluster_wait_acquire();  // the owner's barrier (and, if shared, buffer) is ready
+    } else if (!p.bulk) {
+      // few tokens: push this row's partial straight to the CTA that owns it
+      // (st.async onto the owner's mbarrier)
+      cluster_wait_acquire();  // the owners' barriers (and, if shared, buffers) are ready
       const int owner = r / rows_per;
       const int rr = r - owner * rows_per;
       const uint32_t dst = map_shared_rank(smem_u32(smem + L.recv), static_cast<uint32_t>(owner)) +
@@ -303,6 +332,33 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
         if (t < p.M)
           st_async_v4_f32(dst + static_cast<uint32_t>(t * 4), __uint_as_float(acc[t]), __uint_as_float(acc[t + 1]),
                           __uint_as_float(acc[t + 2]), __uint_as_float(acc[t + 3]), bar);
+    } else {
+      // stage this row's partial where its owner keeps slice `split`:
+      // stage[owner][row - owner * rows_per][t], then one bulk copy a owner
+      const int owner = r / rows_per;
+      const int rr = r - owner * rows_per;
+      float* stage = reinterpret_cast<float*>(smem + L.stage) + (owner * rows_per + rr) * Mp;
+#pragma unroll
+      for (int t = 0; t < kTok; t += 4)
+        if (t < p.M)
+          *reinterpret_cast<float4*>(stage + t) = make_float4(__uint_as_float(acc[t]), __uint_as_float(acc[t + 1]),
+                                                              __uint_as_float(acc[t + 2]), __uint_as_float(acc[t + 3]));
+      fence_proxy_async_smem();   // the staged partials -> visible to the bulk copies
+      named_barrier(1, 128);      // the 4 epilogue warps
+      cluster_wait_acquire();     // the owners' barriers (and, if shared, buffers) are ready
+      if (threadIdx.x == 64) {
+        for (int o = 0; o < S; ++o) {
+          const int lo = o * rows_per;
+          const int rows = (lo + rows_per < kRows ? rows_per : kRows - lo);
+          if (rows <= 0) continue;
+          const uint32_t src = smem_u32(smem + L.stage) + static_cast<uint32_t>(lo * Mp * 4);
+          const uint32_t dst = map_shared_rank(smem_u32(smem + L.recv), static_cast<uint32_t>(o)) +
+                               static_cast<uint32_t>(split * rows_per * Mp * 4);
+          bulk_copy_to_peer(dst, src, static_cast<uint32_t>(rows * Mp * 4),
+                            map_shared_rank(smem_u32(redbar), static_cast<uint32_t>(o)));
+        }
+        bulk_commit();
+      }
     }
   }
 
@@ -340,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
       }
     }
   }
+  if (S > 1 && p.bulk && threadIdx.x == 64) bulk_wait_read_all();  // the staged partials were read
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -390,6 +447,8 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   p.own_recv = p.splits > 1 && layout_for(p.ring, steps, p.splits, a.M, true).total + 1024 <= four_per_sm ? 1 : 0;
   const Layout L = layout_for(p.ring, steps, p.splits, a.M, p.own_recv != 0);
   const int smem = (L.total + 1024 > kMinSmem) ? L.total + 1024 : kMinSmem;
+  // per-thread pushes win only for few tokens spread over many owners
+  p.bulk = (a.M > kPushMaxM || p.splits <= 2 || a.force_bulk) ? 1 : 0;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)
     return set_error(MX_ERR_UNSUPPORTED, "gemv: %d K steps a CTA (%d bytes of shared memory) is too many", steps, smem);
   if (reinterpret_cast<uintptr_t>(a.xq ? static_cast<const void*>(a.xq) : a.x) % 16 != 0)

@@ -190,6 +190,23 @@ MX_DEV void st_async_v4_f32(uint32_t addr, float a, float b, float c, float d, u
                : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory into the shared memory of a CTA of the cluster
+// (dst and bar from map_shared_rank); the bytes complete on that CTA's mbarrier.
+MX_DEV void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+MX_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the committed bulk copies have read their sources.
+MX_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Barrier over the `count` threads (a multiple of 32) that use barrier `id` (1..15).
+MX_DEV void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Store to the shared memory of another CTA of the cluster (address from map_shared_rank).
 MX_DEV void st_shared_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -308,6 +325,43 @@ MX_DEV void bf16x8_to_f32(const uint4& u, float (&v)[8]) {
     v[2 * i] = __uint_as_float(w[i] << 16);
     v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
+}
+
+// One whole MX block in one thread: u[0..3] hold the block's 32 bf16 elements
+// in order (8 per uint4, element 0 in the low half of u[0].x).  Same rule and
+// same bits as mx_quant_bf16x8, without shuffles: out[0..1] receive the 32
+// e4m3 bytes (element 0 in the lowest byte of out[0].x), the return value is
+// the E8M0 code (255 for a block with NaN or inf, bytes 0x7F).
+MX_DEV uint32_t mx_quant_bf16x32(const uint4 (&u)[4], uint4 (&out)[2]) {
+  uint32_t m2 = 0u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(u[q].x & 0x7fff7fffu, u[q].y & 0x7fff7fffu),
+                               __vmaxu2(u[q].z & 0x7fff7fffu, u[q].w & 0x7fff7fffu)));
+  const uint32_t m = max(m2 & 0xffffu, m2 >> 16);
+  if (m >= 0x7f80u) {  // NaN or inf in the block
+    out[0] = out[1] = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+    return 255u;
+  }
+  const uint32_t code = mx_block_code(__uint_as_float(m << 16));
+  const uint32_t ef = 254u - code;
+  const float rescale = ef ? __uint_as_float(ef << 23) : __uint_as_float(0x00400000u);
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t in[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t p0 = f32x2_to_e4m3x2(__uint_as_float(in[2 * h] << 16) * rescale,
+                                          __uint_as_float(in[2 * h] & 0xffff0000u) * rescale);
+      const uint32_t p1 = f32x2_to_e4m3x2(__uint_as_float(in[2 * h + 1] << 16) * rescale,
+                                          __uint_as_float(in[2 * h + 1] & 0xffff0000u) * rescale);
+      w[2 * q + h] = p0 | (p1 << 16);
+    }
+  }
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return code;
 }
 
 // u: this lane's 8 consecutive bf16 elements of the block (element 0 in the

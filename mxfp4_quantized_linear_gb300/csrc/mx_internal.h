@@ -97,6 +97,7 @@ struct TcGemvArgs {
   const uint8_t* xcodes;  // its codes [M, K/32]
   int force_splits;  // 0 = heuristic
   int force_ring;    // 0 = default weight ring depth
+  int force_bulk;    // 1 = bulk-copy reduction at every M
 };
 int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream);
 int gemv_tc_splits(int N, int Kp, int sms, int force);
