@@ -120,6 +120,8 @@ constexpr int kMinSmem = 48 * 1024;
 // Two weight stages a CTA: with three or four CTAs per SM that keeps 96-128 KB
 // of weight requests in flight on every SM.
 constexpr int kDefaultRing = 2;
+constexpr int kMaxAutoRing = 4;
+constexpr int kLongSlice = 8;             // K steps a CTA from which the ring is kMaxAutoRing deep
 
 __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const TcGemvParams p) {
@@ -440,13 +442,26 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   if (p.splits < 1 || p.splits > 8) return set_error(MX_ERR_ARG, "gemv: split count %d outside 1..8", p.splits);
   if (p.splits > 8) return set_error(MX_ERR_UNSUPPORTED, "gemv: K = %d is too long for the decode GEMV", w->K);
   const int steps = (p.KT + p.splits - 1) / p.splits;
-  const int ring_max = a.force_ring > 0 ? (a.force_ring < kMaxRing ? a.force_ring : kMaxRing) : kDefaultRing;
-  p.ring = steps < ring_max ? steps : ring_max;
   // its own receive buffer when four CTAs per SM still fit
   const int four_per_sm = static_cast<int>(di.smem_per_sm / 4) - static_cast<int>(di.smem_reserved_per_block);
-  p.own_recv = p.splits > 1 && layout_for(p.ring, steps, p.splits, a.M, true).total + 1024 <= four_per_sm ? 1 : 0;
-  const Layout L = layout_for(p.ring, steps, p.splits, a.M, p.own_recv != 0);
-  const int smem = (L.total + 1024 > kMinSmem) ? L.total + 1024 : kMinSmem;
+  auto smem_for = [&](int ring, int* own) {
+    *own = p.splits > 1 && layout_for(ring, steps, p.splits, a.M, true).total + 1024 <= four_per_sm ? 1 : 0;
+    const int t = layout_for(ring, steps, p.splits, a.M, *own != 0).total + 1024;
+    return t > kMinSmem ? t : kMinSmem;
+  };
+  static int smem_set[64];
+  // Weight ring depth: two stages keep 3-4 CTAs per SM resident; a long K
+  // slice (8 steps and more, where the grid needs a second wave anyway)
+  // streams better with four (measured on GB300).  The depth never changes a
+  // result.
+  if (a.force_ring > 0) {
+    const int r = a.force_ring < kMaxRing ? a.force_ring : kMaxRing;
+    p.ring = steps < r ? steps : r;
+  } else {
+    const int r = steps >= kLongSlice ? kMaxAutoRing : kDefaultRing;
+    p.ring = steps < r ? steps : r;
+  }
+  const int smem = smem_for(p.ring, &p.own_recv);
   // per-thread pushes win only for few tokens spread over many owners
   p.bulk = (a.M > kPushMaxM || p.splits <= 2 || a.force_bulk) ? 1 : 0;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)
@@ -457,7 +472,6 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   const int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->Kp, w->N, w->Kp, kStepB,
                                       kRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != MX_OK) return rc;
-  static int smem_set[64];
   if (raise_smem_limit(reinterpret_cast<const void*>(gemv_tc_kernel), smem, di, smem_set) != MX_OK) return MX_ERR_CUDA;
   cudaError_t e;
   cudaLaunchConfig_t cfg = {};
