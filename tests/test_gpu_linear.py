@@ -85,6 +85,20 @@ def test_large_m_path():
         check(p, w, c, inputs.bf16_normal((M, 512), g))
 
 
+@pytest.mark.parametrize("M", [33, 150, 300])
+def test_large_m_row_codes_ragged_k_with_bias(M):
+    """1x32 per-row weight codes that do not fold into 32x32 blocks, K not a
+    multiple of 128 (padded to Kp), on the block-scaled GEMM (M > 32)."""
+    g = inputs.generator(400 + M)
+    N, K = 200, 1056
+    w = inputs.e4m3_bytes((N, K), g)
+    c = inputs.e8m0_codes((N, K // 32), 116, 134, g)
+    b = inputs.bf16_normal((N,), g)
+    p = pack(w, c)
+    assert p.scale_mode == mx.MX_SCALE_ROW1X32
+    check(p, w, c, inputs.bf16_normal((M, K), g), bias=b)
+
+
 def test_batch_invariance_and_fused_equals_unfused():
     c = inputs.decode_linear(K=2080, Ms=(32,), seed=3)
     p = pack(c["w"], c["codes"])
