@@ -57,3 +57,44 @@ def test_product_path_fails_loudly_without_library(tmp_path):
     from mxfp4_quantized_linear_gb300 import binding
     with pytest.raises(RuntimeError, match="not built"):
         binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_host_side_checks_of_the_newer_entry_points():
+    """mxfp8_linear_q, mxfp4_moe_expert, mx_e4m3_from_dequant and the gate/up pack
+    flag reject bad arguments before any device work."""
+    lib = ensure_built()
+    from mxfp4_quantized_linear_gb300 import binding as b
+    e4 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=64, K=64, Kp=128)
+    e2 = b.MxPackedWeightC(fmt=b.MX_FMT_E2M1, E=2, N=64, K=256, Kp=256, layout=b.MX_LAYOUT_GATE_UP)
+    e2p = b.MxPackedWeightC(fmt=b.MX_FMT_E2M1, E=2, N=256, K=32, Kp=128, layout=b.MX_LAYOUT_PLAIN)
+    # pre-quantized linear
+    assert lib.mxfp8_linear_q(None, None, 1, ctypes.byref(e2p), None, None, 0, None, 0, None) == b.MX_ERR_ARG
+    assert lib.mxfp8_linear_q(None, None, 1, ctypes.byref(e4), None, None, 8, None, 0, None) == b.MX_ERR_ARG
+    assert lib.mxfp8_linear_q(None, None, 0, ctypes.byref(e4), None, None, 0, None, 0, None) == b.MX_OK
+    assert lib.mxfp8_linear_q_workspace_size(32, ctypes.byref(e4)) == 0
+    assert lib.mxfp8_linear_q_workspace_size(33, ctypes.byref(e4)) == 512
+    # expert: w13 must carry the gate/up layout, w2 must fit it
+    assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2p), ctypes.byref(e2p), None, None, 0, None,
+                                None) == b.MX_ERR_ARG
+    assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2), ctypes.byref(e2), None, None, 0, None,
+                                None) == b.MX_ERR_ARG                  # w2 packed with the interleave
+    assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2), ctypes.byref(e2p), None, None, 0, None,
+                                None) == b.MX_ERR_ARG                  # shapes fit (I = 32 = w2 K): NULL x
+    w2_bad = b.MxPackedWeightC(fmt=b.MX_FMT_E2M1, E=2, N=256, K=64, Kp=128, layout=b.MX_LAYOUT_PLAIN)
+    assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2), ctypes.byref(w2_bad), None, None, 0, None,
+                                None) == b.MX_ERR_SHAPE                # w2 K = 64 != I = 32
+    assert b"does not fit" in lib.mx_last_error()
+    assert lib.mxfp4_moe_expert_workspace_size(4, 2, 8, 64, 128) > lib.mxfp4_moe_workspace_size(4, 2, 8)
+    # from-dequant
+    n = ctypes.c_int64(7)
+    assert lib.mx_e4m3_from_dequant(None, None, 5, 32, 64, None, None, ctypes.byref(n), None) == b.MX_ERR_ARG
+    assert n.value == 0
+    assert lib.mx_e4m3_from_dequant(None, None, b.MX_SCALE_BLOCK32X32, 40, 64, None, None, None, None) == b.MX_ERR_SHAPE
+    assert lib.mx_e4m3_from_dequant(None, None, b.MX_SCALE_ROW1X32, 0, 64, None, None, None, None) == b.MX_OK
+    # gate/up flag only for E2M1 and 2 I a multiple of 16
+    dst = b.MxPackedWeightC()
+    buf = ctypes.c_void_p(0x100000)   # aligned, never dereferenced: rejected first
+    assert lib.mx_pack_weights(buf, buf, b.MX_FMT_E4M3, 1, 64, 64, 64, b.MX_PACK_GATE_UP, buf, 1 << 20,
+                               ctypes.byref(dst), None) == b.MX_ERR_ARG
+    assert lib.mx_pack_weights(buf, buf, b.MX_FMT_E2M1, 1, 40, 64, 40, b.MX_PACK_GATE_UP, buf, 1 << 20,
+                               ctypes.byref(dst), None) == b.MX_ERR_SHAPE
