@@ -318,6 +318,17 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
                      const mx_packed_weight* w13, const mx_packed_weight* w2, void* out, void* workspace,
                      size_t workspace_bytes, int* dev_status, void* stream);
 
+/* ------------------------------------------------------------------ self-test */
+
+/*
+ * Exercises the failure path of the library's bounded waits (no counterpart on
+ * the source pages): one GPU thread waits on an mbarrier that nothing arrives
+ * on, gives up after limit_us microseconds (1..100000), writes 1 to the device
+ * int *waited_out, and raises the device timeout flag, so that the next
+ * mx_check_device_errors() returns MX_ERR_TIMEOUT.  Nothing faults or traps.
+ */
+int mx_selftest_bounded_wait(int limit_us, int* waited_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

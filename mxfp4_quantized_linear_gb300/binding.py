@@ -30,7 +30,8 @@ EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_
             "mx_quantize_act", "mx_dequant", "mxfp8_linear_workspace_size", "mxfp8_linear",
             "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear",
             "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert",
-            "mxfp8_linear_q_workspace_size", "mxfp8_linear_q", "mx_e4m3_from_dequant")
+            "mxfp8_linear_q_workspace_size", "mxfp8_linear_q", "mx_e4m3_from_dequant",
+            "mx_selftest_bounded_wait")
 
 
 class MxError(RuntimeError):
@@ -80,6 +81,7 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
         "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "mxfp8_linear_q_workspace_size": (sz, [i32, pw]),
+        "mx_selftest_bounded_wait": (i32, [i32, vp, vp]),
         "mx_e4m3_from_dequant": (i32, [vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(ctypes.c_int64), vp]),
         "mxfp8_linear_q": (i32, [vp, vp, i32, pw, vp, vp, u, vp, sz, vp]),
         "mxfp4_moe_expert": (i32, [vp, vp, vp, i32, i32, pw, pw, vp, vp, sz, vp, vp]),

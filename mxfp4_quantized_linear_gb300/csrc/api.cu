@@ -183,7 +183,9 @@ const char* mx_last_error(void) { return g_msg; }
 int mx_check_device_errors(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  const unsigned int flags = take_error_flags_gemv() | take_error_flags_gemm() | take_error_flags_gemv_tc();
+  const unsigned int flags =
+      take_error_flags_gemv() | take_error_flags_gemm() | take_error_flags_gemv_tc() | take_error_flags_moe() |
+      take_error_flags_selftest();
   if (flags & 0x80000000u) return set_error(MX_ERR_CUDA, "could not read the device error flags");
   if (flags & 1u) return set_error(MX_ERR_TIMEOUT, "a bounded wait inside a kernel timed out");
   return MX_OK;

@@ -393,6 +393,8 @@ __global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_con
 
 }  // namespace
 
+unsigned int take_error_flags_moe() { return take_tu_error_flags(); }
+
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
                          int* dev_status, cudaStream_t stream) {

@@ -89,18 +89,21 @@ MX_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, sets the device timeout flag and returns false.
-MX_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// limit_ns of %globaltimer, sets the device timeout flag and returns false.
+MX_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && globaltimer() - t0 > limit_ns) {
       flag_timeout();
       return false;
     }
   }
 }
+
+// mbar_wait_for with the library's limit, kWaitLimitNs.
+MX_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_for(bar, parity, kWaitLimitNs); }
 
 // mbar_wait with cluster-scope acquire (bounded the same way).
 MX_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {

@@ -132,6 +132,8 @@ struct MoeLaunch {
   void* out_f32;               // f32 [pairs, N]
 };
 int launch_moe(const MoeLaunch& a, cudaStream_t stream);
+unsigned int take_error_flags_moe();
+unsigned int take_error_flags_selftest();
 cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts, int T, int topk, int E, int H,
                            void* out, cudaStream_t stream);
 cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E, int N, void* out,
