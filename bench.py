@@ -19,11 +19,13 @@ through the Python API with pinned host copies each step.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
 import argparse
+import ctypes
 import json
 import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -114,13 +116,59 @@ REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_pow
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock and clock-event (throttle) reasons sampled while the timed
+    region runs: NVML through ctypes every millisecond (read-only queries),
+    else nvidia-smi every 50 ms.  Nothing here changes a GPU setting."""
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+
+    def _nvml(self):
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            found = False
+            try:  # the NVML device of this CUDA device, by PCI address
+                pr = torch.cuda.get_device_properties(self.index)
+                bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+                found = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                found = False
+            if not found:
+                found = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) == 0
+            if not found:
+                return None
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            return lib, h, reasons
+        except Exception:
+            return None
+
+    def _loop(self, lib, h, reasons):
+        NVML_CLOCK_SM = 1
+        cur, mx, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if lib.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) != 0:
+            mx.value = 0
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(cur)) == 0 and \
+                    reasons(h, ctypes.byref(r)) == 0:
+                self.samples.append((float(cur.value), float(mx.value), int(r.value)))
+            time.sleep(0.001)
 
     def __enter__(self):
+        nv = self._nvml()
+        if nv is not None:
+            self._thread = threading.Thread(target=self._loop, args=nv, daemon=True)
+            self._thread.start()
+            while not self.samples and self._thread.is_alive():  # the first sample precedes the region
+                time.sleep(0.001)
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index),
@@ -132,31 +180,36 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
-        self.lines = []
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
-                self.lines = [l for l in out.splitlines() if l.strip()]
             except Exception:
                 self.proc.kill()
+                return
+            for l in out.splitlines():
+                parts = [p.strip() for p in l.split(",")]
+                try:
+                    self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+                except Exception:
+                    continue
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        for l in getattr(self, "lines", []):
-            parts = [p.strip() for p in l.split(",")]
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-                bits = int(parts[2], 16)
-            except Exception:
-                continue
+        sm = [c for c, _, _ in self.samples]
+        mx = [m for _, m, _ in self.samples if m > 0]
+        reasons = set()
+        for _, _, bits in self.samples:
             for b, name in REASON_BITS.items():
                 if bits & b and name != "gpu_idle":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvml" if self._thread is not None else "nvidia-smi"}
 
 
 # ------------------------------------------------------------------- our arm

@@ -355,7 +355,8 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
   // tuning overrides of the cluster GEMV (not part of the documented flags):
   // bits 8..11 force its split count, bit 12 forces its fused quantizer;
   // bits 16..18 force the tensor-core GEMV's weight ring depth, bit 23 its
-  // bulk-copy reduction at every M
+  // bulk-copy reduction at every M, bits 24..26 its CTAs per SM, bits 27..28
+  // its receive-buffer placement
   const int force_splits = static_cast<int>((flags >> 8) & 0xfu);
   const bool force_fuse = (flags & (1u << 12)) != 0;
   const bool no_fuse = (flags & MX_LINEAR_NO_FUSED_QUANT) != 0;
@@ -396,6 +397,8 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     g.force_splits = force_splits;
     g.force_ring = static_cast<int>((flags >> 16) & 0x7u);      // tuning: weight ring depth
     g.force_bulk = (flags >> 23) & 1u;                          // tuning: bulk-copy reduction
+    g.force_cap = static_cast<int>((flags >> 24) & 0x7u);       // tuning: CTAs per SM
+    g.force_recv = static_cast<int>((flags >> 27) & 0x3u);      // tuning: receive-buffer placement
     return launch_gemv_tc(g, stream);
   }
   const bool needs_ws = (M > kFusedQuantMaxM && !force_fuse) || no_fuse || M > MX_GEMV_MAX_M;

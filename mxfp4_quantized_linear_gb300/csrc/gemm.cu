@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -87,6 +86,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // only now that this CTA holds its tensor memory: a dependent grid then
+  // never takes columns that a CTA of this grid still waits for
+  pdl_launch_dependents();
   const int ntiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0 && lane == 0) {

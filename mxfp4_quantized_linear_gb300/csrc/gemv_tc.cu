@@ -47,8 +47,20 @@ constexpr int kPushMaxM = 8;              // up to this M, partials go by per-th
 constexpr int kMaxSteps = 8;              // K steps a CTA (slice)
 constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 quant + epilogue
 constexpr int kWBox = kRows * kStepB;     // 16 KB
-constexpr int kXq = kTok * kStepB;        // 4 KB quantized activation a step
-constexpr uint32_t kTmemCols = 128;       // accumulator 32 + one (SFw 4 + SFx 4) slot a step
+constexpr int kMaxCtasPerSm = 5;          // register budget (launch bounds)
+
+// MMA N (token columns) for M tokens, and the quantized-activation bytes a step.
+__host__ __device__ inline int mma_n(int M) { return M <= 16 ? 16 : 32; }
+__host__ __device__ inline int xq_step_bytes(int M) { return mma_n(M) * kStepB; }
+
+// Tensor-memory columns: the accumulator (MMA N columns) and one scale-factor
+// slot (SFw 4 + SFx 4 columns) a step, rounded up to a power of two >= 32.
+__host__ __device__ inline int tmem_cols_for(int M, int steps) {
+  const int need = mma_n(M) + steps * 8;
+  int c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
 constexpr uint32_t kIdesc32 = mxf8_idesc(kRows, 32);  // 17..32 tokens
 constexpr uint32_t kIdesc16 = mxf8_idesc(kRows, 16);  // 1..16 tokens: half the tensor work
 
@@ -62,6 +74,7 @@ struct TcGemvParams {
   int M, N, K, KT, splits, ring;
   int own_recv;                // 1: the receive buffer has its own shared memory
   int bulk;                    // 1: partials go by bulk copy, 0: by per-thread st.async
+  int tmem_cols;               // tensor-memory allocation (tmem_cols_for)
 };
 
 struct Layout {
@@ -92,7 +105,7 @@ __host__ __device__ inline Layout layout_for(int ring, int steps, int splits, in
   const int stage_bytes = splits > 1 ? kRows * recv_stride(M) * 4 : 0;
   L.w = 0;                                   // ring x 16 KB
   L.xq = own_recv ? ring_bytes : ((ring_bytes > recv_bytes ? ring_bytes : recv_bytes) + 1023) & ~1023;
-  L.sfw = L.xq + steps * kXq;                // ring x 512
+  L.sfw = L.xq + steps * xq_step_bytes(M);   // ring x 512
   L.sfx = L.sfw + ring * 512;                // steps x 512
   const int dead_end = L.sfx + steps * 512;  // ring, xq and scale atoms: dead after the MMAs
   if (own_recv) {
@@ -112,18 +125,13 @@ __host__ __device__ inline Layout layout_for(int ring, int steps, int splits, in
   return L;
 }
 
-// At most four CTAs per SM: four 128-column tensor-memory allocations fill
-// the 512 columns, so a fifth CTA would wait in tcgen05.alloc on CTAs that may
-// themselves wait on cluster peers.  Five CTAs of at least this much shared
-// memory (plus the 1 KB the system reserves a CTA) exceed the 228 KB of an SM.
-constexpr int kMinSmem = 48 * 1024;
 // Two weight stages a CTA: with three or four CTAs per SM that keeps 96-128 KB
 // of weight requests in flight on every SM.
 constexpr int kDefaultRing = 2;
 constexpr int kMaxAutoRing = 4;
 constexpr int kLongSlice = 8;             // K steps a CTA from which the ring is kMaxAutoRing deep
 
-__global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const TcGemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -135,13 +143,14 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
   const int ns = base + (split < rem ? 1 : 0);
   const int ring = p.ring;
   const Layout L = layout_for(ring, (p.KT + p.splits - 1) / p.splits, p.splits, p.M, p.own_recv != 0);
+  const int xqb = xq_step_bytes(p.M);                          // quantized activation a step
+  const uint32_t sf_base = static_cast<uint32_t>(mma_n(p.M));  // scale-factor slots after the accumulator
   const int S = p.splits;
   const int rows_per = (kRows + S - 1) / S;        // rows each CTA of the cluster owns
   const int Mp = recv_stride(p.M);                 // receive-buffer floats a (slice, row)
   const int own_lo = split * rows_per;
   const int own_hi = own_lo + rows_per < kRows ? own_lo + rows_per : kRows;
   const int own_rows = own_hi > own_lo ? own_hi - own_lo : 0;
-  pdl_launch_dependents();  // the next kernel may start streaming its own weights
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* wempty = wfull + kMaxRing;
   uint64_t* xready = wempty + kMaxRing;  // quantized activation written (128 arrivals)
@@ -166,11 +175,15 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
     if (S > 1)
       mbar_arrive_expect_tx(redbar, static_cast<uint32_t>(S * own_rows * (p.bulk ? Mp : (p.M + 3) & ~3) * 4));
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The next kernel may start streaming its own weights.  Triggered only
+  // once this CTA holds its tensor memory: a dependent grid's CTAs then never
+  // take columns that a CTA of this grid still waits for.
+  pdl_launch_dependents();
   // with its own receive buffer a CTA may be pushed to as soon as its
   // barriers exist: the cluster barrier's arrive goes here, its wait just
   // before the first push (off the critical path)
@@ -207,13 +220,13 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
     for (int i = 0; i < pre && ok; ++i) {
       if (!mbar_wait(&wfull[i], 0u)) { *abort_flag = 1u; ok = false; break; }
       tc_fence_after();
-      tc_cp_sf(tmem + kTok + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
+      tc_cp_sf(tmem + sf_base + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
     }
     if (ok && !mbar_wait(xready, 0)) { *abort_flag = 1u; ok = false; }
     tc_fence_after();
     for (int i = 0; i < ns && ok; ++i) {
       const int stage = i % ring;
-      const uint32_t sf = tmem + kTok + static_cast<uint32_t>(i * 8);
+      const uint32_t sf = tmem + sf_base + static_cast<uint32_t>(i * 8);
       if (i >= pre) {
         if (!mbar_wait(&wfull[stage], static_cast<uint32_t>(i / ring) & 1u)) { *abort_flag = 1u; ok = false; break; }
         tc_fence_after();
@@ -221,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
       }
       tc_cp_sf(sf + 4, sf_desc(smem_u32(smem + L.sfx + i * 512)));
       const uint64_t adesc = sw128_desc(smem_u32(smem + L.w + stage * kWBox));
-      const uint64_t bdesc = sw128_desc(smem_u32(smem + L.xq + i * kXq));
+      const uint64_t bdesc = sw128_desc(smem_u32(smem + L.xq + i * xqb));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t idesc = idesc_n | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
           code = p.xcodes[static_cast<long long>(t) * (p.K >> 5) + (col >> 5)];
         }
         const int c = g8 >> 1;  // 16-byte chunk of the 128-byte row, 128B swizzle
-        *reinterpret_cast<uint2*>(smem + L.xq + step * kXq + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) = v;
+        *reinterpret_cast<uint2*>(smem + L.xq + step * xqb + t * kStepB + ((c ^ (t & 7)) << 4) + (g8 & 1) * 8) = v;
         if ((g8 & 3) == 0) smem[L.sfx + step * 512 + t * 16 + (g8 >> 2)] = code;
       }
     }
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
         const uint32_t code = mx_quant_bf16x32(u[j], q8);
         // the block's 32 bytes are 16-byte chunks 2 kb and 2 kb + 1 of the
         // 128-byte row, 128B swizzle
-        uint8_t* rowp = smem + L.xq + step * kXq + t * kStepB;
+        uint8_t* rowp = smem + L.xq + step * xqb + t * kStepB;
         *reinterpret_cast<uint4*>(rowp + (((2 * kb) ^ (t & 7)) << 4)) = q8[0];
         *reinterpret_cast<uint4*>(rowp + (((2 * kb + 1) ^ (t & 7)) << 4)) = q8[1];
         smem[L.sfx + step * 512 + t * 16 + kb] = static_cast<uint8_t>(code);
@@ -402,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 4) gemv_tc_kernel(const __grid_const
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
   }
 }
 
@@ -442,12 +455,28 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   if (p.splits < 1 || p.splits > 8) return set_error(MX_ERR_ARG, "gemv: split count %d outside 1..8", p.splits);
   if (p.splits > 8) return set_error(MX_ERR_UNSUPPORTED, "gemv: K = %d is too long for the decode GEMV", w->K);
   const int steps = (p.KT + p.splits - 1) / p.splits;
-  // its own receive buffer when four CTAs per SM still fit
-  const int four_per_sm = static_cast<int>(di.smem_per_sm / 4) - static_cast<int>(di.smem_reserved_per_block);
+  // Shared memory and CTAs per SM (measured on GB300): its own receive buffer
+  // as long as that keeps min(4, what sharing the weight ring would keep)
+  // CTAs on an SM; five CTAs per SM for a few tokens, four above (the
+  // activation quantization of five co-resident CTAs then costs more than the
+  // extra overlap gains).  Never so little shared memory that more CTAs
+  // would be resident than the tensor memory holds (their tcgen05.alloc
+  // would wait on CTAs that may themselves wait on cluster peers) or than the
+  // register budget allows.
+  const int smem_sm = static_cast<int>(di.smem_per_sm), reserved = static_cast<int>(di.smem_reserved_per_block);
+  auto per_sm = [&](int bytes) { return smem_sm / (bytes + reserved); };
   auto smem_for = [&](int ring, int* own) {
-    *own = p.splits > 1 && layout_for(ring, steps, p.splits, a.M, true).total + 1024 <= four_per_sm ? 1 : 0;
-    const int t = layout_for(ring, steps, p.splits, a.M, *own != 0).total + 1024;
-    return t > kMinSmem ? t : kMinSmem;
+    const int alias = layout_for(ring, steps, p.splits, a.M, false).total + 1024;
+    const int sep = layout_for(ring, steps, p.splits, a.M, true).total + 1024;
+    const int keep = per_sm(alias) < 4 ? per_sm(alias) : 4;
+    *own = p.splits > 1 && (a.force_recv ? a.force_recv == 2 : per_sm(sep) >= keep) ? 1 : 0;
+    const int t = *own ? sep : alias;
+    const int tmem_cap = 512 / tmem_cols_for(a.M, steps);
+    int cap = a.force_cap > 0 ? a.force_cap : (a.M <= kPushMaxM ? kMaxCtasPerSm : 4);
+    if (cap > kMaxCtasPerSm) cap = kMaxCtasPerSm;
+    if (cap > tmem_cap) cap = tmem_cap;
+    const int floor_bytes = smem_sm / (cap + 1) - reserved + 16;  // cap + 1 CTAs never fit
+    return t > floor_bytes ? t : floor_bytes;
   };
   static int smem_set[64];
   // Weight ring depth: two stages keep 3-4 CTAs per SM resident; a long K
@@ -462,6 +491,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
     p.ring = steps < r ? steps : r;
   }
   const int smem = smem_for(p.ring, &p.own_recv);
+  p.tmem_cols = tmem_cols_for(a.M, steps);
   // per-thread pushes win only for few tokens spread over many owners
   p.bulk = (a.M > kPushMaxM || p.splits <= 2 || a.force_bulk) ? 1 : 0;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)

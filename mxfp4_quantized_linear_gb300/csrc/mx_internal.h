@@ -98,6 +98,8 @@ struct TcGemvArgs {
   int force_splits;  // 0 = heuristic
   int force_ring;    // 0 = default weight ring depth
   int force_bulk;    // 1 = bulk-copy reduction at every M
+  int force_cap;     // 0 = heuristic, else at most this many CTAs per SM
+  int force_recv;    // 0 = heuristic, 1 = receive buffer over the weight ring, 2 = its own
 };
 int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream);
 int gemv_tc_splits(int N, int Kp, int sms, int force);
