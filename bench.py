@@ -383,7 +383,7 @@ def bench_moe(mx, inputs, dev, stream, hbm_peak):
         p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
         x, ids = m["x"].to(dev), m["ids"].to(dev)
         out = torch.empty((64, 8, 4096), dtype=torch.bfloat16, device=dev)
-        work = torch.empty(mx.mxfp4_moe_workspace_size(64, 8, 64), dtype=torch.uint8, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(64, 8, 64, 4096), dtype=torch.uint8, device=dev)
         for _ in range(3):
             mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work)
         torch.cuda.synchronize()
@@ -414,7 +414,7 @@ def bench_expert(mx, inputs, dev, stream, hbm_peak):
         w2 = mx.mx_pack_weights(m["w2"].to(dev), m["c2"].to(dev), "e2m1", 0)
         x, ids, wts = m["x"].to(dev), m["ids"].to(dev), m["weights"].to(dev)
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        work = torch.empty(mx.mxfp4_moe_expert_workspace_size(T, topk, E, I, H), dtype=torch.uint8, device=dev)
+        work = torch.empty(mx.mxfp4_moe_expert_workspace_size(T, topk, E, H, I, H), dtype=torch.uint8, device=dev)
         for _ in range(3):
             mx.mxfp4_moe_expert(x, ids, wts, w13, w2, out=out, workspace=work)
         torch.cuda.synchronize()
@@ -558,7 +558,7 @@ def bench_sweep(mx, inputs, dev, stream, hbm_peak, bf16_peak):
         x = m["x"][:T].contiguous()
         ids = m["ids"][:T].contiguous()
         out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
-        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E), dtype=torch.uint8, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, K), dtype=torch.uint8, device=dev)
         ms = timed(lambda i=0: mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work), 4)
         D = int(torch.unique(ids).numel())
         b = moe_bytes(D, N, K, T, topk)

@@ -94,14 +94,18 @@ enum { MX_SCALE_BLOCK32X32 = 0, MX_SCALE_ROW1X32 = 1 };
  *          n = 128 rt + m and K block j = 4 kt + kb at byte
  *          (m % 32) * 16 + (m / 32) * 4 + kb of atom (rt, kt); 127 past N.
  * E2M1 (MXFP4 experts):
- *   bytes  [E, N, Kp/2]  each 64-byte chunk of a row (4 K blocks x 4 words of
- *          4 bytes) stored word-transposed: word w of block b at word 4 w + b;
- *          inside each word, element e (nibble e, low nibble of byte 0 first)
- *          at nibble slot e / 2 + 4 (e % 2), so elements 2i and 2i+1 sit at
- *          bits 4i and 16 + 4i; -0 nibbles rewritten to +0
- *          (weights942, fp4_drop_negative_zero_)
- *   codes  [E, N, Kp/32] per-row codes
- *   sf     NULL
+ *   bytes  [E, ceil(N/128), Kp/128, 128, 64]  128-row x 128-value tiles, each
+ *          a contiguous 8 KB block: tile (rt, kt) row m holds values
+ *          128 kt .. 128 kt + 127 of row 128 rt + m as 64 fp4x2 bytes in the
+ *          input order (element 2i in the low nibble of byte i); zero past K
+ *          and past N; -0 nibbles rewritten to +0 (weights942,
+ *          fp4_drop_negative_zero_)
+ *   codes  [E, N, Kp/32] per-row codes, 128 past K
+ *   sf     [E, ceil(N/128), Kp/128, 512]  the per-row codes in 512-byte atoms
+ *          as for E4M3 (127 past N)
+ *   With MX_PACK_GATE_UP the rows of bytes, codes and sf are interleaved in
+ *   8-row groups: packed row 16 q + i holds gate row 8 q + i (i < 8) or up row
+ *   8 q + i - 8 (i >= 8) of the gate-then-up tensor (layout MX_LAYOUT_GATE_UP).
  */
 typedef struct mx_packed_weight {
   int32_t fmt;         /* MX_FMT_*                                 */
@@ -276,8 +280,9 @@ int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* c
                      int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
                      int* dev_status, void* stream);
 
-/* Workspace bytes mxfp4_moe_linear needs. */
-size_t mxfp4_moe_workspace_size(int T, int topk, int E);
+/* Workspace bytes mxfp4_moe_linear needs for T tokens, top-k slots, E experts
+ * and activations of K values (0 for a shape it refuses). */
+size_t mxfp4_moe_workspace_size(int T, int topk, int E, int K);
 
 /*
  * Routed A16W4 expert GEMM (a16w4 module text, dequant / step_mfma): for every
@@ -292,9 +297,10 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk,
                      const mx_packed_weight* w, void* out, void* workspace,
                      size_t workspace_bytes, int* dev_status, void* stream);
 
-/* Workspace bytes mxfp4_moe_expert needs (routing, the activation [T*topk, I]
+/* Workspace bytes mxfp4_moe_expert needs for x [T, K], w13 [E, 2 I, K] and
+ * w2 [E, H, I] (routing, the activation pieces, the activation [T*topk, I]
  * bf16 and the down projection [T*topk, H] f32). */
-size_t mxfp4_moe_expert_workspace_size(int T, int topk, int E, int I, int H);
+size_t mxfp4_moe_expert_workspace_size(int T, int topk, int E, int K, int I, int H);
 
 /*
  * The routed expert MLP (A16W4 throughout), from the tensors weights942

@@ -76,10 +76,10 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp8_linear_workspace_size": (sz, [i32, pw]),
         "mxfp8_linear": (i32, [vp, i32, pw, vp, vp, u, vp, sz, vp]),
         "mx_route_experts": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
-        "mxfp4_moe_workspace_size": (sz, [i32, i32, i32]),
+        "mxfp4_moe_workspace_size": (sz, [i32, i32, i32, i32]),
         "mxfp4_moe_linear": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
-        "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "mxfp8_linear_q_workspace_size": (sz, [i32, pw]),
         "mx_selftest_bounded_wait": (i32, [i32, vp, vp]),
         "mx_e4m3_from_dequant": (i32, [vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(ctypes.c_int64), vp]),
@@ -142,9 +142,12 @@ class PackedWeight:
         return self.buf[off: off + n]
 
     def bytes_tensor(self) -> torch.Tensor:
+        """E4M3: [E, N, Kp]; E2M1: tiles [E, ceil(N/128), Kp/128, 128, 64]."""
         d = self.desc
-        per = d.Kp if d.fmt == MX_FMT_E4M3 else d.Kp // 2
-        return self._region(d.bytes, d.E * d.N * per).view(d.E, d.N, per)
+        if d.fmt == MX_FMT_E4M3:
+            return self._region(d.bytes, d.E * d.N * d.Kp).view(d.E, d.N, d.Kp)
+        rt, kt = (d.N + 127) // 128, d.Kp // 128
+        return self._region(d.bytes, d.E * rt * kt * 8192).view(d.E, rt, kt, 128, 64)
 
     def codes_tensor(self) -> torch.Tensor:
         d = self.desc
@@ -313,8 +316,8 @@ def mx_route_experts(topk_ids: torch.Tensor, E: int, dev_status: torch.Tensor = 
     return r
 
 
-def mxfp4_moe_workspace_size(T: int, topk: int, E: int) -> int:
-    return int(load_library().mxfp4_moe_workspace_size(T, topk, E))
+def mxfp4_moe_workspace_size(T: int, topk: int, E: int, K: int) -> int:
+    return int(load_library().mxfp4_moe_workspace_size(T, topk, E, K))
 
 
 def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, out: torch.Tensor = None,
@@ -326,7 +329,7 @@ def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, o
     if out is None:
         out = torch.empty((T, topk, w.N), dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, "out")
-    need = mxfp4_moe_workspace_size(T, topk, w.E)
+    need = mxfp4_moe_workspace_size(T, topk, w.E, w.K)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(load_library().mxfp4_moe_linear(_ptr(x), _ptr(topk_ids), T, topk, ctypes.byref(w.desc), _ptr(out),
@@ -334,8 +337,8 @@ def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, o
     return out
 
 
-def mxfp4_moe_expert_workspace_size(T: int, topk: int, E: int, I: int, H: int) -> int:
-    return int(load_library().mxfp4_moe_expert_workspace_size(T, topk, E, I, H))
+def mxfp4_moe_expert_workspace_size(T: int, topk: int, E: int, K: int, I: int, H: int) -> int:
+    return int(load_library().mxfp4_moe_expert_workspace_size(T, topk, E, K, I, H))
 
 
 def mxfp4_moe_expert(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, w13: PackedWeight,
@@ -352,7 +355,7 @@ def mxfp4_moe_expert(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torc
         out = torch.empty((T, w2.N), dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, "out")
     if workspace is None:
-        need = mxfp4_moe_expert_workspace_size(T, topk, w13.E, w13.N // 2, w2.N)
+        need = mxfp4_moe_expert_workspace_size(T, topk, w13.E, w13.K, w13.N // 2, w2.N)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(load_library().mxfp4_moe_expert(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), T, topk,
                                            ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(out),

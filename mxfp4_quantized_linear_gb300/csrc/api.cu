@@ -55,9 +55,11 @@ struct PackRegions {
 PackRegions pack_regions(int fmt, int E, int N, int K) {
   PackRegions r;
   const int Kp = padded_k(K);
-  const size_t nbytes = static_cast<size_t>(E) * N * (fmt == MX_FMT_E4M3 ? Kp : Kp / 2);
+  // E2M1: 128-row tiles, so N rounds up to a multiple of 128
+  const size_t nbytes = fmt == MX_FMT_E4M3 ? static_cast<size_t>(E) * N * Kp
+                                           : static_cast<size_t>(E) * ((N + 127) / 128) * 128 * (Kp / 2);
   const size_t ncodes = static_cast<size_t>(E) * N * (Kp / 32);  // row mode is the larger
-  const size_t nsf = fmt == MX_FMT_E4M3 ? static_cast<size_t>(E) * ((N + 127) / 128) * (Kp / 128) * 512 : 0;
+  const size_t nsf = static_cast<size_t>(E) * ((N + 127) / 128) * (Kp / 128) * 512;
   r.bytes_off = kAlign;
   r.codes_off = r.bytes_off + align_up(nbytes, kAlign);
   r.sf_off = r.codes_off + align_up(ncodes, kAlign);
@@ -82,10 +84,12 @@ LinearWs linear_ws(int M, int Kp) {
 }
 
 struct MoeWs {
-  size_t counts, offsets, pairs, active, n_active, status, total;
+  size_t counts, offsets, pairs, active, n_active, status, act, act_bytes, total;
 };
 
-MoeWs moe_ws(int T, int topk, int E) {
+// Routing outputs, then the activation pieces of the T * topk pairs for K
+// values padded to Kp (Kp = 0: routing only).
+MoeWs moe_ws(int T, int topk, int E, int Kp) {
   MoeWs r;
   const size_t P = static_cast<size_t>(T) * topk;
   size_t o = 0;
@@ -95,7 +99,9 @@ MoeWs moe_ws(int T, int topk, int E) {
   r.active = o;   o += align_up(4 * static_cast<size_t>(E), 16);
   r.n_active = o; o += 16;
   r.status = o;   o += 16;
-  r.total = o;
+  r.act = align_up(o, 256);
+  r.act_bytes = Kp > 0 ? moe_act_bytes(static_cast<long long>(P), Kp) : 0;
+  r.total = r.act + r.act_bytes;
   return r;
 }
 
@@ -245,7 +251,7 @@ int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, 
   w.Kp = Kp;
   w.bytes = base + R.bytes_off;
   w.codes = base + R.codes_off;
-  w.sf = fmt == MX_FMT_E4M3 ? base + R.sf_off : nullptr;
+  w.sf = base + R.sf_off;
   if (fmt == MX_FMT_E4M3) {
     bool block;
     if (blocks_given) {
@@ -264,9 +270,8 @@ int mx_pack_weights(const uint8_t* bytes, const uint8_t* codes, int fmt, int E, 
   } else {
     w.scale_mode = MX_SCALE_ROW1X32;
     w.layout = gate_up ? MX_LAYOUT_GATE_UP : MX_LAYOUT_PLAIN;
-    if ((e = launch_pack_e2m1(bytes, codes, E, N, K, Kp, codes_rows, gate_up, w.bytes, w.codes, negz, stream)) !=
-        cudaSuccess)
-      return cuda_fail(e, "pack e2m1");
+    e = launch_pack_e2m1(bytes, codes, E, N, K, Kp, codes_rows, gate_up, w.bytes, w.codes, w.sf, negz, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pack e2m1");
   }
   unsigned long long nz = 0;
   if ((e = cudaMemcpyAsync(&nz, negz, sizeof(nz), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
@@ -493,9 +498,9 @@ int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* c
   return e == cudaSuccess ? MX_OK : cuda_fail(e, "route launch");
 }
 
-size_t mxfp4_moe_workspace_size(int T, int topk, int E) {
-  if (T < 0 || topk < 1 || E < 1) return 0;
-  return moe_ws(T, topk, E).total;
+size_t mxfp4_moe_workspace_size(int T, int topk, int E, int K) {
+  if (T < 0 || topk < 1 || E < 1 || K < 32 || K % 32) return 0;
+  return moe_ws(T, topk, E, padded_k(K)).total;
 }
 
 int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, const mx_packed_weight* w,
@@ -509,7 +514,7 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, co
   if (!x || !topk_ids || !out || !workspace) return set_error(MX_ERR_ARG, "NULL pointer");
   if (!aligned16(x) || !aligned16(out) || !aligned16(workspace))
     return set_error(MX_ERR_ALIGN, "x, out and workspace need 16-byte alignment");
-  const MoeWs R = moe_ws(T, topk, w->E);
+  const MoeWs R = moe_ws(T, topk, w->E, w->Kp);
   if (workspace_bytes < R.total) return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, R.total);
   int rc = check_device();
   if (rc != MX_OK) return rc;
@@ -533,8 +538,11 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, co
   a.pairs = pairs;
   a.active = active;
   a.n_active = n_active;
+  a.lo = 1;
   a.out_mode = 0;
   a.out = out;
+  a.act = ws + R.act;
+  a.act_bytes = R.act_bytes;
   return launch_moe(a, stream);
 }
 
@@ -544,9 +552,11 @@ struct ExpertWs {
   size_t act, y2, total;
 };
 
-static ExpertWs expert_ws(int T, int topk, int E, int I, int H) {
+static ExpertWs expert_ws(int T, int topk, int E, int K, int I, int H) {
   ExpertWs r;
-  r.route = moe_ws(T, topk, E);
+  // the activation pieces serve both projections in turn: sized for the longer K
+  const int Kp = padded_k(K) > padded_k(I) ? padded_k(K) : padded_k(I);
+  r.route = moe_ws(T, topk, E, Kp);
   const size_t P = static_cast<size_t>(T) * topk;
   r.act = align_up(r.route.total, 256);
   r.y2 = align_up(r.act + P * static_cast<size_t>(I) * 2, 256);
@@ -554,9 +564,9 @@ static ExpertWs expert_ws(int T, int topk, int E, int I, int H) {
   return r;
 }
 
-size_t mxfp4_moe_expert_workspace_size(int T, int topk, int E, int I, int H) {
-  if (T < 0 || topk < 1 || E < 1 || I < 1 || H < 1) return 0;
-  return expert_ws(T, topk, E, I, H).total;
+size_t mxfp4_moe_expert_workspace_size(int T, int topk, int E, int K, int I, int H) {
+  if (T < 0 || topk < 1 || E < 1 || K < 32 || K % 32 || I < 32 || I % 32 || H < 1) return 0;
+  return expert_ws(T, topk, E, K, I, H).total;
 }
 
 int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_weights, int T, int topk,
@@ -580,7 +590,7 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   if (!x || !topk_ids || !topk_weights || !out || !workspace) return set_error(MX_ERR_ARG, "NULL pointer");
   if (!aligned16(x) || !aligned16(out) || !aligned16(workspace))
     return set_error(MX_ERR_ALIGN, "x, out and workspace need 16-byte alignment");
-  const ExpertWs R = expert_ws(T, topk, E, I, H);
+  const ExpertWs R = expert_ws(T, topk, E, w13->K, I, H);
   if (workspace_bytes < R.total)
     return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, R.total);
   int rc = check_device();
@@ -597,6 +607,9 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   MoeLaunch a = {};
   a.T = T;
   a.topk = topk;
+  a.lo = 1;
+  a.act = ws + R.route.act;
+  a.act_bytes = R.route.act_bytes;
   a.offsets = offsets;
   a.pairs = pairs;
   a.active = active;

@@ -1,27 +1,22 @@
 // K-ROUTE (token -> expert grouping) and K-MOE (routed A16W4 expert GEMM).
 //
 // A16W4 product (a16w4 = vllm.models.minimax_m3.amd.specialized_decode.mono.a16w4,
-// module text, dequant, step_mfma): MXFP4 weights are dequantized to bf16 in
-// registers and multiplied by the bf16 token activations on tensor cores with
-// f32 accumulation.  Here, as on the page, every e2m1 nibble becomes the bf16
-// value of the dequantized weight e2m1 x 2^(c - 127) (exact: a power-of-two
-// multiply of an exact bf16), and the m16n8k16 bf16 MMAs accumulate the whole
-// K extent straight into the f32 accumulators.
-//
-// The packed weight stores, per 64-byte chunk of a row, word w of K block b at
-// word 4 w + b, and inside each word the element pair (2i, 2i+1) at nibble slots
-// (i, i + 4).  Lane (g, t) of a warp then reads its rows' four words for four K
-// blocks with one 16-byte load (the "16 bytes a lane" lesson of weights942,
-// fp4_lane_major / fp4_tile_major), and each bf16 pair is
-//   ((w >> 4i) & 0x000F000F) * (2^6 + 2^12) & 0x81C081C0   (sign -> bit 15,
-// exponent/mantissa -> bits 6..8, i.e. the value times 2^-126), times 2^126,
-// times the block's 2^(c - 127).
+// module text, dequant, step_mfma): every MXFP4 weight is its e2m1 value times
+// the row's E8M0 block scale, multiplied by the bf16 token activations with f32
+// accumulation.  On the 5th-generation tensor cores this is a block-scaled
+// product of kind::mxf8f6f4 with an e2m1 A operand (the weight, its codes E8M0
+// scale factors in tensor memory) and an e4m3 B operand: the bf16 activation
+// enters as two MXFP8 pieces hi + lo (see act_pieces_kernel) whose products
+// accumulate into the same f32 accumulator.  The MXFP8-activation variant (MXFP4 x MXFP8, the
+// prefill form of the same layer) uses hi alone, which is exactly the per-token
+// MXFP8 quantization of the activation.
 //
 // Routing is the plainest reading of "routed experts" (the pages show no
 // router): pairs grouped by expert id, stable in (token, slot) order.
 
 #include "mx_common.cuh"
 #include "mx_internal.h"
+#include "tc_common.cuh"
 
 namespace mx {
 namespace {
@@ -145,65 +140,149 @@ constexpr int kMoeOutBf16 = 0;    // out [pairs, N] bf16 (rows in gate-then-up o
 constexpr int kMoeOutSwiglu = 1;  // out [pairs, N/2] bf16 = silu(gate) * up
 constexpr int kMoeOutF32 = 2;     // out_f32 [pairs, N] f32
 
-constexpr int kMoeWarps = 8;
-constexpr int kMoeRows = kMoeWarps * 16;  // 128 weight rows a CTA
-constexpr int kMoeTok = 16;               // tokens a chunk (two n8 tiles)
-constexpr int kStageSteps = 4;            // 128-wide K steps a ring stage (256 bytes a row)
-constexpr int kStageK = kStageSteps * 128;                   // 512 K elements
-constexpr int kWarpStageBytes = 16 * kStageSteps * 64;       // 4 KB: two 16x128-byte boxes
-constexpr int kRing = 2;                                     // stages a warp keeps in flight
-constexpr int kChunkBytes = kMoeTok * kStageK * 2;           // 16 KB of bf16 activations a stage
-constexpr int kMoeSmem = kMoeWarps * kRing * kWarpStageBytes + 2 * kChunkBytes + 1024;
+// ---------------------------------------------------------------- activation pieces
+//
+// The routed pairs' activation rows, gathered in the expert-sorted pair order
+// and cut into 32-wide MX blocks.  A16 (bf16 activations): each block is
+// written as two MXFP8 pieces, hi = the per-token MXFP8 quantization of x and
+// lo = the same quantization of the residual x - hi (exact in f32), so that
+// hi + lo = x except where an element lies below the e4m3 normal range of its
+// block's residual scale (|x - hi - lo| <= 2^-21.8 max|x| over the block).
+// MXFP8 activations: hi only.  Row j of xh / xl is pair pairs[j]; its codes
+// for K step s sit at cs[j][s][0..3] (hi) and cs[j][s][4..7] (lo): one
+// 16-byte row of a tcgen05 scale-factor atom, whose first column scales B
+// rows 0..31 (the hi pieces of 32 pairs) and second column rows 32..63 (their
+// lo pieces).
+__device__ __forceinline__ uint32_t mx_quant_f32x32(const float (&v)[32], uint4 (&out)[2]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  const uint32_t code = mx_block_code(amax);
+  const uint32_t ef = 254u - code;
+  const float rescale = ef ? __uint_as_float(ef << 23) : __uint_as_float(0x00400000u);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = f32x2_to_e4m3x2(v[4 * i] * rescale, v[4 * i + 1] * rescale) |
+           (f32x2_to_e4m3x2(v[4 * i + 2] * rescale, v[4 * i + 3] * rescale) << 16);
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return code;
+}
+
+// Rows past the routed pairs (slots with an invalid id are in no expert's
+// list, so the list holds *n_pairs <= P entries) are left as they are: they
+// only ever fill unused columns of a pass's last 32-row box.
+__global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pairs,
+                                  const int32_t* __restrict__ n_pairs, int P, int topk, int x_per_pair, int K,
+                                  int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl,
+                                  uint8_t* __restrict__ cs) {
+  const int KBp = Kp >> 5, KB = K >> 5, KT = Kp >> 7;
+  const int nv = *n_pairs;
+  const long long total = static_cast<long long>(nv < P ? nv : P) * KBp;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long j = i / KBp;
+    const int b = static_cast<int>(i % KBp);
+    const int pr = pairs[j];
+    const long long src = x_per_pair ? pr : pr / topk;
+    uint4 qh[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    uint4 ql[2] = {qh[0], qh[1]};
+    uint32_t ch = 127u, cl = 127u;  // padded K blocks: zero bytes, a finite code
+    if (b < KB) {
+      const uint4* sp = reinterpret_cast<const uint4*>(x + src * K + 32 * b);
+      const uint4 u[4] = {sp[0], sp[1], sp[2], sp[3]};
+      ch = mx_quant_bf16x32(u, qh);
+      if (lo && ch != 255u) {
+        const float scale = e8m0_to_f32(ch);
+        const uint32_t hw[8] = {qh[0].x, qh[0].y, qh[0].z, qh[0].w, qh[1].x, qh[1].y, qh[1].z, qh[1].w};
+        const uint32_t xw[16] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w,
+                                 u[2].x, u[2].y, u[2].z, u[2].w, u[3].x, u[3].y, u[3].z, u[3].w};
+        float r[32];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          // elements 2q, 2q + 1: bf16 -> f32 exactly, minus the dequantized hi piece
+          const __half2 h = e4m3x2_to_f16x2(static_cast<uint16_t>(hw[q >> 1] >> (16 * (q & 1))));
+          r[2 * q] = __uint_as_float(xw[q] << 16) - __low2float(h) * scale;
+          r[2 * q + 1] = __uint_as_float(xw[q] & 0xffff0000u) - __high2float(h) * scale;
+        }
+        cl = mx_quant_f32x32(r, ql);
+      }
+    }
+    uint4* hp = reinterpret_cast<uint4*>(xh + j * Kp + 32 * b);
+    hp[0] = qh[0];
+    hp[1] = qh[1];
+    uint8_t* cp = cs + (j * KT + (b >> 2)) * 16 + (b & 3);
+    cp[0] = static_cast<uint8_t>(ch);
+    if (lo) {
+      uint4* lp = reinterpret_cast<uint4*>(xl + j * Kp + 32 * b);
+      lp[0] = ql[0];
+      lp[1] = ql[1];
+      cp[4] = static_cast<uint8_t>(cl);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- expert GEMM
+//
+// CTA = one 128-row tile of one active expert, 12 warps:
+//   warp 0 (lane 0)  streams the packed e2m1 weight tile, one contiguous 8 KB
+//                    block (128 rows x 64 bytes) a K step, and the step's
+//                    512-byte weight scale atom (bulk copies);
+//   warp 2 (lane 0)  streams the gathered activation pieces of the expert's
+//                    next 32 pairs: 32 rows x 128 bytes of hi and of lo
+//                    (128B swizzle) and their scale atoms;
+//   warps 4..7       lay each weight step out as the tensor core's e2m1
+//                    operand: 128B-swizzled K-major rows in which every 16
+//                    values (8 packed bytes) take a 16-byte chunk, the E8M0
+//                    scale staying a scale factor; four 16-byte chunks a thread;
+//   warp 1 (lane 0)  allocates tensor memory and issues, per K step, the scale
+//                    copies and 4 block-scaled MMAs (kind::mxf8f6f4,
+//                    scale_vec::1X, M = 128 weight rows, K = 32) whose B
+//                    operand stacks the 32 pairs' hi pieces (rows 0..31) on
+//                    their lo pieces (rows 32..63), N = 64: one f32
+//                    accumulator column a piece of a pair;
+//   warps 8..11      read the accumulator (tcgen05.ld, one lane quarter each),
+//                    add each pair's hi and lo columns and store bf16 /
+//                    SiLU-and-mul / f32 per pair.
+// Rings: 5 weight stages, 2 converted stages, 3 activation stages; two CTAs
+// per SM.
+constexpr int kTok = 32;                   // pairs a pass (MMA N <= 32)
+constexpr int kWStages = 5, kAStages = 2, kXStages = 3;
+constexpr int kWStage = 128 * 64 + 512;   // packed step | weight scale atom
+constexpr int kAStage = 128 * 128;        // e4m3 step, 128B swizzle
+constexpr int kXStage = (2 * kTok * 128 + 512 + 1023) & ~1023;  // hi rows | lo rows | scale atom (1 KB aligned)
+constexpr int kAOff = 0;
+constexpr int kXOff = kAOff + kAStages * kAStage;
+constexpr int kWOff = kXOff + kXStages * kXStage;
+constexpr int kSfaOff = kWOff + kWStages * kWStage;
+constexpr int kBarOff = (kSfaOff + kAStages * 512 + 1023) & ~1023;
+constexpr int kBarBytes = ((2 * (kWStages + kAStages + kXStages) + 2) * 8 + 8 + 255) & ~255;  // + TMEM slot, flag
+constexpr int kTcSmem = kBarOff + kBarBytes + 1024;
+constexpr int kTcThreads = 384;
+// tensor memory: accumulator 64 columns (hi 0..31, lo 32..63) | a (SFA 4,
+// SFB 4) slot per converted stage, rounded up to a power of two
+constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? c : pow2_at_least(v, 2 * c); }
+constexpr uint32_t kAccCols = 2 * kTok;
+constexpr uint32_t kTcTmemCols = pow2_at_least(kAccCols + 8 * kAStages);
+constexpr uint32_t kIdescTok16 = mxf8_idesc_a(128, 16, kFmtE2M1);
+constexpr uint32_t kIdescTok32 = mxf8_idesc_a(128, 32, kFmtE2M1);
+constexpr uint32_t kIdescPieces = mxf8_idesc_a(128, 2 * kTok, kFmtE2M1);
 
 struct MoeParams {
-  const __nv_bfloat16* x;  // [T, K] (one row a token) or [T * topk, K] (one row a pair)
-  const uint8_t* codes;    // [E, N, Kp/32]
+  const uint8_t* w;        // packed weight tiles [E, NT, KT, 128, 64]
+  const uint8_t* sfw;      // weight scale atoms [E, NT, KT, 512]
   const int32_t* offsets;
   const int32_t* pairs;
   const int32_t* active;
   const int32_t* n_active;
   __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
   float* out_f32;          // kMoeOutF32: [T * topk, N]
-  int topk, N, K, Kp, nsteps;
-  int x_per_pair;          // 1: activation row = pair index (the down projection)
+  int N, KT, NT;
+  int lo;                  // 1: hi and lo activation pieces (A16), 0: hi only (MXFP8)
   int gate_up;             // weight rows interleaved gate / up in 8-row groups
   int out_mode;
 };
-
-// E8M0 code c of one block -> bf16x2 {2^(c-127), 2^(c-127)}: exponent field c
-// in both halves; code 0 -> the bf16 subnormal 2^-127 (0x0040).  Weight codes
-// are never 255 (the packer rejects them).
-MX_DEV uint32_t e8m0_to_bf16x2(uint32_t c) { return __vmaxu2(c * 0x00800080u, 0x00400040u); }
-
-// e2m1 x 8 (nibble slots (i, i+4) = elements (2i, 2i+1)) -> 4 bf16 pairs of the
-// dequantized weight e2m1 x 2^(c-127), exact (a16w4, dequant: fp4 with its
-// E8M0 scale to bf16).  The sign and the 3 exponent/mantissa bits land in a
-// bf16 whose value is the e2m1 value x 2^-126 (e2m1 subnormals map onto bf16
-// subnormals); two power-of-two multiplies give the scaled value.
-MX_DEV void e2m1x8_to_bf16x8_scaled(uint32_t w, uint32_t scale2, uint32_t (&r)[4]) {
-  const __nv_bfloat162 two126 = __halves2bfloat162(__ushort_as_bfloat16(0x7e80),
-                                                   __ushort_as_bfloat16(0x7e80));
-  const __nv_bfloat162 sc = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t u = (w >> (4 * i)) & 0x000f000fu;
-    const uint32_t v = (u * 0x1040u) & 0x81c081c0u;
-    const __nv_bfloat162 b = __hmul2(__hmul2(*reinterpret_cast<const __nv_bfloat162*>(&v), two126), sc);
-    r[i] = *reinterpret_cast<const uint32_t*>(&b);
-  }
-}
-
-// 16-byte chunk c (0..63) of token row tk in an activation stage; the XOR by
-// (tk & 1) * 4 keeps the 8 lanes of a quarter warp (2 tokens x 4 chunks) on
-// distinct banks.
-MX_DEV int xs_off(int tk, int c) { return tk * (kStageK * 2) + ((c ^ ((tk & 1) << 2)) << 4); }
-
-MX_DEV void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-MX_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-MX_DEV void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 MX_DEV uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
@@ -219,175 +298,211 @@ MX_DEV int gate_up_row(int r, int N) {
 
 MX_DEV float silu_f32(float v) { return v / (1.0f + expf(-v)); }
 
-__global__ void __launch_bounds__(kMoeWarps * 32, 2) moe_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                                const MoeParams p) {
+__global__ void __launch_bounds__(kTcThreads, 2) moe_kernel(const __grid_constant__ CUtensorMap xhmap,
+                                                             const __grid_constant__ CUtensorMap xlmap,
+                                                             const __grid_constant__ CUtensorMap csmap,
+                                                             const MoeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* wring = smem;                                              // [warp][kRing][4 KB]
-  uint8_t* xs = smem + kMoeWarps * kRing * kWarpStageBytes;           // [2][16 KB]
-  __shared__ uint64_t bars[kMoeWarps][kRing];
-  __shared__ int tok_src[kMoeTok];   // token row of x, or -1
-  __shared__ int tok_pair[kMoeTok];  // output row (pair index), or -1
-
   const int a = blockIdx.y;
-  if (a >= *p.n_active) return;
+  if (a >= *p.n_active) return;  // the whole CTA: no barrier or tensor memory touched yet
   const int e = p.active[a];
   const int o0 = p.offsets[e];
   const int cnt = p.offsets[e + 1] - o0;
-
+  const int nch = (cnt + kTok - 1) / kTok;
+  const int rt = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
-  const int row0 = blockIdx.x * kMoeRows;
-  const int wrow = row0 + warp * 16;        // this warp's first row within the expert
-  const int rg = wrow + g;                   // rows rg and rg + 8
-  const int KBp = p.Kp >> 5;
-  const bool v0 = rg < p.N, v1 = rg + 8 < p.N;
-  const long long erow = static_cast<long long>(e) * p.N;
-  const uint8_t* c0p = p.codes + (erow + (v0 ? rg : 0)) * KBp;
-  const uint8_t* c1p = p.codes + (erow + (v1 ? rg + 8 : 0)) * KBp;
-  const int nst = (p.nsteps + kStageSteps - 1) / kStageSteps;  // ring stages along K
-  uint8_t* myring = wring + warp * kRing * kWarpStageBytes;
-  uint64_t* mybar = bars[warp];
-  const int grow = static_cast<int>(erow) + wrow;               // row in the flattened [E*N] map
-  const uint64_t pol = policy_evict_first();
-  uint32_t uses = 0;  // parity of each ring slot's next completion
 
-  if (lane == 0) {
-    for (int s = 0; s < kRing; ++s) mbar_init(&mybar[s], 1);
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* wempty = wfull + kWStages;
+  uint64_t* afull = wempty + kWStages;
+  uint64_t* aempty = afull + kAStages;
+  uint64_t* xfull = aempty + kAStages;
+  uint64_t* xempty = xfull + kXStages;
+  uint64_t* accfull = xempty + kXStages;
+  uint64_t* accempty = accfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], 4);     // one arrival a converter warp
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&afull[i], 128);    // every converter thread
+      mbar_init(&aempty[i], 1);     // tcgen05.commit
+    }
+    for (int i = 0; i < kXStages; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xempty[i], 1);     // tcgen05.commit
+    }
+    mbar_init(accfull, 1);
+    mbar_init(accempty, 4);         // one arrival an epilogue warp
+    *abort_flag = 0u;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  __syncwarp();
-  auto issue = [&](int st, int slot) {  // weights of ring stage st (4 steps, 16 rows)
-    uint8_t* dst = myring + slot * kWarpStageBytes;
-    mbar_arrive_expect_tx(&mybar[slot], kWarpStageBytes);
-    tma_load_2d(dst, &wmap, &mybar[slot], st * 256, grow, pol);
-    tma_load_2d(dst + 2048, &wmap, &mybar[slot], st * 256 + 128, grow, pol);
-  };
+  if (warp == 1) tmem_alloc(tmem_slot, kTcTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  for (int ch = 0; ch < cnt; ch += kMoeTok) {
-    // ---- 1. weight stages 0..kRing-1 (independent of the tokens)
-    if (lane == 0)
-      for (int s = 0; s < kRing && s < nst; ++s) issue(s, s);
-    // ---- 2. the chunk's tokens and the first two activation stages
-    if (threadIdx.x < kMoeTok) {
-      const int pr = (ch + static_cast<int>(threadIdx.x) < cnt) ? p.pairs[o0 + ch + threadIdx.x] : -1;
-      tok_pair[threadIdx.x] = pr;
-      tok_src[threadIdx.x] = pr >= 0 ? (p.x_per_pair ? pr : pr / p.topk) : -1;
-    }
-    __syncthreads();
-    auto load_x = [&](int st, int buf) {
-      const uint32_t dst = smem_u32(xs + buf * kChunkBytes);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int idx = threadIdx.x + j * kMoeWarps * 32;  // 1024 chunks of 16 bytes
-        const int tk = idx >> 6, cc = idx & 63;
-        const int src = tok_src[tk];
-        const int k = st * kStageK + cc * 8;
-        const bool ok = src >= 0 && k < p.K && st < nst;
-        const __nv_bfloat16* sp = ok ? p.x + static_cast<long long>(src) * p.K + k : p.x;
-        cp_async16(dst + xs_off(tk, cc), sp, ok);
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ weight producer
+    // the tile's K steps are consecutive 8 KB blocks, its scale atoms 512 B each
+    const long long tile = static_cast<long long>(e) * p.NT + rt;
+    const uint8_t* wt = p.w + tile * p.KT * 8192;
+    const uint8_t* sfa = p.sfw + tile * p.KT * 512;
+    int g = 0;
+    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
+      for (int s = 0; s < p.KT; ++s, ++g) {
+        const int st = g % kWStages;
+        if (!mbar_wait(&wempty[st], ((g / kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+        uint8_t* dst = smem + kWOff + st * kWStage;
+        mbar_arrive_expect_tx(&wfull[st], kWStage);
+        bulk_load(dst, wt + s * 8192, 8192, &wfull[st]);
+        bulk_load(dst + 128 * 64, sfa + s * 512, 512, &wfull[st]);
       }
-      cp_async_commit();
-    };
-    load_x(0, 0);
-    load_x(1, 1);
-    uint4 cnext0, cnext1;  // codes of the next stage: 4 steps x 4 blocks, rows rg and rg + 8
-    auto load_codes = [&](int st, uint4& c0, uint4& c1) {
-      const uint32_t* a0 = reinterpret_cast<const uint32_t*>(c0p + st * 16);
-      const uint32_t* a1 = reinterpret_cast<const uint32_t*>(c1p + st * 16);
-      const int nsl = p.nsteps - st * kStageSteps;  // steps of this stage that exist
-      c0.x = a0[0]; c1.x = a1[0];
-      c0.y = nsl > 1 ? a0[1] : 0x7f7f7f7fu; c1.y = nsl > 1 ? a1[1] : 0x7f7f7f7fu;
-      c0.z = nsl > 2 ? a0[2] : 0x7f7f7f7fu; c1.z = nsl > 2 ? a1[2] : 0x7f7f7f7fu;
-      c0.w = nsl > 3 ? a0[3] : 0x7f7f7f7fu; c1.w = nsl > 3 ? a1[3] : 0x7f7f7f7fu;
-    };
-    load_codes(0, cnext0, cnext1);
-    // a chunk of at most 8 tokens needs only the first n8 tile of the MMA
-    const int ntile = (cnt - ch) > 8 ? 2 : 1;
-
-    float acc[2][4];
+    }
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------------ activation producer
+    tma_prefetch_desc(&xhmap);
+    tma_prefetch_desc(&csmap);
+    if (p.lo) tma_prefetch_desc(&xlmap);
+    const uint64_t pol = policy_evict_last();  // every row tile of the expert reads them
+    const uint32_t tx = p.lo ? 2 * kTok * 128 + 512 : kTok * 128 + 512;
+    int g = 0;
+    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
+      const int row0 = o0 + ch * kTok;
+      for (int s = 0; s < p.KT; ++s, ++g) {
+        const int st = g % kXStages;
+        if (!mbar_wait(&xempty[st], ((g / kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+        uint8_t* dst = smem + kXOff + st * kXStage;
+        mbar_arrive_expect_tx(&xfull[st], tx);
+        tma_load_2d(dst, &xhmap, &xfull[st], s * 128, row0, pol);
+        tma_load_2d(dst + 2 * kTok * 128, &csmap, &xfull[st], s * 16, row0, pol);
+        if (p.lo) tma_load_2d(dst + kTok * 128, &xlmap, &xfull[st], s * 128, row0, pol);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int ga = 0, gx = 0;
+    uint32_t acc_phase = 0;
+    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
+      const int ntok = cnt - ch * kTok < kTok ? cnt - ch * kTok : kTok;
+      const uint32_t idesc = p.lo ? kIdescPieces : (ntok <= 16 ? kIdescTok16 : kIdescTok32);
+      if (!mbar_wait(accempty, acc_phase ^ 1u)) { *abort_flag = 1u; break; }
+      tc_fence_after();
+      bool ok = true;
+      for (int s = 0; s < p.KT; ++s, ++ga, ++gx) {
+        const int as = ga % kAStages, xs = gx % kXStages;
+        if (!mbar_wait(&afull[as], (ga / kAStages) & 1u) || !mbar_wait(&xfull[xs], (gx / kXStages) & 1u)) {
+          *abort_flag = 1u;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t xb = smem_u32(smem + kXOff + xs * kXStage);
+        const uint32_t sfc = tmem + kAccCols + static_cast<uint32_t>(as * 8);
+        tc_cp_sf(sfc, sf_desc(smem_u32(smem + kSfaOff + as * 512)));
+        tc_cp_sf(sfc + 4, sf_desc(xb + 2 * kTok * 128));
+        const uint64_t adesc = sw128_desc(smem_u32(smem + kAOff + as * kAStage));
+        const uint64_t bdesc = sw128_desc(xb);  // 64 rows: hi 0..31 then lo 32..63 (A16)
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+          tc_mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, id, sfc, sfc + 4, (s | k) != 0 ? 1u : 0u);
+        }
+        tc_commit(&aempty[as]);
+        tc_commit(&xempty[xs]);
+      }
+      if (!ok) break;
+      tc_commit(accfull);
+      acc_phase ^= 1u;
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ e2m1 operand
+    const int i = threadIdx.x - 128;
+    int g = 0;
+    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
+      bool ok = true;
+      for (int s = 0; s < p.KT; ++s, ++g) {
+        const int ws = g % kWStages, as = g % kAStages;
+        if (!mbar_wait(&wfull[ws], (g / kWStages) & 1u) || !mbar_wait(&aempty[as], ((g / kAStages) & 1u) ^ 1u)) {
+          *abort_flag = 1u;
+          ok = false;
+          break;
+        }
+        const uint32_t src = smem_u32(smem + kWOff + ws * kWStage);
+        uint8_t* dst = smem + kAOff + as * kAStage;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[h][i] = 0.0f;
-
-    for (int st = 0; st < nst; ++st) {
-      const int slot = st % kRing;
-      const uint4 cs0 = cnext0, cs1 = cnext1;
-      if (st + 1 < nst) load_codes(st + 1, cnext0, cnext1);
-      cp_async_wait1();
-      __syncthreads();  // activation stage st is in shared memory for every warp
-      mbar_wait(&mybar[slot], (uses >> slot) & 1u);
-      const uint32_t wbase = smem_u32(myring + slot * kWarpStageBytes);
-      const uint32_t xbase = smem_u32(xs + (st & 1) * kChunkBytes);
-      const uint32_t c0w[4] = {cs0.x, cs0.y, cs0.z, cs0.w};
-      const uint32_t c1w[4] = {cs1.x, cs1.y, cs1.z, cs1.w};
+        for (int it = 0; it < 4; ++it) {
+          // 16-byte chunk idx of the packed step: row r, K block b (32 values)
+          const int idx = it * 128 + i, r = idx >> 2, b = idx & 3;
+          const uint4 v = ld_shared_v4(src + r * 64 + b * 16);
+          // K values 32 b .. 32 b + 15 and + 16 .. + 31: 16-byte chunks 2 b and
+          // 2 b + 1 of row r (128B swizzle), 8 packed bytes then 8 of padding
+          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(v.z, v.w, 0u, 0u);
+        }
+        if (i < 32)  // the weight scale atom moves with the converted step
+          *reinterpret_cast<uint4*>(smem + kSfaOff + as * 512 + i * 16) = ld_shared_v4(src + 128 * 64 + i * 16);
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        mbar_arrive(&afull[as]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[ws]);
+      }
+      if (!ok) break;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter: rows 32 q .. 32 q + 31
+    const int n = rt * 128 + q * 32 + lane;
+    const unsigned full = 0xffffffffu;
+    uint32_t acc_phase = 0;
+    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
+      const int ntok = cnt - ch * kTok < kTok ? cnt - ch * kTok : kTok;
+      const int pr = lane < ntok ? p.pairs[o0 + ch * kTok + lane] : -1;
+      if (!mbar_wait(accfull, acc_phase)) { *abort_flag = 1u; break; }
+      tc_fence_after();
+      uint32_t v[32], vl[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16), v);
+      if (p.lo) {
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kTok, vl);
 #pragma unroll
-      for (int s = 0; s < kStageSteps; ++s) {
-        if (st * kStageSteps + s < p.nsteps) {
-          // this lane's 16 bytes (4 K blocks, word tq) of rows g and g + 8; box s / 2,
-          // 128B swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
-          const int c = (s & 1) * 4 + tq;
-          const uint32_t box = wbase + (s >> 1) * 2048;
-          const uint4 wa4 = ld_shared_v4(box + g * 128 + ((c ^ g) << 4));
-          const uint4 wc4 = ld_shared_v4(box + (g + 8) * 128 + ((c ^ g) << 4));
-          const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w};
-          const uint32_t wc[4] = {wc4.x, wc4.y, wc4.z, wc4.w};
+        for (int t = 0; t < kTok; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(vl[t]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty);  // the next pass may overwrite the accumulator
+      acc_phase ^= 1u;
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            uint32_t ra[4], rc[4];
-            e2m1x8_to_bf16x8_scaled(wa[b], e8m0_to_bf16x2((c0w[s] >> (8 * b)) & 0xffu), ra);
-            e2m1x8_to_bf16x8_scaled(wc[b], e8m0_to_bf16x2((c1w[s] >> (8 * b)) & 0xffu), rc);
-            const int xc = s * 16 + b * 4 + tq;  // 16-byte activation chunk: K = 8 xc .. + 7
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (h >= ntile) break;  // block-uniform
-              const int tk = h * 8 + g;
-              const uint4 xv = ld_shared_v4(xbase + xs_off(tk, xc));
-              // the weights carry their block scale: accumulate straight into acc
-              mma_bf16_16816(acc[h], ra[0], rc[0], ra[1], rc[1], xv.x, xv.y);
-              mma_bf16_16816(acc[h], ra[2], rc[2], ra[3], rc[3], xv.z, xv.w);
-            }
-          }
+      for (int t = 0; t < kTok; ++t) {
+        if (t >= ntok) break;  // warp-uniform
+        const int pt = __shfl_sync(full, pr, t);
+        const float y = __uint_as_float(v[t]);
+        if (p.out_mode == kMoeOutSwiglu) {
+          // lane l (l % 16 < 8) holds gate row 8 (n / 16) + l % 16, lane l + 8 its up row
+          const float u = __shfl_down_sync(full, y, 8);
+          if ((lane & 15) < 8 && n < p.N)
+            p.out[static_cast<long long>(pt) * (p.N >> 1) + (n >> 4) * 8 + (n & 15)] =
+                __float2bfloat16_rn(silu_f32(y) * u);
+        } else if (p.out_mode == kMoeOutF32) {
+          if (n < p.N) p.out_f32[static_cast<long long>(pt) * p.N + n] = y;
+        } else if (p.out_mode == kMoeOutBf16 && n < p.N) {
+          const int nn = p.gate_up ? gate_up_row(n, p.N) : n;
+          p.out[static_cast<long long>(pt) * p.N + nn] = __float2bfloat16_rn(y);
         }
       }
-      uses ^= 1u << slot;
-      __syncwarp();
-      if (lane == 0 && st + kRing < nst) issue(st + kRing, slot);
-      __syncthreads();  // every warp is done with activation stage st
-      load_x(st + 2, st & 1);
     }
-
-    // ---- 3. store the chunk's rows: acc[h][0..1] are row rg, [2..3] row rg + 8,
-    // columns (tokens) h * 8 + 2 tq and + 1
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t0 = h * 8 + 2 * tq;
-      const int pa = tok_pair[t0], pb = tok_pair[t0 + 1];
-      if (p.out_mode == kMoeOutSwiglu) {
-        // rows rg (gate) and rg + 8 (up) are gate / up of intermediate index i
-        const int I = p.N >> 1, i = (wrow >> 1) + g;
-        if (pa >= 0 && v1)
-          p.out[static_cast<long long>(pa) * I + i] = __float2bfloat16_rn(silu_f32(acc[h][0]) * acc[h][2]);
-        if (pb >= 0 && v1)
-          p.out[static_cast<long long>(pb) * I + i] = __float2bfloat16_rn(silu_f32(acc[h][1]) * acc[h][3]);
-      } else if (p.out_mode == kMoeOutF32) {
-        if (pa >= 0 && v0) p.out_f32[static_cast<long long>(pa) * p.N + rg] = acc[h][0];
-        if (pb >= 0 && v0) p.out_f32[static_cast<long long>(pb) * p.N + rg] = acc[h][1];
-        if (pa >= 0 && v1) p.out_f32[static_cast<long long>(pa) * p.N + rg + 8] = acc[h][2];
-        if (pb >= 0 && v1) p.out_f32[static_cast<long long>(pb) * p.N + rg + 8] = acc[h][3];
-      } else {
-        const int n0 = p.gate_up ? gate_up_row(rg, p.N) : rg;
-        const int n1 = p.gate_up ? gate_up_row(rg + 8, p.N) : rg + 8;
-        if (pa >= 0 && v0) p.out[static_cast<long long>(pa) * p.N + n0] = __float2bfloat16_rn(acc[h][0]);
-        if (pb >= 0 && v0) p.out[static_cast<long long>(pb) * p.N + n0] = __float2bfloat16_rn(acc[h][1]);
-        if (pa >= 0 && v1) p.out[static_cast<long long>(pa) * p.N + n1] = __float2bfloat16_rn(acc[h][2]);
-        if (pb >= 0 && v1) p.out[static_cast<long long>(pb) * p.N + n1] = __float2bfloat16_rn(acc[h][3]);
-      }
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();  // tok_* and the buffers are reused by the next chunk of tokens
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
   }
 }
 
@@ -423,49 +538,67 @@ cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts
   return cudaGetLastError();
 }
 
+// Activation pieces of P pairs: xh [P + 32, Kp] | xl [P + 32, Kp] | codes
+// [P + 32, Kp/128, 16], each region 256-byte aligned (32 spare rows: the last
+// pass of pairs loads a full 32-row box).
+static size_t act_region(long long P, int Kp) { return (static_cast<size_t>(P + kTok) * Kp + 255) & ~size_t(255); }
+static size_t act_codes(long long P, int Kp) {
+  return (static_cast<size_t>(P + kTok) * (Kp / 128) * 16 + 255) & ~size_t(255);
+}
+size_t moe_act_bytes(long long P, int Kp) { return 2 * act_region(P, Kp) + act_codes(P, Kp); }
+
 int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   const mx_packed_weight* w = a.w;
-  const void* x = a.x;
-  const int T = a.T, topk = a.topk;
+  const long long P = static_cast<long long>(a.T) * a.topk;
+  const int Kp = w->Kp, KT = Kp / 128;
+  if (!w->sf) return set_error(MX_ERR_ARG, "the E2M1 weight has no scale atoms (pack it with mx_pack_weights)");
+  if (!a.act || a.act_bytes < moe_act_bytes(P, Kp))
+    return set_error(MX_ERR_WORKSPACE, "expert activation workspace of %zu bytes, needs %zu", a.act_bytes,
+                     moe_act_bytes(P, Kp));
+  uint8_t* xh = static_cast<uint8_t*>(a.act);
+  uint8_t* xl = xh + act_region(P, Kp);
+  uint8_t* cs = xl + act_region(P, Kp);
+  const long long nblk = P * (Kp / 32);
+  act_pieces_kernel<<<blocks_for(nblk, 256), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.x), a.pairs, a.offsets + w->E, static_cast<int>(P), a.topk,
+      a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
+
   MoeParams p = {};
-  p.x_per_pair = a.x_per_pair;
+  p.w = w->bytes;
+  p.sfw = w->sf;
+  p.offsets = a.offsets;
+  p.pairs = a.pairs;
+  p.active = a.active;
+  p.n_active = a.n_active;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.out_f32 = static_cast<float*>(a.out_f32);
+  p.N = w->N;
+  p.KT = KT;
+  p.NT = (w->N + 127) / 128;
+  p.lo = a.lo;
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
-  p.out_f32 = static_cast<float*>(a.out_f32);
-  const int32_t* offsets = a.offsets;
-  const int32_t* pairs = a.pairs;
-  const int32_t* active = a.active;
-  const int32_t* n_active = a.n_active;
-  void* out = a.out;
-  p.x = static_cast<const __nv_bfloat16*>(x);
-  p.codes = w->codes;
-  p.offsets = offsets;
-  p.pairs = pairs;
-  p.active = active;
-  p.n_active = n_active;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.topk = topk;
-  p.N = w->N;
-  p.K = w->K;
-  p.Kp = w->Kp;
-  p.nsteps = w->Kp / 128;
-  // a 128-byte weight box per row and step: rows of at least 128 packed bytes
-  if (w->Kp < 256) return set_error(MX_ERR_UNSUPPORTED, "MXFP4 experts need K > 128 (K = %d)", w->K);
-  CUtensorMap wmap;
-  const int KHp = w->Kp / 2;
-  int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_UINT8, KHp,
-                                static_cast<uint64_t>(w->E) * w->N, KHp, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t rows = static_cast<uint64_t>(P + kTok);
+  CUtensorMap xhmap, xlmap, csmap;
+  int rc = encode_tensor_map_2d(&xhmap, xh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == MX_OK)
+    rc = encode_tensor_map_2d(&xlmap, xl, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == MX_OK)
+    rc = encode_tensor_map_2d(&csmap, cs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(KT) * 16, rows,
+                              static_cast<uint64_t>(KT) * 16, 16, kTok, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != MX_OK) return rc;
   DeviceInfo di;
   if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
   static int smem_set[64];
-  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel), kMoeSmem, di, smem_set) != MX_OK)
+  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel), kTcSmem, di, smem_set) != MX_OK)
     return MX_ERR_CUDA;
-  cudaError_t e;
-  const long long P = static_cast<long long>(T) * topk;
   const int zmax = static_cast<int>(P < w->E ? P : w->E);
-  dim3 grid((w->N + kMoeRows - 1) / kMoeRows, zmax, 1);
-  moe_kernel<<<grid, kMoeWarps * 32, kMoeSmem, stream>>>(wmap, p);
+  dim3 grid(p.NT, zmax, 1);
+  moe_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(xhmap, xlmap, csmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;

@@ -67,7 +67,7 @@ cudaError_t launch_from_dequant(const void* w, const uint8_t* codes, int block_s
                                 unsigned long long* mismatches, cudaStream_t stream);
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
                              int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
-                             unsigned long long* negz, cudaStream_t stream);
+                             uint8_t* sf, unsigned long long* negz, cudaStream_t stream);
 
 // ---- decode GEMV (gemv.cu)
 struct GemvArgs {
@@ -129,10 +129,14 @@ struct MoeLaunch {
   const mx_packed_weight* w;
   const int32_t *offsets, *pairs, *active, *n_active;  // routing (mx_route_experts)
   int x_per_pair;
+  int lo;                      // 1: bf16 activation as MXFP8 hi + lo pieces (A16); 0: hi only (MXFP8)
   int out_mode;                // 0: out bf16 [pairs, N]; 1: out bf16 [pairs, N/2] = silu(gate) * up; 2: out_f32
   void* out;
   void* out_f32;               // f32 [pairs, N]
+  void* act;                   // activation pieces, moe_act_bytes(T * topk, Kp) bytes, 256-byte aligned
+  size_t act_bytes;
 };
+size_t moe_act_bytes(long long P, int Kp);
 int launch_moe(const MoeLaunch& a, cudaStream_t stream);
 unsigned int take_error_flags_moe();
 unsigned int take_error_flags_selftest();

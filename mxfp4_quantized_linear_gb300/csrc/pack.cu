@@ -90,7 +90,7 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ codes, int E, int 
 // SF atoms [E, ceil(N/128), Kp/128, 512]: row n = 128 rt + m, block j = 4 kt + kb
 // at byte (m % 32) * 16 + (m / 32) * 4 + kb.
 __global__ void pack_sf_kernel(const uint8_t* __restrict__ codes, int E, int N, int KB, int Kp,
-                               int codes_rows, uint8_t* __restrict__ sf) {
+                               int codes_rows, int gate_up, uint8_t* __restrict__ sf) {
   const int RT = (N + 127) >> 7;
   const int KT = Kp >> 7;
   const long long total = static_cast<long long>(E) * RT * KT * 512;
@@ -109,7 +109,7 @@ __global__ void pack_sf_kernel(const uint8_t* __restrict__ codes, int E, int N, 
     uint8_t c;
     if (n >= N) c = kPadRowCode;
     else if (j >= KB) c = kPadCode;
-    else c = src_row_code(codes, e, n, j, N, KB, codes_rows);
+    else c = src_row_code(codes, e, gate_up ? gate_up_src_row(n, N) : n, j, N, KB, codes_rows);
     sf[i] = c;
   }
 }
@@ -127,37 +127,33 @@ __device__ __forceinline__ uint32_t drop_negative_zero_word(uint32_t w, int* cou
   return w;
 }
 
-// Inside a word, element nibble e (bits 4e..4e+3) moves to slot e / 2 + 4 (e % 2):
-// elements 2i and 2i+1 land at bits 4i and 16 + 4i, one bf16 pair apart.
-__device__ __forceinline__ uint32_t nibble_slot_shuffle(uint32_t w) {
-  uint32_t r = 0u;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) r |= ((w >> (4 * e)) & 0xfu) << (4 * (e / 2 + 4 * (e % 2)));
-  return r;
-}
-
-// E2M1 bytes [E, N, K/2] -> [E, N, Kp/2]; per 64-byte chunk, output word 4 w + b
-// holds input word (block b, word w), nibble-shuffled.  One thread per output word.
-__global__ void pack_e2m1_bytes_kernel(const uint8_t* __restrict__ in, long long rows, int N, int gate_up,
-                                       int KH, int KHp, uint8_t* __restrict__ out,
-                                       unsigned long long* negz) {
-  const int words = KHp >> 2;
-  const long long total = rows * words;
+// E2M1 bytes [E, N, K/2] -> tiles [E, NT, KT, 128, 64]: K step kt (128 values,
+// 64 bytes, low nibble first) of rows 128 rt .. 128 rt + 127, one contiguous
+// 8 KB block; -0 nibbles cleared, zero past K and past N, rows optionally
+// gate / up interleaved.  One thread per output word.
+__global__ void pack_e2m1_bytes_kernel(const uint8_t* __restrict__ in, int E, int N, int gate_up, int KH,
+                                       int KT, uint8_t* __restrict__ out, unsigned long long* negz) {
+  const int NT = (N + 127) >> 7;
+  const long long total = static_cast<long long>(E) * NT * KT * 128 * 16;
   int count = 0;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = i / words;
-    const long long rs = gate_up ? (r / N) * N + gate_up_src_row(static_cast<int>(r % N), N) : r;
-    const int o = static_cast<int>(i % words);  // output word index in the row
-    const int chunk = o >> 4;
-    const int ow = o & 15;
-    const int wsel = ow >> 2, b = ow & 3;
-    const int src = chunk * 64 + b * 16 + wsel * 4;
+    const int w = static_cast<int>(i & 15);
+    const int m = static_cast<int>((i >> 4) & 127);
+    const long long blk = i >> 11;  // (e, rt, kt)
+    const int kt = static_cast<int>(blk % KT);
+    const long long ert = blk / KT;
+    const int rt = static_cast<int>(ert % NT);
+    const int e = static_cast<int>(ert / NT);
+    const int n = rt * 128 + m;
+    const int src = kt * 64 + w * 4;
     uint32_t v = 0u;
-    if (src < KH)
-      v = nibble_slot_shuffle(
-          drop_negative_zero_word(*reinterpret_cast<const uint32_t*>(in + rs * KH + src), &count));
-    *reinterpret_cast<uint32_t*>(out + r * KHp + o * 4) = v;
+    if (n < N && src < KH) {
+      const int ns = gate_up ? gate_up_src_row(n, N) : n;
+      v = drop_negative_zero_word(
+          *reinterpret_cast<const uint32_t*>(in + (static_cast<long long>(e) * N + ns) * KH + src), &count);
+    }
+    *reinterpret_cast<uint32_t*>(out + i * 4) = v;
   }
   // warp-reduce the -0 count, one atomic a warp (integer: order-independent)
   for (int off = 16; off > 0; off >>= 1) count += __shfl_xor_sync(0xffffffffu, count, off);
@@ -185,26 +181,28 @@ cudaError_t launch_pack_e4m3(const uint8_t* bytes, const uint8_t* codes, int E, 
   pack_codes_kernel<<<blocks_for(ncodes, 256), 256, 0, stream>>>(codes, E, N, KB, KBp, codes_rows,
                                                                  block_out ? 1 : 0, 0, codes_out);
   const long long nsf = static_cast<long long>(E) * ((N + 127) / 128) * (Kp / 128) * 512;
-  pack_sf_kernel<<<blocks_for(nsf, 256), 256, 0, stream>>>(codes, E, N, KB, Kp, codes_rows, sf);
+  pack_sf_kernel<<<blocks_for(nsf, 256), 256, 0, stream>>>(codes, E, N, KB, Kp, codes_rows, 0, sf);
   return cudaGetLastError();
 }
 
 cudaError_t launch_act_sf_atoms(const uint8_t* codes, int M, int K, int Kp, uint8_t* sf, cudaStream_t stream) {
   const long long total = static_cast<long long>((M + 127) >> 7) * (Kp >> 7) * 512;
-  pack_sf_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(codes, 1, M, K >> 5, Kp, M, sf);
+  pack_sf_kernel<<<blocks_for(total, 256), 256, 0, stream>>>(codes, 1, M, K >> 5, Kp, M, 0, sf);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pack_e2m1(const uint8_t* bytes, const uint8_t* codes, int E, int N, int K,
                              int Kp, int codes_rows, bool gate_up, uint8_t* wq, uint8_t* codes_out,
-                             unsigned long long* negz, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(E) * N;
-  pack_e2m1_bytes_kernel<<<blocks_for(rows * (Kp >> 3), 256), 256, 0, stream>>>(
-      bytes, rows, N, gate_up ? 1 : 0, K >> 1, Kp >> 1, wq, negz);
+                             uint8_t* sf, unsigned long long* negz, cudaStream_t stream) {
+  const long long words = static_cast<long long>(E) * ((N + 127) / 128) * (Kp / 128) * 128 * 16;
+  pack_e2m1_bytes_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(bytes, E, N, gate_up ? 1 : 0, K >> 1,
+                                                                     Kp >> 7, wq, negz);
   const int KB = K >> 5, KBp = Kp >> 5;
   const long long ncodes = static_cast<long long>(E) * N * KBp;
   pack_codes_kernel<<<blocks_for(ncodes, 256), 256, 0, stream>>>(codes, E, N, KB, KBp, codes_rows,
                                                                  0, gate_up ? 1 : 0, codes_out);
+  const long long nsf = static_cast<long long>(E) * ((N + 127) / 128) * (Kp / 128) * 512;
+  pack_sf_kernel<<<blocks_for(nsf, 256), 256, 0, stream>>>(codes, E, N, KB, Kp, codes_rows, gate_up ? 1 : 0, sf);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,13 @@ constexpr uint32_t mxf8_idesc(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// A operand format code for e2m1 (bits 7-9).  In shared memory a K-major e2m1
+// operand of kind::mxf8f6f4 takes a byte a value: every 16-byte chunk holds 16
+// consecutive values packed (8 bytes, low nibble first) followed by 8 bytes of
+// padding, so its rows, swizzle and descriptors are those of an e4m3 operand.
+constexpr uint32_t kFmtE2M1 = 5u;
+constexpr uint32_t mxf8_idesc_a(int M, int N, uint32_t afmt) { return mxf8_idesc(M, N) | (afmt << 7); }
+
 // K-major operand in 128B-swizzled 8-row x 128-byte atoms, atoms 1024 bytes apart.
 MX_DEV uint64_t sw128_desc(uint32_t saddr) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3fffu) | (static_cast<uint64_t>(1) << 16) |

@@ -25,21 +25,20 @@ Packed E4M3 weight (dense MXFP8), E experts of [N, K]:
          hold 127, blocks past K hold 128.
 
 Packed E2M1 weight (MXFP4 experts), E experts of [N, K]:
-  wq     [E, N, Kp/2]   in every 64-byte chunk of a row (4 K blocks of 16 bytes,
-         each 4 words of 4 bytes) word w of block b moves to word position
-         4 w + b, i.e. a 4x4 transpose of 4-byte words; inside every word the
-         element at nibble e (0..7, low nibble of byte 0 first) moves to nibble
-         slot e // 2 + 4 (e % 2), so elements 2i and 2i+1 sit at bits 4i and
-         16 + 4i; -0 nibbles are +0
+  wq     [E, ceil(N/128), Kp/128, 128, 64]   128-row x 128-value tiles: tile
+         (rt, kt) row m holds values 128 kt .. 128 kt + 127 of row 128 rt + m
+         as 64 fp4x2 bytes in the input order (element 2i in the low nibble of
+         byte i); zero past K and past N; -0 nibbles are +0
   codes  [E, N, Kp/32]  per-row codes (32x32 block codes are expanded), 128
          past K
+  sf     [E, ceil(N/128), Kp/128, 512]   the per-row codes in atoms, as for E4M3
   gate / up experts (w13 [E, 2 I, K/2], gate rows then up rows, weights942
   ``moe_copies``) can be packed with their halves interleaved in 8-row groups:
   packed row 16 q + i holds gate row 8 q + i for i < 8 and up row
-  8 q + i - 8 for i >= 8 (codes alike), so the 16 rows of one MMA fragment
-  hold the gate and up rows of the same 8 intermediate indices.  (The page's
-  gfx942 copy interleaves single rows, 2 i and 2 i + 1, for its own MFMA
-  fragment.)
+  8 q + i - 8 for i >= 8 (codes and atoms alike), so a 32-row slice of the
+  accumulator holds the gate and up rows of the same 16 intermediate indices
+  (lane l and lane l + 8).  (The page's gfx942 copy interleaves single rows,
+  2 i and 2 i + 1, for its own MFMA fragment.)
 
 Pinned by tests/test_oracle_layout.py: unpack(pack(w)) == w, the padding
 values, the fold / refuse decisions on agreeing and disagreeing rows, and the
@@ -171,33 +170,6 @@ def unpack_e4m3(p: dict) -> tuple:
     return w, row
 
 
-def _word_transpose(row_bytes: np.ndarray) -> np.ndarray:
-    """[..., L] with L % 64 == 0: in every 64-byte chunk, word (b, w) -> 4 w + b."""
-    *lead, L = row_bytes.shape
-    v = row_bytes.reshape(*lead, L // 64, 4, 4, 4)      # [chunk, block b, word w, byte]
-    return np.swapaxes(v, -3, -2).reshape(*lead, L).copy()  # [chunk, w, b, byte]
-
-
-def _nibble_slot_shuffle(row_bytes: np.ndarray, inverse: bool = False) -> np.ndarray:
-    """Inside every 4-byte word, element nibble e -> slot e // 2 + 4 (e % 2)
-    (or back, with ``inverse``).  Nibble n of a word is bits 4n..4n+3, i.e. the
-    low nibble of byte n // 2 for even n."""
-    *lead, L = row_bytes.shape
-    words = row_bytes.reshape(*lead, L // 4, 4)
-    nib = np.empty(words.shape[:-1] + (8,), dtype=np.uint8)
-    nib[..., 0::2] = words & 0x0F
-    nib[..., 1::2] = words >> 4
-    out = np.empty_like(nib)
-    for e in range(8):
-        slot = e // 2 + 4 * (e % 2)
-        if inverse:
-            out[..., e] = nib[..., slot]
-        else:
-            out[..., slot] = nib[..., e]
-    packed = (out[..., 0::2] | (out[..., 1::2] << 4)).astype(np.uint8)
-    return packed.reshape(*lead, L)
-
-
 def count_negative_zero(w) -> int:
     w = np.asarray(w, dtype=np.uint8)
     return int(np.count_nonzero((w & 0x0F) == 0x08) + np.count_nonzero((w & 0xF0) == 0x80))
@@ -247,19 +219,26 @@ def pack_e2m1(w, codes, gate_up: bool = False) -> dict:
     Kp = padded_k(K)
     negz = count_negative_zero(w)
     clean = drop_negative_zero(w)
-    padded = np.zeros((E, N, Kp // 2), dtype=np.uint8)
-    padded[:, :, :KH] = clean
+    RT, KT = -(-N // ATOM_ROWS), Kp // KSTEP
+    padded = np.zeros((E, RT * ATOM_ROWS, Kp // 2), dtype=np.uint8)
+    padded[:, :N, :KH] = clean
+    tiles = padded.reshape(E, RT, ATOM_ROWS, KT, KSTEP // 2).transpose(0, 1, 3, 2, 4).copy()
     return {"fmt": "e2m1", "mode": "row", "E": E, "N": N, "K": K, "Kp": Kp,
-            "wq": _nibble_slot_shuffle(_word_transpose(padded)),
-            "codes": _pad_codes(row, Kp // 32),
+            "wq": tiles, "codes": _pad_codes(row, Kp // 32), "sf": sf_atoms(row, Kp),
             "neg_zero_count": negz, "gate_up": bool(gate_up)}
+
+
+def e2m1_rows(p: dict) -> np.ndarray:
+    """Packed E2M1 tiles -> rows [E, N, Kp/2] (packed row order)."""
+    E, RT, KT = p["wq"].shape[:3]
+    rows = p["wq"].transpose(0, 1, 3, 2, 4).reshape(E, RT * ATOM_ROWS, KT * KSTEP // 2)
+    return rows[:, : p["N"]]
 
 
 def unpack_e2m1(p: dict) -> tuple:
     """Inverse of pack_e2m1 (up to -0 -> +0): (bytes [E, N, K/2], codes [E, N, K/32])."""
     K = p["K"]
-    # the 4x4 word transpose is its own inverse
-    back = _word_transpose(_nibble_slot_shuffle(p["wq"], inverse=True))[:, :, : K // 2]
+    back = e2m1_rows(p)[:, :, : K // 2]
     codes = p["codes"][:, :, : K // 32]
     if p.get("gate_up"):
         src = gate_up_source_rows(p["N"])

@@ -74,6 +74,7 @@ def check_e2m1(w, c, experts=None):
     assert p.Kp == ref["Kp"] and p.scale_mode == mx.MX_SCALE_ROW1X32
     assert np.array_equal(u8(p.bytes_tensor())[sel], ref["wq"])
     assert np.array_equal(u8(p.codes_tensor())[sel], ref["codes"])
+    assert np.array_equal(u8(p.sf_tensor())[sel], ref["sf"])
     if experts is None:
         assert p.neg_zero_count == ref["neg_zero_count"]
     else:
@@ -109,6 +110,7 @@ def test_e2m1_gate_up_interleave():
     assert p.desc.layout == mx.MX_LAYOUT_GATE_UP
     assert np.array_equal(u8(p.bytes_tensor()), ref["wq"])
     assert np.array_equal(u8(p.codes_tensor()), ref["codes"])
+    assert np.array_equal(u8(p.sf_tensor()), ref["sf"])
     assert p.neg_zero_count == ref["neg_zero_count"]
     plain = gpu_pack(w, c, "e2m1", 0)
     assert plain.desc.layout == mx.MX_LAYOUT_PLAIN

@@ -61,19 +61,24 @@ def test_fold_decisions():
     assert ei.value.code == L.MX_ERR_SCALE
 
 
-def test_e2m1_word_transpose_and_nibble_slots_by_positions():
+def test_e2m1_plain_order_and_atoms_by_positions():
     rng = np.random.default_rng(9)
-    w = (rng.integers(0, 256, size=(1, 1, 64)) & 0x77).astype(np.uint8)   # no -0 nibbles
-    codes = np.full((1, 1, 4), 127, dtype=np.uint8)
-    out = L.pack_e2m1(w, codes)["wq"][0, 0]
-    outword = [int.from_bytes(bytes(out[4 * i: 4 * i + 4]), "little") for i in range(16)]
-    for o in range(16):                      # output word o = 4 w + b
-        wd, b = o // 4, o % 4
-        src = w[0, 0, 16 * b + 4 * wd: 16 * b + 4 * wd + 4]
-        for e in range(8):                   # element e of the source word
-            nib = (int(src[e // 2]) >> (4 * (e % 2))) & 0xF
-            slot = e // 2 + 4 * (e % 2)
-            assert (outword[o] >> (4 * slot)) & 0xF == nib
+    E, N, K = 2, 136, 160                    # two row tiles, ragged K (Kp = 256)
+    w = (rng.integers(0, 256, size=(E, N, K // 2)) & 0x77).astype(np.uint8)   # no -0 nibbles
+    codes = rng.integers(118, 133, size=(E, N, K // 32), dtype=np.uint8)
+    p = L.pack_e2m1(w, codes)
+    assert p["wq"].shape == (E, 2, 2, 128, 64) and p["sf"].shape == (E, 2, 2, 512)
+    for e, n, k in [(0, 0, 0), (1, 5, 77), (0, 135, 159), (1, 129, 33)]:
+        byte = int(p["wq"][e, n // 128, k // 128, n % 128, (k % 128) // 2])
+        assert (byte >> (4 * (k % 2))) & 0xF == (int(w[e, n, k // 2]) >> (4 * (k % 2))) & 0xF
+        m, rt = n % 128, n // 128
+        j = k // 32
+        assert p["sf"][e, rt, j // 4, (m % 32) * 16 + (m // 32) * 4 + j % 4] == codes[e, n, j]
+    assert np.all(L.e2m1_rows(p)[:, :, K // 2:] == 0)
+    assert np.all(p["wq"][:, 1, :, N - 128:] == 0)       # rows 136..255 of tile 1
+    # K blocks 5..7 of the second step are padding (128); rows 136..255 of tile 1 are 127
+    assert p["sf"][0, 0, 1, 1 * 4 + 1] == 128            # row 32, block 5
+    assert p["sf"][1, 1, 0, (8 % 32) * 16] == 127         # row 136 >= N
 
 
 def test_e2m1_roundtrip_padding_and_negative_zero_count():
@@ -92,9 +97,8 @@ def test_e2m1_roundtrip_padding_and_negative_zero_count():
     assert np.array_equal(c2, codes)
     assert np.all(p["codes"][:, :, K // 32:] == 128)
     assert not np.any((p["wq"] & 0x0F) == 0x08) and not np.any((p["wq"] & 0xF0) == 0x80)
-    # the padded tail (past K/2 bytes, before the transpose) is zero
-    untransposed = L._word_transpose(L._nibble_slot_shuffle(p["wq"], inverse=True))
-    assert np.all(untransposed[:, :, K // 2:] == 0)
+    # the padded tail past K/2 bytes is zero
+    assert np.all(L.e2m1_rows(p)[:, :, K // 2:] == 0)
 
 
 def test_gate_up_interleave_rows_and_inverse():
@@ -110,6 +114,7 @@ def test_gate_up_interleave_rows_and_inverse():
     p = L.pack_e2m1(w, c, gate_up=True)
     plain = L.pack_e2m1(w[:, src], c[:, src])
     assert np.array_equal(p["wq"], plain["wq"]) and np.array_equal(p["codes"], plain["codes"])
+    assert np.array_equal(p["sf"], plain["sf"])
     back, cb = L.unpack_e2m1(p)
     assert np.array_equal(back, L.drop_negative_zero(w)) and np.array_equal(cb, c)
     with pytest.raises(L.PackError):
