@@ -149,10 +149,9 @@ constexpr int kMoeOutF32 = 2;     // out_f32 [pairs, N] f32
 // hi + lo = x except where an element lies below the e4m3 normal range of its
 // block's residual scale (|x - hi - lo| <= 2^-21.8 max|x| over the block).
 // MXFP8 activations: hi only.  Row j of xh / xl is pair pairs[j]; its codes
-// for K step s sit at cs[j][s][0..3] (hi) and cs[j][s][4..7] (lo): one
-// 16-byte row of a tcgen05 scale-factor atom, whose first column scales B
-// rows 0..31 (the hi pieces of 32 pairs) and second column rows 32..63 (their
-// lo pieces).
+// for K step s sit at cs[j][s][0..3] (hi) and cs[j][s][16..19] (lo): 16-byte
+// rows of a tcgen05 scale-factor atom whose rows 0..15 scale the hi pieces of
+// 16 pairs (B rows 0..15) and rows 16..31 their lo pieces (B rows 16..31).
 __device__ __forceinline__ uint32_t mx_quant_f32x32(const float (&v)[32], uint4 (&out)[2]) {
   float amax = 0.0f;
 #pragma unroll
@@ -212,65 +211,65 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
     uint4* hp = reinterpret_cast<uint4*>(xh + j * Kp + 32 * b);
     hp[0] = qh[0];
     hp[1] = qh[1];
-    uint8_t* cp = cs + (j * KT + (b >> 2)) * 16 + (b & 3);
+    uint8_t* cp = cs + (j * KT + (b >> 2)) * 32 + (b & 3);
     cp[0] = static_cast<uint8_t>(ch);
     if (lo) {
       uint4* lp = reinterpret_cast<uint4*>(xl + j * Kp + 32 * b);
       lp[0] = ql[0];
       lp[1] = ql[1];
-      cp[4] = static_cast<uint8_t>(cl);
+      cp[16] = static_cast<uint8_t>(cl);
     }
   }
 }
 
 // ---------------------------------------------------------------- expert GEMM
 //
-// CTA = one 128-row tile of one active expert, 12 warps:
-//   warp 0 (lane 0)  streams the packed e2m1 weight tile, one contiguous 8 KB
-//                    block (128 rows x 64 bytes) a K step, and the step's
-//                    512-byte weight scale atom (bulk copies);
+// Persistent CTAs (three an SM), each walking (expert, 128-row tile) work
+// items; 8 warps:
+//   warp 0 (lane 0)  streams the weight tile, one K step (128 rows x 128 e2m1
+//                    values, a contiguous 8 KB block) a stage: a TMA load with
+//                    the 16U4_ALIGN16B data type writes it straight in the
+//                    tensor core's e2m1 operand form (16 values = 8 packed
+//                    bytes a 16-byte chunk, the other 8 bytes not written and
+//                    not read, 128B swizzle), plus the step's 512-byte weight
+//                    scale atom;
 //   warp 2 (lane 0)  streams the gathered activation pieces of the expert's
-//                    next 32 pairs: 32 rows x 128 bytes of hi and of lo
-//                    (128B swizzle) and their scale atoms;
-//   warps 4..7       lay each weight step out as the tensor core's e2m1
-//                    operand: 128B-swizzled K-major rows in which every 16
-//                    values (8 packed bytes) take a 16-byte chunk, the E8M0
-//                    scale staying a scale factor; four 16-byte chunks a thread;
-//   warp 1 (lane 0)  allocates tensor memory and issues, per K step, the scale
-//                    copies and 4 block-scaled MMAs (kind::mxf8f6f4,
-//                    scale_vec::1X, M = 128 weight rows, K = 32) whose B
-//                    operand stacks the 32 pairs' hi pieces (rows 0..31) on
-//                    their lo pieces (rows 32..63), N = 64: one f32
-//                    accumulator column a piece of a pair;
-//   warps 8..11      read the accumulator (tcgen05.ld, one lane quarter each),
+//                    next 16 pairs: 16 rows x 128 bytes of hi and of lo
+//                    (128B swizzle) and their scale atom;
+//   warp 1 (lane 0)  allocates tensor memory and issues, per K step, the two
+//                    scale copies and 4 block-scaled MMAs (kind::mxf8f6f4,
+//                    scale_vec::1X, A e2m1, B e4m3, M = 128 weight rows,
+//                    K = 32) whose B operand stacks the 16 pairs' hi pieces
+//                    (rows 0..15) on their lo pieces (rows 16..31), N = 32:
+//                    one f32 accumulator column a piece of a pair;
+//   warps 4..7       read the accumulator (tcgen05.ld, one lane quarter each),
 //                    add each pair's hi and lo columns and store bf16 /
-//                    SiLU-and-mul / f32 per pair.
-// Rings: 5 weight stages, 2 converted stages, 3 activation stages; two CTAs
-// per SM.
-constexpr int kTok = 32;                   // pairs a pass (MMA N <= 32)
-constexpr int kWStages = 5, kAStages = 2, kXStages = 3;
-constexpr int kWStage = 128 * 64 + 512;   // packed step | weight scale atom
-constexpr int kAStage = 128 * 128;        // e4m3 step, 128B swizzle
-constexpr int kXStage = (2 * kTok * 128 + 512 + 1023) & ~1023;  // hi rows | lo rows | scale atom (1 KB aligned)
-constexpr int kAOff = 0;
-constexpr int kXOff = kAOff + kAStages * kAStage;
-constexpr int kWOff = kXOff + kXStages * kXStage;
-constexpr int kSfaOff = kWOff + kWStages * kWStage;
-constexpr int kBarOff = (kSfaOff + kAStages * 512 + 1023) & ~1023;
-constexpr int kBarBytes = ((2 * (kWStages + kAStages + kXStages) + 2) * 8 + 8 + 255) & ~255;  // + TMEM slot, flag
+//                    SiLU-and-mul / f32 per pair; two accumulators in tensor
+//                    memory let the next pass's MMAs run meanwhile.
+// Rings: 3 weight stages, 5 activation stages (the activation pieces come from
+// L2, whose latency the deeper ring covers); three CTAs per SM.
+constexpr int kTok = 16;                   // pairs a pass (16 B rows a piece)
+constexpr int kWStages = 3, kXStages = 5;
+constexpr int kWStage = 128 * 128;        // e2m1 operand step, 128B swizzle
+constexpr int kWTx = 128 * 64;            // bytes the TMA writes (the packed half of each chunk)
+constexpr int kXStage = 2 * kTok * 128;   // hi rows | lo rows (4 KB, 1 KB aligned)
+constexpr int kWOff = 0;
+constexpr int kXOff = kWOff + kWStages * kWStage;
+constexpr int kSfaOff = kXOff + kXStages * kXStage;  // a weight scale atom a weight stage
+constexpr int kSfbOff = kSfaOff + kWStages * 512;      // an activation scale atom an activation stage
+constexpr int kBarOff = (kSfbOff + kXStages * 512 + 1023) & ~1023;
+constexpr int kBarBytes = ((2 * (kWStages + kXStages) + 4) * 8 + 8 + 255) & ~255;  // + TMEM slot, flag
 constexpr int kTcSmem = kBarOff + kBarBytes + 1024;
-constexpr int kTcThreads = 384;
-// tensor memory: accumulator 64 columns (hi 0..31, lo 32..63) | a (SFA 4,
-// SFB 4) slot per converted stage, rounded up to a power of two
+constexpr int kTcThreads = 256;
+// tensor memory: two accumulators of 32 columns (hi 0..15, lo 16..31) | a
+// (SFA 4, SFB 4) slot a weight stage, rounded up to a power of two
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? c : pow2_at_least(v, 2 * c); }
 constexpr uint32_t kAccCols = 2 * kTok;
-constexpr uint32_t kTcTmemCols = pow2_at_least(kAccCols + 8 * kAStages);
-constexpr uint32_t kIdescTok16 = mxf8_idesc_a(128, 16, kFmtE2M1);
-constexpr uint32_t kIdescTok32 = mxf8_idesc_a(128, 32, kFmtE2M1);
-constexpr uint32_t kIdescPieces = mxf8_idesc_a(128, 2 * kTok, kFmtE2M1);
+constexpr uint32_t kTcTmemCols = pow2_at_least(2 * kAccCols + 8 * kWStages);
+constexpr uint32_t kIdescHi = mxf8_idesc_a(128, kTok, kFmtE2M1);         // hi pieces only
+constexpr uint32_t kIdescPieces = mxf8_idesc_a(128, 2 * kTok, kFmtE2M1);  // hi and lo pieces
 
 struct MoeParams {
-  const uint8_t* w;        // packed weight tiles [E, NT, KT, 128, 64]
   const uint8_t* sfw;      // weight scale atoms [E, NT, KT, 512]
   const int32_t* offsets;
   const int32_t* pairs;
@@ -284,12 +283,6 @@ struct MoeParams {
   int out_mode;
 };
 
-MX_DEV uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
 // Packed row r of a gate / up interleaved weight -> its row in gate-then-up order.
 MX_DEV int gate_up_row(int r, int N) {
   const int q = r >> 4, i = r & 15;
@@ -298,47 +291,56 @@ MX_DEV int gate_up_row(int r, int N) {
 
 MX_DEV float silu_f32(float v) { return v / (1.0f + expf(-v)); }
 
-__global__ void __launch_bounds__(kTcThreads, 2) moe_kernel(const __grid_constant__ CUtensorMap xhmap,
+// A work item is one 128-row tile rt of the a-th active expert (items a-major);
+// every role of a CTA walks the same items blockIdx.x, + gridDim.x, ...
+struct Item {
+  int e, o0, cnt, nch, rt;
+};
+
+MX_DEV Item item_at(const MoeParams& p, int i) {
+  Item it;
+  const int a = i / p.NT;
+  it.rt = i - a * p.NT;
+  it.e = p.active[a];
+  it.o0 = p.offsets[it.e];
+  it.cnt = p.offsets[it.e + 1] - it.o0;
+  it.nch = (it.cnt + kTok - 1) / kTok;
+  return it;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                             const __grid_constant__ CUtensorMap xhmap,
                                                              const __grid_constant__ CUtensorMap xlmap,
                                                              const __grid_constant__ CUtensorMap csmap,
                                                              const MoeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int a = blockIdx.y;
-  if (a >= *p.n_active) return;  // the whole CTA: no barrier or tensor memory touched yet
-  const int e = p.active[a];
-  const int o0 = p.offsets[e];
-  const int cnt = p.offsets[e + 1] - o0;
-  const int nch = (cnt + kTok - 1) / kTok;
-  const int rt = blockIdx.x;
+  const int n_items = *p.n_active * p.NT;
+  if (static_cast<int>(blockIdx.x) >= n_items) return;  // the whole CTA, before any barrier or tensor memory
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* wempty = wfull + kWStages;
-  uint64_t* afull = wempty + kWStages;
-  uint64_t* aempty = afull + kAStages;
-  uint64_t* xfull = aempty + kAStages;
+  uint64_t* xfull = wempty + kWStages;
   uint64_t* xempty = xfull + kXStages;
-  uint64_t* accfull = xempty + kXStages;
-  uint64_t* accempty = accfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 1);
+  uint64_t* accfull = xempty + kXStages;  // [2]
+  uint64_t* accempty = accfull + 2;       // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWStages; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], 4);     // one arrival a converter warp
-    }
-    for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&afull[i], 128);    // every converter thread
-      mbar_init(&aempty[i], 1);     // tcgen05.commit
+      mbar_init(&wempty[i], 1);     // tcgen05.commit
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(&xfull[i], 1);
       mbar_init(&xempty[i], 1);     // tcgen05.commit
     }
-    mbar_init(accfull, 1);
-    mbar_init(accempty, 4);         // one arrival an epilogue warp
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accfull[i], 1);    // tcgen05.commit
+      mbar_init(&accempty[i], 4);   // one arrival an epilogue warp
+    }
     *abort_flag = 0u;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -351,19 +353,24 @@ __global__ void __launch_bounds__(kTcThreads, 2) moe_kernel(const __grid_constan
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
-    // the tile's K steps are consecutive 8 KB blocks, its scale atoms 512 B each
-    const long long tile = static_cast<long long>(e) * p.NT + rt;
-    const uint8_t* wt = p.w + tile * p.KT * 8192;
-    const uint8_t* sfa = p.sfw + tile * p.KT * 512;
+    tma_prefetch_desc(&wmap);
     int g = 0;
-    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
-      for (int s = 0; s < p.KT; ++s, ++g) {
-        const int st = g % kWStages;
-        if (!mbar_wait(&wempty[st], ((g / kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
-        uint8_t* dst = smem + kWOff + st * kWStage;
-        mbar_arrive_expect_tx(&wfull[st], kWStage);
-        bulk_load(dst, wt + s * 8192, 8192, &wfull[st]);
-        bulk_load(dst + 128 * 64, sfa + s * 512, 512, &wfull[st]);
+    for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
+      const Item it = item_at(p, i);
+      // a weight tile read once streams past L2; read again (more than one
+      // pass of pairs) it is kept
+      const uint64_t pol = it.nch > 1 ? policy_evict_last() : policy_evict_first();
+      const long long tile = static_cast<long long>(it.e) * p.NT + it.rt;
+      const int row0 = static_cast<int>(tile * p.KT * 128);  // the tile's first 128-value row
+      const uint8_t* sfa = p.sfw + tile * p.KT * 512;
+      for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
+        for (int s = 0; s < p.KT; ++s, ++g) {
+          const int st = g % kWStages;
+          if (!mbar_wait(&wempty[st], ((g / kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+          mbar_arrive_expect_tx(&wfull[st], kWTx + 512);
+          tma_load_2d(smem + kWOff + st * kWStage, &wmap, &wfull[st], 0, row0 + s * 128, pol);
+          bulk_load(smem + kSfaOff + st * 512, sfa + s * 512, 512, &wfull[st]);
+        }
       }
     }
   } else if (warp == 2 && lane == 0) {
@@ -372,128 +379,103 @@ __global__ void __launch_bounds__(kTcThreads, 2) moe_kernel(const __grid_constan
     tma_prefetch_desc(&csmap);
     if (p.lo) tma_prefetch_desc(&xlmap);
     const uint64_t pol = policy_evict_last();  // every row tile of the expert reads them
-    const uint32_t tx = p.lo ? 2 * kTok * 128 + 512 : kTok * 128 + 512;
+    const uint32_t tx = p.lo ? 2 * kTok * (128 + 16) : kTok * (128 + 16);
     int g = 0;
-    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
-      const int row0 = o0 + ch * kTok;
-      for (int s = 0; s < p.KT; ++s, ++g) {
-        const int st = g % kXStages;
-        if (!mbar_wait(&xempty[st], ((g / kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
-        uint8_t* dst = smem + kXOff + st * kXStage;
-        mbar_arrive_expect_tx(&xfull[st], tx);
-        tma_load_2d(dst, &xhmap, &xfull[st], s * 128, row0, pol);
-        tma_load_2d(dst + 2 * kTok * 128, &csmap, &xfull[st], s * 16, row0, pol);
-        if (p.lo) tma_load_2d(dst + kTok * 128, &xlmap, &xfull[st], s * 128, row0, pol);
+    for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
+      const Item it = item_at(p, i);
+      for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
+        const int row0 = it.o0 + ch * kTok;
+        for (int s = 0; s < p.KT; ++s, ++g) {
+          const int st = g % kXStages;
+          if (!mbar_wait(&xempty[st], ((g / kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+          uint8_t* dst = smem + kXOff + st * kXStage;
+          uint8_t* atom = smem + kSfbOff + st * 512;
+          mbar_arrive_expect_tx(&xfull[st], tx);
+          tma_load_2d(dst, &xhmap, &xfull[st], s * 128, row0, pol);
+          tma_load_2d(atom, &csmap, &xfull[st], s * 32, row0, pol);
+          if (p.lo) {
+            tma_load_2d(dst + kTok * 128, &xlmap, &xfull[st], s * 128, row0, pol);
+            tma_load_2d(atom + kTok * 16, &csmap, &xfull[st], s * 32 + 16, row0, pol);
+          }
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    int ga = 0, gx = 0;
-    uint32_t acc_phase = 0;
-    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
-      const int ntok = cnt - ch * kTok < kTok ? cnt - ch * kTok : kTok;
-      const uint32_t idesc = p.lo ? kIdescPieces : (ntok <= 16 ? kIdescTok16 : kIdescTok32);
-      if (!mbar_wait(accempty, acc_phase ^ 1u)) { *abort_flag = 1u; break; }
-      tc_fence_after();
-      bool ok = true;
-      for (int s = 0; s < p.KT; ++s, ++ga, ++gx) {
-        const int as = ga % kAStages, xs = gx % kXStages;
-        if (!mbar_wait(&afull[as], (ga / kAStages) & 1u) || !mbar_wait(&xfull[xs], (gx / kXStages) & 1u)) {
-          *abort_flag = 1u;
-          ok = false;
-          break;
-        }
+    const uint32_t idesc = p.lo ? kIdescPieces : kIdescHi;
+    int gw = 0, gx = 0, gp = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const Item it = item_at(p, i);
+      for (int ch = 0; ch < it.nch && ok; ++ch, ++gp) {
+        const int buf = gp & 1;  // accumulator buffer: the epilogue drains the other
+        if (!mbar_wait(&accempty[buf], ((gp >> 1) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t xb = smem_u32(smem + kXOff + xs * kXStage);
-        const uint32_t sfc = tmem + kAccCols + static_cast<uint32_t>(as * 8);
-        tc_cp_sf(sfc, sf_desc(smem_u32(smem + kSfaOff + as * 512)));
-        tc_cp_sf(sfc + 4, sf_desc(xb + 2 * kTok * 128));
-        const uint64_t adesc = sw128_desc(smem_u32(smem + kAOff + as * kAStage));
-        const uint64_t bdesc = sw128_desc(xb);  // 64 rows: hi 0..31 then lo 32..63 (A16)
+        const uint32_t acc = tmem + static_cast<uint32_t>(buf) * kAccCols;
+        for (int s = 0; s < p.KT; ++s, ++gw, ++gx) {
+          const int ws = gw % kWStages, xs = gx % kXStages;
+          if (!mbar_wait(&wfull[ws], (gw / kWStages) & 1u) || !mbar_wait(&xfull[xs], (gx / kXStages) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfc = tmem + 2 * kAccCols + static_cast<uint32_t>(ws * 8);
+          tc_cp_sf(sfc, sf_desc(smem_u32(smem + kSfaOff + ws * 512)));
+          tc_cp_sf(sfc + 4, sf_desc(smem_u32(smem + kSfbOff + xs * 512)));
+          const uint64_t adesc = sw128_desc(smem_u32(smem + kWOff + ws * kWStage));
+          const uint64_t bdesc = sw128_desc(smem_u32(smem + kXOff + xs * kXStage));  // hi 0..15, lo 16..31
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-          tc_mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, id, sfc, sfc + 4, (s | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+            tc_mma_mxf8(acc, adesc + 2 * k, bdesc + 2 * k, id, sfc, sfc + 4, (s | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&wempty[ws]);
+          tc_commit(&xempty[xs]);
         }
-        tc_commit(&aempty[as]);
-        tc_commit(&xempty[xs]);
+        if (ok) tc_commit(&accfull[buf]);
       }
-      if (!ok) break;
-      tc_commit(accfull);
-      acc_phase ^= 1u;
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ e2m1 operand
-    const int i = threadIdx.x - 128;
-    int g = 0;
-    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
-      bool ok = true;
-      for (int s = 0; s < p.KT; ++s, ++g) {
-        const int ws = g % kWStages, as = g % kAStages;
-        if (!mbar_wait(&wfull[ws], (g / kWStages) & 1u) || !mbar_wait(&aempty[as], ((g / kAStages) & 1u) ^ 1u)) {
-          *abort_flag = 1u;
-          ok = false;
-          break;
-        }
-        const uint32_t src = smem_u32(smem + kWOff + ws * kWStage);
-        uint8_t* dst = smem + kAOff + as * kAStage;
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          // 16-byte chunk idx of the packed step: row r, K block b (32 values)
-          const int idx = it * 128 + i, r = idx >> 2, b = idx & 3;
-          const uint4 v = ld_shared_v4(src + r * 64 + b * 16);
-          // K values 32 b .. 32 b + 15 and + 16 .. + 31: 16-byte chunks 2 b and
-          // 2 b + 1 of row r (128B swizzle), 8 packed bytes then 8 of padding
-          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
-          *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(v.z, v.w, 0u, 0u);
-        }
-        if (i < 32)  // the weight scale atom moves with the converted step
-          *reinterpret_cast<uint4*>(smem + kSfaOff + as * 512 + i * 16) = ld_shared_v4(src + 128 * 64 + i * 16);
-        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-        mbar_arrive(&afull[as]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty[ws]);
-      }
-      if (!ok) break;
-    }
-  } else if (warp >= 8) {
+    if (!ok) *abort_flag = 1u;
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quarter: rows 32 q .. 32 q + 31
-    const int n = rt * 128 + q * 32 + lane;
     const unsigned full = 0xffffffffu;
-    uint32_t acc_phase = 0;
-    for (int ch = 0; ch < nch && !*abort_flag; ++ch) {
-      const int ntok = cnt - ch * kTok < kTok ? cnt - ch * kTok : kTok;
-      const int pr = lane < ntok ? p.pairs[o0 + ch * kTok + lane] : -1;
-      if (!mbar_wait(accfull, acc_phase)) { *abort_flag = 1u; break; }
-      tc_fence_after();
-      uint32_t v[32], vl[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16), v);
-      if (p.lo) {
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kTok, vl);
+    int gp = 0;
+    for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
+      const Item it = item_at(p, i);
+      const int n = it.rt * 128 + q * 32 + lane;
+      for (int ch = 0; ch < it.nch; ++ch, ++gp) {
+        const int buf = gp & 1;
+        const int ntok = it.cnt - ch * kTok < kTok ? it.cnt - ch * kTok : kTok;
+        const int pr = lane < ntok ? p.pairs[it.o0 + ch * kTok + lane] : -1;
+        if (!mbar_wait(&accfull[buf], (gp >> 1) & 1u)) { *abort_flag = 1u; break; }
+        tc_fence_after();
+        uint32_t v[32];  // columns 0..15: hi pieces, 16..31: lo pieces
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * kAccCols, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[buf]);  // the MMAs of a later pass may overwrite it
+        if (p.lo) {
 #pragma unroll
-        for (int t = 0; t < kTok; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(vl[t]));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(accempty);  // the next pass may overwrite the accumulator
-      acc_phase ^= 1u;
+          for (int t = 0; t < kTok; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[kTok + t]));
+        }
 #pragma unroll
-      for (int t = 0; t < kTok; ++t) {
-        if (t >= ntok) break;  // warp-uniform
-        const int pt = __shfl_sync(full, pr, t);
-        const float y = __uint_as_float(v[t]);
-        if (p.out_mode == kMoeOutSwiglu) {
-          // lane l (l % 16 < 8) holds gate row 8 (n / 16) + l % 16, lane l + 8 its up row
-          const float u = __shfl_down_sync(full, y, 8);
-          if ((lane & 15) < 8 && n < p.N)
-            p.out[static_cast<long long>(pt) * (p.N >> 1) + (n >> 4) * 8 + (n & 15)] =
-                __float2bfloat16_rn(silu_f32(y) * u);
-        } else if (p.out_mode == kMoeOutF32) {
-          if (n < p.N) p.out_f32[static_cast<long long>(pt) * p.N + n] = y;
-        } else if (p.out_mode == kMoeOutBf16 && n < p.N) {
-          const int nn = p.gate_up ? gate_up_row(n, p.N) : n;
-          p.out[static_cast<long long>(pt) * p.N + nn] = __float2bfloat16_rn(y);
+        for (int t = 0; t < kTok; ++t) {
+          if (t >= ntok) break;  // warp-uniform
+          const int pt = __shfl_sync(full, pr, t);
+          const float y = __uint_as_float(v[t]);
+          if (p.out_mode == kMoeOutSwiglu) {
+            // lane l (l % 16 < 8) holds gate row 8 (n / 16) + l % 16, lane l + 8 its up row
+            const float u = __shfl_down_sync(full, y, 8);
+            if ((lane & 15) < 8 && n < p.N)
+              p.out[static_cast<long long>(pt) * (p.N >> 1) + (n >> 4) * 8 + (n & 15)] =
+                  __float2bfloat16_rn(silu_f32(y) * u);
+          } else if (p.out_mode == kMoeOutF32) {
+            if (n < p.N) p.out_f32[static_cast<long long>(pt) * p.N + n] = y;
+          } else if (p.out_mode == kMoeOutBf16 && n < p.N) {
+            const int nn = p.gate_up ? gate_up_row(n, p.N) : n;
+            p.out[static_cast<long long>(pt) * p.N + nn] = __float2bfloat16_rn(y);
+          }
         }
       }
     }
@@ -538,12 +520,12 @@ cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts
   return cudaGetLastError();
 }
 
-// Activation pieces of P pairs: xh [P + 32, Kp] | xl [P + 32, Kp] | codes
-// [P + 32, Kp/128, 16], each region 256-byte aligned (32 spare rows: the last
-// pass of pairs loads a full 32-row box).
+// Activation pieces of P pairs: xh [P + 16, Kp] | xl [P + 16, Kp] | codes
+// [P + 16, Kp/128, 32], each region 256-byte aligned (16 spare rows: the last
+// pass of pairs loads a full 16-row box).
 static size_t act_region(long long P, int Kp) { return (static_cast<size_t>(P + kTok) * Kp + 255) & ~size_t(255); }
 static size_t act_codes(long long P, int Kp) {
-  return (static_cast<size_t>(P + kTok) * (Kp / 128) * 16 + 255) & ~size_t(255);
+  return (static_cast<size_t>(P + kTok) * (Kp / 128) * 32 + 255) & ~size_t(255);
 }
 size_t moe_act_bytes(long long P, int Kp) { return 2 * act_region(P, Kp) + act_codes(P, Kp); }
 
@@ -566,7 +548,6 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
 
   MoeParams p = {};
-  p.w = w->bytes;
   p.sfw = w->sf;
   p.offsets = a.offsets;
   p.pairs = a.pairs;
@@ -581,24 +562,33 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
   const uint64_t rows = static_cast<uint64_t>(P + kTok);
-  CUtensorMap xhmap, xlmap, csmap;
-  int rc = encode_tensor_map_2d(&xhmap, xh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
+  CUtensorMap wmap, xhmap, xlmap, csmap;
+  // the packed tiles as rows of 128 e2m1 values (64 bytes), unpacked by the TMA
+  const uint64_t wrows = static_cast<uint64_t>(w->E) * p.NT * KT * 128;
+  int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 128, wrows, 64, 128, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc == MX_OK)
+    rc = encode_tensor_map_2d(&xhmap, xh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == MX_OK)
     rc = encode_tensor_map_2d(&xlmap, xl, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == MX_OK)
-    rc = encode_tensor_map_2d(&csmap, cs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(KT) * 16, rows,
-                              static_cast<uint64_t>(KT) * 16, 16, kTok, CU_TENSOR_MAP_SWIZZLE_NONE);
+    rc = encode_tensor_map_2d(&csmap, cs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(KT) * 32, rows,
+                              static_cast<uint64_t>(KT) * 32, 16, kTok, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != MX_OK) return rc;
   DeviceInfo di;
   if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
   static int smem_set[64];
   if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel), kTcSmem, di, smem_set) != MX_OK)
     return MX_ERR_CUDA;
-  const int zmax = static_cast<int>(P < w->E ? P : w->E);
-  dim3 grid(p.NT, zmax, 1);
-  moe_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(xhmap, xlmap, csmap, p);
+  // persistent: three CTAs an SM (shared and tensor memory allow three), never
+  // more than the largest possible number of work items
+  const long long zmax = P < w->E ? P : w->E;
+  const long long items = zmax * p.NT;
+  const long long slots = 3LL * di.sm_count;
+  const int grid = static_cast<int>(items < slots ? items : slots);
+  moe_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(wmap, xhmap, xlmap, csmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;
