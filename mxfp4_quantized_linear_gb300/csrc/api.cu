@@ -525,10 +525,10 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, co
   int32_t* active = reinterpret_cast<int32_t*>(ws + R.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.n_active);
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.status);
-  cudaError_t e = launch_route(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream);
+  // routing, and zero rows for the pairs whose id is not a valid expert
+  cudaError_t e = launch_route(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream, out,
+                               w->N);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
-  if ((e = launch_zero_invalid_pairs(topk_ids, T, topk, w->E, w->N, out, stream)) != cudaSuccess)
-    return cuda_fail(e, "zero launch");
   MoeLaunch a = {};
   a.x = x;
   a.T = T;

@@ -24,11 +24,15 @@ namespace {
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
+// zero_out (optional): bf16 [P, zero_N] rows of the pairs whose id is not a
+// valid expert are set to zero (they belong to no expert's list).
 __global__ void __launch_bounds__(kRouteThreads)
     route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ pairs,
-                 int32_t* __restrict__ active, int32_t* __restrict__ n_active, int* dev_status) {
+                 int32_t* __restrict__ active, int32_t* __restrict__ n_active, int* dev_status,
+                 __nv_bfloat16* __restrict__ zero_out, int zero_N) {
   extern __shared__ int rs[];
+  pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid
   int* cnt = rs;           // [E]
   int* base = rs + E;      // [E]
   int* wcnt = rs + 2 * E;  // [warps][E]
@@ -39,8 +43,16 @@ __global__ void __launch_bounds__(kRouteThreads)
   int bad = 0;
   for (int p = tid; p < P; p += blockDim.x) {
     const int e = ids[p];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);  // integer counts: order-independent
-    else if (e != -1) bad = 1;
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[e], 1);  // integer counts: order-independent
+    } else {
+      if (e != -1) bad = 1;
+      if (zero_out) {
+        __nv_bfloat16* row = zero_out + static_cast<long long>(p) * zero_N;
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
+        for (int n = 0; n < zero_N; ++n) row[n] = z;
+      }
+    }
   }
   bad = __syncthreads_or(bad);
   if (warp == 0) {  // exclusive scan of the counts, and the ascending list of active experts
@@ -96,17 +108,6 @@ __global__ void __launch_bounds__(kRouteThreads)
     }
     __syncthreads();
   }
-}
-
-// One warp per pair: rows of pairs whose id is not a valid expert are zero.
-__global__ void zero_invalid_pairs_kernel(const int32_t* __restrict__ ids, int P, int E, int N,
-                                          __nv_bfloat16* __restrict__ out) {
-  const int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (p >= P) return;
-  const int e = ids[p];
-  if (e >= 0 && e < E) return;
-  const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
-  for (int n = threadIdx.x & 31; n < N; n += 32) out[static_cast<long long>(p) * N + n] = z;
 }
 
 // out[t, h] = bf16(sum_j w[t, j] y2[t * topk + j, h]) over the slots j with a
@@ -176,6 +177,8 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
                                   const int32_t* __restrict__ n_pairs, int P, int topk, int x_per_pair, int K,
                                   int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl,
                                   uint8_t* __restrict__ cs) {
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();  // the routing (and the activation, when a kernel wrote it) is complete
   const int KBp = Kp >> 5, KB = K >> 5, KT = Kp >> 7;
   const int nv = *n_pairs;
   const long long total = static_cast<long long>(nv < P ? nv : P) * KBp;
@@ -315,8 +318,6 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
                                                              const MoeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int n_items = *p.n_active * p.NT;
-  if (static_cast<int>(blockIdx.x) >= n_items) return;  // the whole CTA, before any barrier or tensor memory
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + kBarOff);
@@ -350,6 +351,11 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the next kernel may start its prologue once every CTA holds its tensor
+  // memory (a dependent grid then never takes columns this grid waits for)
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();  // the routing and the activation pieces are complete
+  const int n_items = *p.n_active * p.NT;  // CTAs past the last item go straight to the exit
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
@@ -494,21 +500,13 @@ unsigned int take_error_flags_moe() { return take_tu_error_flags(); }
 
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
-                         int* dev_status, cudaStream_t stream) {
+                         int* dev_status, cudaStream_t stream, void* zero_out, int zero_N) {
   const int smem = (2 * E + kRouteWarps * E) * static_cast<int>(sizeof(int));
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, T * topk, E, counts, offsets, pairs, active,
-                                                   n_active, dev_status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E, int N, void* out,
-                                      cudaStream_t stream) {
-  const int P = T * topk;
-  const int warps = 8;
-  zero_invalid_pairs_kernel<<<(P + warps - 1) / warps, warps * 32, 0, stream>>>(
-      ids, P, E, N, static_cast<__nv_bfloat16*>(out));
+                                                   n_active, dev_status,
+                                                   static_cast<__nv_bfloat16*>(zero_out), zero_N);
   return cudaGetLastError();
 }
 
@@ -541,10 +539,18 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   uint8_t* xl = xh + act_region(P, Kp);
   uint8_t* cs = xl + act_region(P, Kp);
   const long long nblk = P * (Kp / 32);
-  act_pieces_kernel<<<blocks_for(nblk, 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.x), a.pairs, a.offsets + w->E, static_cast<int>(P), a.topk,
-      a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(nblk, 256)), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, act_pieces_kernel, static_cast<const __nv_bfloat16*>(a.x),
+                                     static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
+                                     static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
 
   MoeParams p = {};
@@ -588,8 +594,10 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   const long long items = zmax * p.NT;
   const long long slots = 3LL * di.sm_count;
   const int grid = static_cast<int>(items < slots ? items : slots);
-  moe_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(wmap, xhmap, xlmap, csmap, p);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kTcSmem;
+  e = cudaLaunchKernelEx(&cfg, moe_kernel, wmap, xhmap, xlmap, csmap, p);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;
 }

@@ -122,7 +122,7 @@ unsigned int take_error_flags_gemm();
 // ---- routing + MoE (moe.cu)
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
-                         int* dev_status, cudaStream_t stream);
+                         int* dev_status, cudaStream_t stream, void* zero_out = nullptr, int zero_N = 0);
 struct MoeLaunch {
   const void* x;               // bf16 [T, K] (x_per_pair = 0) or [T * topk, K] (x_per_pair = 1)
   int T, topk;
@@ -142,7 +142,5 @@ unsigned int take_error_flags_moe();
 unsigned int take_error_flags_selftest();
 cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts, int T, int topk, int E, int H,
                            void* out, cudaStream_t stream);
-cudaError_t launch_zero_invalid_pairs(const int32_t* ids, int T, int topk, int E, int N, void* out,
-                                      cudaStream_t stream);
 
 }  // namespace mx
