@@ -345,6 +345,7 @@ def run_ours(args, ws, rank, local):
         result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
         result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
         result["moe_expert"] = bench_expert(mx, inputs, dev, stream, hbm_peak)
+        result["moe_w4a8_prefill"] = bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind)
         result["e2e"] = bench_e2e(mx, packed, dev, stream, args)
     del graphs, g_all
     return result
@@ -438,6 +439,37 @@ def bench_expert(mx, inputs, dev, stream, hbm_peak):
     return {"workload": "MXFP4 routed expert E=64 I=2048 H=4096 T=64 top-8: gate/up + SiLU-and-mul, "
                         "down projection, top-k combine", "ms": round(ms, 4), "GB/s": round(gbs, 1),
             "frac_hbm": round(gbs / hbm_peak, 4), "experts_touched": D}
+
+
+def bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind):
+    """The routed expert GEMM with MXFP8 activations (MXFP4 x MXFP8, the prefill
+    form): E=64 N=4096 K=4096, T=4096 tokens top-8, TFLOP/s against twice the
+    bf16 dense peak (the nominal 8-bit ratio)."""
+    E, N, K, T, topk = 64, 4096, 4096, 4096, 8
+    m = inputs.moe_gate_up(E=E, N=N, K=K, T=T, topk=topk, seed=3, device=dev)
+    with torch.cuda.stream(stream):
+        p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
+        out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, K), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            mx.mxfp4_moe_linear_w4a8(m["x"], m["ids"], p, out=out, workspace=work)
+        torch.cuda.synchronize()
+        reps = 5
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(1e6))
+        e0.record(stream)
+        for _ in range(reps):
+            mx.mxfp4_moe_linear_w4a8(m["x"], m["ids"], p, out=out, workspace=work)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    tflops = 2.0 * T * topk * N * K / (ms * 1e-3) / 1e12
+    peak8 = 2.0 * bf16_peak
+    del p, m, out, work
+    return {"workload": "MXFP4 x MXFP8 routed expert GEMM E=64 N=4096 K=4096 T=4096 top-8 "
+                        "(activations quantized per token in the call)",
+            "ms": round(ms, 4), "TFLOP/s": round(tflops, 1), "frac_tensor": round(tflops / peak8, 4),
+            "note": f"fraction of 2 x the {peak_kind} bf16 dense peak (8-bit nominal ratio)"}
 
 
 def bench_e2e(mx, packed, dev, stream, args):

@@ -297,6 +297,21 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk,
                      const mx_packed_weight* w, void* out, void* workspace,
                      size_t workspace_bytes, int* dev_status, void* stream);
 
+/*
+ * The routed expert GEMM with MXFP8 activations (MXFP4 x MXFP8, the prefill
+ * form of the layer): x is quantized per token inside the call exactly as
+ * mx_quantize_act does (rocm_native, _quant_mxfp8_tile), then for every pair
+ * (t, j) with e = topk_ids[t, j] in [0, E)
+ *   out[t, j, n] = sum_k e2m1(W_e[n,k]) 2^(c_e[n,k/32] - 127)
+ *                        e4m3(q[t,k]) 2^(cx[t,k/32] - 127)
+ * in fp32 on the tensor cores (kind::mxf8f6f4, both scales applied by the
+ * MMA), rounded to bf16; pairs with an invalid id get zeros.  Arguments,
+ * workspace (mxfp4_moe_workspace_size) and errors as mxfp4_moe_linear.
+ */
+int mxfp4_moe_linear_w4a8(const void* x, const int32_t* topk_ids, int T, int topk,
+                          const mx_packed_weight* w, void* out, void* workspace,
+                          size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Workspace bytes mxfp4_moe_expert needs for x [T, K], w13 [E, 2 I, K] and
  * w2 [E, H, I] (routing, the activation pieces, the activation [T*topk, I]
  * bf16 and the down projection [T*topk, H] f32). */

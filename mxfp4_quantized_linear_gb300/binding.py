@@ -28,7 +28,7 @@ MX_MAX_EXPERTS = 512
 
 EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_weights",
             "mx_quantize_act", "mx_dequant", "mxfp8_linear_workspace_size", "mxfp8_linear",
-            "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear",
+            "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear", "mxfp4_moe_linear_w4a8",
             "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert",
             "mxfp8_linear_q_workspace_size", "mxfp8_linear_q", "mx_e4m3_from_dequant",
             "mx_selftest_bounded_wait")
@@ -78,6 +78,7 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mx_route_experts": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "mxfp4_moe_workspace_size": (sz, [i32, i32, i32, i32]),
         "mxfp4_moe_linear": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
+        "mxfp4_moe_linear_w4a8": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
         "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "mxfp8_linear_q_workspace_size": (sz, [i32, pw]),
@@ -334,6 +335,25 @@ def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, o
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(load_library().mxfp4_moe_linear(_ptr(x), _ptr(topk_ids), T, topk, ctypes.byref(w.desc), _ptr(out),
                                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream()))
+    return out
+
+
+def mxfp4_moe_linear_w4a8(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, out: torch.Tensor = None,
+                          workspace: torch.Tensor = None, dev_status: torch.Tensor = None) -> torch.Tensor:
+    """bf16 x [T, K] (quantized per token to MXFP8 inside the call), int32
+    topk_ids [T, topk] -> bf16 [T, topk, N]."""
+    _need(x, torch.bfloat16, "x")
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, topk = topk_ids.shape
+    if out is None:
+        out = torch.empty((T, topk, w.N), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    need = mxfp4_moe_workspace_size(T, topk, w.E, w.K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(load_library().mxfp4_moe_linear_w4a8(_ptr(x), _ptr(topk_ids), T, topk, ctypes.byref(w.desc),
+                                                _ptr(out), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                                _stream()))
     return out
 
 

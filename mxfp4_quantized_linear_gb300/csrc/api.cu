@@ -503,11 +503,14 @@ size_t mxfp4_moe_workspace_size(int T, int topk, int E, int K) {
   return moe_ws(T, topk, E, padded_k(K)).total;
 }
 
-int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, const mx_packed_weight* w,
-                     void* out, void* workspace, size_t workspace_bytes, int* dev_status, void* stream_) {
+// (internal) the routed expert GEMM with bf16 activations (lo = 1: hi and lo
+// MXFP8 pieces) or MXFP8-quantized activations (lo = 0: hi alone)
+static int moe_linear_impl(int lo, const char* name, const void* x, const int32_t* topk_ids, int T, int topk,
+                           const mx_packed_weight* w, void* out, void* workspace, size_t workspace_bytes,
+                           int* dev_status, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (!w) return set_error(MX_ERR_ARG, "NULL weight");
-  if (w->fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "mxfp4_moe_linear needs an E2M1 weight");
+  if (w->fmt != MX_FMT_E2M1) return set_error(MX_ERR_ARG, "%s needs an E2M1 weight", name);
   if (T < 0 || topk < 1) return set_error(MX_ERR_SHAPE, "T=%d topk=%d", T, topk);
   if (w->E > MX_MAX_EXPERTS) return set_error(MX_ERR_UNSUPPORTED, "E=%d exceeds %d", w->E, MX_MAX_EXPERTS);
   if (T == 0) return MX_OK;
@@ -538,12 +541,24 @@ int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, co
   a.pairs = pairs;
   a.active = active;
   a.n_active = n_active;
-  a.lo = 1;
+  a.lo = lo;
   a.out_mode = 0;
   a.out = out;
   a.act = ws + R.act;
   a.act_bytes = R.act_bytes;
   return launch_moe(a, stream);
+}
+
+int mxfp4_moe_linear(const void* x, const int32_t* topk_ids, int T, int topk, const mx_packed_weight* w,
+                     void* out, void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  return moe_linear_impl(1, "mxfp4_moe_linear", x, topk_ids, T, topk, w, out, workspace, workspace_bytes,
+                         dev_status, stream);
+}
+
+int mxfp4_moe_linear_w4a8(const void* x, const int32_t* topk_ids, int T, int topk, const mx_packed_weight* w,
+                          void* out, void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
+  return moe_linear_impl(0, "mxfp4_moe_linear_w4a8", x, topk_ids, T, topk, w, out, workspace, workspace_bytes,
+                         dev_status, stream);
 }
 
 // (internal: static inside the extern "C" block)

@@ -238,7 +238,8 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
 //                    scale atom;
 //   warp 2 (lane 0)  streams the gathered activation pieces of the expert's
 //                    next 16 pairs: 16 rows x 128 bytes of hi and of lo
-//                    (128B swizzle) and their scale atom;
+//                    (128B swizzle) and their scale atom (MXFP8 activations:
+//                    32 rows of hi for the next 32 pairs);
 //   warp 1 (lane 0)  allocates tensor memory and issues, per K step, the two
 //                    scale copies and 4 block-scaled MMAs (kind::mxf8f6f4,
 //                    scale_vec::1X, A e2m1, B e4m3, M = 128 weight rows,
@@ -251,11 +252,14 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
 //                    memory let the next pass's MMAs run meanwhile.
 // Rings: 3 weight stages, 5 activation stages (the activation pieces come from
 // L2, whose latency the deeper ring covers); three CTAs per SM.
-constexpr int kTok = 16;                   // pairs a pass (16 B rows a piece)
+// Pairs a pass: 16 with hi and lo pieces (A16), 32 with hi alone (MXFP8
+// activations); either way the B operand has 32 rows (MMA N = 32).
+constexpr int kTokA16 = 16, kTokMx8 = 32;
+constexpr int kBRows = 32;
 constexpr int kWStages = 3, kXStages = 5;
 constexpr int kWStage = 128 * 128;        // e2m1 operand step, 128B swizzle
 constexpr int kWTx = 128 * 64;            // bytes the TMA writes (the packed half of each chunk)
-constexpr int kXStage = 2 * kTok * 128;   // hi rows | lo rows (4 KB, 1 KB aligned)
+constexpr int kXStage = kBRows * 128;    // B rows, 128B swizzle (4 KB, 1 KB aligned)
 constexpr int kWOff = 0;
 constexpr int kXOff = kWOff + kWStages * kWStage;
 constexpr int kSfaOff = kXOff + kXStages * kXStage;  // a weight scale atom a weight stage
@@ -267,10 +271,9 @@ constexpr int kTcThreads = 256;
 // tensor memory: two accumulators of 32 columns (hi 0..15, lo 16..31) | a
 // (SFA 4, SFB 4) slot a weight stage, rounded up to a power of two
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? c : pow2_at_least(v, 2 * c); }
-constexpr uint32_t kAccCols = 2 * kTok;
+constexpr uint32_t kAccCols = kBRows;
 constexpr uint32_t kTcTmemCols = pow2_at_least(2 * kAccCols + 8 * kWStages);
-constexpr uint32_t kIdescHi = mxf8_idesc_a(128, kTok, kFmtE2M1);         // hi pieces only
-constexpr uint32_t kIdescPieces = mxf8_idesc_a(128, 2 * kTok, kFmtE2M1);  // hi and lo pieces
+constexpr uint32_t kIdescB32 = mxf8_idesc_a(128, kBRows, kFmtE2M1);
 
 struct MoeParams {
   const uint8_t* sfw;      // weight scale atoms [E, NT, KT, 512]
@@ -300,6 +303,8 @@ struct Item {
   int e, o0, cnt, nch, rt;
 };
 
+MX_DEV int pass_pairs(const MoeParams& p) { return p.lo ? kTokA16 : kTokMx8; }
+
 MX_DEV Item item_at(const MoeParams& p, int i) {
   Item it;
   const int a = i / p.NT;
@@ -307,7 +312,7 @@ MX_DEV Item item_at(const MoeParams& p, int i) {
   it.e = p.active[a];
   it.o0 = p.offsets[it.e];
   it.cnt = p.offsets[it.e + 1] - it.o0;
-  it.nch = (it.cnt + kTok - 1) / kTok;
+  it.nch = (it.cnt + pass_pairs(p) - 1) / pass_pairs(p);
   return it;
 }
 
@@ -385,30 +390,32 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
     tma_prefetch_desc(&csmap);
     if (p.lo) tma_prefetch_desc(&xlmap);
     const uint64_t pol = policy_evict_last();  // every row tile of the expert reads them
-    const uint32_t tx = p.lo ? 2 * kTok * (128 + 16) : kTok * (128 + 16);
+    const int tok = pass_pairs(p);
+    const uint32_t tx = kBRows * (128 + 16);  // 32 B rows and their 16-byte code rows, either way
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
       const Item it = item_at(p, i);
       for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
-        const int row0 = it.o0 + ch * kTok;
+        const int row0 = it.o0 + ch * tok;
         for (int s = 0; s < p.KT; ++s, ++g) {
           const int st = g % kXStages;
           if (!mbar_wait(&xempty[st], ((g / kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
           uint8_t* dst = smem + kXOff + st * kXStage;
           uint8_t* atom = smem + kSfbOff + st * 512;
           mbar_arrive_expect_tx(&xfull[st], tx);
+          // hi rows (16 or 32 pairs), then (A16) the lo rows of the same 16 pairs
           tma_load_2d(dst, &xhmap, &xfull[st], s * 128, row0, pol);
           tma_load_2d(atom, &csmap, &xfull[st], s * 32, row0, pol);
           if (p.lo) {
-            tma_load_2d(dst + kTok * 128, &xlmap, &xfull[st], s * 128, row0, pol);
-            tma_load_2d(atom + kTok * 16, &csmap, &xfull[st], s * 32 + 16, row0, pol);
+            tma_load_2d(dst + kTokA16 * 128, &xlmap, &xfull[st], s * 128, row0, pol);
+            tma_load_2d(atom + kTokA16 * 16, &csmap, &xfull[st], s * 32 + 16, row0, pol);
           }
         }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = p.lo ? kIdescPieces : kIdescHi;
+    const uint32_t idesc = kIdescB32;
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -452,21 +459,23 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
       const int n = it.rt * 128 + q * 32 + lane;
       for (int ch = 0; ch < it.nch; ++ch, ++gp) {
         const int buf = gp & 1;
-        const int ntok = it.cnt - ch * kTok < kTok ? it.cnt - ch * kTok : kTok;
-        const int pr = lane < ntok ? p.pairs[it.o0 + ch * kTok + lane] : -1;
+        const int tok = pass_pairs(p);
+        const int ntok = it.cnt - ch * tok < tok ? it.cnt - ch * tok : tok;
+        const int pr = lane < ntok ? p.pairs[it.o0 + ch * tok + lane] : -1;
         if (!mbar_wait(&accfull[buf], (gp >> 1) & 1u)) { *abort_flag = 1u; break; }
         tc_fence_after();
-        uint32_t v[32];  // columns 0..15: hi pieces, 16..31: lo pieces
+        uint32_t v[32];  // A16: columns 0..15 hi pieces, 16..31 lo pieces; MXFP8: 32 pairs
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * kAccCols, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&accempty[buf]);  // the MMAs of a later pass may overwrite it
         if (p.lo) {
 #pragma unroll
-          for (int t = 0; t < kTok; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[kTok + t]));
+          for (int t = 0; t < kTokA16; ++t)
+            v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[kTokA16 + t]));
         }
 #pragma unroll
-        for (int t = 0; t < kTok; ++t) {
+        for (int t = 0; t < kBRows; ++t) {
           if (t >= ntok) break;  // warp-uniform
           const int pt = __shfl_sync(full, pr, t);
           const float y = __uint_as_float(v[t]);
@@ -518,12 +527,12 @@ cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts
   return cudaGetLastError();
 }
 
-// Activation pieces of P pairs: xh [P + 16, Kp] | xl [P + 16, Kp] | codes
-// [P + 16, Kp/128, 32], each region 256-byte aligned (16 spare rows: the last
-// pass of pairs loads a full 16-row box).
-static size_t act_region(long long P, int Kp) { return (static_cast<size_t>(P + kTok) * Kp + 255) & ~size_t(255); }
+// Activation pieces of P pairs: xh [P + 32, Kp] | xl [P + 32, Kp] | codes
+// [P + 32, Kp/128, 32], each region 256-byte aligned (32 spare rows: the last
+// pass of pairs loads a full box).
+static size_t act_region(long long P, int Kp) { return (static_cast<size_t>(P + kBRows) * Kp + 255) & ~size_t(255); }
 static size_t act_codes(long long P, int Kp) {
-  return (static_cast<size_t>(P + kTok) * (Kp / 128) * 32 + 255) & ~size_t(255);
+  return (static_cast<size_t>(P + kBRows) * (Kp / 128) * 32 + 255) & ~size_t(255);
 }
 size_t moe_act_bytes(long long P, int Kp) { return 2 * act_region(P, Kp) + act_codes(P, Kp); }
 
@@ -567,21 +576,22 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.lo = a.lo;
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
-  const uint64_t rows = static_cast<uint64_t>(P + kTok);
+  const uint64_t rows = static_cast<uint64_t>(P + kBRows);
+  const uint32_t tok = a.lo ? kTokA16 : kTokMx8;  // rows a box
   CUtensorMap wmap, xhmap, xlmap, csmap;
   // the packed tiles as rows of 128 e2m1 values (64 bytes), unpacked by the TMA
   const uint64_t wrows = static_cast<uint64_t>(w->E) * p.NT * KT * 128;
   int rc = encode_tensor_map_2d(&wmap, w->bytes, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 128, wrows, 64, 128, 128,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == MX_OK)
-    rc = encode_tensor_map_2d(&xhmap, xh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
+    rc = encode_tensor_map_2d(&xhmap, xh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, tok,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == MX_OK)
-    rc = encode_tensor_map_2d(&xlmap, xl, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, kTok,
+    rc = encode_tensor_map_2d(&xlmap, xl, CU_TENSOR_MAP_DATA_TYPE_UINT8, Kp, rows, Kp, 128, tok,
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == MX_OK)
     rc = encode_tensor_map_2d(&csmap, cs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(KT) * 32, rows,
-                              static_cast<uint64_t>(KT) * 32, 16, kTok, CU_TENSOR_MAP_SWIZZLE_NONE);
+                              static_cast<uint64_t>(KT) * 32, 16, tok, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != MX_OK) return rc;
   DeviceInfo di;
   if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;

@@ -29,18 +29,24 @@ the I up rows, and w2 [E, H, I/2].  Readings where the pages are silent:
   slots are summed: out[t] = sum_j weight[t, j] y2[t, j]; slots whose id is
   not a valid expert contribute nothing.
 
+``moe_linear_w4a8`` is the same routed GEMM with the activation quantized per
+token to MXFP8 first (MXFP4 x MXFP8).
+
 Pinned by tests/test_oracle_moe.py: E = 1 / top-1 reduces to a dense A16W4
 linear checked by exact rational brute force, invariance under permuting the
 tokens, -0 and +0 nibbles giving identical outputs (weights942,
 ``fp4_drop_negative_zero_``), routing against Python's stable sort; silu
 against torch's CPU ``silu``; the full expert at E = 1 / top-1 against the
 same chain in torch CPU ops on a table-decoded weight; gate / up roles,
-slot permutation, linearity in the routing weights and skipped invalid slots.
+slot permutation, linearity in the routing weights and skipped invalid slots;
+W4A8 at E = 1 / top-1 against an exact rational sum over torch's e4m3
+decode, and equal to A16W4 on activations that MXFP8 represents exactly.
 """
 import numpy as np
 
-from .formats import bf16_rne_bits, bf16_value
-from .linear import dequant_values
+from .formats import bf16_rne_bits, bf16_value, e4m3_decode
+from .linear import dequant_values, expand_codes
+from .quant import quantize_act
 
 MX_ERR_EXPERT_ID = 7
 
@@ -97,6 +103,38 @@ def moe_linear(x, topk_ids, w_bytes, codes, wdeq=None) -> np.ndarray:
             if 0 <= e < E:
                 y[t, j] = W[e] @ x[t]
     return y
+
+
+def moe_linear_w4a8(x, topk_ids, w_bytes, codes) -> dict:
+    """The routed expert GEMM with MXFP8 activations (the prefill form of the
+    layer: MXFP4 weights times per-token MXFP8-quantized activations, as the
+    dense MXFP8 linear quantizes its input -- rocm_native, _quant_mxfp8_tile).
+    x fp64 [T, K] (bf16 values) is quantized per token with the block
+    quantizer of quant.quantize_act; then, in fp64,
+
+        y[t, j, n] = sum_k e2m1(W_e[n, k]) 2^(c_e[n, k/32] - 127)
+                           e4m3(q[t, k]) 2^(cx[t, k/32] - 127).
+
+    Returns dict(y=[T, topk, N], A=[T, K] dequantized activation,
+    xq, xcodes)."""
+    x = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    T, topk = ids.shape
+    w_bytes = np.asarray(w_bytes, dtype=np.uint8)
+    E, N, KH = w_bytes.shape
+    K = 2 * KH
+    xq, xcodes = quantize_act(x)
+    A = e4m3_decode(xq) * expand_codes(xcodes, T, K)
+    y = np.zeros((T, topk, N), dtype=np.float64)
+    W = {}
+    for t in range(T):
+        for j in range(topk):
+            e = int(ids[t, j])
+            if 0 <= e < E:
+                if e not in W:
+                    W[e] = dequant_values(w_bytes[e], codes[e], "e2m1", N, K)
+                y[t, j] = W[e] @ A[t]
+    return {"y": y, "A": A, "xq": xq, "xcodes": xcodes}
 
 
 def silu(v) -> np.ndarray:

@@ -258,3 +258,82 @@ def test_moe_single_k_step_and_k_32():
     to a step)."""
     assert check_moe(inputs.moe_gate_up(E=2, N=64, K=128, T=3, topk=1, seed=6)) == 0
     assert check_moe(inputs.moe_gate_up(E=3, N=40, K=32, T=5, topk=2, seed=9)) == 0
+
+
+# ---------------------------------------------------------------- W4A8 (MXFP4 x MXFP8 activations)
+
+def check_w4a8(m, ids=None):
+    from oracle.moe import moe_linear_w4a8
+    dev = cuda_device()
+    ensure_built()
+    ids = m["ids"] if ids is None else ids
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    y = mx.mxfp4_moe_linear_w4a8(m["x"].to(dev), ids.to(dev), p, dev_status=status)
+    torch.cuda.synchronize()
+    y = y.float().cpu().numpy()
+    xv = bf16_np(m["x"])
+    idn = u8(ids)
+    r = moe_linear_w4a8(xv, idn, u8(m["w"]), u8(m["codes"]))
+    E = m["E"]
+    K = xv.shape[1]
+    for t in range(idn.shape[0]):
+        for j in range(idn.shape[1]):
+            e = int(idn[t, j])
+            if 0 <= e < E:
+                W = dequant_values(u8(m["w"])[e], u8(m["codes"])[e], "e2m1", m["N"], K)
+                err = normalized_error(y[t, j][None], r["y"][t, j][None], r["A"][t][None], W)
+                assert err <= TOL, (t, j, err)
+                # exact products, f32 sums, one bf16 rounding: far inside the tolerance
+                den = np.linalg.norm(W, axis=1) * np.linalg.norm(r["A"][t])
+                assert np.all(np.abs(y[t, j] - r["y"][t, j]) <= 2.0 ** -8 * np.abs(r["y"][t, j]) + 1e-5 * den)
+            else:
+                assert np.all(y[t, j] == 0)
+    return int(status.item())
+
+
+def test_w4a8_small_with_invalid_ids():
+    m = inputs.moe_gate_up(E=8, N=256, K=512, T=13, topk=3, seed=21)
+    ids = m["ids"].clone()
+    ids[4, 1] = -1
+    assert check_w4a8(m, ids) == 0
+    ids[6, 2] = 99
+    assert check_w4a8(m, ids) == MX_ERR_EXPERT_ID
+
+
+def test_w4a8_ragged_rows_and_k():
+    assert check_w4a8(inputs.moe_gate_up(E=5, N=136, K=2080, T=9, topk=2, seed=22)) == 0
+
+
+def test_w4a8_several_passes_of_pairs():
+    """75 pairs on one expert: three 32-pair passes (the last one ragged)."""
+    m = inputs.moe_gate_up(E=4, N=200, K=384, T=75, topk=2, seed=23)
+    ids = torch.full((75, 2), 1, dtype=torch.int32)
+    ids[:, 0] = torch.tensor([0, 2, 3], dtype=torch.int32).repeat(25)
+    assert check_w4a8(m, ids) == 0
+
+
+def test_w4a8_full_size_sampled():
+    from oracle.quant import quantize_act
+    from oracle.linear import expand_codes
+    from oracle.formats import e4m3_decode
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_gate_up()
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    y = mx.mxfp4_moe_linear_w4a8(m["x"].to(dev), m["ids"].to(dev), p)
+    torch.cuda.synchronize()
+    y = y.float().cpu().numpy()
+    xv = bf16_np(m["x"])
+    xq, xc = quantize_act(xv)
+    A = e4m3_decode(xq) * expand_codes(xc, xv.shape[0], xv.shape[1])
+    rng = np.random.default_rng(24)
+    wb, cb, ids = u8(m["w"]), u8(m["codes"]), u8(m["ids"])
+    for _ in range(48):
+        t, j = int(rng.integers(0, 64)), int(rng.integers(0, 8))
+        ns = np.sort(rng.choice(4096, size=64, replace=False))
+        e = int(ids[t, j])
+        Wd = dequant_values(wb[e, ns], cb[e, ns], "e2m1", len(ns), 4096)
+        ref = Wd @ A[t]
+        err = normalized_error(y[t, j, ns][None], ref[None], A[t][None], Wd)
+        assert err <= TOL, (t, j, err)

@@ -169,3 +169,52 @@ def test_expert_slot_permutation_weights_and_invalid_ids():
     wts0[:, 1] = 0.0
     assert np.array_equal(moe_expert(x, ids_bad, wts, w13, c13, w2, c2)["out"],
                           moe_expert(x, ids, wts0, w13, c13, w2, c2)["out"])
+
+
+def test_w4a8_single_expert_top1_exact():
+    """W4A8 at E = 1, top-1: the exact rational sum of e2m1(w) 2^(cw-127) times
+    the quantized activation, its e4m3 bytes decoded by torch (not by the
+    oracle's decoder)."""
+    import torch
+    from oracle.moe import moe_linear_w4a8
+    rng = np.random.default_rng(11)
+    T, N, K = 3, 4, 64
+    x = F.bf16_value(F.bf16_rne_bits(rng.standard_normal((T, K)) * 3.0))
+    w = rng.integers(0, 256, size=(1, N, K // 2), dtype=np.uint8)
+    codes = rng.integers(122, 131, size=(1, N, K // 32), dtype=np.uint8)
+    r = moe_linear_w4a8(x, np.zeros((T, 1), dtype=np.int32), w, codes)
+    qv = torch.tensor(r["xq"].astype(np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    tab = e2m1_table()
+    for t in range(T):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                byte = int(w[0, n, k // 2])
+                nib = byte & 0xF if k % 2 == 0 else byte >> 4
+                a = Fraction(float(qv[t, k])) * Fraction(2) ** (int(r["xcodes"][t, k // 32]) - 127)
+                acc += tab[nib] * Fraction(2) ** (int(codes[0, n, k // 32]) - 127) * a
+            assert abs(float(acc) - r["y"][t, 0, n]) <= 1e-13 * max(1.0, abs(float(acc)))
+
+
+def test_w4a8_equals_a16w4_on_exactly_representable_activations():
+    """An activation that MXFP8 represents exactly (every block: e4m3 values
+    under one scale whose largest magnitude is 256..448, so the quantizer
+    keeps that scale) gives the same W4A8 and A16W4 outputs."""
+    from oracle.moe import moe_linear_w4a8
+    rng = np.random.default_rng(12)
+    T, E, N, K, topk = 5, 3, 6, 96, 2
+    vals = F.e4m3_decode(np.arange(256, dtype=np.uint8))
+    ok = np.isfinite(vals) & (np.abs(vals) <= 448)
+    pool = vals[ok]
+    x = rng.choice(pool, size=(T, K))
+    blocks = x.reshape(T, K // 32, 32)
+    blocks[:, :, 0] = 448.0 * np.where(rng.random((T, K // 32)) < 0.5, -1, 1)   # block max 448
+    scale = np.ldexp(1.0, rng.integers(-3, 4, size=(T, K // 32)))
+    x = (blocks * scale[..., None]).reshape(T, K)
+    w = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    codes = rng.integers(120, 133, size=(E, N, K // 32), dtype=np.uint8)
+    ids = np.stack([rng.permutation(E)[:topk] for _ in range(T)]).astype(np.int32)
+    r = moe_linear_w4a8(x, ids, w, codes)
+    assert np.array_equal(r["A"], x)                      # the quantization is exact here
+    y16 = moe_linear(x, ids, w, codes)
+    assert np.allclose(r["y"], y16, rtol=1e-12, atol=0.0)
