@@ -84,7 +84,7 @@ LinearWs linear_ws(int M, int Kp) {
 }
 
 struct MoeWs {
-  size_t counts, offsets, pairs, active, n_active, status, act, act_bytes, total;
+  size_t counts, offsets, pairs, active, n_active, status, pass_off, act, act_bytes, total;
 };
 
 // Routing outputs, then the activation pieces of the T * topk pairs for K
@@ -99,8 +99,9 @@ MoeWs moe_ws(int T, int topk, int E, int Kp) {
   r.active = o;   o += align_up(4 * static_cast<size_t>(E), 16);
   r.n_active = o; o += 16;
   r.status = o;   o += 16;
+  r.pass_off = o; o += align_up(4 * (static_cast<size_t>(E) + 1), 16);
   r.act = align_up(o, 256);
-  r.act_bytes = Kp > 0 ? moe_act_bytes(static_cast<long long>(P), Kp) : 0;
+  r.act_bytes = Kp > 0 ? moe_act_bytes(static_cast<long long>(P), Kp, E) : 0;
   r.total = r.act + r.act_bytes;
   return r;
 }
@@ -528,9 +529,12 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   int32_t* active = reinterpret_cast<int32_t*>(ws + R.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.n_active);
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.status);
-  // routing, and zero rows for the pairs whose id is not a valid expert
+  // routing (with pass offsets when the experts average enough pairs for wide
+  // passes), and zero rows for the pairs whose id is not a valid expert
+  const int pw = moe_wide_pass(static_cast<long long>(T) * topk, w->E, lo);
+  int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.pass_off);
   cudaError_t e = launch_route(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream, out,
-                               w->N);
+                               w->N, pw ? pass_off : nullptr, pw);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
   a.x = x;
@@ -546,6 +550,9 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   a.out = out;
   a.act = ws + R.act;
   a.act_bytes = R.act_bytes;
+  a.wide_pass = pw;
+  a.ids = topk_ids;
+  a.pass_off = pass_off;
   return launch_moe(a, stream);
 }
 
@@ -617,9 +624,15 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   int32_t* active = reinterpret_cast<int32_t*>(ws + R.route.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.route.n_active);
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.route.status);
-  cudaError_t e = launch_route(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream);
+  const int pw = moe_wide_pass(static_cast<long long>(T) * topk, E, 1);
+  int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.route.pass_off);
+  cudaError_t e = launch_route(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream, nullptr,
+                               0, pw ? pass_off : nullptr, pw);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
+  a.wide_pass = pw;
+  a.ids = topk_ids;
+  a.pass_off = pass_off;
   a.T = T;
   a.topk = topk;
   a.lo = 1;

@@ -25,12 +25,14 @@ constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 // zero_out (optional): bf16 [P, zero_N] rows of the pairs whose id is not a
-// valid expert are set to zero (they belong to no expert's list).
+// valid expert are set to zero (they belong to no expert's list).  pass_off
+// (optional): pass_off[e] = the number of passes of pw pairs the experts
+// before e need, pass_off[E] the total.
 __global__ void __launch_bounds__(kRouteThreads)
     route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ pairs,
                  int32_t* __restrict__ active, int32_t* __restrict__ n_active, int* dev_status,
-                 __nv_bfloat16* __restrict__ zero_out, int zero_N) {
+                 __nv_bfloat16* __restrict__ zero_out, int zero_N, int32_t* __restrict__ pass_off, int pw) {
   extern __shared__ int rs[];
   pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid
   int* cnt = rs;           // [E]
@@ -55,28 +57,36 @@ __global__ void __launch_bounds__(kRouteThreads)
     }
   }
   bad = __syncthreads_or(bad);
-  if (warp == 0) {  // exclusive scan of the counts, and the ascending list of active experts
-    int run = 0, arun = 0;
+  if (warp == 0) {  // exclusive scans of the counts (and passes), the ascending list of active experts
+    int run = 0, arun = 0, prun = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       const int c = e < E ? cnt[e] : 0;
-      int incl = c;
+      const int pc = pass_off && pw > 0 ? (c + pw - 1) / pw : 0;
+      int incl = c, pincl = pc;
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(full, incl, o);
-        if (lane >= o) incl += v;
+        const int pv = __shfl_up_sync(full, pincl, o);
+        if (lane >= o) {
+          incl += v;
+          pincl += pv;
+        }
       }
       const unsigned am = __ballot_sync(full, c > 0);
       if (e < E) {
         counts[e] = c;
         offsets[e] = run + incl - c;
         base[e] = run + incl - c;
+        if (pass_off) pass_off[e] = prun + pincl - pc;
         if (c > 0) active[arun + __popc(am & ((1u << lane) - 1u))] = e;
       }
       run += __shfl_sync(full, incl, 31);
+      prun += __shfl_sync(full, pincl, 31);
       arun += __popc(am);
     }
     if (lane == 0) {
       offsets[E] = run;
+      if (pass_off) pass_off[E] = prun;
       *n_active = arun;
       if (dev_status) *dev_status = bad ? MX_ERR_EXPERT_ID : MX_OK;
     }
@@ -173,10 +183,16 @@ __device__ __forceinline__ uint32_t mx_quant_f32x32(const float (&v)[32], uint4 
 // Rows past the routed pairs (slots with an invalid id are in no expert's
 // list, so the list holds *n_pairs <= P entries) are left as they are: they
 // only ever fill unused columns of a pass's last 32-row box.
+// Wide passes (sfb != nullptr): instead of the 16-byte code rows, the codes
+// go to the scale-factor atom of the row's pass: row r of pass c of expert e
+// (r = its rank in the expert's list mod pw) is B row r (hi) and pw + r (lo),
+// byte (m % 32) * 16 + (m / 32) * 4 + kb of atom [pass_off[e] + c][K step].
 __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pairs,
                                   const int32_t* __restrict__ n_pairs, int P, int topk, int x_per_pair, int K,
                                   int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl,
-                                  uint8_t* __restrict__ cs) {
+                                  uint8_t* __restrict__ cs, const int32_t* __restrict__ ids,
+                                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ pass_off, int pw,
+                                  uint8_t* __restrict__ sfb) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();  // the routing (and the activation, when a kernel wrote it) is complete
   const int KBp = Kp >> 5, KB = K >> 5, KT = Kp >> 7;
@@ -214,21 +230,29 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
     uint4* hp = reinterpret_cast<uint4*>(xh + j * Kp + 32 * b);
     hp[0] = qh[0];
     hp[1] = qh[1];
-    uint8_t* cp = cs + (j * KT + (b >> 2)) * 32 + (b & 3);
-    cp[0] = static_cast<uint8_t>(ch);
     if (lo) {
       uint4* lp = reinterpret_cast<uint4*>(xl + j * Kp + 32 * b);
       lp[0] = ql[0];
       lp[1] = ql[1];
-      cp[16] = static_cast<uint8_t>(cl);
+    }
+    if (sfb) {
+      const int e = ids[pr];
+      const int rank = static_cast<int>(j) - offsets[e];
+      const int r = rank % pw;
+      uint8_t* atom = sfb + (static_cast<long long>(pass_off[e] + rank / pw) * KT + (b >> 2)) * 512 + (b & 3);
+      atom[(r & 31) * 16 + (r >> 5) * 4] = static_cast<uint8_t>(ch);
+      if (lo) atom[((pw + r) & 31) * 16 + ((pw + r) >> 5) * 4] = static_cast<uint8_t>(cl);
+    } else {
+      uint8_t* cp = cs + (j * KT + (b >> 2)) * 32 + (b & 3);
+      cp[0] = static_cast<uint8_t>(ch);
+      if (lo) cp[16] = static_cast<uint8_t>(cl);
     }
   }
 }
 
 // ---------------------------------------------------------------- expert GEMM
 //
-// Persistent CTAs (three an SM), each walking (expert, 128-row tile) work
-// items; 8 warps:
+// Persistent CTAs walking (expert, 128-row tile) work items; 8 warps:
 //   warp 0 (lane 0)  streams the weight tile, one K step (128 rows x 128 e2m1
 //                    values, a contiguous 8 KB block) a stage: a TMA load with
 //                    the 16U4_ALIGN16B data type writes it straight in the
@@ -236,51 +260,59 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
 //                    bytes a 16-byte chunk, the other 8 bytes not written and
 //                    not read, 128B swizzle), plus the step's 512-byte weight
 //                    scale atom;
-//   warp 2 (lane 0)  streams the gathered activation pieces of the expert's
-//                    next 16 pairs: 16 rows x 128 bytes of hi and of lo
-//                    (128B swizzle) and their scale atom (MXFP8 activations:
-//                    32 rows of hi for the next 32 pairs);
+//   warp 2 (lane 0)  streams the B operand of the expert's next pass of
+//                    pairs: their hi rows then (A16) their lo rows, 128 bytes
+//                    of e4m3 a row for the K step (128B swizzle), and the scale
+//                    atom of those rows;
 //   warp 1 (lane 0)  allocates tensor memory and issues, per K step, the two
 //                    scale copies and 4 block-scaled MMAs (kind::mxf8f6f4,
 //                    scale_vec::1X, A e2m1, B e4m3, M = 128 weight rows,
-//                    K = 32) whose B operand stacks the 16 pairs' hi pieces
-//                    (rows 0..15) on their lo pieces (rows 16..31), N = 32:
-//                    one f32 accumulator column a piece of a pair;
+//                    N = the B rows, K = 32): one f32 accumulator column a B
+//                    row;
 //   warps 4..7       read the accumulator (tcgen05.ld, one lane quarter each),
 //                    add each pair's hi and lo columns and store bf16 /
-//                    SiLU-and-mul / f32 per pair; two accumulators in tensor
-//                    memory let the next pass's MMAs run meanwhile.
-// Rings: 3 weight stages, 5 activation stages (the activation pieces come from
-// L2, whose latency the deeper ring covers); three CTAs per SM.
-// Pairs a pass: 16 with hi and lo pieces (A16), 32 with hi alone (MXFP8
-// activations); either way the B operand has 32 rows (MMA N = 32).
-constexpr int kTokA16 = 16, kTokMx8 = 32;
-constexpr int kBRows = 32;
-constexpr int kWStages = 3, kXStages = 5;
-constexpr int kWStage = 128 * 128;        // e2m1 operand step, 128B swizzle
-constexpr int kWTx = 128 * 64;            // bytes the TMA writes (the packed half of each chunk)
-constexpr int kXStage = kBRows * 128;    // B rows, 128B swizzle (4 KB, 1 KB aligned)
-constexpr int kWOff = 0;
-constexpr int kXOff = kWOff + kWStages * kWStage;
-constexpr int kSfaOff = kXOff + kXStages * kXStage;  // a weight scale atom a weight stage
-constexpr int kSfbOff = kSfaOff + kWStages * 512;      // an activation scale atom an activation stage
-constexpr int kBarOff = (kSfbOff + kXStages * 512 + 1023) & ~1023;
-constexpr int kBarBytes = ((2 * (kWStages + kXStages) + 4) * 8 + 8 + 255) & ~255;  // + TMEM slot, flag
-constexpr int kTcSmem = kBarOff + kBarBytes + 1024;
-constexpr int kTcThreads = 256;
-// tensor memory: two accumulators of 32 columns (hi 0..15, lo 16..31) | a
-// (SFA 4, SFB 4) slot a weight stage, rounded up to a power of two
+//                    SiLU-and-mul / f32 per pair.
+// Two pass widths.  Narrow (decode: a few pairs an expert): 32 B rows (16
+// pairs with hi and lo, or 32 pairs hi only), the activation scale atom taken
+// by TMA from the pairs' 16-byte code rows, two accumulators, three CTAs an
+// SM.  Wide (prefill: hundreds of pairs an expert): 128 B rows (64 pairs with
+// hi and lo, or 128 hi only), the scale atom of the pass laid out by the
+// activation-pieces kernel and bulk-copied, one accumulator, two CTAs an SM.
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? c : pow2_at_least(v, 2 * c); }
-constexpr uint32_t kAccCols = kBRows;
-constexpr uint32_t kTcTmemCols = pow2_at_least(2 * kAccCols + 8 * kWStages);
-constexpr uint32_t kIdescB32 = mxf8_idesc_a(128, kBRows, kFmtE2M1);
+
+template <bool kWide>
+struct MoeCfg {
+  static constexpr int kBRows = kWide ? 128 : 32;      // B rows a pass (MMA N)
+  static constexpr int kWStages = 3;
+  static constexpr int kXStages = kWide ? 3 : 5;       // the activation comes from L2
+  static constexpr int kAccBufs = kWide ? 1 : 2;
+  static constexpr int kCtasPerSm = kWide ? 2 : 3;
+  static constexpr int kWStage = 128 * 128;           // e2m1 operand step, 128B swizzle
+  static constexpr int kXStage = kBRows * 128;        // B rows, 128B swizzle (1 KB aligned)
+  static constexpr int kWOff = 0;
+  static constexpr int kXOff = kWOff + kWStages * kWStage;
+  static constexpr int kSfaOff = kXOff + kXStages * kXStage;  // a weight scale atom a weight stage
+  static constexpr int kSfbOff = kSfaOff + kWStages * 512;      // an activation scale atom a stage
+  static constexpr int kBarOff = (kSfbOff + kXStages * 512 + 1023) & ~1023;
+  static constexpr int kBarBytes = ((2 * (kWStages + kXStages) + 2 * kAccBufs) * 8 + 8 + 255) & ~255;
+  static constexpr int kSmem = kBarOff + kBarBytes + 1024;
+  static constexpr uint32_t kAccCols = kBRows;
+  // tensor memory: the accumulator(s) | a (SFA 4, SFB 4) slot a weight stage
+  static constexpr uint32_t kTmemCols = pow2_at_least(kAccBufs * kAccCols + 8 * kWStages);
+  static constexpr uint32_t kIdesc = mxf8_idesc_a(128, kBRows, kFmtE2M1);
+};
+constexpr int kWTx = 128 * 64;            // bytes the weight TMA writes (the packed half of each chunk)
+constexpr int kTcThreads = 256;
+constexpr int kWidePairsA16 = 64, kWidePairsMx8 = 128;  // pairs a wide pass
 
 struct MoeParams {
   const uint8_t* sfw;      // weight scale atoms [E, NT, KT, 512]
+  const uint8_t* sfb;      // wide: activation scale atoms [passes, KT, 512]
   const int32_t* offsets;
   const int32_t* pairs;
   const int32_t* active;
   const int32_t* n_active;
+  const int32_t* pass_off; // wide: first pass of each expert [E + 1]
   __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
   float* out_f32;          // kMoeOutF32: [T * topk, N]
   int N, KT, NT;
@@ -303,47 +335,62 @@ struct Item {
   int e, o0, cnt, nch, rt;
 };
 
-MX_DEV int pass_pairs(const MoeParams& p) { return p.lo ? kTokA16 : kTokMx8; }
-
-MX_DEV Item item_at(const MoeParams& p, int i) {
+MX_DEV Item item_at(const MoeParams& p, int i, int tok) {
   Item it;
   const int a = i / p.NT;
   it.rt = i - a * p.NT;
   it.e = p.active[a];
   it.o0 = p.offsets[it.e];
   it.cnt = p.offsets[it.e + 1] - it.o0;
-  it.nch = (it.cnt + pass_pairs(p) - 1) / pass_pairs(p);
+  it.nch = (it.cnt + tok - 1) / tok;
   return it;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                             const __grid_constant__ CUtensorMap xhmap,
-                                                             const __grid_constant__ CUtensorMap xlmap,
-                                                             const __grid_constant__ CUtensorMap csmap,
-                                                             const MoeParams p) {
+// One pair's output value y for weight row n (lane l of the warp holds row n).
+MX_DEV void store_pair(const MoeParams& p, int pt, int n, int lane, float y) {
+  if (p.out_mode == kMoeOutSwiglu) {
+    // lane l (l % 16 < 8) holds gate row 8 (n / 16) + l % 16, lane l + 8 its up row
+    const float u = __shfl_down_sync(0xffffffffu, y, 8);
+    if ((lane & 15) < 8 && n < p.N)
+      p.out[static_cast<long long>(pt) * (p.N >> 1) + (n >> 4) * 8 + (n & 15)] = __float2bfloat16_rn(silu_f32(y) * u);
+  } else if (p.out_mode == kMoeOutF32) {
+    if (n < p.N) p.out_f32[static_cast<long long>(pt) * p.N + n] = y;
+  } else if (p.out_mode == kMoeOutBf16 && n < p.N) {
+    const int nn = p.gate_up ? gate_up_row(n, p.N) : n;
+    p.out[static_cast<long long>(pt) * p.N + nn] = __float2bfloat16_rn(y);
+  }
+}
+
+template <bool kWide>
+__global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
+    moe_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xhmap,
+               const __grid_constant__ CUtensorMap xlmap, const __grid_constant__ CUtensorMap csmap,
+               const MoeParams p) {
+  using C = MoeCfg<kWide>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok = C::kBRows >> p.lo;  // pairs a pass
 
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* wempty = wfull + kWStages;
-  uint64_t* xfull = wempty + kWStages;
-  uint64_t* xempty = xfull + kXStages;
-  uint64_t* accfull = xempty + kXStages;  // [2]
-  uint64_t* accempty = accfull + 2;       // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* wempty = wfull + C::kWStages;
+  uint64_t* xfull = wempty + C::kWStages;
+  uint64_t* xempty = xfull + C::kXStages;
+  uint64_t* accfull = xempty + C::kXStages;      // [kAccBufs]
+  uint64_t* accempty = accfull + C::kAccBufs;    // [kAccBufs]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + C::kAccBufs);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kWStages; ++i) {
+    for (int i = 0; i < C::kWStages; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], 1);     // tcgen05.commit
     }
-    for (int i = 0; i < kXStages; ++i) {
+    for (int i = 0; i < C::kXStages; ++i) {
       mbar_init(&xfull[i], 1);
       mbar_init(&xempty[i], 1);     // tcgen05.commit
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&accfull[i], 1);    // tcgen05.commit
       mbar_init(&accempty[i], 4);   // one arrival an epilogue warp
     }
@@ -351,7 +398,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTcTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -367,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
     tma_prefetch_desc(&wmap);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i);
+      const Item it = item_at(p, i, tok);
       // a weight tile read once streams past L2; read again (more than one
       // pass of pairs) it is kept
       const uint64_t pol = it.nch > 1 ? policy_evict_last() : policy_evict_first();
@@ -376,70 +423,72 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
       const uint8_t* sfa = p.sfw + tile * p.KT * 512;
       for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
         for (int s = 0; s < p.KT; ++s, ++g) {
-          const int st = g % kWStages;
-          if (!mbar_wait(&wempty[st], ((g / kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+          const int st = g % C::kWStages;
+          if (!mbar_wait(&wempty[st], ((g / C::kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
           mbar_arrive_expect_tx(&wfull[st], kWTx + 512);
-          tma_load_2d(smem + kWOff + st * kWStage, &wmap, &wfull[st], 0, row0 + s * 128, pol);
-          bulk_load(smem + kSfaOff + st * 512, sfa + s * 512, 512, &wfull[st]);
+          tma_load_2d(smem + C::kWOff + st * C::kWStage, &wmap, &wfull[st], 0, row0 + s * 128, pol);
+          bulk_load(smem + C::kSfaOff + st * 512, sfa + s * 512, 512, &wfull[st]);
         }
       }
     }
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------------------ activation producer
     tma_prefetch_desc(&xhmap);
-    tma_prefetch_desc(&csmap);
+    if (!kWide) tma_prefetch_desc(&csmap);
     if (p.lo) tma_prefetch_desc(&xlmap);
     const uint64_t pol = policy_evict_last();  // every row tile of the expert reads them
-    const int tok = pass_pairs(p);
-    const uint32_t tx = kBRows * (128 + 16);  // 32 B rows and their 16-byte code rows, either way
+    const uint32_t tx = kWide ? C::kBRows * 128 + 512 : C::kBRows * (128 + 16);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i);
+      const Item it = item_at(p, i, tok);
       for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
         const int row0 = it.o0 + ch * tok;
         for (int s = 0; s < p.KT; ++s, ++g) {
-          const int st = g % kXStages;
-          if (!mbar_wait(&xempty[st], ((g / kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
-          uint8_t* dst = smem + kXOff + st * kXStage;
-          uint8_t* atom = smem + kSfbOff + st * 512;
+          const int st = g % C::kXStages;
+          if (!mbar_wait(&xempty[st], ((g / C::kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+          uint8_t* dst = smem + C::kXOff + st * C::kXStage;
+          uint8_t* atom = smem + C::kSfbOff + st * 512;
           mbar_arrive_expect_tx(&xfull[st], tx);
-          // hi rows (16 or 32 pairs), then (A16) the lo rows of the same 16 pairs
+          // hi rows of the pass's pairs, then (A16) their lo rows
           tma_load_2d(dst, &xhmap, &xfull[st], s * 128, row0, pol);
-          tma_load_2d(atom, &csmap, &xfull[st], s * 32, row0, pol);
-          if (p.lo) {
-            tma_load_2d(dst + kTokA16 * 128, &xlmap, &xfull[st], s * 128, row0, pol);
-            tma_load_2d(atom + kTokA16 * 16, &csmap, &xfull[st], s * 32 + 16, row0, pol);
+          if (p.lo) tma_load_2d(dst + tok * 128, &xlmap, &xfull[st], s * 128, row0, pol);
+          if (kWide) {
+            bulk_load(atom, p.sfb + (static_cast<long long>(p.pass_off[it.e] + ch) * p.KT + s) * 512, 512,
+                      &xfull[st]);
+          } else {
+            tma_load_2d(atom, &csmap, &xfull[st], s * 32, row0, pol);
+            if (p.lo) tma_load_2d(atom + tok * 16, &csmap, &xfull[st], s * 32 + 16, row0, pol);
           }
         }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = kIdescB32;
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = item_at(p, i);
+      const Item it = item_at(p, i, tok);
       for (int ch = 0; ch < it.nch && ok; ++ch, ++gp) {
-        const int buf = gp & 1;  // accumulator buffer: the epilogue drains the other
-        if (!mbar_wait(&accempty[buf], ((gp >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        const int buf = gp % C::kAccBufs;  // the epilogue drains the other accumulator (narrow)
+        if (!mbar_wait(&accempty[buf], ((gp / C::kAccBufs) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t acc = tmem + static_cast<uint32_t>(buf) * kAccCols;
+        const uint32_t acc = tmem + static_cast<uint32_t>(buf) * C::kAccCols;
         for (int s = 0; s < p.KT; ++s, ++gw, ++gx) {
-          const int ws = gw % kWStages, xs = gx % kXStages;
-          if (!mbar_wait(&wfull[ws], (gw / kWStages) & 1u) || !mbar_wait(&xfull[xs], (gx / kXStages) & 1u)) {
+          const int ws = gw % C::kWStages, xs = gx % C::kXStages;
+          if (!mbar_wait(&wfull[ws], (gw / C::kWStages) & 1u) ||
+              !mbar_wait(&xfull[xs], (gx / C::kXStages) & 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfc = tmem + 2 * kAccCols + static_cast<uint32_t>(ws * 8);
-          tc_cp_sf(sfc, sf_desc(smem_u32(smem + kSfaOff + ws * 512)));
-          tc_cp_sf(sfc + 4, sf_desc(smem_u32(smem + kSfbOff + xs * 512)));
-          const uint64_t adesc = sw128_desc(smem_u32(smem + kWOff + ws * kWStage));
-          const uint64_t bdesc = sw128_desc(smem_u32(smem + kXOff + xs * kXStage));  // hi 0..15, lo 16..31
+          const uint32_t sfc = tmem + C::kAccBufs * C::kAccCols + static_cast<uint32_t>(ws * 8);
+          tc_cp_sf(sfc, sf_desc(smem_u32(smem + C::kSfaOff + ws * 512)));
+          tc_cp_sf(sfc + 4, sf_desc(smem_u32(smem + C::kSfbOff + xs * 512)));
+          const uint64_t adesc = sw128_desc(smem_u32(smem + C::kWOff + ws * C::kWStage));
+          const uint64_t bdesc = sw128_desc(smem_u32(smem + C::kXOff + xs * C::kXStage));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+            const uint32_t id = C::kIdesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
             tc_mma_mxf8(acc, adesc + 2 * k, bdesc + 2 * k, id, sfc, sfc + 4, (s | k) != 0 ? 1u : 0u);
           }
           tc_commit(&wempty[ws]);
@@ -452,45 +501,55 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quarter: rows 32 q .. 32 q + 31
-    const unsigned full = 0xffffffffu;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int gp = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i);
+      const Item it = item_at(p, i, tok);
       const int n = it.rt * 128 + q * 32 + lane;
       for (int ch = 0; ch < it.nch; ++ch, ++gp) {
-        const int buf = gp & 1;
-        const int tok = pass_pairs(p);
+        const int buf = gp % C::kAccBufs;
         const int ntok = it.cnt - ch * tok < tok ? it.cnt - ch * tok : tok;
-        const int pr = lane < ntok ? p.pairs[it.o0 + ch * tok + lane] : -1;
-        if (!mbar_wait(&accfull[buf], (gp >> 1) & 1u)) { *abort_flag = 1u; break; }
+        const int* prow = p.pairs + it.o0 + ch * tok;  // this pass's pairs
+        if (!mbar_wait(&accfull[buf], (gp / C::kAccBufs) & 1u)) { *abort_flag = 1u; break; }
         tc_fence_after();
-        uint32_t v[32];  // A16: columns 0..15 hi pieces, 16..31 lo pieces; MXFP8: 32 pairs
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * kAccCols, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[buf]);  // the MMAs of a later pass may overwrite it
-        if (p.lo) {
+        const uint32_t acc = lane_base + static_cast<uint32_t>(buf) * C::kAccCols;
+        if (!kWide) {
+          uint32_t v[32];  // A16: columns 0..15 hi pieces, 16..31 lo pieces; MXFP8: 32 pairs
+          tmem_ld32(acc, v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[buf]);  // a later pass may overwrite it
+          const int pr = lane < ntok ? prow[lane] : -1;
+          if (p.lo) {
 #pragma unroll
-          for (int t = 0; t < kTokA16; ++t)
-            v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[kTokA16 + t]));
-        }
-#pragma unroll
-        for (int t = 0; t < kBRows; ++t) {
-          if (t >= ntok) break;  // warp-uniform
-          const int pt = __shfl_sync(full, pr, t);
-          const float y = __uint_as_float(v[t]);
-          if (p.out_mode == kMoeOutSwiglu) {
-            // lane l (l % 16 < 8) holds gate row 8 (n / 16) + l % 16, lane l + 8 its up row
-            const float u = __shfl_down_sync(full, y, 8);
-            if ((lane & 15) < 8 && n < p.N)
-              p.out[static_cast<long long>(pt) * (p.N >> 1) + (n >> 4) * 8 + (n & 15)] =
-                  __float2bfloat16_rn(silu_f32(y) * u);
-          } else if (p.out_mode == kMoeOutF32) {
-            if (n < p.N) p.out_f32[static_cast<long long>(pt) * p.N + n] = y;
-          } else if (p.out_mode == kMoeOutBf16 && n < p.N) {
-            const int nn = p.gate_up ? gate_up_row(n, p.N) : n;
-            p.out[static_cast<long long>(pt) * p.N + nn] = __float2bfloat16_rn(y);
+            for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[16 + t]));
           }
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            if (t >= ntok) break;  // warp-uniform
+            store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[t]));
+          }
+        } else {
+          // 32 pairs at a time: hi columns 32 c.., (A16) lo columns tok + 32 c..
+          for (int c = 0; c * 32 < ntok; ++c) {
+            uint32_t v[32];
+            tmem_ld32(acc + static_cast<uint32_t>(c * 32), v);
+            if (p.lo) {
+              uint32_t vl[32];
+              tmem_ld32(acc + static_cast<uint32_t>(tok + c * 32), vl);
+#pragma unroll
+              for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(vl[t]));
+            }
+            const int pr = c * 32 + lane < ntok ? prow[c * 32 + lane] : -1;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              if (c * 32 + t >= ntok) break;  // warp-uniform
+              store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[t]));
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[buf]);  // the next pass may overwrite it
         }
       }
     }
@@ -499,7 +558,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) moe_kernel(const __grid_constan
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTcTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -509,13 +568,14 @@ unsigned int take_error_flags_moe() { return take_tu_error_flags(); }
 
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
-                         int* dev_status, cudaStream_t stream, void* zero_out, int zero_N) {
+                         int* dev_status, cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off,
+                         int pw) {
   const int smem = (2 * E + kRouteWarps * E) * static_cast<int>(sizeof(int));
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, T * topk, E, counts, offsets, pairs, active,
                                                    n_active, dev_status,
-                                                   static_cast<__nv_bfloat16*>(zero_out), zero_N);
+                                                   static_cast<__nv_bfloat16*>(zero_out), zero_N, pass_off, pw);
   return cudaGetLastError();
 }
 
@@ -527,57 +587,38 @@ cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts
   return cudaGetLastError();
 }
 
-// Activation pieces of P pairs: xh [P + 32, Kp] | xl [P + 32, Kp] | codes
-// [P + 32, Kp/128, 32], each region 256-byte aligned (32 spare rows: the last
-// pass of pairs loads a full box).
-static size_t act_region(long long P, int Kp) { return (static_cast<size_t>(P + kBRows) * Kp + 255) & ~size_t(255); }
+// Activation pieces of P pairs: xh [P + 128, Kp] | xl [P + 128, Kp] | codes
+// [P + 128, Kp/128, 32] (narrow passes) | wide-pass scale atoms [P/64 + E + 1,
+// Kp/128, 512]; each region 256-byte aligned (spare rows: the last pass of
+// pairs loads a full box).
+constexpr int kSpareRows = 128;
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+static size_t act_region(long long P, int Kp) { return align256(static_cast<size_t>(P + kSpareRows) * Kp); }
 static size_t act_codes(long long P, int Kp) {
-  return (static_cast<size_t>(P + kBRows) * (Kp / 128) * 32 + 255) & ~size_t(255);
+  return align256(static_cast<size_t>(P + kSpareRows) * (Kp / 128) * 32);
 }
-size_t moe_act_bytes(long long P, int Kp) { return 2 * act_region(P, Kp) + act_codes(P, Kp); }
+static size_t act_atoms(long long P, int Kp, int E) {
+  return align256(static_cast<size_t>(P / kWidePairsA16 + E + 1) * (Kp / 128) * 512);
+}
+size_t moe_act_bytes(long long P, int Kp, int E) { return 2 * act_region(P, Kp) + act_codes(P, Kp) + act_atoms(P, Kp, E); }
 
-int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
+// Pairs a wide pass, or 0 for narrow passes: wide once the experts average at
+// least half a wide pass of pairs.
+int moe_wide_pass(long long P, int E, int lo) {
+  const int pw = lo ? kWidePairsA16 : kWidePairsMx8;
+  const long long experts = P < E ? P : E;
+  return experts > 0 && P >= experts * (pw / 2) ? pw : 0;
+}
+
+template <bool kWide>
+static int launch_moe_gemm(const MoeLaunch& a, const MoeParams& p, uint8_t* xh, uint8_t* xl, uint8_t* cs,
+                           cudaLaunchConfig_t cfg) {
+  using C = MoeCfg<kWide>;
   const mx_packed_weight* w = a.w;
   const long long P = static_cast<long long>(a.T) * a.topk;
   const int Kp = w->Kp, KT = Kp / 128;
-  if (!w->sf) return set_error(MX_ERR_ARG, "the E2M1 weight has no scale atoms (pack it with mx_pack_weights)");
-  if (!a.act || a.act_bytes < moe_act_bytes(P, Kp))
-    return set_error(MX_ERR_WORKSPACE, "expert activation workspace of %zu bytes, needs %zu", a.act_bytes,
-                     moe_act_bytes(P, Kp));
-  uint8_t* xh = static_cast<uint8_t*>(a.act);
-  uint8_t* xl = xh + act_region(P, Kp);
-  uint8_t* cs = xl + act_region(P, Kp);
-  const long long nblk = P * (Kp / 32);
-  cudaLaunchAttribute pdl;
-  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl.val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(nblk, 256)), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = stream;
-  cfg.attrs = &pdl;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, act_pieces_kernel, static_cast<const __nv_bfloat16*>(a.x),
-                                     static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
-                                     static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs);
-  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
-
-  MoeParams p = {};
-  p.sfw = w->sf;
-  p.offsets = a.offsets;
-  p.pairs = a.pairs;
-  p.active = a.active;
-  p.n_active = a.n_active;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
-  p.out_f32 = static_cast<float*>(a.out_f32);
-  p.N = w->N;
-  p.KT = KT;
-  p.NT = (w->N + 127) / 128;
-  p.lo = a.lo;
-  p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
-  p.out_mode = a.out_mode;
-  const uint64_t rows = static_cast<uint64_t>(P + kBRows);
-  const uint32_t tok = a.lo ? kTokA16 : kTokMx8;  // rows a box
+  const uint64_t rows = static_cast<uint64_t>(P + kSpareRows);
+  const uint32_t tok = static_cast<uint32_t>(C::kBRows >> a.lo);  // rows a box
   CUtensorMap wmap, xhmap, xlmap, csmap;
   // the packed tiles as rows of 128 e2m1 values (64 bytes), unpacked by the TMA
   const uint64_t wrows = static_cast<uint64_t>(w->E) * p.NT * KT * 128;
@@ -591,25 +632,76 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
                               CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == MX_OK)
     rc = encode_tensor_map_2d(&csmap, cs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(KT) * 32, rows,
-                              static_cast<uint64_t>(KT) * 32, 16, tok, CU_TENSOR_MAP_SWIZZLE_NONE);
+                              static_cast<uint64_t>(KT) * 32, 16, kWide ? 16 : tok, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != MX_OK) return rc;
   DeviceInfo di;
   if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
   static int smem_set[64];
-  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel), kTcSmem, di, smem_set) != MX_OK)
+  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel<kWide>), C::kSmem, di, smem_set) != MX_OK)
     return MX_ERR_CUDA;
-  // persistent: three CTAs an SM (shared and tensor memory allow three), never
-  // more than the largest possible number of work items
+  // persistent: kCtasPerSm CTAs an SM (what shared and tensor memory allow),
+  // never more than the largest possible number of work items
   const long long zmax = P < w->E ? P : w->E;
   const long long items = zmax * p.NT;
-  const long long slots = 3LL * di.sm_count;
+  const long long slots = static_cast<long long>(C::kCtasPerSm) * di.sm_count;
   const int grid = static_cast<int>(items < slots ? items : slots);
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = kTcSmem;
-  e = cudaLaunchKernelEx(&cfg, moe_kernel, wmap, xhmap, xlmap, csmap, p);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_kernel<kWide>, wmap, xhmap, xlmap, csmap, p);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;
+}
+
+int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
+  const mx_packed_weight* w = a.w;
+  const long long P = static_cast<long long>(a.T) * a.topk;
+  const int Kp = w->Kp, KT = Kp / 128;
+  if (!w->sf) return set_error(MX_ERR_ARG, "the E2M1 weight has no scale atoms (pack it with mx_pack_weights)");
+  if (!a.act || a.act_bytes < moe_act_bytes(P, Kp, w->E))
+    return set_error(MX_ERR_WORKSPACE, "expert activation workspace of %zu bytes, needs %zu", a.act_bytes,
+                     moe_act_bytes(P, Kp, w->E));
+  const bool wide = a.wide_pass > 0;
+  if (wide && (!a.pass_off || !a.ids || a.wide_pass != moe_wide_pass(P, w->E, a.lo)))
+    return set_error(MX_ERR_ARG, "wide expert passes need the routing's pass offsets");
+  uint8_t* xh = static_cast<uint8_t*>(a.act);
+  uint8_t* xl = xh + act_region(P, Kp);
+  uint8_t* cs = xl + act_region(P, Kp);
+  uint8_t* sfb = cs + act_codes(P, Kp);
+  const long long nblk = P * (Kp / 32);
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(nblk, 256)), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, act_pieces_kernel, static_cast<const __nv_bfloat16*>(a.x),
+                                     static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
+                                     static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs,
+                                     static_cast<const int32_t*>(a.ids), static_cast<const int32_t*>(a.offsets),
+                                     static_cast<const int32_t*>(a.pass_off), a.wide_pass, wide ? sfb : nullptr);
+  if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
+
+  MoeParams p = {};
+  p.sfw = w->sf;
+  p.sfb = sfb;
+  p.offsets = a.offsets;
+  p.pairs = a.pairs;
+  p.active = a.active;
+  p.n_active = a.n_active;
+  p.pass_off = a.pass_off;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.out_f32 = static_cast<float*>(a.out_f32);
+  p.N = w->N;
+  p.KT = KT;
+  p.NT = (w->N + 127) / 128;
+  p.lo = a.lo;
+  p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
+  p.out_mode = a.out_mode;
+  return wide ? launch_moe_gemm<true>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<false>(a, p, xh, xl, cs, cfg);
 }
 
 }  // namespace mx

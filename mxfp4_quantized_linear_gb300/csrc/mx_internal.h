@@ -122,7 +122,8 @@ unsigned int take_error_flags_gemm();
 // ---- routing + MoE (moe.cu)
 cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* counts,
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
-                         int* dev_status, cudaStream_t stream, void* zero_out = nullptr, int zero_N = 0);
+                         int* dev_status, cudaStream_t stream, void* zero_out = nullptr, int zero_N = 0,
+                         int32_t* pass_off = nullptr, int pw = 0);
 struct MoeLaunch {
   const void* x;               // bf16 [T, K] (x_per_pair = 0) or [T * topk, K] (x_per_pair = 1)
   int T, topk;
@@ -133,10 +134,14 @@ struct MoeLaunch {
   int out_mode;                // 0: out bf16 [pairs, N]; 1: out bf16 [pairs, N/2] = silu(gate) * up; 2: out_f32
   void* out;
   void* out_f32;               // f32 [pairs, N]
-  void* act;                   // activation pieces, moe_act_bytes(T * topk, Kp) bytes, 256-byte aligned
+  void* act;                   // activation pieces, moe_act_bytes(T * topk, Kp, E) bytes, 256-byte aligned
   size_t act_bytes;
+  int wide_pass;               // pairs a wide pass (moe_wide_pass), 0: narrow passes
+  const int32_t* ids;          // topk ids [T * topk] (wide passes)
+  const int32_t* pass_off;     // the routing's pass offsets [E + 1] for wide_pass (wide passes)
 };
-size_t moe_act_bytes(long long P, int Kp);
+size_t moe_act_bytes(long long P, int Kp, int E);
+int moe_wide_pass(long long P, int E, int lo);
 int launch_moe(const MoeLaunch& a, cudaStream_t stream);
 unsigned int take_error_flags_moe();
 unsigned int take_error_flags_selftest();

@@ -337,3 +337,32 @@ def test_w4a8_full_size_sampled():
         ref = Wd @ A[t]
         err = normalized_error(y[t, j, ns][None], ref[None], A[t][None], Wd)
         assert err <= TOL, (t, j, err)
+
+
+# ---------------------------------------------------------------- wide passes (prefill sizes)
+
+def test_w4a8_wide_passes():
+    """Enough pairs an expert for the wide passes (128 pairs each): ragged
+    counts, a ragged last pass, ragged rows and K."""
+    m = inputs.moe_gate_up(E=4, N=200, K=416, T=300, topk=2, seed=31)
+    assert check_w4a8(m) == 0
+
+
+def test_a16w4_wide_passes_and_invalid_ids():
+    """A16W4 with 64-pair wide passes (hi and lo stacked), with invalid ids."""
+    m = inputs.moe_gate_up(E=3, N=136, K=288, T=150, topk=2, seed=32)
+    ids = m["ids"].clone()
+    ids[5, 1] = -1
+    assert check_moe(m, ids) == 0
+
+
+def test_expert_wide_passes():
+    """The full expert at prefill-like pair counts (wide passes in both
+    projections, I = 96 not a multiple of 128)."""
+    m = inputs.moe_expert(E=4, I=96, H=256, T=160, topk=2, seed=33)
+    ids = m["ids"].clone()
+    ids[7, 0] = -1
+    y = gpu_expert(m, ids)
+    ref = oracle_expert(m, ids)
+    err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
+    assert err <= TOL, err
