@@ -677,7 +677,7 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = stream;
   cfg.attrs = &pdl;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.no_pdl ? 0 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, act_pieces_kernel, static_cast<const __nv_bfloat16*>(a.x),
                                      static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
                                      static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs,

@@ -139,6 +139,7 @@ struct MoeLaunch {
   int wide_pass;               // pairs a wide pass (moe_wide_pass), 0: narrow passes
   const int32_t* ids;          // topk ids [T * topk] (wide passes)
   const int32_t* pass_off;     // the routing's pass offsets [E + 1] for wide_pass (wide passes)
+  int no_pdl;                  // 1: launch without programmatic dependent launch
 };
 size_t moe_act_bytes(long long P, int Kp, int E);
 int moe_wide_pass(long long P, int E, int lo);
