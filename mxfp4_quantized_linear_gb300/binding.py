@@ -110,6 +110,21 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+def _stream_int() -> int:
+    """The current stream as a plain int (the decode hot path)."""
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+_BF16 = torch.bfloat16
+
+
+def _ok(t, dtype) -> bool:
+    """The common case of _need, without building an error message."""
+    return type(t) is torch.Tensor and t.dtype is dtype and t.is_cuda and t.is_contiguous()
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -129,6 +144,7 @@ class PackedWeight:
     def __init__(self, buf: torch.Tensor, desc: MxPackedWeightC):
         self.buf = buf
         self.desc = desc
+        self.ref = ctypes.byref(desc)  # passed to every call
 
     fmt = property(lambda self: self.desc.fmt)
     scale_mode = property(lambda self: self.desc.scale_mode)
@@ -243,20 +259,25 @@ def mxfp8_linear_workspace_size(M: int, w: PackedWeight) -> int:
 def mxfp8_linear(x: torch.Tensor, w: PackedWeight, bias: torch.Tensor = None, out: torch.Tensor = None,
                  flags: int = 0, workspace: torch.Tensor = None) -> torch.Tensor:
     """bf16 x [M, K] @ w^T (+ bias) -> bf16 [M, N]."""
-    _need(x, torch.bfloat16, "x")
+    if not _ok(x, _BF16):
+        _need(x, _BF16, "x")
     M = x.shape[0]
     if out is None:
-        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
-    _need(out, torch.bfloat16, "out")
-    if bias is not None:
-        _need(bias, torch.bfloat16, "bias")
+        out = torch.empty((M, w.desc.N), dtype=_BF16, device=x.device)
+    elif not _ok(out, _BF16):
+        _need(out, _BF16, "out")
+    if bias is not None and not _ok(bias, _BF16):
+        _need(bias, _BF16, "bias")
     if workspace is None:  # the library reports a too-small workspace itself
         need = mxfp8_linear_workspace_size(M, w)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-    ws_bytes = workspace.numel() if workspace is not None else 0
-    _check(load_library().mxfp8_linear(_ptr(x), M, ctypes.byref(w.desc), _ptr(bias), _ptr(out), flags,
-                                       _ptr(workspace), ws_bytes, _stream()))
+    lib = _lib if _lib is not None else load_library()
+    rc = lib.mxfp8_linear(x.data_ptr(), M, w.ref, None if bias is None else bias.data_ptr(), out.data_ptr(),
+                          flags, None if workspace is None else workspace.data_ptr(),
+                          0 if workspace is None else workspace.numel(), _stream_int())
+    if rc != MX_OK:
+        _check(rc)
     return out
 
 

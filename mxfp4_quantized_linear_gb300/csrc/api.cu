@@ -6,6 +6,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "mx_common.cuh"
@@ -168,6 +169,29 @@ int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   if (!g_encode) return set_error(MX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  // A map depends only on these parameters, never on the memory's contents:
+  // the last 64 distinct ones are kept (a decode loop re-encodes the same
+  // weight maps every call).
+  struct Key {
+    const void* base;
+    uint64_t dim0, dim1, stride1;
+    uint32_t box0, box1;
+    int dtype, swizzle;
+  };
+  static Key keys[64];
+  static CUtensorMap maps[64];
+  static bool used[64];
+  static std::mutex mu;
+  const Key k = {base, dim0, dim1, stride1_bytes, box0, box1, static_cast<int>(dtype), static_cast<int>(swizzle)};
+  const size_t slot = ((reinterpret_cast<uintptr_t>(base) >> 8) ^ (dim0 * 31u) ^ (dim1 * 131u) ^ box1 ^
+                       (static_cast<uint64_t>(dtype) << 5)) & 63u;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (used[slot] && std::memcmp(&keys[slot], &k, sizeof(Key)) == 0) {
+      *map = maps[slot];
+      return MX_OK;
+    }
+  }
   const cuuint64_t dims[2] = {dim0, dim1};
   const cuuint64_t strides[1] = {stride1_bytes};
   const cuuint32_t box[2] = {box0, box1};
@@ -176,6 +200,10 @@ int encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(MX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  std::lock_guard<std::mutex> lock(mu);
+  keys[slot] = k;
+  maps[slot] = *map;
+  used[slot] = true;
   return MX_OK;
 }
 
