@@ -477,7 +477,7 @@ def bench_e2e(mx, packed, dev, stream, args):
     pinned host, one stream synchronize a step.  ``value``: plain eager calls; ``graph``: the same
     step (copies included) captured once in a CUDA graph and replayed each step, the
     way a decode loop drives it, with each call's output copied back on a side
-    stream while the later calls run (largest output first).""" 
+    stream while the later calls run (largest output first)."""
     # one pinned buffer holds the 4 inputs (and one the 4 outputs): a step moves
     # them with one host->device and one device->host copy
     rows = sum(MS)
