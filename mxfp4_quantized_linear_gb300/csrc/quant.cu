@@ -14,10 +14,12 @@ namespace mx {
 
 namespace {
 
-// One thread = 8 consecutive elements of a row; 4 lanes = one MX block.
-// Grid-stride over 8-element groups of the [M, Kout] output (Kout >= K,
-// multiple of 32).  All lanes of a warp run the same trip count, so the
-// 4-lane shuffles inside mx_quant_bf16x8 always see a full warp.
+// One thread = one whole 32-element MX block (64 bytes of bf16 in, 32 e4m3
+// bytes and one code out), two blocks in flight a thread; consecutive threads
+// take consecutive blocks of a row, so a warp reads 2 KB and writes 1 KB
+// contiguously.  Grid-stride over the blocks of the [M_out, Kout] output
+// (Kout >= K, multiple of 32); 32-bit index arithmetic (M_out * Kout / 32 <
+// 2^31 is checked by the launcher).
 __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
                                                         int M, int K, int Kout,
                                                         uint8_t* __restrict__ q, int ldq,
@@ -32,33 +34,45 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
     pdl_wait_prior_grid();
   }
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
-  const int groups_per_row = Kout >> 3;
-  const long long total = static_cast<long long>(M_out) * groups_per_row;
-  const int lane = threadIdx.x & 31;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-       base < total; base += stride) {
-    const long long g = base + lane;
-    const bool inside = g < total;
-    const int row = inside ? static_cast<int>(g / groups_per_row) : 0;
-    const int k = inside ? static_cast<int>(g % groups_per_row) * 8 : 0;
-    const bool valid = inside && row < M && k < K;
-    const uint4 u = valid ? *reinterpret_cast<const uint4*>(x + static_cast<long long>(row) * K + k)
-                          : make_uint4(0u, 0u, 0u, 0u);
-    const QuantBlock8 b = mx_quant_bf16x8(u);
-    if (!inside) continue;
-    uint2 out = valid ? make_uint2(b.lo, b.hi) : make_uint2(0u, 0u);
-    *reinterpret_cast<uint2*>(q + static_cast<long long>(row) * ldq + k) = out;
-    if ((k & 31) == 0) {
+  const unsigned KBo = static_cast<unsigned>(Kout) >> 5, KB = static_cast<unsigned>(K) >> 5;
+  const unsigned total = static_cast<unsigned>(M_out) * KBo;
+  const unsigned stride = gridDim.x * blockDim.x;
+  for (unsigned b0 = blockIdx.x * blockDim.x + threadIdx.x; b0 < total; b0 += 2 * stride) {
+    uint4 u[2][4];
+    unsigned row[2], kb[2];
+    bool valid[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const unsigned b = b0 + j * stride;
+      row[j] = b / KBo;
+      kb[j] = b - row[j] * KBo;
+      valid[j] = b < total && row[j] < static_cast<unsigned>(M) && kb[j] < KB;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) u[j][c] = make_uint4(0u, 0u, 0u, 0u);
+      if (valid[j]) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(row[j]) * K + kb[j] * 32);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u[j][c] = src[c];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const unsigned b = b0 + j * stride;
+      if (b >= total) break;
+      uint4 o[2];
+      uint32_t code = mx_quant_bf16x32(u[j], o);  // zeros -> zero bytes, code 0
       // blocks past K get pad_code; rows past M are quantized zeros (code 0)
-      const uint8_t c = valid ? static_cast<uint8_t>(b.code) : (k < K ? 0 : pad_code);
-      if (codes) codes[static_cast<long long>(row) * ldc + (k >> 5)] = c;
+      if (!valid[j] && kb[j] >= KB) code = pad_code;
+      uint4* dst = reinterpret_cast<uint4*>(q + static_cast<long long>(row[j]) * ldq + kb[j] * 32);
+      dst[0] = o[0];
+      dst[1] = o[1];
+      const uint8_t c8 = static_cast<uint8_t>(code);
+      if (codes) codes[static_cast<long long>(row[j]) * ldc + kb[j]] = c8;
       if (sf) {
-        // 512-byte atom (row tile, 128-K tile): row m, block kb at (m%32)*16 + (m/32)*4 + kb
-        const int j = k >> 5;
-        const int m = row & 127;
-        const long long atom = static_cast<long long>(row >> 7) * (Kout >> 7) + (j >> 2);
-        sf[atom * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = c;
+        // 512-byte atom (row tile, 128-K tile): row m, block kb at (m%32)*16 + (m/32)*4 + kb%4
+        const unsigned m = row[j] & 127u;
+        const long long atom = static_cast<long long>(row[j] >> 7) * (KBo >> 2) + (kb[j] >> 2);
+        sf[atom * 512 + (m & 31u) * 16 + (m >> 5) * 4 + (kb[j] & 3u)] = c8;
       }
     }
   }
@@ -175,9 +189,10 @@ cudaError_t launch_quant_act(const void* x, int M, int K, int Kout, uint8_t* q, 
                              bool pdl_trigger, cudaStream_t stream, int M_out, int* zero,
                              int nzero) {
   if (M_out < M) M_out = M;
-  const long long groups = static_cast<long long>(M_out) * (Kout / 8);
+  const long long blocks = static_cast<long long>(M_out) * (Kout / 32);
+  if (blocks >= (1LL << 31)) return cudaErrorInvalidValue;  // the kernel indexes blocks in 32 bits
   const int block = 256;
-  const int grid = grid_for(groups, block);
+  const int grid = grid_for((blocks + 1) / 2, block);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(block, 1, 1);
