@@ -85,7 +85,7 @@ LinearWs linear_ws(int M, int Kp) {
 }
 
 struct MoeWs {
-  size_t counts, offsets, pairs, active, n_active, status, pass_off, act, act_bytes, total;
+  size_t counts, offsets, pairs, active, n_active, status, pass_off, route_tmp, act, act_bytes, total;
 };
 
 // Routing outputs, then the activation pieces of the T * topk pairs for K
@@ -101,6 +101,7 @@ MoeWs moe_ws(int T, int topk, int E, int Kp) {
   r.n_active = o; o += 16;
   r.status = o;   o += 16;
   r.pass_off = o; o += align_up(4 * (static_cast<size_t>(E) + 1), 16);
+  r.route_tmp = o; o += align_up(route_scratch_bytes(static_cast<long long>(P), E), 16);
   r.act = align_up(o, 256);
   r.act_bytes = Kp > 0 ? moe_act_bytes(static_cast<long long>(P), Kp, E) : 0;
   r.total = r.act + r.act_bytes;
@@ -561,8 +562,8 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   // passes), and zero rows for the pairs whose id is not a valid expert
   const int pw = moe_wide_pass(static_cast<long long>(T) * topk, w->E, lo);
   int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.pass_off);
-  cudaError_t e = launch_route(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream, out,
-                               w->N, pw ? pass_off : nullptr, pw);
+  cudaError_t e = launch_route_many(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream,
+                                    out, w->N, pw ? pass_off : nullptr, pw, ws + R.route_tmp);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
   a.x = x;
@@ -654,8 +655,8 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.route.status);
   const int pw = moe_wide_pass(static_cast<long long>(T) * topk, E, 1);
   int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.route.pass_off);
-  cudaError_t e = launch_route(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream, nullptr,
-                               0, pw ? pass_off : nullptr, pw);
+  cudaError_t e = launch_route_many(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream,
+                                    nullptr, 0, pw ? pass_off : nullptr, pw, ws + R.route.route_tmp);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
   a.wide_pass = pw;

@@ -120,6 +120,142 @@ __global__ void __launch_bounds__(kRouteThreads)
   }
 }
 
+// ---- the same routing for many pairs, on many CTAs (three launches): each
+// CTA counts a chunk of kRouteChunk pairs, one CTA scans the per-chunk counts
+// (giving each chunk its base in every expert's list), each CTA scatters its
+// chunk stably.  The result is identical to route_kernel's.
+constexpr int kRouteChunk = 4096;
+
+__global__ void __launch_bounds__(kRouteThreads)
+    route_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ ccount,
+                       int* __restrict__ bad_flag, __nv_bfloat16* __restrict__ zero_out, int zero_N) {
+  extern __shared__ int rs[];  // cnt[E]
+  pdl_launch_dependents();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) rs[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kRouteChunk;
+  const int p1 = p0 + kRouteChunk < P ? p0 + kRouteChunk : P;
+  int bad = 0;
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) {
+      atomicAdd(&rs[e], 1);
+    } else {
+      if (e != -1) bad = 1;
+      if (zero_out) {
+        __nv_bfloat16* row = zero_out + static_cast<long long>(p) * zero_N;
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
+        for (int n = 0; n < zero_N; ++n) row[n] = z;
+      }
+    }
+  }
+  bad = __syncthreads_or(bad);
+  if (bad && threadIdx.x == 0) atomicOr(bad_flag, 1);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) ccount[static_cast<long long>(blockIdx.x) * E + e] = rs[e];
+}
+
+// One CTA: per-expert totals, offsets, active list, pass offsets, status, and
+// cbase[c][e] = offsets[e] + the pairs of expert e in chunks before c.
+__global__ void __launch_bounds__(kRouteThreads)
+    route_scan_kernel(const int32_t* __restrict__ ccount, int C, int E, int32_t* __restrict__ cbase,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
+                      int32_t* __restrict__ n_active, int* dev_status, const int* __restrict__ bad_flag,
+                      int32_t* __restrict__ pass_off, int pw) {
+  extern __shared__ int rs[];  // total[E]
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int t = 0;
+    for (int c = 0; c < C; ++c) t += ccount[static_cast<long long>(c) * E + e];
+    rs[e] = t;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned full = 0xffffffffu;
+  if (warp == 0) {
+    int run = 0, arun = 0, prun = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? rs[e] : 0;
+      const int pc = pass_off && pw > 0 ? (c + pw - 1) / pw : 0;
+      int incl = c, pincl = pc;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(full, incl, o);
+        const int pv = __shfl_up_sync(full, pincl, o);
+        if (lane >= o) {
+          incl += v;
+          pincl += pv;
+        }
+      }
+      const unsigned am = __ballot_sync(full, c > 0);
+      if (e < E) {
+        counts[e] = c;
+        offsets[e] = run + incl - c;
+        if (pass_off) pass_off[e] = prun + pincl - pc;
+        if (c > 0) active[arun + __popc(am & ((1u << lane) - 1u))] = e;
+      }
+      run += __shfl_sync(full, incl, 31);
+      prun += __shfl_sync(full, pincl, 31);
+      arun += __popc(am);
+    }
+    if (lane == 0) {
+      offsets[E] = run;
+      if (pass_off) pass_off[E] = prun;
+      *n_active = arun;
+      if (dev_status) *dev_status = *bad_flag ? MX_ERR_EXPERT_ID : MX_OK;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int b = offsets[e];
+    for (int c = 0; c < C; ++c) {
+      cbase[static_cast<long long>(c) * E + e] = b;
+      b += ccount[static_cast<long long>(c) * E + e];
+    }
+  }
+}
+
+// Stable scatter of one chunk, blockDim pairs at a time (as in route_kernel).
+__global__ void __launch_bounds__(kRouteThreads)
+    route_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* __restrict__ cbase,
+                         int32_t* __restrict__ pairs) {
+  extern __shared__ int rs[];
+  int* base = rs;          // [E]
+  int* wcnt = rs + E;      // [warps][E]
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned full = 0xffffffffu;
+  for (int e = tid; e < E; e += blockDim.x) base[e] = cbase[static_cast<long long>(blockIdx.x) * E + e];
+  __syncthreads();
+  const int p0 = blockIdx.x * kRouteChunk;
+  const int p1 = p0 + kRouteChunk < P ? p0 + kRouteChunk : P;
+  for (int c0 = p0; c0 < p1; c0 += blockDim.x) {
+    const int p = c0 + tid;
+    const int e = p < p1 ? ids[p] : -1;
+    const bool valid = e >= 0 && e < E;
+    for (int i = lane; i < E; i += 32) wcnt[warp * E + i] = 0;
+    __syncwarp();
+    const unsigned key = valid ? static_cast<unsigned>(e) : static_cast<unsigned>(E + lane);
+    const unsigned mask = __match_any_sync(full, key);
+    const int rank = __popc(mask & ((1u << lane) - 1u));
+    if (valid && rank == 0) wcnt[warp * E + e] = __popc(mask);
+    __syncthreads();
+    if (valid) {
+      int pos = base[e] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
+      pairs[pos] = p;
+    }
+    __syncthreads();
+    for (int i = tid; i < E; i += blockDim.x) {
+      int t = 0;
+      for (int w = 0; w < kRouteWarps; ++w) t += wcnt[w * E + i];
+      base[i] += t;
+    }
+    __syncthreads();
+  }
+}
+
 // out[t, h] = bf16(sum_j w[t, j] y2[t * topk + j, h]) over the slots j with a
 // valid expert id, in increasing j, in f32: one thread per 4 consecutive h.
 __global__ void combine_kernel(const float* __restrict__ y2, const int32_t* __restrict__ ids,
@@ -197,11 +333,12 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
   pdl_wait_prior_grid();  // the routing (and the activation, when a kernel wrote it) is complete
   const int KBp = Kp >> 5, KB = K >> 5, KT = Kp >> 7;
   const int nv = *n_pairs;
-  const long long total = static_cast<long long>(nv < P ? nv : P) * KBp;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long j = i / KBp;
-    const int b = static_cast<int>(i % KBp);
+  // 32-bit indices: the launcher checks P * Kp / 32 < 2^31
+  const unsigned total = static_cast<unsigned>(nv < P ? nv : P) * static_cast<unsigned>(KBp);
+  for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const unsigned ju = i / static_cast<unsigned>(KBp);
+    const long long j = ju;
+    const int b = static_cast<int>(i - ju * static_cast<unsigned>(KBp));
     const int pr = pairs[j];
     const long long src = x_per_pair ? pr : pr / topk;
     uint4 qh[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
@@ -579,6 +716,51 @@ cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* co
   return cudaGetLastError();
 }
 
+size_t route_scratch_bytes(long long P, int E) {
+  const long long C = (P + kRouteChunk - 1) / kRouteChunk;
+  return static_cast<size_t>(2 * C * E + 4) * sizeof(int32_t);
+}
+
+cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_t* counts, int32_t* offsets,
+                              int32_t* pairs, int32_t* active, int32_t* n_active, int* dev_status,
+                              cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off, int pw,
+                              void* scratch) {
+  const int P = T * topk;
+  if (P <= kRouteChunk)
+    return launch_route(ids, T, topk, E, counts, offsets, pairs, active, n_active, dev_status, stream, zero_out,
+                        zero_N, pass_off, pw);
+  const int C = (P + kRouteChunk - 1) / kRouteChunk;
+  int32_t* ccount = static_cast<int32_t*>(scratch);
+  int32_t* cbase = ccount + static_cast<long long>(C) * E;
+  int* bad = reinterpret_cast<int*>(cbase + static_cast<long long>(C) * E);
+  cudaError_t e = cudaMemsetAsync(bad, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  const int smem1 = E * static_cast<int>(sizeof(int));
+  const int smem3 = (E + kRouteWarps * E) * static_cast<int>(sizeof(int));
+  if ((e = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem3)) !=
+      cudaSuccess)
+    return e;
+  route_count_kernel<<<C, kRouteThreads, smem1, stream>>>(ids, P, E, ccount, bad,
+                                                          static_cast<__nv_bfloat16*>(zero_out), zero_N);
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(kRouteThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem1;
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, route_scan_kernel, static_cast<const int32_t*>(ccount), C, E, cbase, counts,
+                              offsets, active, n_active, dev_status, static_cast<const int*>(bad), pass_off, pw)) !=
+      cudaSuccess)
+    return e;
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.dynamicSmemBytes = smem3;
+  return cudaLaunchKernelEx(&cfg, route_scatter_kernel, ids, P, E, static_cast<const int32_t*>(cbase), pairs);
+}
+
 cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts, int T, int topk, int E, int H,
                            void* out, cudaStream_t stream) {
   const long long total = static_cast<long long>(T) * (H / 4);
@@ -669,6 +851,7 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   uint8_t* cs = xl + act_region(P, Kp);
   uint8_t* sfb = cs + act_codes(P, Kp);
   const long long nblk = P * (Kp / 32);
+  if (nblk >= (1LL << 31)) return set_error(MX_ERR_UNSUPPORTED, "T * topk * K / 32 = %lld exceeds 2^31", nblk);
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;

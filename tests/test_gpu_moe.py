@@ -366,3 +366,16 @@ def test_expert_wide_passes():
     ref = oracle_expert(m, ids)
     err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
     assert err <= TOL, err
+
+
+def test_many_pairs_routing_path():
+    """More pairs than one routing chunk (4096): the many-CTA routing (count,
+    scan, stable scatter) with invalid ids, under both activation forms."""
+    m = inputs.moe_gate_up(E=5, N=64, K=128, T=2300, topk=2, seed=41)
+    ids = m["ids"].clone()
+    ids[17, 0] = -1
+    ids[2222, 1] = -1
+    assert check_moe(m, ids) == 0
+    assert check_w4a8(m, ids) == 0
+    ids[1000, 1] = 9
+    assert check_w4a8(m, ids) == MX_ERR_EXPERT_ID
