@@ -85,7 +85,7 @@ LinearWs linear_ws(int M, int Kp) {
 }
 
 struct MoeWs {
-  size_t counts, offsets, pairs, active, n_active, status, pass_off, route_tmp, act, act_bytes, total;
+  size_t counts, offsets, pairs, inv, active, n_active, status, pass_off, route_tmp, act, act_bytes, total;
 };
 
 // Routing outputs, then the activation pieces of the T * topk pairs for K
@@ -97,6 +97,7 @@ MoeWs moe_ws(int T, int topk, int E, int Kp) {
   r.counts = o;   o += align_up(4 * static_cast<size_t>(E), 16);
   r.offsets = o;  o += align_up(4 * (static_cast<size_t>(E) + 1), 16);
   r.pairs = o;    o += align_up(4 * (P ? P : 1), 16);
+  r.inv = o;      o += align_up(4 * (P ? P : 1), 16);
   r.active = o;   o += align_up(4 * static_cast<size_t>(E), 16);
   r.n_active = o; o += 16;
   r.status = o;   o += 16;
@@ -562,8 +563,9 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   // passes), and zero rows for the pairs whose id is not a valid expert
   const int pw = moe_wide_pass(static_cast<long long>(T) * topk, w->E, lo);
   int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.pass_off);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + R.inv);
   cudaError_t e = launch_route_many(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream,
-                                    out, w->N, pw ? pass_off : nullptr, pw, ws + R.route_tmp);
+                                    out, w->N, pw ? pass_off : nullptr, pw, ws + R.route_tmp, inv);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
   a.x = x;
@@ -582,6 +584,7 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   a.wide_pass = pw;
   a.ids = topk_ids;
   a.pass_off = pass_off;
+  a.inv = route_many_writes_inv(static_cast<long long>(T) * topk) ? inv : nullptr;
   return launch_moe(a, stream);
 }
 
@@ -655,13 +658,15 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.route.status);
   const int pw = moe_wide_pass(static_cast<long long>(T) * topk, E, 1);
   int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.route.pass_off);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + R.route.inv);
   cudaError_t e = launch_route_many(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream,
-                                    nullptr, 0, pw ? pass_off : nullptr, pw, ws + R.route.route_tmp);
+                                    nullptr, 0, pw ? pass_off : nullptr, pw, ws + R.route.route_tmp, inv);
   if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
   a.wide_pass = pw;
   a.ids = topk_ids;
   a.pass_off = pass_off;
+  a.inv = route_many_writes_inv(static_cast<long long>(T) * topk) ? inv : nullptr;
   a.T = T;
   a.topk = topk;
   a.lo = 1;

@@ -128,7 +128,8 @@ constexpr int kRouteChunk = 4096;
 
 __global__ void __launch_bounds__(kRouteThreads)
     route_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ ccount,
-                       int* __restrict__ bad_flag, __nv_bfloat16* __restrict__ zero_out, int zero_N) {
+                       int* __restrict__ bad_flag, __nv_bfloat16* __restrict__ zero_out, int zero_N,
+                       int32_t* __restrict__ inv) {
   extern __shared__ int rs[];  // cnt[E]
   pdl_launch_dependents();
   for (int e = threadIdx.x; e < E; e += blockDim.x) rs[e] = 0;
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(kRouteThreads)
       atomicAdd(&rs[e], 1);
     } else {
       if (e != -1) bad = 1;
+      if (inv) inv[p] = -1;
       if (zero_out) {
         __nv_bfloat16* row = zero_out + static_cast<long long>(p) * zero_N;
         const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(kRouteThreads)
 // Stable scatter of one chunk, blockDim pairs at a time (as in route_kernel).
 __global__ void __launch_bounds__(kRouteThreads)
     route_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* __restrict__ cbase,
-                         int32_t* __restrict__ pairs) {
+                         int32_t* __restrict__ pairs, int32_t* __restrict__ inv) {
   extern __shared__ int rs[];
   int* base = rs;          // [E]
   int* wcnt = rs + E;      // [warps][E]
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kRouteThreads)
       int pos = base[e] + rank;
       for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
       pairs[pos] = p;
+      if (inv) inv[p] = pos;
     }
     __syncthreads();
     for (int i = tid; i < E; i += blockDim.x) {
@@ -328,19 +331,27 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
                                   int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl,
                                   uint8_t* __restrict__ cs, const int32_t* __restrict__ ids,
                                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ pass_off, int pw,
-                                  uint8_t* __restrict__ sfb) {
+                                  uint8_t* __restrict__ sfb, const int32_t* __restrict__ inv, int R) {
   pdl_launch_dependents();
   pdl_wait_prior_grid();  // the routing (and the activation, when a kernel wrote it) is complete
   const int KBp = Kp >> 5, KB = K >> 5, KT = Kp >> 7;
-  const int nv = *n_pairs;
+  // inv == nullptr: one thread a (sorted position, block), the position's
+  // pair read from the list; else one thread a (activation row, block), the
+  // row split once and written to every sorted position inv[] gives it
+  const int fan = inv ? (x_per_pair ? 1 : topk) : 1;
+  const int nv = inv ? R : *n_pairs;
   // 32-bit indices: the launcher checks P * Kp / 32 < 2^31
-  const unsigned total = static_cast<unsigned>(nv < P ? nv : P) * static_cast<unsigned>(KBp);
+  const unsigned total = static_cast<unsigned>(inv ? R : (nv < P ? nv : P)) * static_cast<unsigned>(KBp);
   for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const unsigned ju = i / static_cast<unsigned>(KBp);
-    const long long j = ju;
-    const int b = static_cast<int>(i - ju * static_cast<unsigned>(KBp));
-    const int pr = pairs[j];
-    const long long src = x_per_pair ? pr : pr / topk;
+    const unsigned ru = i / static_cast<unsigned>(KBp);
+    const int b = static_cast<int>(i - ru * static_cast<unsigned>(KBp));
+    long long src;
+    if (inv) {
+      src = ru;  // the activation row itself
+    } else {
+      const int pr = pairs[ru];
+      src = x_per_pair ? pr : pr / topk;
+    }
     uint4 qh[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
     uint4 ql[2] = {qh[0], qh[1]};
     uint32_t ch = 127u, cl = 127u;  // padded K blocks: zero bytes, a finite code
@@ -364,25 +375,37 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
         cl = mx_quant_f32x32(r, ql);
       }
     }
-    uint4* hp = reinterpret_cast<uint4*>(xh + j * Kp + 32 * b);
-    hp[0] = qh[0];
-    hp[1] = qh[1];
-    if (lo) {
-      uint4* lp = reinterpret_cast<uint4*>(xl + j * Kp + 32 * b);
-      lp[0] = ql[0];
-      lp[1] = ql[1];
-    }
-    if (sfb) {
-      const int e = ids[pr];
-      const int rank = static_cast<int>(j) - offsets[e];
-      const int r = rank % pw;
-      uint8_t* atom = sfb + (static_cast<long long>(pass_off[e] + rank / pw) * KT + (b >> 2)) * 512 + (b & 3);
-      atom[(r & 31) * 16 + (r >> 5) * 4] = static_cast<uint8_t>(ch);
-      if (lo) atom[((pw + r) & 31) * 16 + ((pw + r) >> 5) * 4] = static_cast<uint8_t>(cl);
-    } else {
-      uint8_t* cp = cs + (j * KT + (b >> 2)) * 32 + (b & 3);
-      cp[0] = static_cast<uint8_t>(ch);
-      if (lo) cp[16] = static_cast<uint8_t>(cl);
+    for (int f = 0; f < fan; ++f) {
+      long long j;
+      int pr;
+      if (inv) {
+        pr = static_cast<int>(ru) * fan + f;  // the pair
+        j = inv[pr];
+        if (j < 0) continue;                  // an invalid id: in no list
+      } else {
+        j = ru;
+        pr = pairs[ru];
+      }
+      uint4* hp = reinterpret_cast<uint4*>(xh + j * Kp + 32 * b);
+      hp[0] = qh[0];
+      hp[1] = qh[1];
+      if (lo) {
+        uint4* lp = reinterpret_cast<uint4*>(xl + j * Kp + 32 * b);
+        lp[0] = ql[0];
+        lp[1] = ql[1];
+      }
+      if (sfb) {
+        const int e = ids[pr];
+        const int rank = static_cast<int>(j) - offsets[e];
+        const int r = rank % pw;
+        uint8_t* atom = sfb + (static_cast<long long>(pass_off[e] + rank / pw) * KT + (b >> 2)) * 512 + (b & 3);
+        atom[(r & 31) * 16 + (r >> 5) * 4] = static_cast<uint8_t>(ch);
+        if (lo) atom[((pw + r) & 31) * 16 + ((pw + r) >> 5) * 4] = static_cast<uint8_t>(cl);
+      } else {
+        uint8_t* cp = cs + (j * KT + (b >> 2)) * 32 + (b & 3);
+        cp[0] = static_cast<uint8_t>(ch);
+        if (lo) cp[16] = static_cast<uint8_t>(cl);
+      }
     }
   }
 }
@@ -716,6 +739,8 @@ cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* co
   return cudaGetLastError();
 }
 
+int route_many_writes_inv(long long P) { return P > kRouteChunk ? 1 : 0; }
+
 size_t route_scratch_bytes(long long P, int E) {
   const long long C = (P + kRouteChunk - 1) / kRouteChunk;
   return static_cast<size_t>(2 * C * E + 4) * sizeof(int32_t);
@@ -724,7 +749,7 @@ size_t route_scratch_bytes(long long P, int E) {
 cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* pairs, int32_t* active, int32_t* n_active, int* dev_status,
                               cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off, int pw,
-                              void* scratch) {
+                              void* scratch, int32_t* inv) {
   const int P = T * topk;
   if (P <= kRouteChunk)
     return launch_route(ids, T, topk, E, counts, offsets, pairs, active, n_active, dev_status, stream, zero_out,
@@ -741,7 +766,7 @@ cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_
       cudaSuccess)
     return e;
   route_count_kernel<<<C, kRouteThreads, smem1, stream>>>(ids, P, E, ccount, bad,
-                                                          static_cast<__nv_bfloat16*>(zero_out), zero_N);
+                                                          static_cast<__nv_bfloat16*>(zero_out), zero_N, inv);
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -758,7 +783,7 @@ cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_
     return e;
   cfg.gridDim = dim3(C, 1, 1);
   cfg.dynamicSmemBytes = smem3;
-  return cudaLaunchKernelEx(&cfg, route_scatter_kernel, ids, P, E, static_cast<const int32_t*>(cbase), pairs);
+  return cudaLaunchKernelEx(&cfg, route_scatter_kernel, ids, P, E, static_cast<const int32_t*>(cbase), pairs, inv);
 }
 
 cudaError_t launch_combine(const float* y2, const int32_t* ids, const float* wts, int T, int topk, int E, int H,
@@ -850,8 +875,12 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   uint8_t* xl = xh + act_region(P, Kp);
   uint8_t* cs = xl + act_region(P, Kp);
   uint8_t* sfb = cs + act_codes(P, Kp);
-  const long long nblk = P * (Kp / 32);
-  if (nblk >= (1LL << 31)) return set_error(MX_ERR_UNSUPPORTED, "T * topk * K / 32 = %lld exceeds 2^31", nblk);
+  if (P * (Kp / 32) >= (1LL << 31))
+    return set_error(MX_ERR_UNSUPPORTED, "T * topk * K / 32 = %lld exceeds 2^31", P * (Kp / 32));
+  // with the inverse map, one thread a block of each activation row (tokens,
+  // or pairs for a down projection); else one a block of each sorted pair
+  const long long R = a.inv ? (a.x_per_pair ? P : a.T) : P;
+  const long long nblk = R * (Kp / 32);
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -865,7 +894,8 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
                                      static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
                                      static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs,
                                      static_cast<const int32_t*>(a.ids), static_cast<const int32_t*>(a.offsets),
-                                     static_cast<const int32_t*>(a.pass_off), a.wide_pass, wide ? sfb : nullptr);
+                                     static_cast<const int32_t*>(a.pass_off), a.wide_pass, wide ? sfb : nullptr,
+                                     static_cast<const int32_t*>(a.inv), static_cast<int>(R));
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
 
   MoeParams p = {};

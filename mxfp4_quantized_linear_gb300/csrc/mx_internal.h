@@ -140,15 +140,18 @@ struct MoeLaunch {
   const int32_t* ids;          // topk ids [T * topk] (wide passes)
   const int32_t* pass_off;     // the routing's pass offsets [E + 1] for wide_pass (wide passes)
   int no_pdl;                  // 1: launch without programmatic dependent launch
+  const int32_t* inv;          // [T * topk] sorted position of each pair (-1: invalid id), or null
 };
 size_t moe_act_bytes(long long P, int Kp, int E);
-// Routing for any number of pairs: route_kernel up to one chunk of pairs, the
-// three-kernel many-CTA routing above (scratch of route_scratch_bytes).
+// Routing for any number of pairs: route_kernel up to one chunk of pairs (inv
+// untouched, returns 0), the three-kernel many-CTA routing above (scratch of
+// route_scratch_bytes; fills inv, the sorted position of each pair, when given).
+int route_many_writes_inv(long long P);
 size_t route_scratch_bytes(long long P, int E);
 cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_t* counts, int32_t* offsets,
                               int32_t* pairs, int32_t* active, int32_t* n_active, int* dev_status,
                               cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off, int pw,
-                              void* scratch);
+                              void* scratch, int32_t* inv);
 int moe_wide_pass(long long P, int E, int lo);
 int launch_moe(const MoeLaunch& a, cudaStream_t stream);
 unsigned int take_error_flags_moe();

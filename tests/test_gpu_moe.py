@@ -379,3 +379,15 @@ def test_many_pairs_routing_path():
     assert check_w4a8(m, ids) == 0
     ids[1000, 1] = 9
     assert check_w4a8(m, ids) == MX_ERR_EXPERT_ID
+
+
+def test_expert_many_pairs():
+    """The full expert past one routing chunk (4200 pairs): many-CTA routing,
+    activation rows split once per token and per pair, wide passes."""
+    m = inputs.moe_expert(E=4, I=64, H=128, T=2100, topk=2, seed=42)
+    ids = m["ids"].clone()
+    ids[5, 1] = -1
+    y = gpu_expert(m, ids)
+    ref = oracle_expert(m, ids)
+    err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
+    assert err <= TOL, err
