@@ -440,29 +440,42 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
 // activation-pieces kernel and bulk-copied, one accumulator, two CTAs an SM.
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? c : pow2_at_least(v, 2 * c); }
 
-template <bool kWide>
+// A third form for prefill of MXFP8 activations (hi pieces only) when the
+// weight has an even number of 128-row tiles (kMoePair): each work item is two adjacent row tiles multiplied by
+// the same activation stage (8 MMAs a K step into two accumulators), so every
+// activation byte brought from L2 feeds twice the tensor work.  One CTA an SM
+// and 12 warps (8 epilogue warps, one a lane quarter of each accumulator); the
+// epilogue copies its accumulator quarter to registers and releases it before
+// the stores, so the next pass's MMAs overlap them.
+constexpr int kMoeNarrow = 0, kMoeWide = 1, kMoePair = 2;
+
+template <int kMode>
 struct MoeCfg {
-  static constexpr int kBRows = kWide ? 128 : 32;      // B rows a pass (MMA N)
-  static constexpr int kWStages = 3;
-  static constexpr int kXStages = kWide ? 3 : 5;       // the activation comes from L2
+  static constexpr bool kWide = kMode != kMoeNarrow;
+  static constexpr int kATiles = kMode == kMoePair ? 2 : 1;    // 128-row weight tiles an item
+  static constexpr int kBRows = kWide ? 128 : 32;              // B rows a pass (MMA N)
+  static constexpr int kWStages = kMode == kMoePair ? 4 : 3;
+  static constexpr int kXStages = kMode == kMoeWide ? 3 : 5;  // the activation comes from L2
   static constexpr int kAccBufs = kWide ? 1 : 2;
-  static constexpr int kCtasPerSm = kWide ? 2 : 3;
-  static constexpr int kWStage = 128 * 128;           // e2m1 operand step, 128B swizzle
-  static constexpr int kXStage = kBRows * 128;        // B rows, 128B swizzle (1 KB aligned)
+  static constexpr int kCtasPerSm = kMode == kMoeNarrow ? 3 : (kMode == kMoeWide ? 2 : 1);
+  static constexpr int kThreads = kMode == kMoePair ? 384 : 256;
+  static constexpr int kEpiWarps = 4 * kATiles;
+  static constexpr int kWStage = kATiles * 128 * 128;         // e2m1 operand steps, 128B swizzle
+  static constexpr int kXStage = kBRows * 128;                // B rows, 128B swizzle (1 KB aligned)
   static constexpr int kWOff = 0;
   static constexpr int kXOff = kWOff + kWStages * kWStage;
-  static constexpr int kSfaOff = kXOff + kXStages * kXStage;  // a weight scale atom a weight stage
-  static constexpr int kSfbOff = kSfaOff + kWStages * 512;      // an activation scale atom a stage
+  static constexpr int kSfaOff = kXOff + kXStages * kXStage;  // kATiles weight scale atoms a weight stage
+  static constexpr int kSfbOff = kSfaOff + kWStages * kATiles * 512;  // an activation scale atom a stage
   static constexpr int kBarOff = (kSfbOff + kXStages * 512 + 1023) & ~1023;
   static constexpr int kBarBytes = ((2 * (kWStages + kXStages) + 2 * kAccBufs) * 8 + 8 + 255) & ~255;
   static constexpr int kSmem = kBarOff + kBarBytes + 1024;
   static constexpr uint32_t kAccCols = kBRows;
-  // tensor memory: the accumulator(s) | a (SFA 4, SFB 4) slot a weight stage
-  static constexpr uint32_t kTmemCols = pow2_at_least(kAccBufs * kAccCols + 8 * kWStages);
+  // tensor memory: the accumulator(s) | a (SFA 4 a tile, SFB 4) slot a weight stage
+  static constexpr uint32_t kSfSlot = kATiles == 2 ? 16 : 8;
+  static constexpr uint32_t kTmemCols = pow2_at_least(kAccBufs * kATiles * kAccCols + kSfSlot * kWStages);
   static constexpr uint32_t kIdesc = mxf8_idesc_a(128, kBRows, kFmtE2M1);
 };
-constexpr int kWTx = 128 * 64;            // bytes the weight TMA writes (the packed half of each chunk)
-constexpr int kTcThreads = 256;
+constexpr int kWTx = 128 * 64;            // bytes the weight TMA writes a tile (the packed half of each chunk)
 constexpr int kWidePairsA16 = 64, kWidePairsMx8 = 128;  // pairs a wide pass
 
 struct MoeParams {
@@ -495,10 +508,11 @@ struct Item {
   int e, o0, cnt, nch, rt;
 };
 
-MX_DEV Item item_at(const MoeParams& p, int i, int tok) {
+MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles) {
   Item it;
-  const int a = i / p.NT;
-  it.rt = i - a * p.NT;
+  const int nti = p.NT / tiles;  // items an expert (tiles = 2 needs NT even)
+  const int a = i / nti;
+  it.rt = (i - a * nti) * tiles;  // the item's first 128-row tile
   it.e = p.active[a];
   it.o0 = p.offsets[it.e];
   it.cnt = p.offsets[it.e + 1] - it.o0;
@@ -521,12 +535,14 @@ MX_DEV void store_pair(const MoeParams& p, int pt, int n, int lane, float y) {
   }
 }
 
-template <bool kWide>
-__global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
+template <int kMode>
+__global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasPerSm)
     moe_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xhmap,
                const __grid_constant__ CUtensorMap xlmap, const __grid_constant__ CUtensorMap csmap,
                const MoeParams p) {
-  using C = MoeCfg<kWide>;
+  using C = MoeCfg<kMode>;
+  constexpr bool kWide = C::kWide;
+  constexpr int kT = C::kATiles;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -552,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
     }
     for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&accfull[i], 1);    // tcgen05.commit
-      mbar_init(&accempty[i], 4);   // one arrival an epilogue warp
+      mbar_init(&accempty[i], C::kEpiWarps);  // one arrival an epilogue warp
     }
     *abort_flag = 0u;
     fence_mbar_init();
@@ -567,27 +583,31 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
   // memory (a dependent grid then never takes columns this grid waits for)
   pdl_launch_dependents();
   pdl_wait_prior_grid();  // the routing and the activation pieces are complete
-  const int n_items = *p.n_active * p.NT;  // CTAs past the last item go straight to the exit
+  const int n_items = *p.n_active * (p.NT / kT);  // CTAs past the last item go straight to the exit
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
     tma_prefetch_desc(&wmap);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok);
+      const Item it = item_at(p, i, tok, kT);
       // a weight tile read once streams past L2; read again (more than one
       // pass of pairs) it is kept
       const uint64_t pol = it.nch > 1 ? policy_evict_last() : policy_evict_first();
-      const long long tile = static_cast<long long>(it.e) * p.NT + it.rt;
-      const int row0 = static_cast<int>(tile * p.KT * 128);  // the tile's first 128-value row
-      const uint8_t* sfa = p.sfw + tile * p.KT * 512;
+      const long long tile = static_cast<long long>(it.e) * p.NT + it.rt;  // the item's first tile
       for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
         for (int s = 0; s < p.KT; ++s, ++g) {
           const int st = g % C::kWStages;
           if (!mbar_wait(&wempty[st], ((g / C::kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
-          mbar_arrive_expect_tx(&wfull[st], kWTx + 512);
-          tma_load_2d(smem + C::kWOff + st * C::kWStage, &wmap, &wfull[st], 0, row0 + s * 128, pol);
-          bulk_load(smem + C::kSfaOff + st * 512, sfa + s * 512, 512, &wfull[st]);
+          mbar_arrive_expect_tx(&wfull[st], kT * (kWTx + 512));
+#pragma unroll
+          for (int t = 0; t < kT; ++t) {
+            // tile (tile + t): its K step s is 128-value row (tile + t) * KT * 128 + 128 s
+            const int row0 = static_cast<int>((tile + t) * p.KT * 128);
+            tma_load_2d(smem + C::kWOff + st * C::kWStage + t * 16384, &wmap, &wfull[st], 0, row0 + s * 128, pol);
+            bulk_load(smem + C::kSfaOff + (st * kT + t) * 512, p.sfw + ((tile + t) * p.KT + s) * 512, 512,
+                      &wfull[st]);
+          }
         }
       }
     }
@@ -600,7 +620,7 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
     const uint32_t tx = kWide ? C::kBRows * 128 + 512 : C::kBRows * (128 + 16);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok);
+      const Item it = item_at(p, i, tok, kT);
       for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
         const int row0 = it.o0 + ch * tok;
         for (int s = 0; s < p.KT; ++s, ++g) {
@@ -627,12 +647,12 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = item_at(p, i, tok);
+      const Item it = item_at(p, i, tok, kT);
       for (int ch = 0; ch < it.nch && ok; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;  // the epilogue drains the other accumulator (narrow)
         if (!mbar_wait(&accempty[buf], ((gp / C::kAccBufs) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t acc = tmem + static_cast<uint32_t>(buf) * C::kAccCols;
+        const uint32_t acc = tmem + static_cast<uint32_t>(buf * kT) * C::kAccCols;
         for (int s = 0; s < p.KT; ++s, ++gw, ++gx) {
           const int ws = gw % C::kWStages, xs = gx % C::kXStages;
           if (!mbar_wait(&wfull[ws], (gw / C::kWStages) & 1u) ||
@@ -641,15 +661,23 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
             break;
           }
           tc_fence_after();
-          const uint32_t sfc = tmem + C::kAccBufs * C::kAccCols + static_cast<uint32_t>(ws * 8);
-          tc_cp_sf(sfc, sf_desc(smem_u32(smem + C::kSfaOff + ws * 512)));
-          tc_cp_sf(sfc + 4, sf_desc(smem_u32(smem + C::kSfbOff + xs * 512)));
-          const uint64_t adesc = sw128_desc(smem_u32(smem + C::kWOff + ws * C::kWStage));
+          // scale slot: SFA of each tile (4 columns each), then SFB
+          const uint32_t sfc = tmem + C::kAccBufs * kT * C::kAccCols + static_cast<uint32_t>(ws) * C::kSfSlot;
+          const uint32_t sfb = sfc + 4 * kT;
+#pragma unroll
+          for (int t = 0; t < kT; ++t)
+            tc_cp_sf(sfc + 4 * t, sf_desc(smem_u32(smem + C::kSfaOff + (ws * kT + t) * 512)));
+          tc_cp_sf(sfb, sf_desc(smem_u32(smem + C::kSfbOff + xs * 512)));
           const uint64_t bdesc = sw128_desc(smem_u32(smem + C::kXOff + xs * C::kXStage));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t id = C::kIdesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-            tc_mma_mxf8(acc, adesc + 2 * k, bdesc + 2 * k, id, sfc, sfc + 4, (s | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int t = 0; t < kT; ++t) {
+              const uint64_t adesc = sw128_desc(smem_u32(smem + C::kWOff + ws * C::kWStage + t * 16384));
+              tc_mma_mxf8(acc + t * C::kAccCols, adesc + 2 * k, bdesc + 2 * k, id, sfc + 4 * t, sfb,
+                          (s | k) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&wempty[ws]);
           tc_commit(&xempty[xs]);
@@ -660,19 +688,20 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
     if (!ok) *abort_flag = 1u;
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // tensor-memory lane quarter: rows 32 q .. 32 q + 31
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int q = warp & 3;            // tensor-memory lane quarter: rows 32 q .. 32 q + 31
+    const int et = (warp - 4) >> 2;    // the item's tile this warp drains
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(et) * C::kAccCols;
     int gp = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok);
-      const int n = it.rt * 128 + q * 32 + lane;
+      const Item it = item_at(p, i, tok, kT);
+      const int n = (it.rt + et) * 128 + q * 32 + lane;
       for (int ch = 0; ch < it.nch; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;
         const int ntok = it.cnt - ch * tok < tok ? it.cnt - ch * tok : tok;
         const int* prow = p.pairs + it.o0 + ch * tok;  // this pass's pairs
         if (!mbar_wait(&accfull[buf], (gp / C::kAccBufs) & 1u)) { *abort_flag = 1u; break; }
         tc_fence_after();
-        const uint32_t acc = lane_base + static_cast<uint32_t>(buf) * C::kAccCols;
+        const uint32_t acc = lane_base + static_cast<uint32_t>(buf * kT) * C::kAccCols;
         if (!kWide) {
           uint32_t v[32];  // A16: columns 0..15 hi pieces, 16..31 lo pieces; MXFP8: 32 pairs
           tmem_ld32(acc, v);
@@ -688,6 +717,30 @@ __global__ void __launch_bounds__(kTcThreads, MoeCfg<kWide>::kCtasPerSm)
           for (int t = 0; t < 32; ++t) {
             if (t >= ntok) break;  // warp-uniform
             store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[t]));
+          }
+        } else if (kMode == kMoePair) {
+          // the whole quarter (128 columns: 128 pairs, or 64 hi | 64 lo) to
+          // registers, release the accumulator, then the stores
+          uint32_t v[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32_async(acc + static_cast<uint32_t>(c * 32), v + 32 * c);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[buf]);  // the next pass may overwrite it
+          if (p.lo) {
+#pragma unroll
+            for (int t = 0; t < 64; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[64 + t]));
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (c * 32 >= ntok) break;  // warp-uniform
+            const int pr = c * 32 + lane < ntok ? prow[c * 32 + lane] : -1;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              if (c * 32 + t >= ntok) break;  // warp-uniform
+              store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[c * 32 + t]));
+            }
           }
         } else {
           // 32 pairs at a time: hi columns 32 c.., (A16) lo columns tok + 32 c..
@@ -817,10 +870,13 @@ int moe_wide_pass(long long P, int E, int lo) {
   return experts > 0 && P >= experts * (pw / 2) ? pw : 0;
 }
 
-template <bool kWide>
+template <int kMode>
 static int launch_moe_gemm(const MoeLaunch& a, const MoeParams& p, uint8_t* xh, uint8_t* xl, uint8_t* cs,
                            cudaLaunchConfig_t cfg) {
-  using C = MoeCfg<kWide>;
+  using C = MoeCfg<kMode>;
+  constexpr bool kWide = C::kWide;
+  static_assert(C::kSmem <= 227 * 1024 && C::kTmemCols <= 512 && C::kXStage % 1024 == 0, "expert kernel budget");
+  static_assert(C::kAccBufs * C::kATiles * C::kAccCols + C::kSfSlot * C::kWStages <= C::kTmemCols, "tmem");
   const mx_packed_weight* w = a.w;
   const long long P = static_cast<long long>(a.T) * a.topk;
   const int Kp = w->Kp, KT = Kp / 128;
@@ -844,18 +900,18 @@ static int launch_moe_gemm(const MoeLaunch& a, const MoeParams& p, uint8_t* xh, 
   DeviceInfo di;
   if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
   static int smem_set[64];
-  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel<kWide>), C::kSmem, di, smem_set) != MX_OK)
+  if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel<kMode>), C::kSmem, di, smem_set) != MX_OK)
     return MX_ERR_CUDA;
   // persistent: kCtasPerSm CTAs an SM (what shared and tensor memory allow),
   // never more than the largest possible number of work items
   const long long zmax = P < w->E ? P : w->E;
-  const long long items = zmax * p.NT;
+  const long long items = zmax * (p.NT / C::kATiles);
   const long long slots = static_cast<long long>(C::kCtasPerSm) * di.sm_count;
   const int grid = static_cast<int>(items < slots ? items : slots);
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_kernel<kWide>, wmap, xhmap, xlmap, csmap, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_kernel<kMode>, wmap, xhmap, xlmap, csmap, p);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe launch: %s", cudaGetErrorString(e));
   return MX_OK;
 }
@@ -869,6 +925,7 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
     return set_error(MX_ERR_WORKSPACE, "expert activation workspace of %zu bytes, needs %zu", a.act_bytes,
                      moe_act_bytes(P, Kp, w->E));
   const bool wide = a.wide_pass > 0;
+  const int NT = (w->N + 127) / 128;
   if (wide && (!a.pass_off || !a.ids || a.wide_pass != moe_wide_pass(P, w->E, a.lo)))
     return set_error(MX_ERR_ARG, "wide expert passes need the routing's pass offsets");
   uint8_t* xh = static_cast<uint8_t*>(a.act);
@@ -910,11 +967,16 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.out_f32 = static_cast<float*>(a.out_f32);
   p.N = w->N;
   p.KT = KT;
-  p.NT = (w->N + 127) / 128;
+  p.NT = NT;
   p.lo = a.lo;
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
-  return wide ? launch_moe_gemm<true>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<false>(a, p, xh, xl, cs, cfg);
+  if (!wide) return launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
+  // two 128-row tiles an item when the tiles pair up evenly, for MXFP8
+  // activations (measured on GB300, E=64 N=K=4096 top-8: W4A8 T=4096 775 ->
+  // 698 us; A16W4, whose 64-pair passes re-read the weights twice as often,
+  // gained nothing)
+  return NT % 2 == 0 && !a.lo ? launch_moe_gemm<kMoePair>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeWide>(a, p, xh, xl, cs, cfg);
 }
 
 }  // namespace mx

@@ -391,3 +391,44 @@ def test_expert_many_pairs():
     ref = oracle_expert(m, ids)
     err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
     assert err <= TOL, err
+
+
+@pytest.mark.parametrize("N", [300, 456, 584])
+def test_wide_passes_odd_and_even_row_tiles(N):
+    """Prefill pair counts with 3, 4 and 5 ragged 128-row weight tiles: with
+    MXFP8 activations an even count runs the two-tile items (two accumulators
+    on one activation stage), an odd count the one-tile items; A16 runs the
+    one-tile items at every count."""
+    m = inputs.moe_gate_up(E=3, N=N, K=544, T=200, topk=2, seed=50 + N)
+    ids = m["ids"].clone()
+    ids[3, 0] = -1
+    assert check_w4a8(m, ids) == 0
+    assert check_moe(m, ids) == 0
+
+
+def test_w4a8_prefill_size_sampled():
+    """The W4A8 prefill workload itself (E=64, N=K=4096, T=4096, top-8: wide
+    two-tile passes, many-CTA routing, per-token activation rows) on sampled
+    (token, slot, rows) against the oracle's quantized activation."""
+    from oracle.quant import quantize_act
+    from oracle.linear import expand_codes
+    from oracle.formats import e4m3_decode
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_gate_up(T=4096)
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    y = mx.mxfp4_moe_linear_w4a8(m["x"].to(dev), m["ids"].to(dev), p)
+    torch.cuda.synchronize()
+    xv = bf16_np(m["x"])
+    rng = np.random.default_rng(25)
+    wb, cb, ids = u8(m["w"]), u8(m["codes"]), u8(m["ids"])
+    for _ in range(32):
+        t, j = int(rng.integers(0, 4096)), int(rng.integers(0, 8))
+        xq, xc = quantize_act(xv[t:t + 1])
+        a = (e4m3_decode(xq) * expand_codes(xc, 1, 4096))[0]
+        ns = np.sort(rng.choice(4096, size=64, replace=False))
+        e = int(ids[t, j])
+        Wd = dequant_values(wb[e, ns], cb[e, ns], "e2m1", len(ns), 4096)
+        got = y[t, j, torch.from_numpy(ns).to(dev)].float().cpu().numpy()
+        err = normalized_error(got[None], (Wd @ a)[None], a[None], Wd)
+        assert err <= TOL, (t, j, err)
