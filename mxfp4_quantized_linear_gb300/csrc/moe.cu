@@ -488,7 +488,7 @@ struct MoeParams {
   const int32_t* pass_off; // wide: first pass of each expert [E + 1]
   __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
   float* out_f32;          // kMoeOutF32: [T * topk, N]
-  int N, KT, NT;
+  int N, KT, NT, E;
   int lo;                  // 1: hi and lo activation pieces (A16), 0: hi only (MXFP8)
   int gate_up;             // weight rows interleaved gate / up in 8-row groups
   int out_mode;
@@ -502,21 +502,48 @@ MX_DEV int gate_up_row(int r, int N) {
 
 MX_DEV float silu_f32(float v) { return v / (1.0f + expf(-v)); }
 
-// A work item is one 128-row tile rt of the a-th active expert (items a-major);
-// every role of a CTA walks the same items blockIdx.x, + gridDim.x, ...
+// Narrow passes: a work item is one group of `tiles` 128-row tiles of the
+// a-th active expert, all its passes of pairs (items a-major).  Wide passes
+// (po = the experts' pass offsets): a work item is one pass of one tile group,
+// items expert-major, then tile group, then pass, so the CTAs that read the
+// same weight tiles for the passes of an expert run side by side and share
+// them through L2.  Every role of a CTA walks the same items blockIdx.x,
+// + gridDim.x, ...
 struct Item {
-  int e, o0, cnt, nch, rt;
+  int e, o0, cnt, rt;
+  int ch0, nch;  // the item's passes
+  int npass;     // the passes of its expert
 };
 
-MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles) {
+MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po) {
   Item it;
-  const int nti = p.NT / tiles;  // items an expert (tiles = 2 needs NT even)
+  const int nti = p.NT / tiles;  // tile groups an expert (tiles = 2 needs NT even)
+  if (po) {
+    // the expert: the largest e with po[e] * nti <= i (po[E] * nti > i)
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (po[mid] * nti <= i) lo = mid; else hi = mid;
+    }
+    it.e = lo;
+    it.npass = po[lo + 1] - po[lo];
+    const int local = i - po[lo] * nti;
+    const int g = local / it.npass;
+    it.rt = g * tiles;
+    it.ch0 = local - g * it.npass;
+    it.nch = 1;
+    it.o0 = p.offsets[it.e];
+    it.cnt = p.offsets[it.e + 1] - it.o0;
+    return it;
+  }
   const int a = i / nti;
   it.rt = (i - a * nti) * tiles;  // the item's first 128-row tile
   it.e = p.active[a];
   it.o0 = p.offsets[it.e];
   it.cnt = p.offsets[it.e + 1] - it.o0;
   it.nch = (it.cnt + tok - 1) / tok;
+  it.ch0 = 0;
+  it.npass = it.nch;
   return it;
 }
 
@@ -583,19 +610,29 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   // memory (a dependent grid then never takes columns this grid waits for)
   pdl_launch_dependents();
   pdl_wait_prior_grid();  // the routing and the activation pieces are complete
-  const int n_items = *p.n_active * (p.NT / kT);  // CTAs past the last item go straight to the exit
+  // wide passes: the experts' pass offsets in shared memory (items are found by
+  // a binary search over them)
+  __shared__ int po_s[kWide ? MX_MAX_EXPERTS + 1 : 1];
+  const int* po = nullptr;
+  if (kWide) {
+    for (int e = threadIdx.x; e <= p.E; e += blockDim.x) po_s[e] = p.pass_off[e];
+    __syncthreads();
+    po = po_s;
+  }
+  // CTAs past the last item go straight to the exit
+  const int n_items = kWide ? po_s[p.E] * (p.NT / kT) : *p.n_active * (p.NT / kT);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
     tma_prefetch_desc(&wmap);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT);
+      const Item it = item_at(p, i, tok, kT, po);
       // a weight tile read once streams past L2; read again (more than one
       // pass of pairs) it is kept
-      const uint64_t pol = it.nch > 1 ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol = it.npass > 1 ? policy_evict_last() : policy_evict_first();
       const long long tile = static_cast<long long>(it.e) * p.NT + it.rt;  // the item's first tile
-      for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
+      for (int ch = it.ch0; ch < it.ch0 + it.nch && !*abort_flag; ++ch) {
         for (int s = 0; s < p.KT; ++s, ++g) {
           const int st = g % C::kWStages;
           if (!mbar_wait(&wempty[st], ((g / C::kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
@@ -620,8 +657,8 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const uint32_t tx = kWide ? C::kBRows * 128 + 512 : C::kBRows * (128 + 16);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT);
-      for (int ch = 0; ch < it.nch && !*abort_flag; ++ch) {
+      const Item it = item_at(p, i, tok, kT, po);
+      for (int ch = it.ch0; ch < it.ch0 + it.nch && !*abort_flag; ++ch) {
         const int row0 = it.o0 + ch * tok;
         for (int s = 0; s < p.KT; ++s, ++g) {
           const int st = g % C::kXStages;
@@ -647,8 +684,8 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT);
-      for (int ch = 0; ch < it.nch && ok; ++ch, ++gp) {
+      const Item it = item_at(p, i, tok, kT, po);
+      for (int ch = it.ch0; ch < it.ch0 + it.nch && ok; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;  // the epilogue drains the other accumulator (narrow)
         if (!mbar_wait(&accempty[buf], ((gp / C::kAccBufs) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
@@ -693,9 +730,9 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(et) * C::kAccCols;
     int gp = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT);
+      const Item it = item_at(p, i, tok, kT, po);
       const int n = (it.rt + et) * 128 + q * 32 + lane;
-      for (int ch = 0; ch < it.nch; ++ch, ++gp) {
+      for (int ch = it.ch0; ch < it.ch0 + it.nch; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;
         const int ntok = it.cnt - ch * tok < tok ? it.cnt - ch * tok : tok;
         const int* prow = p.pairs + it.o0 + ch * tok;  // this pass's pairs
@@ -905,7 +942,8 @@ static int launch_moe_gemm(const MoeLaunch& a, const MoeParams& p, uint8_t* xh, 
   // persistent: kCtasPerSm CTAs an SM (what shared and tensor memory allow),
   // never more than the largest possible number of work items
   const long long zmax = P < w->E ? P : w->E;
-  const long long items = zmax * (p.NT / C::kATiles);
+  // wide: one pass an item, and the experts' passes number at most P / pw + zmax
+  const long long items = (kWide ? P / a.wide_pass + zmax : zmax) * (p.NT / C::kATiles);
   const long long slots = static_cast<long long>(C::kCtasPerSm) * di.sm_count;
   const int grid = static_cast<int>(items < slots ? items : slots);
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -968,6 +1006,7 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.N = w->N;
   p.KT = KT;
   p.NT = NT;
+  p.E = w->E;
   p.lo = a.lo;
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
