@@ -440,8 +440,8 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
 // activation-pieces kernel and bulk-copied, one accumulator, two CTAs an SM.
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? c : pow2_at_least(v, 2 * c); }
 
-// A third form for prefill of MXFP8 activations (hi pieces only) when the
-// weight has an even number of 128-row tiles (kMoePair): each work item is two adjacent row tiles multiplied by
+// A third form for prefill when the weight has an even number of 128-row
+// tiles (kMoePair): each work item is two adjacent row tiles multiplied by
 // the same activation stage (8 MMAs a K step into two accumulators), so every
 // activation byte brought from L2 feeds twice the tensor work.  One CTA an SM
 // and 12 warps (8 epilogue warps, one a lane quarter of each accumulator); the
@@ -1011,11 +1011,11 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
   if (!wide) return launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
-  // two 128-row tiles an item when the tiles pair up evenly, for MXFP8
-  // activations (measured on GB300, E=64 N=K=4096 top-8: W4A8 T=4096 775 ->
-  // 698 us; A16W4, whose 64-pair passes re-read the weights twice as often,
-  // gained nothing)
-  return NT % 2 == 0 && !a.lo ? launch_moe_gemm<kMoePair>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeWide>(a, p, xh, xl, cs, cfg);
+  // two 128-row tiles an item when the tiles pair up evenly (measured on
+  // GB300, E=64 N=K=4096 top-8 T=4096: W4A8 775 -> 698 us; the full A16W4
+  // expert, whose SiLU-and-mul and f32 epilogues the one-tile form cannot
+  // hide, 2737 -> 2007 us; the plain A16W4 GEMM within 1 %)
+  return NT % 2 == 0 ? launch_moe_gemm<kMoePair>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeWide>(a, p, xh, xl, cs, cfg);
 }
 
 }  // namespace mx

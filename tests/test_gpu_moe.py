@@ -395,10 +395,9 @@ def test_expert_many_pairs():
 
 @pytest.mark.parametrize("N", [300, 456, 584])
 def test_wide_passes_odd_and_even_row_tiles(N):
-    """Prefill pair counts with 3, 4 and 5 ragged 128-row weight tiles: with
-    MXFP8 activations an even count runs the two-tile items (two accumulators
-    on one activation stage), an odd count the one-tile items; A16 runs the
-    one-tile items at every count."""
+    """Prefill pair counts with 3, 4 and 5 ragged 128-row weight tiles: an even
+    count runs the two-tile items (two accumulators on one activation stage),
+    an odd count the one-tile items; both activation forms."""
     m = inputs.moe_gate_up(E=3, N=N, K=544, T=200, topk=2, seed=50 + N)
     ids = m["ids"].clone()
     ids[3, 0] = -1
