@@ -384,7 +384,7 @@ def bench_moe(mx, inputs, dev, stream, hbm_peak):
         p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
         x, ids = m["x"].to(dev), m["ids"].to(dev)
         out = torch.empty((64, 8, 4096), dtype=torch.bfloat16, device=dev)
-        work = torch.empty(mx.mxfp4_moe_workspace_size(64, 8, 64, 4096), dtype=torch.uint8, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(64, 8, 64, 4096, 4096), dtype=torch.uint8, device=dev)
         for _ in range(3):
             mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work)
         torch.cuda.synchronize()
@@ -450,7 +450,7 @@ def bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind):
     with torch.cuda.stream(stream):
         p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
         out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
-        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, K), dtype=torch.uint8, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, N, K), dtype=torch.uint8, device=dev)
         for _ in range(2):
             mx.mxfp4_moe_linear_w4a8(m["x"], m["ids"], p, out=out, workspace=work)
         torch.cuda.synchronize()
@@ -612,7 +612,7 @@ def bench_sweep(mx, inputs, dev, stream, hbm_peak, bf16_peak):
         x = m["x"][:T].contiguous()
         ids = m["ids"][:T].contiguous()
         out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
-        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, K), dtype=torch.uint8, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, N, K), dtype=torch.uint8, device=dev)
         ms = timed(lambda i=0: mx.mxfp4_moe_linear(x, ids, p, out=out, workspace=work), 4)
         D = int(torch.unique(ids).numel())
         b = moe_bytes(D, N, K, T, topk)

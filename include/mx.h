@@ -281,8 +281,11 @@ int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* c
                      int* dev_status, void* stream);
 
 /* Workspace bytes mxfp4_moe_linear needs for T tokens, top-k slots, E experts
- * and activations of K values (0 for a shape it refuses). */
-size_t mxfp4_moe_workspace_size(int T, int topk, int E, int K);
+ * of N output rows and activations of K values (0 for a shape it refuses).
+ * It holds the routing, the activation pieces and, at decode sizes (T * topk
+ * <= 64), f32 partial sums for splitting K when the few touched experts would
+ * leave SMs idle. */
+size_t mxfp4_moe_workspace_size(int T, int topk, int E, int N, int K);
 
 /*
  * Routed A16W4 expert GEMM (a16w4 module text, dequant / step_mfma): for every

@@ -76,7 +76,7 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp8_linear_workspace_size": (sz, [i32, pw]),
         "mxfp8_linear": (i32, [vp, i32, pw, vp, vp, u, vp, sz, vp]),
         "mx_route_experts": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
-        "mxfp4_moe_workspace_size": (sz, [i32, i32, i32, i32]),
+        "mxfp4_moe_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "mxfp4_moe_linear": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
         "mxfp4_moe_linear_w4a8": (i32, [vp, vp, i32, i32, pw, vp, vp, sz, vp, vp]),
         "mxfp8_linear_noalloc": (i32, [vp, i32, pw, vp, vp, vp]),
@@ -338,8 +338,8 @@ def mx_route_experts(topk_ids: torch.Tensor, E: int, dev_status: torch.Tensor = 
     return r
 
 
-def mxfp4_moe_workspace_size(T: int, topk: int, E: int, K: int) -> int:
-    return int(load_library().mxfp4_moe_workspace_size(T, topk, E, K))
+def mxfp4_moe_workspace_size(T: int, topk: int, E: int, N: int, K: int) -> int:
+    return int(load_library().mxfp4_moe_workspace_size(T, topk, E, N, K))
 
 
 def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, out: torch.Tensor = None,
@@ -351,7 +351,7 @@ def mxfp4_moe_linear(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeight, o
     if out is None:
         out = torch.empty((T, topk, w.N), dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, "out")
-    need = mxfp4_moe_workspace_size(T, topk, w.E, w.K)
+    need = mxfp4_moe_workspace_size(T, topk, w.E, w.N, w.K)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(load_library().mxfp4_moe_linear(_ptr(x), _ptr(topk_ids), T, topk, ctypes.byref(w.desc), _ptr(out),
@@ -369,7 +369,7 @@ def mxfp4_moe_linear_w4a8(x: torch.Tensor, topk_ids: torch.Tensor, w: PackedWeig
     if out is None:
         out = torch.empty((T, topk, w.N), dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, "out")
-    need = mxfp4_moe_workspace_size(T, topk, w.E, w.K)
+    need = mxfp4_moe_workspace_size(T, topk, w.E, w.N, w.K)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(load_library().mxfp4_moe_linear_w4a8(_ptr(x), _ptr(topk_ids), T, topk, ctypes.byref(w.desc),

@@ -85,12 +85,14 @@ LinearWs linear_ws(int M, int Kp) {
 }
 
 struct MoeWs {
-  size_t counts, offsets, pairs, inv, active, n_active, status, pass_off, route_tmp, act, act_bytes, total;
+  size_t counts, offsets, pairs, inv, active, n_active, status, pass_off, route_tmp, act, act_bytes, part,
+      part_bytes, total;
 };
 
 // Routing outputs, then the activation pieces of the T * topk pairs for K
-// values padded to Kp (Kp = 0: routing only).
-MoeWs moe_ws(int T, int topk, int E, int Kp) {
+// values padded to Kp (Kp = 0: routing only), then the split-K partial sums
+// for N outputs a pair.
+MoeWs moe_ws(int T, int topk, int E, int N, int Kp) {
   MoeWs r;
   const size_t P = static_cast<size_t>(T) * topk;
   size_t o = 0;
@@ -105,7 +107,9 @@ MoeWs moe_ws(int T, int topk, int E, int Kp) {
   r.route_tmp = o; o += align_up(route_scratch_bytes(static_cast<long long>(P), E), 16);
   r.act = align_up(o, 256);
   r.act_bytes = Kp > 0 ? moe_act_bytes(static_cast<long long>(P), Kp, E) : 0;
-  r.total = r.act + r.act_bytes;
+  r.part = align_up(r.act + r.act_bytes, 256);
+  r.part_bytes = Kp > 0 ? moe_part_bytes(static_cast<long long>(P), N) : 0;
+  r.total = r.part + r.part_bytes;
   return r;
 }
 
@@ -529,9 +533,9 @@ int mx_route_experts(const int32_t* topk_ids, int T, int topk, int E, int32_t* c
   return e == cudaSuccess ? MX_OK : cuda_fail(e, "route launch");
 }
 
-size_t mxfp4_moe_workspace_size(int T, int topk, int E, int K) {
-  if (T < 0 || topk < 1 || E < 1 || K < 32 || K % 32) return 0;
-  return moe_ws(T, topk, E, padded_k(K)).total;
+size_t mxfp4_moe_workspace_size(int T, int topk, int E, int N, int K) {
+  if (T < 0 || topk < 1 || E < 1 || N < 1 || K < 32 || K % 32) return 0;
+  return moe_ws(T, topk, E, N, padded_k(K)).total;
 }
 
 // (internal) the routed expert GEMM with bf16 activations (lo = 1: hi and lo
@@ -548,7 +552,7 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   if (!x || !topk_ids || !out || !workspace) return set_error(MX_ERR_ARG, "NULL pointer");
   if (!aligned16(x) || !aligned16(out) || !aligned16(workspace))
     return set_error(MX_ERR_ALIGN, "x, out and workspace need 16-byte alignment");
-  const MoeWs R = moe_ws(T, topk, w->E, w->Kp);
+  const MoeWs R = moe_ws(T, topk, w->E, w->N, w->Kp);
   if (workspace_bytes < R.total) return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, R.total);
   int rc = check_device();
   if (rc != MX_OK) return rc;
@@ -581,6 +585,8 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   a.out = out;
   a.act = ws + R.act;
   a.act_bytes = R.act_bytes;
+  a.part = ws + R.part;
+  a.part_bytes = R.part_bytes;
   a.wide_pass = pw;
   a.ids = topk_ids;
   a.pass_off = pass_off;
@@ -610,7 +616,8 @@ static ExpertWs expert_ws(int T, int topk, int E, int K, int I, int H) {
   ExpertWs r;
   // the activation pieces serve both projections in turn: sized for the longer K
   const int Kp = padded_k(K) > padded_k(I) ? padded_k(K) : padded_k(I);
-  r.route = moe_ws(T, topk, E, Kp);
+  // the partial sums serve both projections in turn: sized for the wider N
+  r.route = moe_ws(T, topk, E, 2 * I > H ? 2 * I : H, Kp);
   const size_t P = static_cast<size_t>(T) * topk;
   r.act = align_up(r.route.total, 256);
   r.y2 = align_up(r.act + P * static_cast<size_t>(I) * 2, 256);
@@ -672,6 +679,8 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   a.lo = 1;
   a.act = ws + R.route.act;
   a.act_bytes = R.route.act_bytes;
+  a.part = ws + R.route.part;
+  a.part_bytes = R.route.part_bytes;
   a.offsets = offsets;
   a.pairs = pairs;
   a.active = active;

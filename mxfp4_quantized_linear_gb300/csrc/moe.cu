@@ -489,6 +489,9 @@ struct MoeParams {
   __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
   float* out_f32;          // kMoeOutF32: [T * topk, N]
   int N, KT, NT, E;
+  int ksplit;              // narrow passes: K ranges an item (1, or split-K into part)
+  int P;                   // T * topk
+  float* part;             // ksplit > 1: f32 partial sums [ksplit, P, N]
   int lo;                  // 1: hi and lo activation pieces (A16), 0: hi only (MXFP8)
   int gate_up;             // weight rows interleaved gate / up in 8-row groups
   int out_mode;
@@ -513,6 +516,8 @@ struct Item {
   int e, o0, cnt, rt;
   int ch0, nch;  // the item's passes
   int npass;     // the passes of its expert
+  int s0, s1;    // the item's K steps (narrow passes split K into ksplit ranges)
+  int ks;        // ... the range's index
 };
 
 MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po) {
@@ -534,10 +539,20 @@ MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po
     it.nch = 1;
     it.o0 = p.offsets[it.e];
     it.cnt = p.offsets[it.e + 1] - it.o0;
+    it.s0 = 0;
+    it.s1 = p.KT;
+    it.ks = 0;
     return it;
   }
-  const int a = i / nti;
-  it.rt = (i - a * nti) * tiles;  // the item's first 128-row tile
+  // narrow: items (active expert, tile group, K range), the K range fastest
+  const int S = p.ksplit;
+  const int a = i / (nti * S);
+  const int rem = i - a * nti * S;
+  const int g = rem / S, ks = rem - g * S;
+  it.s0 = ks * p.KT / S;
+  it.s1 = (ks + 1) * p.KT / S;
+  it.ks = ks;
+  it.rt = g * tiles;  // the item's first 128-row tile
   it.e = p.active[a];
   it.o0 = p.offsets[it.e];
   it.cnt = p.offsets[it.e + 1] - it.o0;
@@ -559,6 +574,43 @@ MX_DEV void store_pair(const MoeParams& p, int pt, int n, int lane, float y) {
   } else if (p.out_mode == kMoeOutBf16 && n < p.N) {
     const int nn = p.gate_up ? gate_up_row(n, p.N) : n;
     p.out[static_cast<long long>(pt) * p.N + nn] = __float2bfloat16_rn(y);
+  }
+}
+
+// Split-K finish: each valid pair's output from the ksplit f32 partial sums
+// part [ksplit, P, N], added in range order (deterministic), in the pass's
+// output form.  Launched as a programmatic dependent of the expert GEMM; it
+// never releases its own dependents early (the next call's routing rewrites
+// the pair list it reads).
+__global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part, int S, int P, int N,
+                                                         const int32_t* __restrict__ pairs,
+                                                         const int32_t* __restrict__ n_valid, int out_mode,
+                                                         int gate_up, __nv_bfloat16* __restrict__ out,
+                                                         float* __restrict__ out_f32) {
+  pdl_wait_prior_grid();
+  const int cols = out_mode == kMoeOutSwiglu ? N / 2 : N;
+  const long long total = static_cast<long long>(*n_valid) * cols;
+  const long long PN = static_cast<long long>(P) * N;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(idx / cols), c = static_cast<int>(idx - static_cast<long long>(j) * cols);
+    const int pt = pairs[j];
+    const float* src = part + static_cast<long long>(pt) * N;
+    if (out_mode == kMoeOutSwiglu) {
+      // packed rows 16 (c / 8) + c % 8 (gate) and 8 further on (up)
+      const int ng = (c >> 3) * 16 + (c & 7);
+      float g = 0.0f, u = 0.0f;
+      for (int k = 0; k < S; ++k) {
+        g += src[k * PN + ng];
+        u += src[k * PN + ng + 8];
+      }
+      out[static_cast<long long>(pt) * cols + c] = __float2bfloat16_rn(silu_f32(g) * u);
+    } else {
+      float y = 0.0f;
+      for (int k = 0; k < S; ++k) y += src[k * PN + c];
+      if (out_mode == kMoeOutF32) out_f32[static_cast<long long>(pt) * N + c] = y;
+      else out[static_cast<long long>(pt) * N + (gate_up ? gate_up_row(c, N) : c)] = __float2bfloat16_rn(y);
+    }
   }
 }
 
@@ -620,7 +672,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     po = po_s;
   }
   // CTAs past the last item go straight to the exit
-  const int n_items = kWide ? po_s[p.E] * (p.NT / kT) : *p.n_active * (p.NT / kT);
+  const int n_items = kWide ? po_s[p.E] * (p.NT / kT) : *p.n_active * (p.NT / kT) * p.ksplit;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
@@ -633,7 +685,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
       const uint64_t pol = it.npass > 1 ? policy_evict_last() : policy_evict_first();
       const long long tile = static_cast<long long>(it.e) * p.NT + it.rt;  // the item's first tile
       for (int ch = it.ch0; ch < it.ch0 + it.nch && !*abort_flag; ++ch) {
-        for (int s = 0; s < p.KT; ++s, ++g) {
+        for (int s = it.s0; s < it.s1; ++s, ++g) {
           const int st = g % C::kWStages;
           if (!mbar_wait(&wempty[st], ((g / C::kWStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
           mbar_arrive_expect_tx(&wfull[st], kT * (kWTx + 512));
@@ -660,7 +712,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
       const Item it = item_at(p, i, tok, kT, po);
       for (int ch = it.ch0; ch < it.ch0 + it.nch && !*abort_flag; ++ch) {
         const int row0 = it.o0 + ch * tok;
-        for (int s = 0; s < p.KT; ++s, ++g) {
+        for (int s = it.s0; s < it.s1; ++s, ++g) {
           const int st = g % C::kXStages;
           if (!mbar_wait(&xempty[st], ((g / C::kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
           uint8_t* dst = smem + C::kXOff + st * C::kXStage;
@@ -690,7 +742,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
         if (!mbar_wait(&accempty[buf], ((gp / C::kAccBufs) & 1u) ^ 1u)) { ok = false; break; }
         tc_fence_after();
         const uint32_t acc = tmem + static_cast<uint32_t>(buf * kT) * C::kAccCols;
-        for (int s = 0; s < p.KT; ++s, ++gw, ++gx) {
+        for (int s = it.s0; s < it.s1; ++s, ++gw, ++gx) {
           const int ws = gw % C::kWStages, xs = gx % C::kXStages;
           if (!mbar_wait(&wfull[ws], (gw / C::kWStages) & 1u) ||
               !mbar_wait(&xfull[xs], (gx / C::kXStages) & 1u)) {
@@ -713,7 +765,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
             for (int t = 0; t < kT; ++t) {
               const uint64_t adesc = sw128_desc(smem_u32(smem + C::kWOff + ws * C::kWStage + t * 16384));
               tc_mma_mxf8(acc + t * C::kAccCols, adesc + 2 * k, bdesc + 2 * k, id, sfc + 4 * t, sfb,
-                          (s | k) != 0 ? 1u : 0u);
+                          (s != it.s0 || k != 0) ? 1u : 0u);
             }
           }
           tc_commit(&wempty[ws]);
@@ -750,10 +802,21 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
 #pragma unroll
             for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[16 + t]));
           }
+          if (p.ksplit > 1) {
+            // split K: this K range's f32 sums; the finishing kernel adds the ranges
+            float* part = p.part + static_cast<long long>(it.ks) * p.P * p.N + n;
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            if (t >= ntok) break;  // warp-uniform
-            store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[t]));
+            for (int t = 0; t < 32; ++t) {
+              if (t >= ntok) break;  // warp-uniform
+              const int pt = __shfl_sync(0xffffffffu, pr, t);
+              if (n < p.N) part[static_cast<long long>(pt) * p.N] = __uint_as_float(v[t]);
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              if (t >= ntok) break;  // warp-uniform
+              store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[t]));
+            }
           }
         } else if (kMode == kMoePair) {
           // the whole quarter (128 columns: 128 pairs, or 64 hi | 64 lo) to
@@ -899,6 +962,30 @@ static size_t act_atoms(long long P, int Kp, int E) {
 }
 size_t moe_act_bytes(long long P, int Kp, int E) { return 2 * act_region(P, Kp) + act_codes(P, Kp) + act_atoms(P, Kp, E); }
 
+// Split K of the narrow passes: at most kMaxKSplit ranges, for at most
+// kSplitMaxPairs pairs (the decode sizes whose few experts leave SM slots idle).
+constexpr int kMaxKSplit = 4, kSplitMaxPairs = 64;
+size_t moe_part_bytes(long long P, int N) {
+  return P <= kSplitMaxPairs ? static_cast<size_t>(kMaxKSplit) * P * N * sizeof(float) : 0;
+}
+
+// The K ranges an item of the narrow passes: the count that minimises the
+// rounds of work items over the resident CTAs (slots), counting each extra
+// range as 8 % of an unsplit item (its pipeline fill, partial sums and the
+// finishing pass); items = an upper bound of the (expert, row tile) items.
+static int moe_ksplit(long long items, long long slots, int KT) {
+  int best_s = 1;
+  double best = static_cast<double>((items + slots - 1) / slots);
+  for (int S = 2; S <= kMaxKSplit && S <= KT; ++S) {
+    const double t = static_cast<double>((items * S + slots - 1) / slots) / S + 0.08 * (S - 1);
+    if (t < best - 1e-9) {
+      best = t;
+      best_s = S;
+    }
+  }
+  return best_s;
+}
+
 // Pairs a wide pass, or 0 for narrow passes: wide once the experts average at
 // least half a wide pass of pairs.
 int moe_wide_pass(long long P, int E, int lo) {
@@ -943,7 +1030,7 @@ static int launch_moe_gemm(const MoeLaunch& a, const MoeParams& p, uint8_t* xh, 
   // never more than the largest possible number of work items
   const long long zmax = P < w->E ? P : w->E;
   // wide: one pass an item, and the experts' passes number at most P / pw + zmax
-  const long long items = (kWide ? P / a.wide_pass + zmax : zmax) * (p.NT / C::kATiles);
+  const long long items = (kWide ? P / a.wide_pass + zmax : zmax * p.ksplit) * (p.NT / C::kATiles);
   const long long slots = static_cast<long long>(C::kCtasPerSm) * di.sm_count;
   const int grid = static_cast<int>(items < slots ? items : slots);
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -1007,10 +1094,33 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.KT = KT;
   p.NT = NT;
   p.E = w->E;
+  p.P = static_cast<int>(P);
+  p.ksplit = 1;
+  if (!wide && a.part && a.part_bytes >= moe_part_bytes(P, w->N) && moe_part_bytes(P, w->N) > 0) {
+    DeviceInfo di;
+    if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
+    const long long zmax = P < w->E ? P : w->E;
+    p.ksplit = moe_ksplit(zmax * NT, static_cast<long long>(MoeCfg<kMoeNarrow>::kCtasPerSm) * di.sm_count, KT);
+    p.part = static_cast<float*>(a.part);
+  }
   p.lo = a.lo;
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
-  if (!wide) return launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
+  if (!wide) {
+    int rc = launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
+    if (rc != MX_OK || p.ksplit == 1) return rc;
+    // add the K ranges' partial sums (programmatic dependent of the GEMM)
+    const long long total = P * static_cast<long long>(w->N);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(total, 256)), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, moe_finish_kernel, static_cast<const float*>(p.part), p.ksplit, p.P, w->N,
+                           a.pairs, a.offsets + w->E, a.out_mode, p.gate_up, static_cast<__nv_bfloat16*>(a.out),
+                           static_cast<float*>(a.out_f32));
+    if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe finish launch: %s", cudaGetErrorString(e));
+    return MX_OK;
+  }
   // two 128-row tiles an item when the tiles pair up evenly (measured on
   // GB300, E=64 N=K=4096 top-8 T=4096: W4A8 775 -> 698 us; the full A16W4
   // expert, whose SiLU-and-mul and f32 epilogues the one-tile form cannot

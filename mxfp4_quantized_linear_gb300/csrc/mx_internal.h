@@ -141,8 +141,12 @@ struct MoeLaunch {
   const int32_t* pass_off;     // the routing's pass offsets [E + 1] for wide_pass (wide passes)
   int no_pdl;                  // 1: launch without programmatic dependent launch
   const int32_t* inv;          // [T * topk] sorted position of each pair (-1: invalid id), or null
+  void* part;                  // split-K partial sums (moe_part_bytes), or null: no split
+  size_t part_bytes;
 };
 size_t moe_act_bytes(long long P, int Kp, int E);
+// f32 partial sums of the split-K narrow passes for P pairs of N outputs (0: never split)
+size_t moe_part_bytes(long long P, int N);
 // Routing for any number of pairs: route_kernel up to one chunk of pairs (inv
 // untouched, returns 0), the three-kernel many-CTA routing above (scratch of
 // route_scratch_bytes; fills inv, the sorted position of each pair, when given).

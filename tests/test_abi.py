@@ -50,7 +50,7 @@ def test_host_side_argument_checks_without_gpu():
     assert lib.mxfp8_linear(None, 1, ctypes.byref(w), None, None, 0, None, 0, None) == b.MX_ERR_ARG
     bad = ctypes.c_void_p(0x1001)  # misaligned (never dereferenced: rejected first)
     assert lib.mx_quantize_act(bad, 2, 64, bad, bad, None) == b.MX_ERR_ALIGN
-    assert lib.mxfp4_moe_workspace_size(4, 2, 8, 256) > 0
+    assert lib.mxfp4_moe_workspace_size(4, 2, 8, 128, 256) > 0
 
 
 def test_product_path_fails_loudly_without_library(tmp_path):
@@ -84,7 +84,7 @@ def test_host_side_checks_of_the_newer_entry_points():
     assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2), ctypes.byref(w2_bad), None, None, 0, None,
                                 None) == b.MX_ERR_SHAPE                # w2 K = 64 != I = 32
     assert b"does not fit" in lib.mx_last_error()
-    assert lib.mxfp4_moe_expert_workspace_size(4, 2, 8, 128, 64, 128) > lib.mxfp4_moe_workspace_size(4, 2, 8, 128)
+    assert lib.mxfp4_moe_expert_workspace_size(4, 2, 8, 128, 64, 128) > lib.mxfp4_moe_workspace_size(4, 2, 8, 128, 128)
     # from-dequant
     n = ctypes.c_int64(7)
     assert lib.mx_e4m3_from_dequant(None, None, 5, 32, 64, None, None, ctypes.byref(n), None) == b.MX_ERR_ARG

@@ -431,3 +431,20 @@ def test_w4a8_prefill_size_sampled():
         got = y[t, j, torch.from_numpy(ns).to(dev)].float().cpu().numpy()
         err = normalized_error(got[None], (Wd @ a)[None], a[None], Wd)
         assert err <= TOL, (t, j, err)
+
+
+def test_decode_split_k():
+    """Few pairs on few experts (decode): the K steps of each (expert, row
+    tile) are split over several CTAs (17 steps into uneven ranges), partial
+    sums added in range order by the finishing kernel; both activation forms,
+    an invalid id, and the full expert (SiLU-and-mul and f32 outputs)."""
+    m = inputs.moe_gate_up(E=64, N=256, K=2080, T=2, topk=8, seed=61)
+    ids = m["ids"].clone()
+    ids[1, 3] = -1
+    assert check_moe(m, ids) == 0
+    assert check_w4a8(m, ids) == 0
+    e = inputs.moe_expert(E=32, I=128, H=256, T=1, topk=8, seed=62)
+    y = gpu_expert(e, e["ids"])
+    ref = oracle_expert(e, e["ids"])
+    err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
+    assert err <= TOL, err
