@@ -448,3 +448,19 @@ def test_decode_split_k():
     ref = oracle_expert(e, e["ids"])
     err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
     assert err <= TOL, err
+
+
+def test_more_items_than_resident_ctas():
+    """More (expert, row tile) items than resident CTAs (64 experts x 8 tiles
+    over 3 CTAs an SM, a partly filled last round), ragged N and K, an invalid
+    id, both activation forms, and the full expert."""
+    m = inputs.moe_gate_up(E=64, N=1000, K=544, T=64, topk=8, seed=71)
+    ids = m["ids"].clone()
+    ids[9, 2] = -1
+    assert check_moe(m, ids) == 0
+    assert check_w4a8(m, ids) == 0
+    e = inputs.moe_expert(E=64, I=512, H=1024, T=64, topk=8, seed=72)
+    y = gpu_expert(e, e["ids"])
+    ref = oracle_expert(e, e["ids"])
+    err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
+    assert err <= TOL, err
