@@ -210,3 +210,14 @@ def test_prequantized_arbitrary_bytes_vs_oracle(M):
     y = mx.mxfp8_linear_q(xq.to(dev), xc.to(dev), p).float().cpu().numpy()
     ref = ref_q(u8(xq), u8(xc), u8(w), row_codes(u8(wc), N))
     assert normalized_error(y, ref["y"], ref["A"], ref["B"]) <= TOL
+
+
+def test_zero_tokens_linear():
+    """M = 0: the linear returns at once with an empty output."""
+    dev = cuda_device()
+    ensure_built()
+    c = inputs.gemv_small()
+    p = mx.mx_pack_weights(c["w"].to(dev), c["codes"].to(dev), "e4m3")
+    y = mx.mxfp8_linear(c["x"][:0].to(dev), p)
+    torch.cuda.synchronize()
+    assert y.shape == (0, p.desc.N)

@@ -464,3 +464,32 @@ def test_more_items_than_resident_ctas():
     ref = oracle_expert(e, e["ids"])
     err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
     assert err <= TOL, err
+
+
+@pytest.mark.parametrize("T", [2, 300])
+def test_every_id_invalid(T):
+    """No pair routed anywhere (every id -1): no active expert, no pass, no
+    split item; every output row is zero and the status is OK, at a decode
+    size (split-K path) and a prefill size (wide passes), both activation forms
+    and the full expert."""
+    m = inputs.moe_gate_up(E=8, N=256, K=256, T=T, topk=2, seed=80 + T)
+    ids = torch.full_like(m["ids"], -1)
+    assert check_moe(m, ids) == 0
+    assert check_w4a8(m, ids) == 0
+    e = inputs.moe_expert(E=4, I=64, H=128, T=T, topk=2, seed=82 + T)
+    status = torch.full((1,), -1, dtype=torch.int32, device=cuda_device())
+    y = gpu_expert(e, torch.full_like(e["ids"], -1), status)
+    assert np.all(y == 0) and int(status.item()) == 0
+
+
+def test_zero_tokens():
+    """T = 0: every MoE entry returns at once with an empty output."""
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_gate_up(E=4, N=128, K=128, T=1, topk=2, seed=90)
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    x = m["x"][:0].to(dev)
+    ids = m["ids"][:0].to(dev)
+    assert mx.mxfp4_moe_linear(x, ids, p).shape == (0, 2, 128)
+    assert mx.mxfp4_moe_linear_w4a8(x, ids, p).shape == (0, 2, 128)
+    torch.cuda.synchronize()
