@@ -221,3 +221,15 @@ def test_zero_tokens_linear():
     y = mx.mxfp8_linear(c["x"][:0].to(dev), p)
     torch.cuda.synchronize()
     assert y.shape == (0, p.desc.N)
+
+
+def test_large_m_padded_rows_and_k():
+    """The block-scaled GEMM with a large activation, padded rows (M = 1000 ->
+    1024) and padded K (4160 -> 4224, pad code 127), per-row weight codes and
+    a bias; every output against the oracle."""
+    g = inputs.generator(77)
+    N, K, M = 320, 4160, 1000
+    w = inputs.e4m3_bytes((N, K), g)
+    c = inputs.e8m0_codes((N, K // 32), 118, 132, g)
+    b = inputs.bf16_normal((N,), g)
+    check(pack(w, c), w, c, inputs.bf16_normal((M, K), g), bias=b)

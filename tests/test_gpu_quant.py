@@ -163,3 +163,14 @@ def test_from_dequant_refusals_count_like_the_oracle():
     assert ei.value.code == mx.binding.MX_ERR_INEXACT
     _, bad = mx.mx_e4m3_from_dequant(w.to(dev), cb.to(dev), strict=False)
     assert bad == e4m3_from_dequant(bf16_np(w), u8(cb))[1]
+
+
+def test_large_activation_every_element():
+    """A large activation (4.3 M elements, an odd row count, several rounds
+    of the grid-stride loop): every byte and code against the oracle, with
+    NaN / inf / all-zero blocks."""
+    x = inputs.bf16_normal((1031, 4128), inputs.generator(5))
+    x[3, 40] = float("nan")
+    x[500, 4127] = float("inf")
+    x[1030, :64] = 0.0
+    check_quant(x)
