@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kRouteThreads)
 // CTA counts a chunk of kRouteChunk pairs, one CTA scans the per-chunk counts
 // (giving each chunk its base in every expert's list), each CTA scatters its
 // chunk stably.  The result is identical to route_kernel's.
-constexpr int kRouteChunk = 4096;
+constexpr int kRouteChunk = 1024;     // pairs a CTA of the many-CTA routing
+constexpr int kRouteManyMin = 4096;   // pairs from which the many-CTA routing is used
 
 __global__ void __launch_bounds__(kRouteThreads)
     route_count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ ccount,
@@ -892,7 +893,7 @@ cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* co
   return cudaGetLastError();
 }
 
-int route_many_writes_inv(long long P) { return P > kRouteChunk ? 1 : 0; }
+int route_many_writes_inv(long long P) { return P > kRouteManyMin ? 1 : 0; }
 
 size_t route_scratch_bytes(long long P, int E) {
   const long long C = (P + kRouteChunk - 1) / kRouteChunk;
@@ -904,7 +905,7 @@ cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_
                               cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off, int pw,
                               void* scratch, int32_t* inv) {
   const int P = T * topk;
-  if (P <= kRouteChunk)
+  if (P <= kRouteManyMin)
     return launch_route(ids, T, topk, E, counts, offsets, pairs, active, n_active, dev_status, stream, zero_out,
                         zero_N, pass_off, pw);
   const int C = (P + kRouteChunk - 1) / kRouteChunk;
