@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kRouteThreads)
   int* base = rs + E;      // [E]
   int* wcnt = rs + 2 * E;  // [warps][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = static_cast<int>(blockDim.x) >> 5;  // the launch sizes the CTA by the pairs
   const unsigned full = 0xffffffffu;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kRouteThreads)
     __syncthreads();
     for (int i = tid; i < E; i += blockDim.x) {
       int s = 0;
-      for (int w = 0; w < kRouteWarps; ++w) s += wcnt[w * E + i];
+      for (int w = 0; w < nwarps; ++w) s += wcnt[w * E + i];
       base[i] += s;
     }
     __syncthreads();
@@ -884,10 +885,15 @@ cudaError_t launch_route(const int32_t* ids, int T, int topk, int E, int32_t* co
                          int32_t* offsets, int32_t* pairs, int32_t* active, int32_t* n_active,
                          int* dev_status, cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off,
                          int pw) {
-  const int smem = (2 * E + kRouteWarps * E) * static_cast<int>(sizeof(int));
-  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // one CTA, as many warps as a pass of pairs needs (a warp's count row of E
+  // entries is zeroed and summed every pass: few pairs, few warps)
+  const int P = T * topk;
+  const int threads = P <= 128 ? 128 : (P <= 256 ? 256 : (P <= 512 ? 512 : kRouteThreads));
+  const int smem = (2 * E + (threads / 32) * E) * static_cast<int>(sizeof(int));
+  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (2 * E + kRouteWarps * E) * static_cast<int>(sizeof(int)));
   if (e != cudaSuccess) return e;
-  route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, T * topk, E, counts, offsets, pairs, active,
+  route_kernel<<<1, threads, smem, stream>>>(ids, T * topk, E, counts, offsets, pairs, active,
                                                    n_active, dev_status,
                                                    static_cast<__nv_bfloat16*>(zero_out), zero_N, pass_off, pw);
   return cudaGetLastError();
