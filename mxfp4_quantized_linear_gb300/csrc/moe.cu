@@ -24,6 +24,31 @@ namespace {
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
+// Zero the bf16 rows [P, N] of the pairs in [p0, p1) whose id is not a valid
+// expert: each warp finds the invalid ids among 32 pairs and writes each such
+// row with all its lanes (16-byte stores when N % 8 == 0).  Called by every
+// thread of the CTA.
+MX_DEV void zero_invalid_rows(const int32_t* __restrict__ ids, int p0, int p1, int E,
+                              __nv_bfloat16* __restrict__ out, int N) {
+  const int lane = threadIdx.x & 31;
+  for (int w0 = p0 + static_cast<int>(threadIdx.x & ~31u); w0 < p1; w0 += blockDim.x) {  // warp-uniform
+    const int p = w0 + lane;
+    const int e = p < p1 ? ids[p] : 0;
+    unsigned m = __ballot_sync(0xffffffffu, p < p1 && (e < 0 || e >= E));
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1;
+      __nv_bfloat16* row = out + static_cast<long long>(w0 + src) * N;
+      if ((N & 7) == 0) {
+        uint4* r4 = reinterpret_cast<uint4*>(row);
+        for (int n = lane; n < (N >> 3); n += 32) r4[n] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        for (int n = lane; n < N; n += 32) row[n] = __float2bfloat16_rn(0.0f);
+      }
+    }
+  }
+}
+
 // zero_out (optional): bf16 [P, zero_N] rows of the pairs whose id is not a
 // valid expert are set to zero (they belong to no expert's list).  pass_off
 // (optional): pass_off[e] = the number of passes of pw pairs the experts
@@ -48,15 +73,11 @@ __global__ void __launch_bounds__(kRouteThreads)
     const int e = ids[p];
     if (e >= 0 && e < E) {
       atomicAdd(&cnt[e], 1);  // integer counts: order-independent
-    } else {
-      if (e != -1) bad = 1;
-      if (zero_out) {
-        __nv_bfloat16* row = zero_out + static_cast<long long>(p) * zero_N;
-        const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
-        for (int n = 0; n < zero_N; ++n) row[n] = z;
-      }
+    } else if (e != -1) {
+      bad = 1;
     }
   }
+  if (zero_out) zero_invalid_rows(ids, 0, P, E, zero_out, zero_N);
   bad = __syncthreads_or(bad);
   if (warp == 0) {  // exclusive scans of the counts (and passes), the ascending list of active experts
     int run = 0, arun = 0, prun = 0;
@@ -146,13 +167,9 @@ __global__ void __launch_bounds__(kRouteThreads)
     } else {
       if (e != -1) bad = 1;
       if (inv) inv[p] = -1;
-      if (zero_out) {
-        __nv_bfloat16* row = zero_out + static_cast<long long>(p) * zero_N;
-        const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
-        for (int n = 0; n < zero_N; ++n) row[n] = z;
-      }
     }
   }
+  if (zero_out) zero_invalid_rows(ids, p0, p1, E, zero_out, zero_N);
   bad = __syncthreads_or(bad);
   if (bad && threadIdx.x == 0) atomicOr(bad_flag, 1);
   for (int e = threadIdx.x; e < E; e += blockDim.x) ccount[static_cast<long long>(blockIdx.x) * E + e] = rs[e];
