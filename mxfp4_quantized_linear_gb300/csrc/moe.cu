@@ -361,9 +361,15 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
   const int nv = inv ? R : *n_pairs;
   // 32-bit indices: the launcher checks P * Kp / 32 < 2^31
   const unsigned total = static_cast<unsigned>(inv ? R : (nv < P ? nv : P)) * static_cast<unsigned>(KBp);
-  for (unsigned i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const unsigned ru = i / static_cast<unsigned>(KBp);
-    const int b = static_cast<int>(i - ru * static_cast<unsigned>(KBp));
+  const int lane = threadIdx.x & 31;
+  // warp-uniform loop (the code words below are gathered by shuffles): lanes
+  // past the end take part but load and store nothing; total and the groups
+  // of four lanes are multiples of 4, so a group is wholly in or out
+  for (unsigned iw = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); iw < total; iw += gridDim.x * blockDim.x) {
+    const unsigned i = iw + lane;
+    const bool act = i < total;
+    const unsigned ru = act ? i / static_cast<unsigned>(KBp) : 0u;
+    const int b = act ? static_cast<int>(i - ru * static_cast<unsigned>(KBp)) : lane;
     long long src;
     if (inv) {
       src = ru;  // the activation row itself
@@ -374,7 +380,7 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
     uint4 qh[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
     uint4 ql[2] = {qh[0], qh[1]};
     uint32_t ch = 127u, cl = 127u;  // padded K blocks: zero bytes, a finite code
-    if (b < KB) {
+    if (act && b < KB) {
       const uint4* sp = reinterpret_cast<const uint4*>(x + src * K + 32 * b);
       const uint4 u[4] = {sp[0], sp[1], sp[2], sp[3]};
       ch = mx_quant_bf16x32(u, qh);
@@ -394,6 +400,16 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
         cl = mx_quant_f32x32(r, ql);
       }
     }
+    // the codes of blocks 4 g .. 4 g + 3 are 4 consecutive bytes of a scale
+    // atom row (or of a code row): lane 4 g writes them as one word
+    uint32_t wh = ch & 0xffu, wl = cl & 0xffu;
+#pragma unroll
+    for (int d = 1; d < 4; ++d) {
+      wh |= (__shfl_down_sync(0xffffffffu, ch, d) & 0xffu) << (8 * d);
+      wl |= (__shfl_down_sync(0xffffffffu, cl, d) & 0xffu) << (8 * d);
+    }
+    const bool leader = (b & 3) == 0;
+    if (!act) continue;
     for (int f = 0; f < fan; ++f) {
       long long j;
       int pr;
@@ -417,13 +433,15 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
         const int e = ids[pr];
         const int rank = static_cast<int>(j) - offsets[e];
         const int r = rank % pw;
-        uint8_t* atom = sfb + (static_cast<long long>(pass_off[e] + rank / pw) * KT + (b >> 2)) * 512 + (b & 3);
-        atom[(r & 31) * 16 + (r >> 5) * 4] = static_cast<uint8_t>(ch);
-        if (lo) atom[((pw + r) & 31) * 16 + ((pw + r) >> 5) * 4] = static_cast<uint8_t>(cl);
-      } else {
-        uint8_t* cp = cs + (j * KT + (b >> 2)) * 32 + (b & 3);
-        cp[0] = static_cast<uint8_t>(ch);
-        if (lo) cp[16] = static_cast<uint8_t>(cl);
+        uint8_t* atom = sfb + (static_cast<long long>(pass_off[e] + rank / pw) * KT + (b >> 2)) * 512;
+        if (leader) {
+          *reinterpret_cast<uint32_t*>(atom + (r & 31) * 16 + (r >> 5) * 4) = wh;
+          if (lo) *reinterpret_cast<uint32_t*>(atom + ((pw + r) & 31) * 16 + ((pw + r) >> 5) * 4) = wl;
+        }
+      } else if (leader) {
+        uint8_t* cp = cs + (j * KT + (b >> 2)) * 32;
+        *reinterpret_cast<uint32_t*>(cp) = wh;
+        if (lo) *reinterpret_cast<uint32_t*>(cp + 16) = wl;
       }
     }
   }
