@@ -242,47 +242,45 @@ def run_ours(args, ws, rank, local):
     def call(M, w):
         mx.mxfp8_linear(xs[M], w, out=outs[M], workspace=work)
 
-    # ---- graphs of whole steps (4 calls on 4 different weight copies each):
-    # one graph runs all nslots steps of the rotation back to back (calls of
-    # consecutive steps overlap through programmatic dependent launch), and
-    # one graph per slot covers a remainder
+    # ---- graphs of whole steps (4 calls on 4 different weight copies each;
+    # step s uses rotation slot s % nslots).  The timed steps run as ONE graph
+    # of exactly --steps steps, so every step boundary overlaps through
+    # programmatic dependent launch the same way whatever the step count; past
+    # CHUNK steps a CHUNK-step graph (a multiple of the rotation, so slots
+    # continue across replays) is replayed and a remainder graph ends the run.
     nslots = ncopies // len(MS)
-    graphs = []
+    CHUNK = nslots * max(1, 1800 // nslots)
+
+    def capture(n_steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(n_steps):
+                for i, M in enumerate(MS):
+                    call(M, packed[(s % nslots) * len(MS) + i])
+        return g
+
     with torch.cuda.stream(stream):
         for M in MS:  # warm up (PDL / cluster launch set-up) before capture
             call(M, packed[0])
         torch.cuda.synchronize()
-        for s in range(nslots):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i, M in enumerate(MS):
-                    call(M, packed[s * len(MS) + i])
-            graphs.append(g)
-        g_all = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_all, stream=stream):
-            for s in range(nslots):
-                for i, M in enumerate(MS):
-                    call(M, packed[s * len(MS) + i])
+        g_warm = capture(args.warmup)
+        q, r = divmod(args.steps, CHUNK) if args.steps > CHUNK else (0, args.steps)
+        g_chunk = capture(CHUNK) if q else None
+        g_rest = capture(r) if r else None
     torch.cuda.synchronize()
 
-    def steps(n, start=0):
-        s = 0
-        while s < n and (start + s) % nslots != 0:
-            graphs[(start + s) % nslots].replay()
-            s += 1
-        while n - s >= nslots:
-            g_all.replay()
-            s += nslots
-        while s < n:
-            graphs[(start + s) % nslots].replay()
-            s += 1
+    def timed_steps():
+        for _ in range(q):
+            g_chunk.replay()
+        if g_rest is not None:
+            g_rest.replay()
 
     def barrier():
         if ws > 1:
             torch.distributed.barrier()
 
     with torch.cuda.stream(stream):
-        steps(args.warmup)
+        g_warm.replay()
     torch.cuda.synchronize()
     # ---- timed region
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -292,7 +290,7 @@ def run_ours(args, ws, rank, local):
         with torch.cuda.stream(stream):
             torch.cuda._sleep(int(2e6))  # keep the queue ahead of the device
             e0.record(stream)
-            steps(args.steps, start=args.warmup)
+            timed_steps()
             e1.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -338,16 +336,22 @@ def run_ours(args, ws, rank, local):
               "config": {"workload": WORKLOAD, "N": N_DEC, "K": K_DEC, "Ms": list(MS),
                          "l2": f"weights rotated over {ncopies} packed copies "
                                f"({ncopies * per_copy / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)",
+                         "graph": f"timed steps in one graph of exactly {args.steps} steps"
+                                  if args.steps <= CHUNK else
+                                  f"timed steps as {q} replays of a {CHUNK}-step graph + {r}",
                          "parallelism": f"replicas x{ws}"},
               "roofline": roofline, "gpu_launches": kernels_per_step * args.steps,
               "clocks": clk.summary()}
     if rank == 0 and not args.no_extras:
-        result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
-        result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
-        result["moe_expert"] = bench_expert(mx, inputs, dev, stream, hbm_peak)
-        result["moe_w4a8_prefill"] = bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind)
+        with ClockSampler(dev.index if dev.index is not None else 0) as clk_x:
+            result["gemm_m4096"] = bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind)
+            result["moe_gate_up"] = bench_moe(mx, inputs, dev, stream, hbm_peak)
+            result["moe_expert"] = bench_expert(mx, inputs, dev, stream, hbm_peak)
+            result["moe_w4a8_prefill"] = bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind)
+            result["configs"] = bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind)
+        result["extras_clocks"] = clk_x.summary()
         result["e2e"] = bench_e2e(mx, packed, dev, stream, args)
-    del graphs, g_all
+    del g_warm, g_chunk, g_rest
     return result
 
 
@@ -447,6 +451,7 @@ def bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind):
     bf16 dense peak (the nominal 8-bit ratio)."""
     E, N, K, T, topk = 64, 4096, 4096, 4096, 8
     m = inputs.moe_gate_up(E=E, N=N, K=K, T=T, topk=topk, seed=3, device=dev)
+    torch.cuda.synchronize()  # drawn on the default stream; packed and used on `stream`
     with torch.cuda.stream(stream):
         p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
         out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
@@ -470,6 +475,110 @@ def bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind):
                         "(activations quantized per token in the call)",
             "ms": round(ms, 4), "TFLOP/s": round(tflops, 1), "frac_tensor": round(tflops / peak8, 4),
             "note": f"fraction of 2 x the {peak_kind} bf16 dense peak (8-bit nominal ratio)"}
+
+
+def graph_ms(stream, fns, reps=5):
+    """Median over ``reps`` replays of one graph holding every call of ``fns``
+    back to back, divided by the number of calls (ms a call).  Each replay is
+    queued behind a short device sleep and timed with CUDA events on
+    ``stream``."""
+    with torch.cuda.stream(stream):
+        for f in fns[:2]:
+            f()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f in fns:
+                f()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(reps):
+            torch.cuda._sleep(int(1e6))
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / len(fns))
+    del g
+    return statistics.median(times)
+
+
+def bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind):
+    """The other workloads of the layer, each timed as a graph of back-to-back
+    calls whose weights (or routed experts) rotate over more than 4x L2:
+    the small GEMV M=1 N=512 K=1024 with 1x32 row codes; the decode linear at
+    K=2080 (K % 128 != 0, padded) for M = 1 and 32; the sweep linear N=7168
+    K=8192 at M = 1, 32 and 256; the sweep experts E=256 N=4096 K=7168 top-8
+    at T = 1, 8 and 64 (A16W4), the top-k ids rotating over 16 draws so
+    consecutive calls touch different experts."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    lines = []
+
+    def linear_lines(name, c, Ms, block):
+        N, K = c["N"], c["K"]
+        wd, cd = c["w"].to(dev), c["codes"].to(dev)
+        per_copy = mx.mx_pack_size("e4m3", 1, N, K)
+        ncopies = max(8, -(-4 * l2 // per_copy))
+        with torch.cuda.stream(stream):
+            packed = [mx.mx_pack_weights(wd, cd, "e4m3") for _ in range(ncopies)]
+        calls = max(ncopies, 64)
+        work = torch.empty(max(256, max(mx.mxfp8_linear_workspace_size(M, packed[0]) for M in Ms)),
+                           dtype=torch.uint8, device=dev)
+        for M in Ms:
+            x = c["xs"][M].to(dev) if "xs" in c else c["x"][:M].to(dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fns = [lambda w=packed[i % ncopies]: mx.mxfp8_linear(x, w, out=out, workspace=work)
+                   for i in range(calls)]
+            ms = graph_ms(stream, fns)
+            b = linear_bytes(M, N, K, block)
+            gbs = b / (ms * 1e-3) / 1e9
+            line = {"workload": f"{name} M={M} N={N} K={K}", "us_per_call": round(ms * 1e3, 3),
+                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
+                    "path": "decode GEMV" if M <= 32 else "block-scaled GEMM",
+                    "l2": f"{ncopies} weight copies, {ncopies * per_copy / 1e6:.0f} MB"}
+            if M > 32:
+                tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+                line["TFLOP/s"] = round(tf, 1)
+            lines.append(line)
+        del packed, work
+
+    linear_lines("MXFP8 GEMV, 1x32 row codes 120..130", inputs.gemv_small(), (1,), False)
+    linear_lines("MXFP8 decode linear, 32x32 codes, K padded to 2176",
+                 inputs.decode_linear(K=2080, Ms=(1, 32)), (1, 32), True)
+    linear_lines("MXFP8 sweep linear, 32x32 codes", inputs.decode_linear(K=8192, Ms=(1, 32, 256), N=7168),
+                 (1, 32, 256), True)
+
+    E, N, K, topk = 256, 4096, 7168, 8
+    Ts = (1, 8, 64)
+    m = inputs.moe_gate_up(E=E, N=N, K=K, T=max(Ts), topk=topk, device=dev)
+    torch.cuda.synchronize()  # drawn on the default stream; packed and used on `stream`
+    with torch.cuda.stream(stream):
+        p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
+    del m["w"], m["codes"]
+    g = inputs.generator(77, dev)
+    nsets = 16
+    id_sets = [inputs.topk_ids(max(Ts), E, topk, g) for _ in range(nsets)]
+    torch.cuda.synchronize()
+    for T in Ts:
+        x = m["x"][:T].contiguous()
+        ids = [s_[:T].contiguous() for s_ in id_sets]
+        out = torch.empty((T, topk, N), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, N, K), dtype=torch.uint8, device=dev)
+        fns = [lambda i=i: mx.mxfp4_moe_linear(x, ids[i % nsets], p, out=out, workspace=work)
+               for i in range(2 * nsets)]
+        ms = graph_ms(stream, fns)
+        D = statistics.mean(int(torch.unique(i_).numel()) for i_ in ids)
+        b = moe_bytes(D, N, K, T, topk)
+        gbs = b / (ms * 1e-3) / 1e9
+        lines.append({"workload": f"MXFP4 A16W4 sweep experts E={E} N={N} K={K} T={T} top-{topk}",
+                      "us_per_call": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
+                      "frac_hbm": round(gbs / hbm_peak, 4), "experts_touched": round(D, 2),
+                      "l2": f"top-k ids rotate over {nsets} draws"})
+    del p
+    torch.cuda.empty_cache()
+    return lines
 
 
 def bench_e2e(mx, packed, dev, stream, args):
@@ -605,6 +714,7 @@ def bench_sweep(mx, inputs, dev, stream, hbm_peak, bf16_peak):
         del packed, work
     E, N, K, topk = 256, 4096, 7168, 8
     m = inputs.moe_gate_up(E=E, N=N, K=K, T=max(Ms), topk=topk, device=dev)
+    torch.cuda.synchronize()  # drawn on the default stream; packed and used on `stream`
     with torch.cuda.stream(stream):
         p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
     del m["w"], m["codes"]
@@ -638,7 +748,6 @@ def blas_threads():
 def oracle_step(c):
     """One step of the workload on the oracle: the four calls, fp64."""
     from oracle.linear import mxfp8_linear as ref_linear
-    from tests.helpers import bf16_np  # noqa: F401  (same exact bf16 -> fp64 conversion)
     w = c["w"].numpy()
     codes = c["codes"].numpy()
     for M in MS:

@@ -257,6 +257,9 @@ int mxfp8_linear_q(const uint8_t* xq, const uint8_t* xcodes, int M, const mx_pac
  *     MX_ERR_UNSUPPORTED with a message.  M == 0 is a no-op.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept per device together with the id of the context it
+ *     belongs to; after a device reset (a new context) the next call looks it
+ *     up again, so make that call outside a stream capture too.
  *   - All calls share the array: calls that overlap on the GPU (e.g. on two
  *     streams at once) race and must be serialised by the caller.  Each call
  *     writes every scratch byte it reads, so stale contents are harmless.

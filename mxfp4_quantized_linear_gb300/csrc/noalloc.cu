@@ -15,9 +15,14 @@
 // code must not pass the array's name to a kernel (on the host it is only a
 // stand-in, not a device address): the device address is looked up once per
 // device with cudaGetSymbolAddress, with that device current, on the first
-// call made on it.  All calls share the array and each call overwrites what
-// the previous one left there; every byte a call reads it writes first, so
-// nothing needs clearing.
+// call made on it.  The address belongs to the device's context: when that
+// context is replaced (cudaDeviceReset, or the primary context released and
+// created again) the module is loaded anew, so the lookup is keyed by the
+// context's unique id and made again for a new context.  All calls share the
+// array and each call overwrites what the previous one left there; every byte
+// a call reads it writes first, so nothing needs clearing.
+
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -29,24 +34,61 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MX_NOALLOC_SCRATCH_BYTES];
 
+struct ScratchSlot {
+  void* ptr;                   // device address of the array in that context
+  unsigned long long ctx_id;   // unique id of the context it was looked up in
+};
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {nullptr};
+ScratchSlot g_scratch[64] = {};
 
-// Device address of this device's scratch array (looked up on first use).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Unique id of the context current on this thread; false when there is none
+// yet (or the driver cannot say), in which case the address is looked up again.
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the current device's scratch array: looked up with
+// cudaGetSymbolAddress (that device current) on the first call in a context,
+// then taken from the cache while the context stays the same.
 int scratch_for_current_device(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return set_error(MX_ERR_UNSUPPORTED, "device ordinal %d", dev);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  if (!have_id || g_scratch[dev].ptr == nullptr || g_scratch[dev].ctx_id != id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
       return set_error(MX_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
+    // the lookup made the device's context current if it was not yet
+    unsigned long long id_now = 0;
+    g_scratch[dev].ptr = p;
+    g_scratch[dev].ctx_id = current_context_id(&id_now) ? id_now : 0ull;
+    *out = static_cast<uint8_t*>(p);
+    return MX_OK;
   }
-  *out = static_cast<uint8_t*>(g_scratch_ptr[dev]);
+  *out = static_cast<uint8_t*>(g_scratch[dev].ptr);
   return MX_OK;
 }
 

@@ -6,6 +6,21 @@ import torch
 TOL = 1e-2  # max-abs error normalised by ||w_n||_2 ||x_m||_2 of the operands
 
 
+def elementwise_excess(y, ref) -> float:
+    """Largest excess of |y - y_ref| over 2^-8 |y_ref| + 1e-5 ||A_m|| ||B_n||,
+    normalised by ||A_m|| ||B_n|| (<= 0 passes); ``ref`` holds the oracle's
+    y, A (activation rows as multiplied) and B (weight rows).  Exact products
+    with f32 sums and one bf16 rounding stay far inside this bound; one 32-wide
+    K block dropped or scaled by a wrong code moves an output by about
+    sqrt(32) / K of ||A_m|| ||B_n|| (7e-4 at K = 8192), which the 1e-2 gate
+    alone does not see."""
+    y = np.asarray(y, dtype=np.float64)
+    den = np.linalg.norm(ref["A"], axis=1)[:, None] * np.linalg.norm(ref["B"], axis=1)[None, :]
+    den = np.where(den > 0, den, 1.0)
+    excess = np.abs(y - ref["y"]) - (2.0 ** -8 * np.abs(ref["y"]) + 1e-5 * den)
+    return float(np.max(excess / den)) if excess.size else 0.0
+
+
 def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")

@@ -8,7 +8,7 @@ import torch
 import mxfp4_quantized_linear_gb300 as mx
 from mxfp4_quantized_linear_gb300 import inputs
 from oracle.linear import mxfp8_linear as ref_linear, normalized_error
-from tests.helpers import TOL, bf16_np, cuda_device, ensure_built, u8
+from tests.helpers import TOL, bf16_np, cuda_device, elementwise_excess, ensure_built, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -38,6 +38,8 @@ def check(p, w, c, x, bias=None, rows=None, flags=0, tol=TOL):
     ref = ref_linear(bf16_np(x), wn, cn, None if bias is None else bf16_np(bias)[rows if rows is not None else slice(None)])
     err = normalized_error(y, ref["y"], ref["A"], ref["B"])
     assert err <= tol, err
+    excess = elementwise_excess(y, ref)
+    assert excess <= 0.0, excess
     return err
 
 
@@ -120,7 +122,7 @@ def test_layer_sweep_linears_sampled_rows(N, K):
     c = inputs.e8m0_codes((N // 32, K // 32), 118, 132, g)
     p = pack(w, c)
     rows = np.sort(np.random.default_rng(1).choice(N, size=256, replace=False))
-    for M in (1, 8, 32, 64):
+    for M in (1, 8, 32, 64, 128, 256):
         check(p, w, c, inputs.bf16_normal((M, K), g), rows=rows)
 
 
@@ -136,6 +138,7 @@ def test_prefill_full_size_sampled():
     ref = ref_linear(bf16_np(c["x"][ms]), wn, cn)
     err = normalized_error(y[np.ix_(ms, ns)], ref["y"], ref["A"], ref["B"])
     assert err <= TOL, err
+    assert elementwise_excess(y[np.ix_(ms, ns)], ref) <= 0.0
 
 
 @pytest.mark.parametrize("M", [1, 5, 9, 32])
@@ -210,6 +213,7 @@ def test_prequantized_arbitrary_bytes_vs_oracle(M):
     y = mx.mxfp8_linear_q(xq.to(dev), xc.to(dev), p).float().cpu().numpy()
     ref = ref_q(u8(xq), u8(xc), u8(w), row_codes(u8(wc), N))
     assert normalized_error(y, ref["y"], ref["A"], ref["B"]) <= TOL
+    assert elementwise_excess(y, ref) <= 0.0
 
 
 def test_zero_tokens_linear():

@@ -493,3 +493,113 @@ def test_zero_tokens():
     assert mx.mxfp4_moe_linear(x, ids, p).shape == (0, 2, 128)
     assert mx.mxfp4_moe_linear_w4a8(x, ids, p).shape == (0, 2, 128)
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- the layer sweep's experts
+
+@pytest.fixture(scope="module")
+def sweep_experts():
+    """E=256 experts of N=4096 rows, K=7168, top-8 routing of up to 256 tokens
+    (3.8 GB of expert bytes, drawn on the device by the seeded generator)."""
+    dev = cuda_device()
+    ensure_built()
+    m = inputs.moe_gate_up(E=256, N=4096, K=7168, T=256, topk=8, seed=5, device=dev)
+    p = mx.mx_pack_weights(m["w"], m["codes"], "e2m1")
+    torch.cuda.synchronize()
+    yield m, p
+    del p
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [1, 2, 8, 256])
+@pytest.mark.parametrize("form", ["a16w4", "w4a8"])
+def test_sweep_experts_sampled(sweep_experts, T, form):
+    """The layer sweep's expert shape (E=256, N=4096, K=7168, top-8) at decode
+    token counts (K steps split over several CTAs, 56 steps into uneven
+    ranges) and at T=256, against the oracle on sampled (token, slot, rows):
+    the 1e-2 gate and the per-element bound 2^-8 |y_ref| + c ||w|| ||x||
+    (c = 1e-5 for MXFP8 activations; 5e-5 for bf16 activations, which carry
+    the hi/lo splitting term)."""
+    from oracle.quant import quantize_act
+    from oracle.linear import expand_codes
+    from oracle.formats import e4m3_decode
+    m, p = sweep_experts
+    dev = cuda_device()
+    K = 7168
+    x = m["x"][:T].contiguous()
+    ids = m["ids"][:T].contiguous()
+    fn = mx.mxfp4_moe_linear if form == "a16w4" else mx.mxfp4_moe_linear_w4a8
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    y = fn(x, ids, p, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    xv = bf16_np(x)
+    idn = u8(ids)
+    rng = np.random.default_rng(100 + T)
+    pairs = [(t, j) for t in range(T) for j in range(8)]
+    if len(pairs) > 40:
+        pairs = [pairs[i] for i in rng.choice(len(pairs), size=40, replace=False)]
+    c = 5e-5 if form == "a16w4" else 1e-5
+    for t, j in pairs:
+        e = int(idn[t, j])
+        ns = np.sort(rng.choice(4096, size=48, replace=False))
+        ns_d = torch.from_numpy(ns).to(dev)
+        wb = m["w"][e].index_select(0, ns_d).cpu().numpy()
+        cb = m["codes"][e].index_select(0, ns_d).cpu().numpy()
+        Wd = dequant_values(wb, cb, "e2m1", len(ns), K)
+        if form == "a16w4":
+            a = xv[t]
+        else:
+            xq, xc = quantize_act(xv[t:t + 1])
+            a = (e4m3_decode(xq) * expand_codes(xc, 1, K))[0]
+        ref = Wd @ a
+        got = y[t, j].index_select(0, ns_d).float().cpu().numpy()
+        err = normalized_error(got[None], ref[None], a[None], Wd)
+        assert err <= TOL, (t, j, err)
+        den = np.linalg.norm(Wd, axis=1) * np.linalg.norm(a)
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + c * den), (t, j)
+
+
+def test_a16w4_wide_dynamic_range_blocks():
+    """bf16 activations whose 32-element blocks span many binades, where the
+    hi + lo MXFP8 pieces lose their smallest elements: bf16 subnormals next to
+    values near 1, single outliers 2^20 above and 2^-20 below the rest of
+    their block, blocks at 2^-120 and 2^100, and ordinary N(0,1) blocks.  Each
+    token takes one pattern so that its norm is set by it.  Per element,
+    |y - y_ref| <= 2^-8 |y_ref| + 5e-5 ||w|| ||x|| (the bound of the hi/lo
+    reading: the pieces miss at most 2^-21.8 of a block's max |x| a value)."""
+    K, T = 2048, 6
+    m = inputs.moe_gate_up(E=4, N=256, K=K, T=T, topk=2, seed=12)
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((T, K))
+    blocks = x.reshape(T, K // 32, 32)
+    # token 0: every block holds bf16 subnormals (2^-130 .. 2^-133) next to N(0,1) values
+    sub = rng.integers(1, 8, size=(K // 32, 8)) * 2.0 ** -133 * rng.choice([-1.0, 1.0], size=(K // 32, 8))
+    blocks[0, :, :8] = sub
+    # token 1: one element of every block 2^20 above the rest
+    blocks[1, :, 5] *= 2.0 ** 20
+    # token 2: one element of every block 2^-20 below the rest
+    blocks[2, :, 7] *= 2.0 ** -20
+    # token 3: a tiny token (2^-120 scale) with one 2^20 outlier in every fourth block
+    blocks[3] *= 2.0 ** -120
+    blocks[3, ::4, 0] *= 2.0 ** 20
+    # token 4: a huge token (2^100 scale)
+    blocks[4] *= 2.0 ** 100
+    # token 5: blocks alternate between the patterns above
+    blocks[5, 0::4, 3] *= 2.0 ** 20
+    blocks[5, 1::4, :16] *= 2.0 ** -125
+    blocks[5, 2::4, 9] *= 2.0 ** -20
+    m["x"] = torch.from_numpy(x).float().to(torch.bfloat16)
+    xv = bf16_np(m["x"])
+    assert np.any((np.abs(xv[0]) < 2.0 ** -126) & (xv[0] != 0))   # subnormals survived the cast
+    y = gpu_moe(m)
+    W = dequant_experts_bf16(u8(m["w"]), u8(m["codes"]))
+    ids = u8(m["ids"])
+    ref = moe_linear(xv, ids, u8(m["w"]), u8(m["codes"]), wdeq=W)
+    for t in range(T):
+        for j in range(2):
+            e = int(ids[t, j])
+            den = np.linalg.norm(W[e].astype(np.float64), axis=1) * np.linalg.norm(xv[t])
+            assert normalized_error(y[t, j][None], ref[t, j][None], xv[t][None], W[e]) <= TOL, (t, j)
+            bound = 2.0 ** -8 * np.abs(ref[t, j]) + 5e-5 * den
+            assert np.all(np.abs(y[t, j] - ref[t, j]) <= bound), (t, j, float(np.max(np.abs(y[t, j] - ref[t, j]) / den)))

@@ -203,3 +203,29 @@ def test_e4m3_from_dequant_round_trip_and_refusals():
     w2[0, 0] = -0.0                                            # -0 is e4m3 0x80
     q, bad = e4m3_from_dequant(w2, codes)
     assert bad == 0 and q[0, 0] == 0x80
+
+
+def test_elementwise_bound_sees_a_lost_k_block_the_gate_misses():
+    """The GPU tests' per-element bound (tests/helpers.elementwise_excess)
+    against planted mistakes, on the CPU: at K = 8192 a y that drops one
+    32-wide K block, or applies that block's weight code one binade off,
+    passes the 1e-2 normalised gate but fails the bound; the exact y and y
+    rounded once to bf16 pass both."""
+    from tests.helpers import elementwise_excess
+    rng = np.random.default_rng(11)
+    M, N, K = 2, 64, 8192
+    x = bf16_vals(rng, (M, K))
+    w = rand_e4m3(rng, (N, K))
+    codes = rng.integers(118, 133, size=(N // 32, K // 32)).astype(np.uint8)
+    ref = mxfp8_linear(x, w, codes)
+    A, B = ref["A"], ref["B"]
+    b = 100
+    blk = slice(32 * b, 32 * b + 32)
+    dropped = ref["y"] - A[:, blk] @ B[:, blk].T
+    doubled = ref["y"] + A[:, blk] @ B[:, blk].T
+    rounded = F.bf16_value(F.bf16_rne_bits(ref["y"]))
+    for bad in (dropped, doubled):
+        assert normalized_error(bad, ref["y"], A, B) <= 1e-2
+        assert elementwise_excess(bad, ref) > 0.0
+    assert elementwise_excess(rounded, ref) <= 0.0
+    assert elementwise_excess(ref["y"], ref) <= 0.0
