@@ -356,6 +356,23 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
  */
 int mx_selftest_bounded_wait(int limit_us, int* waited_out, void* stream);
 
+/* --------------------------------------------------------------- measurement */
+
+/*
+ * Measures the dense MXFP8 tensor throughput of the current device (no
+ * counterpart on the source pages; the denominator of the block-scaled GEMM's
+ * roofline fraction): every SM runs `iters` rounds of 8 block-scaled
+ * tcgen05.mma kind::mxf8f6f4 (M = 128, N = 224, K = 32, e4m3 operands already
+ * in shared memory, UE8M0 scales in tensor memory) from two issuing threads,
+ * `reps` launches back to back on `stream` after one warm-up launch, timed with
+ * CUDA events.  Writes TFLOP/s (2 flops a multiply-add) to *tflops.
+ * Synchronizes the stream; allocates nothing.  1 <= iters <= 65536 (about
+ * 2000 runs 1 ms), 1 <= reps <= 1000.  Errors: MX_ERR_ARG, MX_ERR_UNSUPPORTED
+ * (not sm_103), MX_ERR_CUDA, MX_ERR_TIMEOUT (a bounded wait ran out or an
+ * accumulator did not hold the expected sum).
+ */
+int mx_measure_mxf8_peak(int iters, int reps, double* tflops, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ EXPORTED = ("mx_last_error", "mx_check_device_errors", "mx_pack_size", "mx_pack_
             "mx_route_experts", "mxfp4_moe_workspace_size", "mxfp4_moe_linear", "mxfp4_moe_linear_w4a8",
             "mxfp8_linear_noalloc", "mxfp4_moe_expert_workspace_size", "mxfp4_moe_expert",
             "mxfp8_linear_q_workspace_size", "mxfp8_linear_q", "mx_e4m3_from_dequant",
-            "mx_selftest_bounded_wait")
+            "mx_selftest_bounded_wait", "mx_measure_mxf8_peak")
 
 
 class MxError(RuntimeError):
@@ -83,6 +83,7 @@ def load_library(path: str = None) -> ctypes.CDLL:
         "mxfp4_moe_expert_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "mxfp8_linear_q_workspace_size": (sz, [i32, pw]),
         "mx_selftest_bounded_wait": (i32, [i32, vp, vp]),
+        "mx_measure_mxf8_peak": (i32, [i32, i32, ctypes.POINTER(ctypes.c_double), vp]),
         "mx_e4m3_from_dequant": (i32, [vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(ctypes.c_int64), vp]),
         "mxfp8_linear_q": (i32, [vp, vp, i32, pw, vp, vp, u, vp, sz, vp]),
         "mxfp4_moe_expert": (i32, [vp, vp, vp, i32, i32, pw, pw, vp, vp, sz, vp, vp]),
@@ -402,6 +403,14 @@ def mxfp4_moe_expert(x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torc
                                            ctypes.byref(w13.desc), ctypes.byref(w2.desc), _ptr(out),
                                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream()))
     return out
+
+
+def mx_measure_mxf8_peak(iters: int = 2000, reps: int = 5) -> float:
+    """Dense MXFP8 tensor TFLOP/s of the current device, measured by an
+    MMA-only loop on every SM (see include/mx.h); synchronizes."""
+    v = ctypes.c_double(0.0)
+    _check(load_library().mx_measure_mxf8_peak(iters, reps, ctypes.byref(v), _stream()))
+    return float(v.value)
 
 
 def mx_check_device_errors() -> None:

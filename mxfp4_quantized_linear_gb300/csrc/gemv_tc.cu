@@ -17,8 +17,12 @@
 //     tensor core reads, plus the activation scale atom;
 //   * warp 1 issues, per K step, tcgen05.cp of both scale atoms into tensor
 //     memory and four tcgen05.mma kind::mxf8f6f4.block_scale (M = 128 weight
-//     rows, N = 32 token columns, K = 32): the block scales are applied by the
-//     tensor core, the f32 sums stay in tensor memory;
+//     rows, N = 16 or 32 token columns, K = 32): the block scales are applied
+//     by the tensor core, the f32 sums stay in tensor memory.  One thread
+//     issues a block-scaled MMA only about every 150 cycles (measured on
+//     GB300), so when the whole slice sits in the ring (no refills) the TMA
+//     thread, idle once its loads are issued, takes the odd ring stages into a
+//     second accumulator; the epilogue adds the two in a fixed order;
 //   * the epilogue reads the 128 x 32 accumulator (tcgen05.ld) and sends each
 //     row's partial to the CTA of the cluster that owns the row, completing on
 //     that CTA's mbarrier: per-thread st.async for M <= 8 over more than two
@@ -53,10 +57,24 @@ constexpr int kMaxCtasPerSm = 5;          // register budget (launch bounds)
 __host__ __device__ inline int mma_n(int M) { return M <= 16 ? 16 : 32; }
 __host__ __device__ inline int xq_step_bytes(int M) { return mma_n(M) * kStepB; }
 
-// Tensor-memory columns: the accumulator (MMA N columns) and one scale-factor
-// slot (SFw 4 + SFx 4 columns) a step, rounded up to a power of two >= 32.
-__host__ __device__ inline int tmem_cols_for(int M, int steps) {
-  const int need = mma_n(M) + steps * 8;
+// MMA issuers of a CTA with `steps` K steps and a `ring`-stage weight ring:
+// two (warp 1 the even stages, the TMA thread the odd ones) when the slice
+// fits the ring, so that the TMA thread has no refills to make; else one.
+__host__ __device__ inline int issuers_for(int steps, int ring) { return steps >= 2 && steps <= ring ? 2 : 1; }
+
+// The slices of one call hold KT / S or KT / S + 1 steps; the tensor-memory
+// layout has room for the most issuers any of them uses.
+__host__ __device__ inline int issuers_layout(int KT, int S, int ring) {
+  const int a = issuers_for(KT / S, ring), b = issuers_for((KT + S - 1) / S, ring);
+  return a > b ? a : b;
+}
+
+// Tensor-memory columns: one accumulator (MMA N columns) a issuer of the
+// layout and one scale-factor slot (SFw 4 + SFx 4 columns) a step, rounded up
+// to a power of two >= 32.
+__host__ __device__ inline int tmem_cols_for(int M, int KT, int S, int ring) {
+  const int steps = (KT + S - 1) / S;
+  const int need = issuers_layout(KT, S, ring) * mma_n(M) + steps * 8;
   int c = 32;
   while (c < need) c <<= 1;
   return c;
@@ -144,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
   const int ring = p.ring;
   const Layout L = layout_for(ring, (p.KT + p.splits - 1) / p.splits, p.splits, p.M, p.own_recv != 0);
   const int xqb = xq_step_bytes(p.M);                          // quantized activation a step
-  const uint32_t sf_base = static_cast<uint32_t>(mma_n(p.M));  // scale-factor slots after the accumulator
+  const int nN = mma_n(p.M);
+  const int n_iss = issuers_for(ns, ring);                                 // this CTA's MMA issuers
+  const uint32_t sf_base =                                                  // scale-factor slots after the accumulators
+      static_cast<uint32_t>(issuers_layout(p.KT, p.splits, ring) * nN);
   const int S = p.splits;
   const int rows_per = (kRows + S - 1) / S;        // rows each CTA of the cluster owns
   const int Mp = recv_stride(p.M);                 // receive-buffer floats a (slice, row)
@@ -165,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
       mbar_init(&wempty[s], 1);
     }
     mbar_init(xready, 128);
-    mbar_init(accfull, 1);
+    mbar_init(accfull, static_cast<uint32_t>(n_iss));  // one commit a issuer
     mbar_init(redbar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -208,6 +229,34 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
       bulk_load(smem + L.sfw + stage * 512, p.sfw + (static_cast<long long>(tile) * p.KT + st0 + i) * 512, 512,
                 &wfull[stage]);
     }
+    if (n_iss == 2) {
+      // ---------------------------------------------------- second MMA issuer
+      // every load is issued (the slice fits the ring): the odd stages' scale
+      // atoms, then, once the activation is ready, their MMAs into the second
+      // accumulator (columns nN .. 2 nN - 1)
+      bool ok = true;
+      for (int i = 1; i < ns && ok; i += 2) {
+        if (!mbar_wait(&wfull[i], 0u)) { *abort_flag = 1u; ok = false; break; }
+        tc_fence_after();
+        tc_cp_sf(tmem + sf_base + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
+      }
+      if (ok && !mbar_wait(xready, 0)) { *abort_flag = 1u; ok = false; }
+      tc_fence_after();
+      const uint32_t idesc_n = p.M <= 16 ? kIdesc16 : kIdesc32;
+      for (int i = 1; i < ns && ok; i += 2) {
+        const uint32_t sf = tmem + sf_base + static_cast<uint32_t>(i * 8);
+        tc_cp_sf(sf + 4, sf_desc(smem_u32(smem + L.sfx + i * 512)));
+        const uint64_t adesc = sw128_desc(smem_u32(smem + L.w + i * kWBox));
+        const uint64_t bdesc = sw128_desc(smem_u32(smem + L.xq + i * xqb));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t idesc = idesc_n | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+          tc_mma_mxf8(tmem + static_cast<uint32_t>(nN), adesc + 2 * k, bdesc + 2 * k, idesc, sf, sf + 4,
+                      (i > 1 || k > 0) ? 1u : 0u);
+        }
+      }
+      tc_commit(accfull);
+    }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     // a scale-factor slot per step (SFw in its first 4 columns, SFx in the
@@ -217,14 +266,14 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
     bool ok = true;
     const int pre = ns < ring ? ns : ring;
     const uint32_t idesc_n = p.M <= 16 ? kIdesc16 : kIdesc32;
-    for (int i = 0; i < pre && ok; ++i) {
+    for (int i = 0; i < pre && ok; i += n_iss) {
       if (!mbar_wait(&wfull[i], 0u)) { *abort_flag = 1u; ok = false; break; }
       tc_fence_after();
       tc_cp_sf(tmem + sf_base + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
     }
     if (ok && !mbar_wait(xready, 0)) { *abort_flag = 1u; ok = false; }
     tc_fence_after();
-    for (int i = 0; i < ns && ok; ++i) {
+    for (int i = 0; i < ns && ok; i += n_iss) {
       const int stage = i % ring;
       const uint32_t sf = tmem + sf_base + static_cast<uint32_t>(i * 8);
       if (i >= pre) {
@@ -238,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t idesc = idesc_n | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-        tc_mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sf, sf + 4, (i | k) != 0 ? 1u : 0u);
+        tc_mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sf, sf + 4, (i | k) != 0 ? 1u : 0u);  // i = 0 first
       }
       if (i + ring < ns) tc_commit(&wempty[stage]);  // the producer refills this stage
     }
@@ -319,7 +368,26 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
     if (S > 1 && !p.own_recv) cluster_arrive_release();
     if (done) {
       tc_fence_after();
-      tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16), acc);
+      // the accumulator(s), 16 columns at a time: the first, plus the second
+      // issuer's in a fixed order (the result does not depend on M)
+      const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+#pragma unroll
+      for (int c0 = 0; c0 < kTok; c0 += 16) {
+        if (c0 < p.M) {
+          uint32_t t2[16];
+          tmem_ld16_async(tmem + lanes + static_cast<uint32_t>(c0), acc + c0);
+          if (n_iss == 2) tmem_ld16_async(tmem + lanes + static_cast<uint32_t>(nN + c0), t2);
+          tmem_wait_ld();
+          if (n_iss == 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[c0 + j] = __float_as_uint(__uint_as_float(acc[c0 + j]) + __uint_as_float(t2[j]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c0 + j] = 0u;
+        }
+      }
     } else {
       *abort_flag = 1u;
 #pragma unroll
@@ -471,7 +539,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
     const int keep = per_sm(alias) < 4 ? per_sm(alias) : 4;
     *own = p.splits > 1 && (a.force_recv ? a.force_recv == 2 : per_sm(sep) >= keep) ? 1 : 0;
     const int t = *own ? sep : alias;
-    const int tmem_cap = 512 / tmem_cols_for(a.M, steps);
+    const int tmem_cap = 512 / tmem_cols_for(a.M, p.KT, p.splits, p.ring);
     int cap = a.force_cap > 0 ? a.force_cap : (a.M <= kPushMaxM ? kMaxCtasPerSm : 4);
     if (cap > kMaxCtasPerSm) cap = kMaxCtasPerSm;
     if (cap > tmem_cap) cap = tmem_cap;
@@ -491,7 +559,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
     p.ring = steps < r ? steps : r;
   }
   const int smem = smem_for(p.ring, &p.own_recv);
-  p.tmem_cols = tmem_cols_for(a.M, steps);
+  p.tmem_cols = tmem_cols_for(a.M, p.KT, p.splits, p.ring);
   // per-thread pushes win only for few tokens spread over many owners
   p.bulk = (a.M > kPushMaxM || p.splits <= 2 || a.force_bulk) ? 1 : 0;
   if (steps > kMaxSteps || static_cast<size_t>(smem) > di.max_smem_optin)
