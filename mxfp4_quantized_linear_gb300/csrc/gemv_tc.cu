@@ -525,8 +525,9 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   const int steps = (p.KT + p.splits - 1) / p.splits;
   // Shared memory and CTAs per SM (measured on GB300): its own receive buffer
   // as long as that keeps min(4, what sharing the weight ring would keep)
-  // CTAs on an SM; five CTAs per SM for a few tokens, four above (the
-  // activation quantization of five co-resident CTAs then costs more than the
+  // CTAs on an SM; five CTAs per SM up to 16 tokens (N = 16 MMAs), four above
+  // (the two 32-column accumulators then take 128 tensor-memory columns, and
+  // the activation quantization of five co-resident CTAs costs more than the
   // extra overlap gains).  Never so little shared memory that more CTAs
   // would be resident than the tensor memory holds (their tcgen05.alloc
   // would wait on CTAs that may themselves wait on cluster peers) or than the
@@ -540,7 +541,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
     *own = p.splits > 1 && (a.force_recv ? a.force_recv == 2 : per_sm(sep) >= keep) ? 1 : 0;
     const int t = *own ? sep : alias;
     const int tmem_cap = 512 / tmem_cols_for(a.M, p.KT, p.splits, p.ring);
-    int cap = a.force_cap > 0 ? a.force_cap : (a.M <= kPushMaxM ? kMaxCtasPerSm : 4);
+    int cap = a.force_cap > 0 ? a.force_cap : (a.M <= 16 ? kMaxCtasPerSm : 4);
     if (cap > kMaxCtasPerSm) cap = kMaxCtasPerSm;
     if (cap > tmem_cap) cap = tmem_cap;
     const int floor_bytes = smem_sm / (cap + 1) - reserved + 16;  // cap + 1 CTAs never fit

@@ -480,7 +480,11 @@ constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? 
 // A third form for prefill when the weight has an even number of 128-row
 // tiles (kMoePair): each work item is two adjacent row tiles multiplied by
 // the same activation stage (8 MMAs a K step into two accumulators), so every
-// activation byte brought from L2 feeds twice the tensor work.  One CTA an SM
+// activation byte brought from L2 feeds twice the tensor work.  Each tile's
+// MMAs are issued by a thread of their own (warps 1 and 3): one thread issues
+// a block-scaled MMA only about every 150 cycles (measured on GB300), about
+// twice the tensor time of an M=128 N=128 K=32 MMA, so one issuer would leave
+// the tensor core idle half the time.  One CTA an SM
 // and 12 warps (8 epilogue warps, one a lane quarter of each accumulator); the
 // epilogue copies its accumulator quarter to registers and releases it before
 // the stores, so the next pass's MMAs overlap them.
@@ -507,7 +511,8 @@ struct MoeCfg {
   static constexpr int kBarBytes = ((2 * (kWStages + kXStages) + 2 * kAccBufs) * 8 + 8 + 255) & ~255;
   static constexpr int kSmem = kBarOff + kBarBytes + 1024;
   static constexpr uint32_t kAccCols = kBRows;
-  // tensor memory: the accumulator(s) | a (SFA 4 a tile, SFB 4) slot a weight stage
+  // tensor memory: the accumulator(s) | a (SFA 4 a tile, SFB 4 a tile) slot a
+  // weight stage (each tile's issuer copies its own SFB)
   static constexpr uint32_t kSfSlot = kATiles == 2 ? 16 : 8;
   static constexpr uint32_t kTmemCols = pow2_at_least(kAccBufs * kATiles * kAccCols + kSfSlot * kWStages);
   static constexpr uint32_t kIdesc = mxf8_idesc_a(128, kBRows, kFmtE2M1);
@@ -676,14 +681,14 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kWStages; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], 1);     // tcgen05.commit
+      mbar_init(&wempty[i], kT);    // tcgen05.commit of each tile's issuer
     }
     for (int i = 0; i < C::kXStages; ++i) {
       mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], 1);     // tcgen05.commit
+      mbar_init(&xempty[i], kT);    // tcgen05.commit of each tile's issuer
     }
     for (int i = 0; i < C::kAccBufs; ++i) {
-      mbar_init(&accfull[i], 1);    // tcgen05.commit
+      mbar_init(&accfull[i], kT);   // tcgen05.commit of each tile's issuer
       mbar_init(&accempty[i], C::kEpiWarps);  // one arrival an epilogue warp
     }
     *abort_flag = 0u;
@@ -768,8 +773,11 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if ((warp == 1 || (kT == 2 && warp == 3)) && lane == 0) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues tile 0's MMAs, warp 3 (two-tile items) tile 1's, each into
+    // its own accumulator with its own scale copies
+    const int t = warp == 1 ? 0 : 1;
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -787,23 +795,18 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
             break;
           }
           tc_fence_after();
-          // scale slot: SFA of each tile (4 columns each), then SFB
+          // scale slot: SFA of each tile (4 columns each), then SFB once a tile
           const uint32_t sfc = tmem + C::kAccBufs * kT * C::kAccCols + static_cast<uint32_t>(ws) * C::kSfSlot;
-          const uint32_t sfb = sfc + 4 * kT;
-#pragma unroll
-          for (int t = 0; t < kT; ++t)
-            tc_cp_sf(sfc + 4 * t, sf_desc(smem_u32(smem + C::kSfaOff + (ws * kT + t) * 512)));
+          const uint32_t sfb = sfc + 4 * kT + 4 * t;
+          tc_cp_sf(sfc + 4 * t, sf_desc(smem_u32(smem + C::kSfaOff + (ws * kT + t) * 512)));
           tc_cp_sf(sfb, sf_desc(smem_u32(smem + C::kSfbOff + xs * 512)));
           const uint64_t bdesc = sw128_desc(smem_u32(smem + C::kXOff + xs * C::kXStage));
+          const uint64_t adesc = sw128_desc(smem_u32(smem + C::kWOff + ws * C::kWStage + t * 16384));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t id = C::kIdesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
-#pragma unroll
-            for (int t = 0; t < kT; ++t) {
-              const uint64_t adesc = sw128_desc(smem_u32(smem + C::kWOff + ws * C::kWStage + t * 16384));
-              tc_mma_mxf8(acc + t * C::kAccCols, adesc + 2 * k, bdesc + 2 * k, id, sfc + 4 * t, sfb,
-                          (s != it.s0 || k != 0) ? 1u : 0u);
-            }
+            tc_mma_mxf8(acc + t * C::kAccCols, adesc + 2 * k, bdesc + 2 * k, id, sfc + 4 * t, sfb,
+                        (s != it.s0 || k != 0) ? 1u : 0u);
           }
           tc_commit(&wempty[ws]);
           tc_commit(&xempty[xs]);
