@@ -817,6 +817,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="print one JSON line per shape of the linear / MoE sweep instead of the step")
+    ap.add_argument("--case", default=None,
+                    choices=["mxf8_peak", "gemm_m4096", "moe_gate_up", "moe_expert", "moe_w4a8_prefill", "configs"],
+                    help="run only this secondary workload and print its JSON (e.g. to profile one kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()
@@ -826,6 +829,22 @@ def main():
         res = run_reference(args, ws, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+    if args.case:
+        if rank == 0:
+            import mxfp4_quantized_linear_gb300 as mx
+            from mxfp4_quantized_linear_gb300 import inputs
+            dev = torch.device("cuda", local)
+            torch.cuda.set_device(dev)
+            hbm_peak, bf16_peak, peak_kind = peaks()
+            stream = torch.cuda.Stream(dev)
+            fns = {"mxf8_peak": lambda: mx_peak(mx, stream),
+                   "gemm_m4096": lambda: bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind),
+                   "moe_gate_up": lambda: bench_moe(mx, inputs, dev, stream, hbm_peak),
+                   "moe_expert": lambda: bench_expert(mx, inputs, dev, stream, hbm_peak),
+                   "moe_w4a8_prefill": lambda: bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind),
+                   "configs": lambda: bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind)}
+            print(json.dumps({args.case: fns[args.case]()}), flush=True)
         return
     if args.sweep:
         if rank == 0:
