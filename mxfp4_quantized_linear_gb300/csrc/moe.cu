@@ -531,9 +531,10 @@ struct MoeParams {
   __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
   float* out_f32;          // kMoeOutF32: [T * topk, N]
   int N, KT, NT, E;
-  int ksplit;              // narrow passes: K ranges an item (1, or split-K into part)
+  int ksplit;              // narrow passes: at most this many K ranges an item (1: no split;
+                           // the count itself is moe_split_for of the active experts)
   int P;                   // T * topk
-  float* part;             // ksplit > 1: f32 partial sums [ksplit, P, N]
+  float* part;             // ksplit > 1: f32 partial sums [ranges, P, N]
   int lo;                  // 1: hi and lo activation pieces (A16), 0: hi only (MXFP8)
   int gate_up;             // weight rows interleaved gate / up in 8-row groups
   int out_mode;
@@ -547,8 +548,9 @@ MX_DEV int gate_up_row(int r, int N) {
 
 MX_DEV float silu_f32(float v) { return v / (1.0f + expf(-v)); }
 
-// Narrow passes: a work item is one group of `tiles` 128-row tiles of the
-// a-th active expert, all its passes of pairs (items a-major).  Wide passes
+// Narrow passes: a work item is one K range of one group of `tiles` 128-row
+// tiles of the a-th active expert, all its passes of pairs (items a-major,
+// the K range fastest).  Wide passes
 // (po = the experts' pass offsets): a work item is one pass of one tile group,
 // items expert-major, then tile group, then pass, so the CTAs that read the
 // same weight tiles for the passes of an expert run side by side and share
@@ -562,7 +564,7 @@ struct Item {
   int ks;        // ... the range's index
 };
 
-MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po) {
+MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po, int S) {
   Item it;
   const int nti = p.NT / tiles;  // tile groups an expert (tiles = 2 needs NT even)
   if (po) {
@@ -587,7 +589,8 @@ MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po
     return it;
   }
   // narrow: items (active expert, tile group, K range), the K range fastest
-  const int S = p.ksplit;
+  // (the ranges of a tile run side by side; numbered range-slowest instead, the
+  // E=256 K=7168 top-8 decode calls ran 7-14 % slower on GB300)
   const int a = i / (nti * S);
   const int rem = i - a * nti * S;
   const int g = rem / S, ks = rem - g * S;
@@ -619,17 +622,58 @@ MX_DEV void store_pair(const MoeParams& p, int pt, int n, int lane, float y) {
   }
 }
 
-// Split-K finish: each valid pair's output from the ksplit f32 partial sums
-// part [ksplit, P, N], added in range order (deterministic), in the pass's
-// output form.  Launched as a programmatic dependent of the expert GEMM; it
+// The K ranges an item of the narrow passes (1 .. kmax), from the number of
+// (active expert, row tile) items and the CTAs that walk them (slots): the
+// count that minimises the K steps of the busiest CTA, ceil(items S / slots)
+// ranges of at most ceil(KT / S) steps each, plus 0.5 % of an item for each
+// extra range (its accumulator switch, its partial sums and their final sum).
+// Each range is charged at the longest one's length: CTA b takes items b,
+// b + slots, ..., the K range fastest, so when slots is a multiple of S every
+// CTA keeps one range index and the longer ranges of an uneven split land on
+// the same CTAs.  Costs in 1/200 K steps; items * S and the rounds stay
+// within 32 bits (items <= 512 experts x 2^16 row tiles), a cost within 38.
+// The expert GEMM and the finishing kernel both evaluate it on the device from
+// the routing's count of active experts, so the host never needs that count:
+// one warp, lane S - 1 costing S, then a minimum over the lanes (ties to the
+// smaller S), so no thread runs a chain of divisions.
+MX_DEV int moe_split_for(unsigned items, unsigned slots, unsigned KT, int kmax, int lane) {
+  const unsigned S = static_cast<unsigned>(lane) + 1u;
+  unsigned long long key = ~0ull;
+  if (S <= static_cast<unsigned>(kmax)) {
+    const unsigned rounds = (items * S + slots - 1) / slots;
+    const unsigned long long c =
+        static_cast<unsigned long long>(rounds) * ((KT + S - 1) / S) * 200u + static_cast<unsigned long long>(KT) * (S - 1);
+    key = (c << 5) | static_cast<unsigned>(lane);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+    key = other < key ? other : key;
+  }
+  return static_cast<int>(key & 31u) + 1;
+}
+
+// Split-K finish: each valid pair's output from the S f32 partial sums
+// part [S, P, N] (S = moe_split_for of the active experts, as the GEMM chose),
+// added in range order (deterministic), in the pass's output form.  Launched as a programmatic dependent of the expert GEMM; it
 // never releases its own dependents early (the next call's routing rewrites
 // the pair list it reads).
-__global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part, int S, int P, int N,
-                                                         const int32_t* __restrict__ pairs,
+__global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part, int kmax,
+                                                         const int32_t* __restrict__ n_active, int NT, int KT,
+                                                         int slots,
+                                                         int P, int N, const int32_t* __restrict__ pairs,
                                                          const int32_t* __restrict__ n_valid, int out_mode,
                                                          int gate_up, __nv_bfloat16* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   pdl_wait_prior_grid();
+  __shared__ int s_split;
+  if (threadIdx.x < 32) {
+    const int split = moe_split_for(*n_active * NT, slots, KT, kmax, threadIdx.x);
+    if (threadIdx.x == 0) s_split = split;
+  }
+  __syncthreads();
+  const int S = s_split;
+  if (S == 1) return;  // the GEMM did not split K and wrote the outputs itself
   const int cols = out_mode == kMoeOutSwiglu ? N / 2 : N;
   const long long total = static_cast<long long>(*n_valid) * cols;
   const long long PN = static_cast<long long>(P) * N;
@@ -710,18 +754,29 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   const int* po = nullptr;
   if (kWide) {
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) po_s[e] = p.pass_off[e];
-    __syncthreads();
     po = po_s;
   }
-  // CTAs past the last item go straight to the exit
-  const int n_items = kWide ? po_s[p.E] * (p.NT / kT) : *p.n_active * (p.NT / kT) * p.ksplit;
+  // narrow passes: the K ranges an item, and the items (CTAs past the last
+  // item go straight to the exit)
+  __shared__ int s_items[2];
+  if (!kWide && warp == 0) {
+    const int na = *p.n_active;
+    const int split = p.ksplit == 1 ? 1 : moe_split_for(na * (p.NT / kT), gridDim.x, p.KT, p.ksplit, lane);
+    if (lane == 0) {
+      s_items[0] = split;
+      s_items[1] = na * (p.NT / kT) * split;
+    }
+  }
+  __syncthreads();
+  const int S = kWide ? 1 : s_items[0];
+  const int n_items = kWide ? po_s[p.E] * (p.NT / kT) : s_items[1];
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
     tma_prefetch_desc(&wmap);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po);
+      const Item it = item_at(p, i, tok, kT, po, S);
       // a weight tile read once streams past L2; read again (more than one
       // pass of pairs) it is kept
       const uint64_t pol = it.npass > 1 ? policy_evict_last() : policy_evict_first();
@@ -751,7 +806,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const uint32_t tx = kWide ? C::kBRows * 128 + 512 : C::kBRows * (128 + 16);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po);
+      const Item it = item_at(p, i, tok, kT, po, S);
       for (int ch = it.ch0; ch < it.ch0 + it.nch && !*abort_flag; ++ch) {
         const int row0 = it.o0 + ch * tok;
         for (int s = it.s0; s < it.s1; ++s, ++g) {
@@ -781,7 +836,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po);
+      const Item it = item_at(p, i, tok, kT, po, S);
       for (int ch = it.ch0; ch < it.ch0 + it.nch && ok; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;  // the epilogue drains the other accumulator (narrow)
         if (!mbar_wait(&accempty[buf], ((gp / C::kAccBufs) & 1u) ^ 1u)) { ok = false; break; }
@@ -822,7 +877,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(et) * C::kAccCols;
     int gp = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po);
+      const Item it = item_at(p, i, tok, kT, po, S);
       const int n = (it.rt + et) * 128 + q * 32 + lane;
       for (int ch = it.ch0; ch < it.ch0 + it.nch; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;
@@ -842,7 +897,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
 #pragma unroll
             for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[16 + t]));
           }
-          if (p.ksplit > 1) {
+          if (S > 1) {
             // split K: this K range's f32 sums; the finishing kernel adds the ranges
             float* part = p.part + static_cast<long long>(it.ks) * p.P * p.N + n;
 #pragma unroll
@@ -1009,26 +1064,10 @@ size_t moe_act_bytes(long long P, int Kp, int E) { return 2 * act_region(P, Kp) 
 
 // Split K of the narrow passes: at most kMaxKSplit ranges, for at most
 // kSplitMaxPairs pairs (the decode sizes whose few experts leave SM slots idle).
-constexpr int kMaxKSplit = 4, kSplitMaxPairs = 64;
+constexpr int kMaxKSplit = 8, kSplitMaxPairs = 64;
+static_assert(kMaxKSplit <= 32, "the split choice costs one count a lane");
 size_t moe_part_bytes(long long P, int N) {
   return P <= kSplitMaxPairs ? static_cast<size_t>(kMaxKSplit) * P * N * sizeof(float) : 0;
-}
-
-// The K ranges an item of the narrow passes: the count that minimises the
-// rounds of work items over the resident CTAs (slots), counting each extra
-// range as 8 % of an unsplit item (its pipeline fill, partial sums and the
-// finishing pass); items = an upper bound of the (expert, row tile) items.
-static int moe_ksplit(long long items, long long slots, int KT) {
-  int best_s = 1;
-  double best = static_cast<double>((items + slots - 1) / slots);
-  for (int S = 2; S <= kMaxKSplit && S <= KT; ++S) {
-    const double t = static_cast<double>((items * S + slots - 1) / slots) / S + 0.08 * (S - 1);
-    if (t < best - 1e-9) {
-      best = t;
-      best_s = S;
-    }
-  }
-  return best_s;
 }
 
 // Pairs a wide pass, or 0 for narrow passes: wide once the experts average at
@@ -1037,6 +1076,19 @@ int moe_wide_pass(long long P, int E, int lo) {
   const int pw = lo ? kWidePairsA16 : kWidePairsMx8;
   const long long experts = P < E ? P : E;
   return experts > 0 && P >= experts * (pw / 2) ? pw : 0;
+}
+
+// Persistent grid of the expert GEMM: kCtasPerSm CTAs an SM (what shared and
+// tensor memory allow), never more than the largest possible number of work
+// items (narrow: every one of the at most min(P, E) experts split into kmax
+// ranges; wide: one pass an item, the passes numbering at most P / pw + min(P, E)).
+template <int kMode>
+static int moe_grid(long long P, int E, int kmax, int NT, int pw, const DeviceInfo& di) {
+  using C = MoeCfg<kMode>;
+  const long long zmax = P < E ? P : E;
+  const long long items = (C::kWide ? P / pw + zmax : zmax * kmax) * (NT / C::kATiles);
+  const long long slots = static_cast<long long>(C::kCtasPerSm) * di.sm_count;
+  return static_cast<int>(items < slots ? items : slots);
 }
 
 template <int kMode>
@@ -1071,13 +1123,7 @@ static int launch_moe_gemm(const MoeLaunch& a, const MoeParams& p, uint8_t* xh, 
   static int smem_set[64];
   if (raise_smem_limit(reinterpret_cast<const void*>(moe_kernel<kMode>), C::kSmem, di, smem_set) != MX_OK)
     return MX_ERR_CUDA;
-  // persistent: kCtasPerSm CTAs an SM (what shared and tensor memory allow),
-  // never more than the largest possible number of work items
-  const long long zmax = P < w->E ? P : w->E;
-  // wide: one pass an item, and the experts' passes number at most P / pw + zmax
-  const long long items = (kWide ? P / a.wide_pass + zmax : zmax * p.ksplit) * (p.NT / C::kATiles);
-  const long long slots = static_cast<long long>(C::kCtasPerSm) * di.sm_count;
-  const int grid = static_cast<int>(items < slots ? items : slots);
+  const int grid = moe_grid<kMode>(P, w->E, p.ksplit, p.NT, a.wide_pass, di);
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
@@ -1142,10 +1188,8 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.P = static_cast<int>(P);
   p.ksplit = 1;
   if (!wide && a.part && a.part_bytes >= moe_part_bytes(P, w->N) && moe_part_bytes(P, w->N) > 0) {
-    DeviceInfo di;
-    if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
-    const long long zmax = P < w->E ? P : w->E;
-    p.ksplit = moe_ksplit(zmax * NT, static_cast<long long>(MoeCfg<kMoeNarrow>::kCtasPerSm) * di.sm_count, KT);
+    // ranges of at least two K steps; the count is chosen on the device
+    p.ksplit = KT / 2 < kMaxKSplit ? (KT / 2 > 1 ? KT / 2 : 1) : kMaxKSplit;
     p.part = static_cast<float*>(a.part);
   }
   p.lo = a.lo;
@@ -1154,15 +1198,18 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   if (!wide) {
     int rc = launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
     if (rc != MX_OK || p.ksplit == 1) return rc;
+    DeviceInfo di;
+    if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
+    const int slots = moe_grid<kMoeNarrow>(P, w->E, p.ksplit, NT, 0, di);
     // add the K ranges' partial sums (programmatic dependent of the GEMM)
     const long long total = P * static_cast<long long>(w->N);
     cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(total, 256)), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, moe_finish_kernel, static_cast<const float*>(p.part), p.ksplit, p.P, w->N,
-                           a.pairs, a.offsets + w->E, a.out_mode, p.gate_up, static_cast<__nv_bfloat16*>(a.out),
-                           static_cast<float*>(a.out_f32));
+    e = cudaLaunchKernelEx(&cfg, moe_finish_kernel, static_cast<const float*>(p.part), p.ksplit, a.n_active, NT,
+                           KT, slots, p.P, w->N, a.pairs, a.offsets + w->E, a.out_mode, p.gate_up,
+                           static_cast<__nv_bfloat16*>(a.out), static_cast<float*>(a.out_f32));
     if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe finish launch: %s", cudaGetErrorString(e));
     return MX_OK;
   }

@@ -450,6 +450,47 @@ def test_decode_split_k():
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("n_act", [1, 5, 19, 28, 56, 57, 58, 64])
+def test_decode_split_over_active_experts(n_act):
+    """The decode K split is chosen on the device from the number of active
+    experts: 64 pairs spread over exactly n_act experts (N = 1024, eight row
+    tiles an expert; K = 1024, eight K steps) reach every choice on a
+    152-SM part, unsplit ones among them (56 and 57 experts fill whole rounds
+    of resident CTAs), and one expert with four passes of pairs.  Both
+    activation forms against the oracle, per pair, the 1e-2 gate and the
+    per-element bound."""
+    from oracle.moe import moe_linear_w4a8
+    E, N, K, T, topk = 64, 1024, 1024, 8, 8
+    m = inputs.moe_gate_up(E=E, N=N, K=K, T=T, topk=topk, seed=300 + n_act)
+    rng = np.random.default_rng(n_act)
+    chosen = rng.permutation(E)[:n_act]
+    ids = torch.from_numpy(chosen[np.arange(T * topk) % n_act].reshape(T, topk).astype(np.int32))
+    dev = cuda_device()
+    ensure_built()
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    xv = bf16_np(m["x"])
+    idn = u8(ids)
+    r8 = moe_linear_w4a8(xv, idn, u8(m["w"]), u8(m["codes"]))
+    W = {int(e): dequant_values(u8(m["w"])[e], u8(m["codes"])[e], "e2m1", N, K) for e in chosen}
+    for form in ("a16w4", "w4a8"):
+        fn = mx.mxfp4_moe_linear if form == "a16w4" else mx.mxfp4_moe_linear_w4a8
+        status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+        y = fn(m["x"].to(dev), ids.to(dev), p, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        y = y.float().cpu().numpy()
+        c = 5e-5 if form == "a16w4" else 1e-5
+        for t in range(T):
+            a = xv[t] if form == "a16w4" else r8["A"][t]
+            for j in range(topk):
+                Wd = W[int(idn[t, j])]
+                ref = Wd @ a
+                err = normalized_error(y[t, j][None], ref[None], a[None], Wd)
+                assert err <= TOL, (form, t, j, err)
+                den = np.linalg.norm(Wd, axis=1) * np.linalg.norm(a)
+                assert np.all(np.abs(y[t, j] - ref) <= 2.0 ** -8 * np.abs(ref) + c * den), (form, t, j)
+
+
 def test_more_items_than_resident_ctas():
     """More (expert, row tile) items than resident CTAs (64 experts x 8 tiles
     over 3 CTAs an SM, a partly filled last round), ragged N and K, an invalid
