@@ -564,14 +564,27 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.n_active);
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.status);
   // routing (with pass offsets when the experts average enough pairs for wide
-  // passes), and zero rows for the pairs whose id is not a valid expert
-  const int pw = moe_wide_pass(static_cast<long long>(T) * topk, w->E, lo);
+  // passes), and zero rows for the pairs whose id is not a valid expert; at
+  // decode sizes the activation kernel routes
+  const long long P = static_cast<long long>(T) * topk;
+  const int pw = moe_wide_pass(P, w->E, lo);
   int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.pass_off);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + R.inv);
-  cudaError_t e = launch_route_many(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream,
-                                    out, w->N, pw ? pass_off : nullptr, pw, ws + R.route_tmp, inv);
-  if (e != cudaSuccess) return cuda_fail(e, "route launch");
   MoeLaunch a = {};
+  a.route_in_act = moe_route_in_act(P, w->E, lo);
+  if (a.route_in_act) {
+    a.route.offsets = offsets;
+    a.route.pairs = pairs;
+    a.route.active = active;
+    a.route.n_active = n_active;
+    a.route.dev_status = st;
+    a.route.zero_out = out;
+    a.route.zero_N = w->N;
+  } else {
+    cudaError_t e = launch_route_many(topk_ids, T, topk, w->E, counts, offsets, pairs, active, n_active, st, stream,
+                                      out, w->N, pw ? pass_off : nullptr, pw, ws + R.route_tmp, inv);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+  }
   a.x = x;
   a.T = T;
   a.topk = topk;
@@ -663,13 +676,26 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   int32_t* active = reinterpret_cast<int32_t*>(ws + R.route.active);
   int32_t* n_active = reinterpret_cast<int32_t*>(ws + R.route.n_active);
   int* st = dev_status ? dev_status : reinterpret_cast<int*>(ws + R.route.status);
-  const int pw = moe_wide_pass(static_cast<long long>(T) * topk, E, 1);
+  const long long P = static_cast<long long>(T) * topk;
+  const int pw = moe_wide_pass(P, E, 1);
   int32_t* pass_off = reinterpret_cast<int32_t*>(ws + R.route.pass_off);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + R.route.inv);
-  cudaError_t e = launch_route_many(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream,
-                                    nullptr, 0, pw ? pass_off : nullptr, pw, ws + R.route.route_tmp, inv);
-  if (e != cudaSuccess) return cuda_fail(e, "route launch");
+  cudaError_t e = cudaSuccess;
   MoeLaunch a = {};
+  // at decode sizes the gate / up activation kernel routes (the down
+  // projection then reads its routing)
+  a.route_in_act = moe_route_in_act(P, E, 1);
+  if (a.route_in_act) {
+    a.route.offsets = offsets;
+    a.route.pairs = pairs;
+    a.route.active = active;
+    a.route.n_active = n_active;
+    a.route.dev_status = st;
+  } else {
+    e = launch_route_many(topk_ids, T, topk, E, counts, offsets, pairs, active, n_active, st, stream, nullptr, 0,
+                          pw ? pass_off : nullptr, pw, ws + R.route.route_tmp, inv);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+  }
   a.wide_pass = pw;
   a.ids = topk_ids;
   a.pass_off = pass_off;
@@ -692,6 +718,7 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   a.out_mode = 1;
   a.out = ws + R.act;
   if ((rc = launch_moe(a, stream)) != MX_OK) return rc;
+  a.route_in_act = 0;
   // down projection: one activation row a pair, f32 [T * topk, H].  Launched
   // without programmatic dependent launch: letting its kernels start while the
   // gate/up GEMM drains cost ~6 us a call at E=64 I=2048 H=4096 T=64 (GB300)

@@ -338,6 +338,34 @@ __device__ __forceinline__ uint32_t mx_quant_f32x32(const float (&v)[32], uint4 
   return code;
 }
 
+// One 32-value block of a bf16 activation row as MXFP8 pieces: the hi piece
+// (qh, code ch) and, when lo, the residual x - hi quantized again (ql, cl).
+// Blocks past K (valid = false): zero bytes and code 127.
+MX_DEV void quant_pieces(const uint4 (&u)[4], bool valid, int lo, uint4 (&qh)[2], uint4 (&ql)[2], uint32_t& ch,
+                         uint32_t& cl) {
+  qh[0] = qh[1] = make_uint4(0u, 0u, 0u, 0u);
+  ql[0] = ql[1] = qh[0];
+  ch = 127u;
+  cl = 127u;
+  if (!valid) return;
+  ch = mx_quant_bf16x32(u, qh);
+  if (lo && ch != 255u) {
+    const float scale = e8m0_to_f32(ch);
+    const uint32_t hw[8] = {qh[0].x, qh[0].y, qh[0].z, qh[0].w, qh[1].x, qh[1].y, qh[1].z, qh[1].w};
+    const uint32_t xw[16] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w,
+                             u[2].x, u[2].y, u[2].z, u[2].w, u[3].x, u[3].y, u[3].z, u[3].w};
+    float r[32];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      // elements 2q, 2q + 1: bf16 -> f32 exactly, minus the dequantized hi piece
+      const __half2 h = e4m3x2_to_f16x2(static_cast<uint16_t>(hw[q >> 1] >> (16 * (q & 1))));
+      r[2 * q] = __uint_as_float(xw[q] << 16) - __low2float(h) * scale;
+      r[2 * q + 1] = __uint_as_float(xw[q] & 0xffff0000u) - __high2float(h) * scale;
+    }
+    cl = mx_quant_f32x32(r, ql);
+  }
+}
+
 // Rows past the routed pairs (slots with an invalid id are in no expert's
 // list, so the list holds *n_pairs <= P entries) are left as they are: they
 // only ever fill unused columns of a pass's last 32-row box.
@@ -345,20 +373,20 @@ __device__ __forceinline__ uint32_t mx_quant_f32x32(const float (&v)[32], uint4 
 // go to the scale-factor atom of the row's pass: row r of pass c of expert e
 // (r = its rank in the expert's list mod pw) is B row r (hi) and pw + r (lo),
 // byte (m % 32) * 16 + (m / 32) * 4 + kb of atom [pass_off[e] + c][K step].
-__global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pairs,
-                                  const int32_t* __restrict__ n_pairs, int P, int topk, int x_per_pair, int K,
-                                  int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl,
-                                  uint8_t* __restrict__ cs, const int32_t* __restrict__ ids,
-                                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ pass_off, int pw,
-                                  uint8_t* __restrict__ sfb, const int32_t* __restrict__ inv, int R) {
-  pdl_launch_dependents();
-  pdl_wait_prior_grid();  // the routing (and the activation, when a kernel wrote it) is complete
+// The pieces of every (sorted position, block) (inv == nullptr: pairs [nv]
+// lists the pair of each sorted position) or of every (activation row,
+// block) (inv: the sorted position of each pair), split over the grid.
+MX_DEV void act_pieces_body(const __nv_bfloat16* __restrict__ x, const int32_t* pairs, int nv, int P, int topk,
+                            int x_per_pair, int K, int Kp, int lo, uint8_t* __restrict__ xh,
+                            uint8_t* __restrict__ xl, uint8_t* __restrict__ cs, const int32_t* __restrict__ ids,
+                            const int32_t* __restrict__ offsets, const int32_t* __restrict__ pass_off, int pw,
+                            uint8_t* __restrict__ sfb, const int32_t* __restrict__ inv, int R) {
   const int KBp = Kp >> 5, KB = K >> 5, KT = Kp >> 7;
   // inv == nullptr: one thread a (sorted position, block), the position's
   // pair read from the list; else one thread a (activation row, block), the
   // row split once and written to every sorted position inv[] gives it
   const int fan = inv ? (x_per_pair ? 1 : topk) : 1;
-  const int nv = inv ? R : *n_pairs;
+  if (inv) nv = R;
   // 32-bit indices: the launcher checks P * Kp / 32 < 2^31
   const unsigned total = static_cast<unsigned>(inv ? R : (nv < P ? nv : P)) * static_cast<unsigned>(KBp);
   const int lane = threadIdx.x & 31;
@@ -377,29 +405,17 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
       const int pr = pairs[ru];
       src = x_per_pair ? pr : pr / topk;
     }
-    uint4 qh[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-    uint4 ql[2] = {qh[0], qh[1]};
-    uint32_t ch = 127u, cl = 127u;  // padded K blocks: zero bytes, a finite code
-    if (act && b < KB) {
+    uint4 u[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                  make_uint4(0u, 0u, 0u, 0u)};
+    const bool valid = act && b < KB;  // padded K blocks: zero bytes, a finite code
+    if (valid) {
       const uint4* sp = reinterpret_cast<const uint4*>(x + src * K + 32 * b);
-      const uint4 u[4] = {sp[0], sp[1], sp[2], sp[3]};
-      ch = mx_quant_bf16x32(u, qh);
-      if (lo && ch != 255u) {
-        const float scale = e8m0_to_f32(ch);
-        const uint32_t hw[8] = {qh[0].x, qh[0].y, qh[0].z, qh[0].w, qh[1].x, qh[1].y, qh[1].z, qh[1].w};
-        const uint32_t xw[16] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w,
-                                 u[2].x, u[2].y, u[2].z, u[2].w, u[3].x, u[3].y, u[3].z, u[3].w};
-        float r[32];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          // elements 2q, 2q + 1: bf16 -> f32 exactly, minus the dequantized hi piece
-          const __half2 h = e4m3x2_to_f16x2(static_cast<uint16_t>(hw[q >> 1] >> (16 * (q & 1))));
-          r[2 * q] = __uint_as_float(xw[q] << 16) - __low2float(h) * scale;
-          r[2 * q + 1] = __uint_as_float(xw[q] & 0xffff0000u) - __high2float(h) * scale;
-        }
-        cl = mx_quant_f32x32(r, ql);
-      }
+      for (int q = 0; q < 4; ++q) u[q] = sp[q];
     }
+    uint4 qh[2], ql[2];
+    uint32_t ch, cl;
+    quant_pieces(u, valid, lo, qh, ql, ch, cl);
     // the codes of blocks 4 g .. 4 g + 3 are 4 consecutive bytes of a scale
     // atom row (or of a code row): lane 4 g writes them as one word
     uint32_t wh = ch & 0xffu, wl = cl & 0xffu;
@@ -447,6 +463,123 @@ __global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int
   }
 }
 
+__global__ void act_pieces_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pairs,
+                                  const int32_t* __restrict__ n_pairs, int P, int topk, int x_per_pair, int K,
+                                  int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl,
+                                  uint8_t* __restrict__ cs, const int32_t* __restrict__ ids,
+                                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ pass_off, int pw,
+                                  uint8_t* __restrict__ sfb, const int32_t* __restrict__ inv, int R) {
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();  // the routing (and the activation, when a kernel wrote it) is complete
+  act_pieces_body(x, pairs, inv ? R : *n_pairs, P, topk, x_per_pair, K, Kp, lo, xh, xl, cs, ids, offsets, pass_off,
+                  pw, sfb, inv, R);
+}
+
+// Routing and activation pieces in one kernel for decode sizes (at most
+// kRoutePairs pairs, narrow passes): every CTA sorts the ids in shared memory
+// (the routing kernel's order: experts ascending, each expert's pairs in pair
+// order), CTA 0 publishes the routing the expert GEMM and the finishing kernel
+// read (offsets [E + 1], active, n_active, pairs, status) and zeroes the bf16
+// rows [zero_N] of the pairs whose id is not an expert, and every CTA writes
+// the pieces of its share of the sorted positions.  One launch less on the
+// decode chain: on GB300 (E=256 N=4096 K=7168 top-8, T=1) the separate
+// routing kernel kept the pieces waiting about 3.5 us.
+constexpr int kRoutePairs = 64;
+__global__ void __launch_bounds__(256) act_route_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int topk, const __nv_bfloat16* __restrict__ x, int x_per_pair,
+    int K, int Kp, int lo, uint8_t* __restrict__ xh, uint8_t* __restrict__ xl, uint8_t* __restrict__ cs,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ pairs, int32_t* __restrict__ active,
+    int32_t* __restrict__ n_active, int* dev_status, __nv_bfloat16* __restrict__ zero_out, int zero_N) {
+  __shared__ int r_ids[kRoutePairs], r_pairs[kRoutePairs], r_act[kRoutePairs], r_off[kRoutePairs + 1];
+  __shared__ unsigned r_bits[MX_MAX_EXPERTS / 32];
+  __shared__ int r_na;
+  pdl_launch_dependents();
+  // the ids and x are complete, and the previous call's kernels no longer read the routing
+  pdl_wait_prior_grid();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < MX_MAX_EXPERTS / 32) r_bits[tid] = 0u;
+  __syncthreads();
+  bool valid = false, bad = false;
+  if (tid < P) {
+    const int e = ids[tid];
+    valid = e >= 0 && e < E;
+    bad = !valid && e != -1;
+    r_ids[tid] = valid ? e : -1;
+    if (valid) atomicOr(&r_bits[e >> 5], 1u << (e & 31));
+  }
+  const int n_valid = __syncthreads_count(valid);
+  const int any_bad = __syncthreads_or(bad);
+  if (warp == 0) {
+    // the active experts in ascending order: lane l owns bit word l
+    unsigned wb = lane < (E + 31) / 32 ? r_bits[lane] : 0u;
+    const int c = __popc(wb);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int k = incl - c;
+    while (wb) {
+      r_act[k++] = lane * 32 + __ffs(wb) - 1;
+      wb &= wb - 1;
+    }
+    const int na = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      r_na = na;
+      r_off[na] = n_valid;
+    }
+  } else if (warp == 1 || warp == 2) {
+    // sorted position of pair q: the valid pairs of smaller experts, then the
+    // earlier pairs of its own
+    const int q = tid - 32;
+    if (q < P && r_ids[q] >= 0) {
+      const int eq = r_ids[q];
+      int below = 0, before = 0;
+      for (int j = 0; j < P; ++j) {
+        const int ej = r_ids[j];
+        below += (ej >= 0 && ej < eq) ? 1 : 0;
+        before += (j < q && ej == eq) ? 1 : 0;
+      }
+      r_pairs[below + before] = q;
+      if (before == 0) {
+        int a = __popc(r_bits[eq >> 5] & ((1u << (eq & 31)) - 1u));  // the expert's rank among the active
+        for (int wd = 0; wd < (eq >> 5); ++wd) a += __popc(r_bits[wd]);
+        r_off[a] = below;
+      }
+    }
+  }
+  __syncthreads();
+  const int na = r_na;
+  if (blockIdx.x == 0) {
+    // offsets[e]: the valid pairs of the experts below e
+    for (int e = tid; e <= E; e += blockDim.x) {
+      int a = 0;
+      for (int wd = 0; wd < (e >> 5); ++wd) a += __popc(r_bits[wd]);
+      if ((e & 31) && (e >> 5) < MX_MAX_EXPERTS / 32) a += __popc(r_bits[e >> 5] & ((1u << (e & 31)) - 1u));
+      offsets[e] = r_off[a];
+    }
+    for (int j = tid; j < n_valid; j += blockDim.x) pairs[j] = r_pairs[j];
+    for (int a = tid; a < na; a += blockDim.x) active[a] = r_act[a];
+    if (tid == 0) {
+      *n_active = na;
+      if (dev_status) *dev_status = any_bad ? MX_ERR_EXPERT_ID : MX_OK;
+    }
+    if (zero_out && warp == 7) {
+      for (int w0 = 0; w0 < P; w0 += 32) {
+        unsigned m = __ballot_sync(0xffffffffu, w0 + lane < P && r_ids[w0 + lane] < 0);
+        while (m) {
+          const int q = w0 + __ffs(m) - 1;
+          m &= m - 1;
+          for (int n = lane; n < zero_N; n += 32) zero_out[static_cast<long long>(q) * zero_N + n] = __float2bfloat16_rn(0.0f);
+        }
+      }
+    }
+  }
+  act_pieces_body(x, r_pairs, n_valid, P, topk, x_per_pair, K, Kp, lo, xh, xl, cs, nullptr, nullptr, nullptr, 0,
+                  nullptr, nullptr, 0);
+}
+
 // ---------------------------------------------------------------- expert GEMM
 //
 // Persistent CTAs walking (expert, 128-row tile) work items; 8 warps:
@@ -488,17 +621,26 @@ constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? 
 // and 12 warps (8 epilogue warps, one a lane quarter of each accumulator); the
 // epilogue copies its accumulator quarter to registers and releases it before
 // the stores, so the next pass's MMAs overlap them.
-constexpr int kMoeNarrow = 0, kMoeWide = 1, kMoePair = 2;
+//
+// A fourth form for decode (kMoeNarrow16, at most kSplitMaxPairs pairs): narrow
+// passes of 16 B rows (8 pairs with hi and lo, or 16 hi only).  Its 2 KB
+// activation stages leave room for four weight stages at three CTAs an SM
+// instead of three (E=256 N=4096 K=7168 top-8 on GB300: the expert kernel
+// alone 28.3 -> 26.9 us at T=1, calls 2-5 % faster at T=1..8).  Fewer,
+// deeper CTAs do not help: two CTAs an SM with five or six weight stages ran
+// 16-24 % slower, each CTA having one MMA issuer.
+constexpr int kMoeNarrow = 0, kMoeWide = 1, kMoePair = 2, kMoeNarrow16 = 3;
 
 template <int kMode>
 struct MoeCfg {
-  static constexpr bool kWide = kMode != kMoeNarrow;
+  static constexpr bool kNarrow = kMode == kMoeNarrow || kMode == kMoeNarrow16;
+  static constexpr bool kWide = !kNarrow;
   static constexpr int kATiles = kMode == kMoePair ? 2 : 1;    // 128-row weight tiles an item
-  static constexpr int kBRows = kWide ? 128 : 32;              // B rows a pass (MMA N)
-  static constexpr int kWStages = kMode == kMoePair ? 4 : 3;
-  static constexpr int kXStages = kMode == kMoeWide ? 3 : 5;  // the activation comes from L2
+  static constexpr int kBRows = kWide ? 128 : (kMode == kMoeNarrow16 ? 16 : 32);  // B rows a pass (MMA N)
+  static constexpr int kWStages = kMode == kMoePair || kMode == kMoeNarrow16 ? 4 : 3;
+  static constexpr int kXStages = kMode == kMoeNarrow || kMode == kMoePair ? 5 : 3;  // the activation comes from L2
   static constexpr int kAccBufs = kWide ? 1 : 2;
-  static constexpr int kCtasPerSm = kMode == kMoeNarrow ? 3 : (kMode == kMoeWide ? 2 : 1);
+  static constexpr int kCtasPerSm = kNarrow ? 3 : (kMode == kMoeWide ? 2 : 1);
   static constexpr int kThreads = kMode == kMoePair ? 384 : 256;
   static constexpr int kEpiWarps = 4 * kATiles;
   static constexpr int kWStage = kATiles * 128 * 128;         // e2m1 operand steps, 128B swizzle
@@ -507,9 +649,15 @@ struct MoeCfg {
   static constexpr int kXOff = kWOff + kWStages * kWStage;
   static constexpr int kSfaOff = kXOff + kXStages * kXStage;  // kATiles weight scale atoms a weight stage
   static constexpr int kSfbOff = kSfaOff + kWStages * kATiles * 512;  // an activation scale atom a stage
-  static constexpr int kBarOff = (kSfbOff + kXStages * 512 + 1023) & ~1023;
-  static constexpr int kBarBytes = ((2 * (kWStages + kXStages) + 2 * kAccBufs) * 8 + 8 + 255) & ~255;
-  static constexpr int kSmem = kBarOff + kBarBytes + 1024;
+  static constexpr int kBarOff = kSfbOff + kXStages * 512;
+  static constexpr int kNumBars = 2 * (kWStages + kXStages) + 2 * kAccBufs;
+  // tensor-memory slot, abort flag, the narrow passes' K ranges and items;
+  // then (wide) the experts' pass offsets.  No static shared memory: it is
+  // allocated in 1 KB units, and the four-stage decode form fits three CTAs an
+  // SM only without it.
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kPoOff = kMiscOff + 16;
+  static constexpr int kSmem = kPoOff + (kWide ? 4 * (MX_MAX_EXPERTS + 1) : 0) + 1024;  // + alignment slack
   static constexpr uint32_t kAccCols = kBRows;
   // tensor memory: the accumulator(s) | a (SFA 4 a tile, SFB 4 a tile) slot a
   // weight stage (each tile's issuer copies its own SFB)
@@ -719,8 +867,9 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   uint64_t* xempty = xfull + C::kXStages;
   uint64_t* accfull = xempty + C::kXStages;      // [kAccBufs]
   uint64_t* accempty = accfull + C::kAccBufs;    // [kAccBufs]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + C::kAccBufs);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  int* s_items = reinterpret_cast<int*>(tmem_slot + 2);  // narrow: [K ranges an item, items]
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kWStages; ++i) {
@@ -750,7 +899,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   pdl_wait_prior_grid();  // the routing and the activation pieces are complete
   // wide passes: the experts' pass offsets in shared memory (items are found by
   // a binary search over them)
-  __shared__ int po_s[kWide ? MX_MAX_EXPERTS + 1 : 1];
+  int* po_s = reinterpret_cast<int*>(smem + C::kPoOff);
   const int* po = nullptr;
   if (kWide) {
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) po_s[e] = p.pass_off[e];
@@ -758,7 +907,6 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   }
   // narrow passes: the K ranges an item, and the items (CTAs past the last
   // item go straight to the exit)
-  __shared__ int s_items[2];
   if (!kWide && warp == 0) {
     const int na = *p.n_active;
     const int split = p.ksplit == 1 ? 1 : moe_split_for(na * (p.NT / kT), gridDim.x, p.KT, p.ksplit, lane);
@@ -887,28 +1035,36 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
         tc_fence_after();
         const uint32_t acc = lane_base + static_cast<uint32_t>(buf * kT) * C::kAccCols;
         if (!kWide) {
-          uint32_t v[32];  // A16: columns 0..15 hi pieces, 16..31 lo pieces; MXFP8: 32 pairs
-          tmem_ld32(acc, v);
+          // A16: columns 0 .. kB/2 - 1 hi pieces, then their lo pieces; MXFP8: kB pairs
+          constexpr int kB = C::kBRows;
+          uint32_t v[kB];
+          if constexpr (kB == 32) {
+            tmem_ld32(acc, v);
+          } else {
+            tmem_ld16_async(acc, v);
+            tmem_wait_ld();
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&accempty[buf]);  // a later pass may overwrite it
           const int pr = lane < ntok ? prow[lane] : -1;
           if (p.lo) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[16 + t]));
+            for (int t = 0; t < kB / 2; ++t)
+              v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(v[kB / 2 + t]));
           }
           if (S > 1) {
             // split K: this K range's f32 sums; the finishing kernel adds the ranges
             float* part = p.part + static_cast<long long>(it.ks) * p.P * p.N + n;
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
+            for (int t = 0; t < kB; ++t) {
               if (t >= ntok) break;  // warp-uniform
               const int pt = __shfl_sync(0xffffffffu, pr, t);
               if (n < p.N) part[static_cast<long long>(pt) * p.N] = __uint_as_float(v[t]);
             }
           } else {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
+            for (int t = 0; t < kB; ++t) {
               if (t >= ntok) break;  // warp-uniform
               store_pair(p, __shfl_sync(0xffffffffu, pr, t), n, lane, __uint_as_float(v[t]));
             }
@@ -1070,6 +1226,8 @@ size_t moe_part_bytes(long long P, int N) {
   return P <= kSplitMaxPairs ? static_cast<size_t>(kMaxKSplit) * P * N * sizeof(float) : 0;
 }
 
+int moe_route_in_act(long long P, int E, int lo) { return P >= 1 && P <= kRoutePairs && moe_wide_pass(P, E, lo) == 0; }
+
 // Pairs a wide pass, or 0 for narrow passes: wide once the experts average at
 // least half a wide pass of pairs.
 int moe_wide_pass(long long P, int E, int lo) {
@@ -1163,12 +1321,24 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = &pdl;
   cfg.numAttrs = a.no_pdl ? 0 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, act_pieces_kernel, static_cast<const __nv_bfloat16*>(a.x),
-                                     static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
-                                     static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs,
-                                     static_cast<const int32_t*>(a.ids), static_cast<const int32_t*>(a.offsets),
-                                     static_cast<const int32_t*>(a.pass_off), a.wide_pass, wide ? sfb : nullptr,
-                                     static_cast<const int32_t*>(a.inv), static_cast<int>(R));
+  cudaError_t e;
+  if (a.route_in_act) {
+    // decode sizes: the routing made by the pieces kernel itself
+    if (!moe_route_in_act(P, w->E, a.lo) || !a.ids || !a.route.offsets || !a.route.pairs || !a.route.active ||
+        !a.route.n_active)
+      return set_error(MX_ERR_ARG, "routing in the activation kernel needs <= %d pairs and its outputs", kRoutePairs);
+    e = cudaLaunchKernelEx(&cfg, act_route_kernel, static_cast<const int32_t*>(a.ids), static_cast<int>(P), w->E,
+                           a.topk, static_cast<const __nv_bfloat16*>(a.x), a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs,
+                           a.route.offsets, a.route.pairs, a.route.active, a.route.n_active, a.route.dev_status,
+                           static_cast<__nv_bfloat16*>(a.route.zero_out), a.route.zero_N);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, act_pieces_kernel, static_cast<const __nv_bfloat16*>(a.x),
+                           static_cast<const int32_t*>(a.pairs), static_cast<const int32_t*>(a.offsets + w->E),
+                           static_cast<int>(P), a.topk, a.x_per_pair, w->K, Kp, a.lo, xh, xl, cs,
+                           static_cast<const int32_t*>(a.ids), static_cast<const int32_t*>(a.offsets),
+                           static_cast<const int32_t*>(a.pass_off), a.wide_pass, wide ? sfb : nullptr,
+                           static_cast<const int32_t*>(a.inv), static_cast<int>(R));
+  }
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "activation pieces launch: %s", cudaGetErrorString(e));
 
   MoeParams p = {};
@@ -1196,11 +1366,14 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
   if (!wide) {
-    int rc = launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
+    // decode sizes: the 16-row form (four weight stages a CTA)
+    const bool n16 = P <= kSplitMaxPairs;
+    int rc = n16 ? launch_moe_gemm<kMoeNarrow16>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
     if (rc != MX_OK || p.ksplit == 1) return rc;
     DeviceInfo di;
     if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
-    const int slots = moe_grid<kMoeNarrow>(P, w->E, p.ksplit, NT, 0, di);
+    const int slots = n16 ? moe_grid<kMoeNarrow16>(P, w->E, p.ksplit, NT, 0, di)
+                          : moe_grid<kMoeNarrow>(P, w->E, p.ksplit, NT, 0, di);
     // add the K ranges' partial sums (programmatic dependent of the GEMM)
     const long long total = P * static_cast<long long>(w->N);
     cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(total, 256)), 1, 1);

@@ -143,6 +143,13 @@ struct MoeLaunch {
   const int32_t* inv;          // [T * topk] sorted position of each pair (-1: invalid id), or null
   void* part;                  // split-K partial sums (moe_part_bytes), or null: no split
   size_t part_bytes;
+  int route_in_act;            // 1 (moe_route_in_act): the activation kernel routes ids itself and writes:
+  struct {
+    int32_t *offsets, *pairs, *active, *n_active;  // the routing, as mx_route_experts lays it out
+    int* dev_status;           // MX_OK / MX_ERR_EXPERT_ID, or null
+    void* zero_out;            // bf16 [P, zero_N] rows of invalid ids set to zero, or null
+    int zero_N;
+  } route;
 };
 size_t moe_act_bytes(long long P, int Kp, int E);
 // f32 partial sums of the split-K narrow passes for P pairs of N outputs (0: never split)
@@ -157,6 +164,8 @@ cudaError_t launch_route_many(const int32_t* ids, int T, int topk, int E, int32_
                               cudaStream_t stream, void* zero_out, int zero_N, int32_t* pass_off, int pw,
                               void* scratch, int32_t* inv);
 int moe_wide_pass(long long P, int E, int lo);
+// 1 when the activation kernel routes P pairs itself (at most 64 pairs, narrow passes)
+int moe_route_in_act(long long P, int E, int lo);
 int launch_moe(const MoeLaunch& a, cudaStream_t stream);
 unsigned int take_error_flags_moe();
 unsigned int take_error_flags_selftest();
