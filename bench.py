@@ -566,8 +566,17 @@ def bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind):
     linear_lines("MXFP8 sweep linear, 32x32 codes", inputs.decode_linear(K=8192, Ms=(1, 32, 256), N=7168),
                  (1, 32, 256), True)
 
+    lines += bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, (1, 8, 64))
+    torch.cuda.empty_cache()
+    return lines
+
+
+def bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, Ts):
+    """The sweep experts E=256 N=4096 K=7168 top-8 (A16W4) at the token counts
+    Ts, each timed as a graph of 32 back-to-back calls whose top-k ids rotate
+    over 16 draws, so consecutive calls touch different experts."""
+    lines = []
     E, N, K, topk = 256, 4096, 7168, 8
-    Ts = (1, 8, 64)
     m = inputs.moe_gate_up(E=E, N=N, K=K, T=max(Ts), topk=topk, device=dev)
     torch.cuda.synchronize()  # drawn on the default stream; packed and used on `stream`
     with torch.cuda.stream(stream):
@@ -593,7 +602,6 @@ def bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind):
                       "frac_hbm": round(gbs / hbm_peak, 4), "experts_touched": round(D, 2),
                       "l2": f"top-k ids rotate over {nsets} draws"})
     del p
-    torch.cuda.empty_cache()
     return lines
 
 
@@ -818,7 +826,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="print one JSON line per shape of the linear / MoE sweep instead of the step")
     ap.add_argument("--case", default=None,
-                    choices=["mxf8_peak", "gemm_m4096", "moe_gate_up", "moe_expert", "moe_w4a8_prefill", "configs"],
+                    choices=["mxf8_peak", "gemm_m4096", "moe_gate_up", "moe_expert", "moe_w4a8_prefill", "configs",
+                             "moe_decode"],
                     help="run only this secondary workload and print its JSON (e.g. to profile one kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -843,7 +852,8 @@ def main():
                    "moe_gate_up": lambda: bench_moe(mx, inputs, dev, stream, hbm_peak),
                    "moe_expert": lambda: bench_expert(mx, inputs, dev, stream, hbm_peak),
                    "moe_w4a8_prefill": lambda: bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind),
-                   "configs": lambda: bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind)}
+                   "configs": lambda: bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind),
+                   "moe_decode": lambda: bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, (1,))}
             print(json.dumps({args.case: fns[args.case]()}), flush=True)
         return
     if args.sweep:
