@@ -493,9 +493,11 @@ __global__ void __launch_bounds__(256) act_route_kernel(
   __shared__ int r_ids[kRoutePairs], r_pairs[kRoutePairs], r_act[kRoutePairs], r_off[kRoutePairs + 1];
   __shared__ unsigned r_bits[MX_MAX_EXPERTS / 32];
   __shared__ int r_na;
-  pdl_launch_dependents();
-  // the ids and x are complete, and the previous call's kernels no longer read the routing
+  // the ids and x are complete, and the previous call's kernels no longer read
+  // the routing; only then may the expert GEMM start (it reads the ids and
+  // the weights before its own dependency wait)
   pdl_wait_prior_grid();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < MX_MAX_EXPERTS / 32) r_bits[tid] = 0u;
   __syncthreads();
@@ -630,6 +632,7 @@ constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? 
 // deeper CTAs do not help: two CTAs an SM with five or six weight stages ran
 // 16-24 % slower, each CTA having one MMA issuer.
 constexpr int kMoeNarrow = 0, kMoeWide = 1, kMoePair = 2, kMoeNarrow16 = 3;
+constexpr int kEarlyPairs = 64;  // pairs the 16-row form can route itself (MoeParams::early)
 
 template <int kMode>
 struct MoeCfg {
@@ -657,7 +660,11 @@ struct MoeCfg {
   // SM only without it.
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kPoOff = kMiscOff + 16;
-  static constexpr int kSmem = kPoOff + (kWide ? 4 * (MX_MAX_EXPERTS + 1) : 0) + 1024;  // + alignment slack
+  // 16-row form routing itself (early): sorted pairs (u8), active experts
+  // (u16), their first sorted positions and the valid count (u8)
+  static constexpr int kEarlyOff = kPoOff + (kWide ? 4 * (MX_MAX_EXPERTS + 1) : 0);
+  static constexpr int kEarlyBytes = kMode == kMoeNarrow16 ? kEarlyPairs + 2 * kEarlyPairs + kEarlyPairs + 2 : 0;
+  static constexpr int kSmem = kEarlyOff + kEarlyBytes + 1024;  // + alignment slack
   static constexpr uint32_t kAccCols = kBRows;
   // tensor memory: the accumulator(s) | a (SFA 4 a tile, SFB 4 a tile) slot a
   // weight stage (each tile's issuer copies its own SFB)
@@ -676,6 +683,8 @@ struct MoeParams {
   const int32_t* active;
   const int32_t* n_active;
   const int32_t* pass_off; // wide: first pass of each expert [E + 1]
+  const int32_t* ids;      // early: the top-k ids [P]
+  int early;               // 16-row form: route from ids before the grid-dependency wait (see moe_kernel)
   __nv_bfloat16* out;      // kMoeOutBf16: [T * topk, N]; kMoeOutSwiglu: [T * topk, N / 2]
   float* out_f32;          // kMoeOutF32: [T * topk, N]
   int N, KT, NT, E;
@@ -755,6 +764,29 @@ MX_DEV Item item_at(const MoeParams& p, int i, int tok, int tiles, const int* po
   return it;
 }
 
+// 16-row form routing itself (early): item i as in item_at's narrow passes,
+// the expert and its pairs from the CTA's shared-memory tables (eact: the
+// active experts ascending; eoff: each one's first sorted position, then the
+// valid count).
+MX_DEV Item item_at_early(const MoeParams& p, int i, int tok, int S, const uint16_t* eact, const uint8_t* eoff) {
+  Item it;
+  const int nti = p.NT;
+  const int a = i / (nti * S);
+  const int rem = i - a * nti * S;
+  const int g = rem / S, ks = rem - g * S;
+  it.s0 = ks * p.KT / S;
+  it.s1 = (ks + 1) * p.KT / S;
+  it.ks = ks;
+  it.rt = g;
+  it.e = eact[a];
+  it.o0 = eoff[a];
+  it.cnt = eoff[a + 1] - it.o0;
+  it.nch = (it.cnt + tok - 1) / tok;
+  it.ch0 = 0;
+  it.npass = it.nch;
+  return it;
+}
+
 // One pair's output value y for weight row n (lane l of the warp holds row n).
 MX_DEV void store_pair(const MoeParams& p, int pt, int n, int lane, float y) {
   if (p.out_mode == kMoeOutSwiglu) {
@@ -803,9 +835,10 @@ MX_DEV int moe_split_for(unsigned items, unsigned slots, unsigned KT, int kmax, 
 
 // Split-K finish: each valid pair's output from the S f32 partial sums
 // part [S, P, N] (S = moe_split_for of the active experts, as the GEMM chose),
-// added in range order (deterministic), in the pass's output form.  Launched as a programmatic dependent of the expert GEMM; it
-// never releases its own dependents early (the next call's routing rewrites
-// the pair list it reads).
+// added in range order (deterministic), in the pass's output form.  Launched
+// as a programmatic dependent of the expert GEMM; it does not release its own
+// dependents early (measured on GB300: letting the next call's activation
+// kernel launch at once was no faster, T=1 28.1 -> 28.4 us).
 __global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part, int kmax,
                                                          const int32_t* __restrict__ n_active, int NT, int KT,
                                                          int slots,
@@ -896,7 +929,79 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   // the next kernel may start its prologue once every CTA holds its tensor
   // memory (a dependent grid then never takes columns this grid waits for)
   pdl_launch_dependents();
-  pdl_wait_prior_grid();  // the routing and the activation pieces are complete
+  // 16-row form, early: this grid starts only once the activation kernel
+  // before it has passed its own dependency wait, so the ids and the weights
+  // are complete; the routing is made here from the ids and the weights
+  // stream at once, and only the activation producer waits for the pieces
+  // (measured on GB300, E=256 N=4096 K=7168 top-8 T=1: the first weight stage
+  // had landed ~4 us after the wait, behind the routing's reads)
+  uint8_t* epairs = smem + C::kEarlyOff;                                        // [64]
+  uint16_t* eact = reinterpret_cast<uint16_t*>(smem + C::kEarlyOff + kEarlyPairs);  // [64]
+  uint8_t* eoff = smem + C::kEarlyOff + 3 * kEarlyPairs;                        // [65]
+  const bool early = kMode == kMoeNarrow16 && p.early;
+  int na_early = 0;
+  if (early) {
+    // the routing kernel's order, built in weight stage 0 (no TMA has written
+    // it yet): ids (-1: invalid) and the used experts' bit set, then the tables
+    int16_t* eids = reinterpret_cast<int16_t*>(smem + C::kWOff);
+    unsigned* ebits = reinterpret_cast<unsigned*>(smem + C::kWOff + 2 * kEarlyPairs);
+    if (threadIdx.x < MX_MAX_EXPERTS / 32) ebits[threadIdx.x] = 0u;
+    __syncthreads();
+    bool valid = false;
+    if (threadIdx.x < kEarlyPairs) {
+      const int e = threadIdx.x < p.P ? p.ids[threadIdx.x] : -1;
+      valid = e >= 0 && e < p.E;
+      eids[threadIdx.x] = static_cast<int16_t>(valid ? e : -1);
+      if (valid) atomicOr(&ebits[e >> 5], 1u << (e & 31));
+    }
+    const int n_valid = __syncthreads_count(valid);
+    if (warp == 0) {
+      // the active experts ascending: lane l owns bit word l
+      unsigned wb = lane < MX_MAX_EXPERTS / 32 ? ebits[lane] : 0u;
+      const int c = __popc(wb);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int k = incl - c;
+      while (wb) {
+        eact[k++] = static_cast<uint16_t>(lane * 32 + __ffs(wb) - 1);
+        wb &= wb - 1u;
+      }
+      if (lane == 31) eoff[incl] = static_cast<uint8_t>(n_valid);
+    } else if (warp == 1 || warp == 2) {
+      // pair q's sorted position: the valid pairs of smaller experts, then its
+      // expert's earlier pairs
+      const int q = threadIdx.x - 32;
+      const int eq = eids[q];
+      if (eq >= 0) {
+        int below = 0, before = 0;
+        for (int j = 0; j < p.P; ++j) {
+          const int ej = eids[j];
+          below += (ej >= 0 && ej < eq) ? 1 : 0;
+          before += (j < q && ej == eq) ? 1 : 0;
+        }
+        epairs[below + before] = static_cast<uint8_t>(q);
+        if (before == 0) {
+          int a = __popc(ebits[eq >> 5] & ((1u << (eq & 31)) - 1u));  // the expert's rank among the active
+          for (int wd = 0; wd < (eq >> 5); ++wd) a += __popc(ebits[wd]);
+          eoff[a] = static_cast<uint8_t>(below);
+        }
+      }
+    }
+    fence_proxy_async_smem();  // stage 0's temporaries before the weight TMA overwrites them
+    __syncthreads();
+    if (warp == 0) {
+      int na = lane < MX_MAX_EXPERTS / 32 ? __popc(ebits[lane]) : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) na += __shfl_xor_sync(0xffffffffu, na, o);
+      na_early = na;
+    }
+  } else {
+    pdl_wait_prior_grid();  // the routing and the activation pieces are complete
+  }
   // wide passes: the experts' pass offsets in shared memory (items are found by
   // a binary search over them)
   int* po_s = reinterpret_cast<int*>(smem + C::kPoOff);
@@ -908,7 +1013,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   // narrow passes: the K ranges an item, and the items (CTAs past the last
   // item go straight to the exit)
   if (!kWide && warp == 0) {
-    const int na = *p.n_active;
+    const int na = early ? na_early : *p.n_active;
     const int split = p.ksplit == 1 ? 1 : moe_split_for(na * (p.NT / kT), gridDim.x, p.KT, p.ksplit, lane);
     if (lane == 0) {
       s_items[0] = split;
@@ -918,13 +1023,16 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   __syncthreads();
   const int S = kWide ? 1 : s_items[0];
   const int n_items = kWide ? po_s[p.E] * (p.NT / kT) : s_items[1];
+  auto get_item = [&](int i) -> Item {
+    return early ? item_at_early(p, i, tok, S, eact, eoff) : item_at(p, i, tok, kT, po, S);
+  };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ weight producer
     tma_prefetch_desc(&wmap);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po, S);
+      const Item it = get_item(i);
       // a weight tile read once streams past L2; read again (more than one
       // pass of pairs) it is kept
       const uint64_t pol = it.npass > 1 ? policy_evict_last() : policy_evict_first();
@@ -947,6 +1055,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     }
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------------------ activation producer
+    if (early) pdl_wait_prior_grid();  // the activation pieces are complete
     tma_prefetch_desc(&xhmap);
     if (!kWide) tma_prefetch_desc(&csmap);
     if (p.lo) tma_prefetch_desc(&xlmap);
@@ -954,7 +1063,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const uint32_t tx = kWide ? C::kBRows * 128 + 512 : C::kBRows * (128 + 16);
     int g = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po, S);
+      const Item it = get_item(i);
       for (int ch = it.ch0; ch < it.ch0 + it.nch && !*abort_flag; ++ch) {
         const int row0 = it.o0 + ch * tok;
         for (int s = it.s0; s < it.s1; ++s, ++g) {
@@ -984,7 +1093,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     int gw = 0, gx = 0, gp = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po, S);
+      const Item it = get_item(i);
       for (int ch = it.ch0; ch < it.ch0 + it.nch && ok; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;  // the epilogue drains the other accumulator (narrow)
         if (!mbar_wait(&accempty[buf], ((gp / C::kAccBufs) & 1u) ^ 1u)) { ok = false; break; }
@@ -1025,7 +1134,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(et) * C::kAccCols;
     int gp = 0;
     for (int i = blockIdx.x; i < n_items && !*abort_flag; i += gridDim.x) {
-      const Item it = item_at(p, i, tok, kT, po, S);
+      const Item it = get_item(i);
       const int n = (it.rt + et) * 128 + q * 32 + lane;
       for (int ch = it.ch0; ch < it.ch0 + it.nch; ++ch, ++gp) {
         const int buf = gp % C::kAccBufs;
@@ -1047,7 +1156,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&accempty[buf]);  // a later pass may overwrite it
-          const int pr = lane < ntok ? prow[lane] : -1;
+          const int pr = lane >= ntok ? -1 : (early ? epairs[it.o0 + ch * tok + lane] : prow[lane]);
           if (p.lo) {
 #pragma unroll
             for (int t = 0; t < kB / 2; ++t)
@@ -1222,6 +1331,7 @@ size_t moe_act_bytes(long long P, int Kp, int E) { return 2 * act_region(P, Kp) 
 // kSplitMaxPairs pairs (the decode sizes whose few experts leave SM slots idle).
 constexpr int kMaxKSplit = 8, kSplitMaxPairs = 64;
 static_assert(kMaxKSplit <= 32, "the split choice costs one count a lane");
+static_assert(kEarlyPairs >= kSplitMaxPairs && kEarlyPairs == 64, "the 16-row form routes its pairs with two ballots");
 size_t moe_part_bytes(long long P, int N) {
   return P <= kSplitMaxPairs ? static_cast<size_t>(kMaxKSplit) * P * N * sizeof(float) : 0;
 }
@@ -1366,8 +1476,12 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
   p.out_mode = a.out_mode;
   if (!wide) {
-    // decode sizes: the 16-row form (four weight stages a CTA)
+    // decode sizes: the 16-row form (four weight stages a CTA), routing itself
+    // from the ids before its dependency wait when the kernel before it has
+    // waited for its own (act_route_kernel) or no early start is asked for
     const bool n16 = P <= kSplitMaxPairs;
+    p.ids = a.ids;
+    p.early = n16 && P <= kEarlyPairs && a.ids && (a.route_in_act || a.no_pdl) ? 1 : 0;
     int rc = n16 ? launch_moe_gemm<kMoeNarrow16>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
     if (rc != MX_OK || p.ksplit == 1) return rc;
     DeviceInfo di;
