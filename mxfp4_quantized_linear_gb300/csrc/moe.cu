@@ -641,7 +641,14 @@ struct MoeCfg {
   static constexpr int kATiles = kMode == kMoePair ? 2 : 1;    // 128-row weight tiles an item
   static constexpr int kBRows = kWide ? 128 : (kMode == kMoeNarrow16 ? 16 : 32);  // B rows a pass (MMA N)
   static constexpr int kWStages = kMode == kMoePair || kMode == kMoeNarrow16 ? 4 : 3;
-  static constexpr int kXStages = kMode == kMoeNarrow || kMode == kMoePair ? 5 : 3;  // the activation comes from L2
+  static constexpr int kXStages = kMode == kMoeNarrow ? 5 : (kMode == kMoePair ? 4 : 3);  // the activation comes from L2
+  // Equal ring depths: one stage-empty barrier serves both rings, so an
+  // issuer makes one tcgen05.commit a K step instead of two.  Each tcgen05
+  // instruction costs the single issuing thread issue time, and that time is
+  // what bounds the prefill forms (measured on GB300, E=64 N=K=4096 T=4096
+  // top-8: W4A8 572 -> 509 us, A16W4 1040 -> 905 us, the two-tile form going
+  // from 5 activation stages to 4 for it).
+  static constexpr bool kSharedEmpty = kWStages == kXStages;
   static constexpr int kAccBufs = kWide ? 1 : 2;
   static constexpr int kCtasPerSm = kNarrow ? 3 : (kMode == kMoeWide ? 2 : 1);
   static constexpr int kThreads = kMode == kMoePair ? 384 : 256;
@@ -897,8 +904,9 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* wempty = wfull + C::kWStages;
   uint64_t* xfull = wempty + C::kWStages;
-  uint64_t* xempty = xfull + C::kXStages;
-  uint64_t* accfull = xempty + C::kXStages;      // [kAccBufs]
+  uint64_t* xempty_own = xfull + C::kXStages;
+  uint64_t* xempty = C::kSharedEmpty ? wempty : xempty_own;  // the stage-empty barriers the x producer waits on
+  uint64_t* accfull = xempty_own + C::kXStages;  // [kAccBufs]
   uint64_t* accempty = accfull + C::kAccBufs;    // [kAccBufs]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -911,7 +919,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     }
     for (int i = 0; i < C::kXStages; ++i) {
       mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], kT);    // tcgen05.commit of each tile's issuer
+      if (!C::kSharedEmpty) mbar_init(&xempty[i], kT);  // tcgen05.commit of each tile's issuer
     }
     for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&accfull[i], kT);   // tcgen05.commit of each tile's issuer
@@ -1120,8 +1128,8 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
             tc_mma_mxf8(acc + t * C::kAccCols, adesc + 2 * k, bdesc + 2 * k, id, sfc + 4 * t, sfb,
                         (s != it.s0 || k != 0) ? 1u : 0u);
           }
-          tc_commit(&wempty[ws]);
-          tc_commit(&xempty[xs]);
+          tc_commit(&wempty[ws]);  // with kSharedEmpty also the activation stage (ws == xs)
+          if (!C::kSharedEmpty) tc_commit(&xempty[xs]);
         }
         if (ok) tc_commit(&accfull[buf]);
       }
