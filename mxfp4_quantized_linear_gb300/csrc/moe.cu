@@ -624,7 +624,8 @@ constexpr uint32_t pow2_at_least(uint32_t v, uint32_t c = 32) { return c >= v ? 
 // epilogue copies its accumulator quarter to registers and releases it before
 // the stores, so the next pass's MMAs overlap them.
 //
-// A fourth form for decode (kMoeNarrow16, at most kSplitMaxPairs pairs): narrow
+// A fourth form for decode (kMoeNarrow16: at most kSplitMaxPairs pairs, or few
+// pairs an expert): narrow
 // passes of 16 B rows (8 pairs with hi and lo, or 16 hi only).  Its 2 KB
 // activation stages leave room for four weight stages at three CTAs an SM
 // instead of three (E=256 N=4096 K=7168 top-8 on GB300: the expert kernel
@@ -1487,7 +1488,11 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
     // decode sizes: the 16-row form (four weight stages a CTA), routing itself
     // from the ids before its dependency wait when the kernel before it has
     // waited for its own (act_route_kernel) or no early start is asked for
-    const bool n16 = P <= kSplitMaxPairs;
+    // also above the decode sizes while the experts average at most half a
+    // 16-row pass of pairs (measured on GB300, E=64 N=K=4096 top-8: A16W4 T=16
+    // 89.3 -> 82.4 us, T=32 100.8 -> 98.8; MXFP8 T=16 / 32 / 64 -8 / -6.5 /
+    // -3 %; A16W4 T=64, 8 pairs an expert, +46 % from the second passes)
+    const bool n16 = P <= kSplitMaxPairs || 2 * P <= static_cast<long long>(w->E) * (16 >> a.lo);
     p.ids = a.ids;
     p.early = n16 && P <= kEarlyPairs && a.ids && (a.route_in_act || a.no_pdl) ? 1 : 0;
     int rc = n16 ? launch_moe_gemm<kMoeNarrow16>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
