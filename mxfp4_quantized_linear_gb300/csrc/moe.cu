@@ -642,13 +642,14 @@ struct MoeCfg {
   static constexpr int kATiles = kMode == kMoePair ? 2 : 1;    // 128-row weight tiles an item
   static constexpr int kBRows = kWide ? 128 : (kMode == kMoeNarrow16 ? 16 : 32);  // B rows a pass (MMA N)
   static constexpr int kWStages = kMode == kMoePair || kMode == kMoeNarrow16 ? 4 : 3;
-  static constexpr int kXStages = kMode == kMoeNarrow ? 5 : (kMode == kMoePair ? 4 : 3);  // the activation comes from L2
+  static constexpr int kXStages = kMode == kMoePair ? 4 : 3;  // the activation comes from L2
   // Equal ring depths: one stage-empty barrier serves both rings, so an
   // issuer makes one tcgen05.commit a K step instead of two.  Each tcgen05
   // instruction costs the single issuing thread issue time, and that time is
   // what bounds the prefill forms (measured on GB300, E=64 N=K=4096 T=4096
   // top-8: W4A8 572 -> 509 us, A16W4 1040 -> 905 us, the two-tile form going
-  // from 5 activation stages to 4 for it).
+  // from 5 activation stages to 4 for it; the 32-row narrow form from 5 to 3:
+  // A16W4 T=64 101.6 -> 99.7 us).
   static constexpr bool kSharedEmpty = kWStages == kXStages;
   static constexpr int kAccBufs = kWide ? 1 : 2;
   static constexpr int kCtasPerSm = kNarrow ? 3 : (kMode == kMoeWide ? 2 : 1);
