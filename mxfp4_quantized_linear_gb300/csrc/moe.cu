@@ -643,14 +643,17 @@ struct MoeCfg {
   static constexpr int kBRows = kWide ? 128 : (kMode == kMoeNarrow16 ? 16 : 32);  // B rows a pass (MMA N)
   static constexpr int kWStages = kMode == kMoePair || kMode == kMoeNarrow16 ? 4 : 3;
   static constexpr int kXStages = kMode == kMoePair ? 4 : 3;  // the activation comes from L2
-  // Equal ring depths: one stage-empty barrier serves both rings, so an
+  // The weight ring's stage-empty barriers also free the activation stages:
+  // activation stage g % X is free once the MMAs of step g - X completed,
+  // which is phase (g - X) / W of weight barrier (g - X) % W (with X <= W it
+  // cannot have run a phase further: that needs step g's activation).  So an
   // issuer makes one tcgen05.commit a K step instead of two.  Each tcgen05
   // instruction costs the single issuing thread issue time, and that time is
   // what bounds the prefill forms (measured on GB300, E=64 N=K=4096 T=4096
   // top-8: W4A8 572 -> 509 us, A16W4 1040 -> 905 us, the two-tile form going
   // from 5 activation stages to 4 for it; the 32-row narrow form from 5 to 3:
   // A16W4 T=64 101.6 -> 99.7 us).
-  static constexpr bool kSharedEmpty = kWStages == kXStages;
+  static_assert(kXStages <= kWStages, "activation stages are freed through the weight ring's barriers");
   static constexpr int kAccBufs = kWide ? 1 : 2;
   static constexpr int kCtasPerSm = kNarrow ? 3 : (kMode == kMoeWide ? 2 : 1);
   static constexpr int kThreads = kMode == kMoePair ? 384 : 256;
@@ -662,7 +665,7 @@ struct MoeCfg {
   static constexpr int kSfaOff = kXOff + kXStages * kXStage;  // kATiles weight scale atoms a weight stage
   static constexpr int kSfbOff = kSfaOff + kWStages * kATiles * 512;  // an activation scale atom a stage
   static constexpr int kBarOff = kSfbOff + kXStages * 512;
-  static constexpr int kNumBars = 2 * (kWStages + kXStages) + 2 * kAccBufs;
+  static constexpr int kNumBars = 2 * kWStages + kXStages + 2 * kAccBufs;  // w full, w empty, x full, acc full, acc empty
   // tensor-memory slot, abort flag, the narrow passes' K ranges and items;
   // then (wide) the experts' pass offsets.  No static shared memory: it is
   // allocated in 1 KB units, and the four-stage decode form fits three CTAs an
@@ -906,9 +909,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* wempty = wfull + C::kWStages;
   uint64_t* xfull = wempty + C::kWStages;
-  uint64_t* xempty_own = xfull + C::kXStages;
-  uint64_t* xempty = C::kSharedEmpty ? wempty : xempty_own;  // the stage-empty barriers the x producer waits on
-  uint64_t* accfull = xempty_own + C::kXStages;  // [kAccBufs]
+  uint64_t* accfull = xfull + C::kXStages;       // [kAccBufs]
   uint64_t* accempty = accfull + C::kAccBufs;    // [kAccBufs]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -919,10 +920,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], kT);    // tcgen05.commit of each tile's issuer
     }
-    for (int i = 0; i < C::kXStages; ++i) {
-      mbar_init(&xfull[i], 1);
-      if (!C::kSharedEmpty) mbar_init(&xempty[i], kT);  // tcgen05.commit of each tile's issuer
-    }
+    for (int i = 0; i < C::kXStages; ++i) mbar_init(&xfull[i], 1);
     for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&accfull[i], kT);   // tcgen05.commit of each tile's issuer
       mbar_init(&accempty[i], C::kEpiWarps);  // one arrival an epilogue warp
@@ -1078,7 +1076,12 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
         const int row0 = it.o0 + ch * tok;
         for (int s = it.s0; s < it.s1; ++s, ++g) {
           const int st = g % C::kXStages;
-          if (!mbar_wait(&xempty[st], ((g / C::kXStages) & 1u) ^ 1u)) { *abort_flag = 1u; break; }
+          // the MMAs of step g - X have completed (weight ring barrier of that step)
+          if (g >= C::kXStages &&
+              !mbar_wait(&wempty[(g - C::kXStages) % C::kWStages], ((g - C::kXStages) / C::kWStages) & 1u)) {
+            *abort_flag = 1u;
+            break;
+          }
           uint8_t* dst = smem + C::kXOff + st * C::kXStage;
           uint8_t* atom = smem + C::kSfbOff + st * 512;
           mbar_arrive_expect_tx(&xfull[st], tx);
@@ -1130,8 +1133,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
             tc_mma_mxf8(acc + t * C::kAccCols, adesc + 2 * k, bdesc + 2 * k, id, sfc + 4 * t, sfb,
                         (s != it.s0 || k != 0) ? 1u : 0u);
           }
-          tc_commit(&wempty[ws]);  // with kSharedEmpty also the activation stage (ws == xs)
-          if (!C::kSharedEmpty) tc_commit(&xempty[xs]);
+          tc_commit(&wempty[ws]);  // frees this step's weight stage and (X steps on) its activation stage
         }
         if (ok) tc_commit(&accfull[buf]);
       }
