@@ -600,6 +600,7 @@ static int moe_linear_impl(int lo, const char* name, const void* x, const int32_
   a.act_bytes = R.act_bytes;
   a.part = ws + R.part;
   a.part_bytes = R.part_bytes;
+  a.split_slot = n_active + 1;  // the n_active slot is 16 bytes
   a.wide_pass = pw;
   a.ids = topk_ids;
   a.pass_off = pass_off;
@@ -707,6 +708,7 @@ int mxfp4_moe_expert(const void* x, const int32_t* topk_ids, const float* topk_w
   a.act_bytes = R.route.act_bytes;
   a.part = ws + R.route.part;
   a.part_bytes = R.route.part_bytes;
+  a.split_slot = n_active + 1;  // the n_active slot is 16 bytes
   a.offsets = offsets;
   a.pairs = pairs;
   a.active = active;

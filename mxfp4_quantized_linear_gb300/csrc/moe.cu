@@ -704,6 +704,7 @@ struct MoeParams {
                            // the count itself is moe_split_for of the active experts)
   int P;                   // T * topk
   float* part;             // ksplit > 1: f32 partial sums [ranges, P, N]
+  int32_t* split_out;      // ksplit > 1: CTA 0 writes the K ranges it chose here (for the finishing kernel)
   int lo;                  // 1: hi and lo activation pieces (A16), 0: hi only (MXFP8)
   int gate_up;             // weight rows interleaved gate / up in 8-row groups
   int out_mode;
@@ -846,26 +847,20 @@ MX_DEV int moe_split_for(unsigned items, unsigned slots, unsigned KT, int kmax, 
 }
 
 // Split-K finish: each valid pair's output from the S f32 partial sums
-// part [S, P, N] (S = moe_split_for of the active experts, as the GEMM chose),
+// part [S, P, N] (S = moe_split_for of the active experts, read from where the
+// GEMM wrote it),
 // added in range order (deterministic), in the pass's output form.  Launched
 // as a programmatic dependent of the expert GEMM; it does not release its own
 // dependents early (measured on GB300: letting the next call's activation
 // kernel launch at once was no faster, T=1 28.1 -> 28.4 us).
-__global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part, int kmax,
-                                                         const int32_t* __restrict__ n_active, int NT, int KT,
-                                                         int slots,
-                                                         int P, int N, const int32_t* __restrict__ pairs,
+__global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part,
+                                                         const int32_t* __restrict__ split, int P, int N,
+                                                         const int32_t* __restrict__ pairs,
                                                          const int32_t* __restrict__ n_valid, int out_mode,
                                                          int gate_up, __nv_bfloat16* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   pdl_wait_prior_grid();
-  __shared__ int s_split;
-  if (threadIdx.x < 32) {
-    const int split = moe_split_for(*n_active * NT, slots, KT, kmax, threadIdx.x);
-    if (threadIdx.x == 0) s_split = split;
-  }
-  __syncthreads();
-  const int S = s_split;
+  const int S = *split;  // the count the GEMM chose (its CTA 0 wrote it)
   if (S == 1) return;  // the GEMM did not split K and wrote the outputs itself
   const int cols = out_mode == kMoeOutSwiglu ? N / 2 : N;
   const long long total = static_cast<long long>(*n_valid) * cols;
@@ -1024,6 +1019,7 @@ __global__ void __launch_bounds__(MoeCfg<kMode>::kThreads, MoeCfg<kMode>::kCtasP
     const int na = early ? na_early : *p.n_active;
     const int split = p.ksplit == 1 ? 1 : moe_split_for(na * (p.NT / kT), gridDim.x, p.KT, p.ksplit, lane);
     if (lane == 0) {
+      if (p.ksplit > 1 && blockIdx.x == 0) *p.split_out = split;
       s_items[0] = split;
       s_items[1] = na * (p.NT / kT) * split;
     }
@@ -1479,10 +1475,11 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
   p.E = w->E;
   p.P = static_cast<int>(P);
   p.ksplit = 1;
-  if (!wide && a.part && a.part_bytes >= moe_part_bytes(P, w->N) && moe_part_bytes(P, w->N) > 0) {
+  if (!wide && a.part && a.split_slot && a.part_bytes >= moe_part_bytes(P, w->N) && moe_part_bytes(P, w->N) > 0) {
     // ranges of at least two K steps; the count is chosen on the device
     p.ksplit = KT / 2 < kMaxKSplit ? (KT / 2 > 1 ? KT / 2 : 1) : kMaxKSplit;
     p.part = static_cast<float*>(a.part);
+    p.split_out = a.split_slot;
   }
   p.lo = a.lo;
   p.gate_up = w->layout == MX_LAYOUT_GATE_UP ? 1 : 0;
@@ -1500,19 +1497,15 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
     p.early = n16 && P <= kEarlyPairs && a.ids && (a.route_in_act || a.no_pdl) ? 1 : 0;
     int rc = n16 ? launch_moe_gemm<kMoeNarrow16>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
     if (rc != MX_OK || p.ksplit == 1) return rc;
-    DeviceInfo di;
-    if (current_device_info(&di) != MX_OK) return MX_ERR_CUDA;
-    const int slots = n16 ? moe_grid<kMoeNarrow16>(P, w->E, p.ksplit, NT, 0, di)
-                          : moe_grid<kMoeNarrow>(P, w->E, p.ksplit, NT, 0, di);
     // add the K ranges' partial sums (programmatic dependent of the GEMM)
     const long long total = P * static_cast<long long>(w->N);
     cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(total, 256)), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, moe_finish_kernel, static_cast<const float*>(p.part), p.ksplit, a.n_active, NT,
-                           KT, slots, p.P, w->N, a.pairs, a.offsets + w->E, a.out_mode, p.gate_up,
-                           static_cast<__nv_bfloat16*>(a.out), static_cast<float*>(a.out_f32));
+    e = cudaLaunchKernelEx(&cfg, moe_finish_kernel, static_cast<const float*>(p.part),
+                           static_cast<const int32_t*>(a.split_slot), p.P, w->N, a.pairs, a.offsets + w->E,
+                           a.out_mode, p.gate_up, static_cast<__nv_bfloat16*>(a.out), static_cast<float*>(a.out_f32));
     if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "moe finish launch: %s", cudaGetErrorString(e));
     return MX_OK;
   }

@@ -143,6 +143,7 @@ struct MoeLaunch {
   const int32_t* inv;          // [T * topk] sorted position of each pair (-1: invalid id), or null
   void* part;                  // split-K partial sums (moe_part_bytes), or null: no split
   size_t part_bytes;
+  int32_t* split_slot;         // split K: one int the GEMM writes its K-range count to (the finish reads it)
   int route_in_act;            // 1 (moe_route_in_act): the activation kernel routes ids itself and writes:
   struct {
     int32_t *offsets, *pairs, *active, *n_active;  // the routing, as mx_route_experts lays it out
