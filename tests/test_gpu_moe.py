@@ -491,6 +491,24 @@ def test_decode_split_over_active_experts(n_act):
                 assert np.all(np.abs(y[t, j] - ref) <= 2.0 ** -8 * np.abs(ref) + c * den), (form, t, j)
 
 
+@pytest.mark.parametrize("T", [9, 32])
+def test_sixteen_row_form_above_decode_sizes(T):
+    """More than 64 pairs on experts that average at most half a 16-row pass
+    (E=64, top-8, T=9 or 32: 72 or 256 pairs, 2 P <= 8 E), so the A16W4 and
+    MXFP8 calls take the 16-row narrow form with the routing kernel's arrays
+    (no K split, no routing of its own); an expert with more than 8 pairs
+    takes two passes.  Ragged N (3 row tiles, the last partial) and K (two
+    steps and a tail), an invalid id."""
+    m = inputs.moe_gate_up(E=64, N=320, K=352, T=T, topk=8, seed=400 + T)
+    ids = m["ids"].clone()
+    ids[T - 1, 5] = -1
+    ids[0, :] = torch.arange(8, dtype=torch.int32)       # experts 0..7 ...
+    ids[1, :] = torch.arange(8, dtype=torch.int32)       # ... twice more,
+    ids[2, :] = torch.arange(8, dtype=torch.int32)       # so some hold > 8 pairs at T=32
+    assert check_moe(m, ids) == 0
+    assert check_w4a8(m, ids) == 0
+
+
 def test_more_items_than_resident_ctas():
     """More (expert, row tile) items than resident CTAs (64 experts x 8 tiles
     over 3 CTAs an SM, a partly filled last round), ragged N and K, an invalid
