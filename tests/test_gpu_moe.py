@@ -509,6 +509,72 @@ def test_sixteen_row_form_above_decode_sizes(T):
     assert check_w4a8(m, ids) == 0
 
 
+def test_decode_inputs_written_just_before_each_call():
+    """Decode calls read the ids (and, through the activation kernel, x) that
+    a device copy on the same stream wrote right before each call, six calls
+    back to back with no synchronization between them: the expert kernel,
+    which routes from the ids before its dependency wait, must see each
+    call's own ids.  Both activation forms and the full expert, against the
+    oracle per call."""
+    from oracle.moe import moe_linear_w4a8
+    dev = cuda_device()
+    ensure_built()
+    E, N, K, T, topk = 32, 256, 512, 2, 8
+    m = inputs.moe_gate_up(E=E, N=N, K=K, T=T, topk=topk, seed=500)
+    p = mx.mx_pack_weights(m["w"].to(dev), m["codes"].to(dev), "e2m1")
+    g = torch.Generator().manual_seed(501)
+    n = 6
+    ids_h = [torch.randperm(E, generator=g)[: T * topk].reshape(T, topk).to(torch.int32) for _ in range(n)]
+    x_h = [torch.randn((T, K), generator=g).to(torch.bfloat16) for _ in range(n)]
+    ids_src = [t.to(dev) for t in ids_h]
+    x_src = [t.to(dev) for t in x_h]
+    ids_d = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    x_d = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    work = torch.empty(mx.mxfp4_moe_workspace_size(T, topk, E, N, K), dtype=torch.uint8, device=dev)
+    W = dequant_experts_bf16(u8(m["w"]), u8(m["codes"]))
+    for form, fn in (("a16w4", mx.mxfp4_moe_linear), ("w4a8", mx.mxfp4_moe_linear_w4a8)):
+        torch.cuda.synchronize()
+        outs = []
+        for k in range(n):
+            ids_d.copy_(ids_src[k])
+            x_d.copy_(x_src[k])
+            outs.append(fn(x_d, ids_d, p, workspace=work))
+        torch.cuda.synchronize()
+        for k in range(n):
+            y = outs[k].float().cpu().numpy()
+            xv = bf16_np(x_h[k])
+            idn = u8(ids_h[k])
+            if form == "a16w4":
+                ref = moe_linear(xv, idn, u8(m["w"]), u8(m["codes"]), wdeq=W)
+                A = xv
+            else:
+                r = moe_linear_w4a8(xv, idn, u8(m["w"]), u8(m["codes"]))
+                ref, A = r["y"], r["A"]
+            for t in range(T):
+                for j in range(topk):
+                    err = normalized_error(y[t, j][None], ref[t, j][None], A[t][None], W[int(idn[t, j])])
+                    assert err <= TOL, (form, k, t, j, err)
+    # the full expert: both projections at decode size
+    e = inputs.moe_expert(E=16, I=128, H=256, T=T, topk=topk, seed=502)
+    w13 = mx.mx_pack_weights(e["w13"].to(dev), e["c13"].to(dev), "e2m1", mx.MX_PACK_GATE_UP)
+    w2 = mx.mx_pack_weights(e["w2"].to(dev), e["c2"].to(dev), "e2m1", 0)
+    wts = e["weights"].to(dev)
+    ids_e = [torch.randperm(16, generator=g)[: T * topk].reshape(T, topk).to(torch.int32) for _ in range(n)]
+    ids_e_src = [t.to(dev) for t in ids_e]
+    x_e_src = e["x"].to(dev)
+    torch.cuda.synchronize()
+    outs = []
+    for k in range(n):
+        ids_d.copy_(ids_e_src[k])
+        outs.append(mx.mxfp4_moe_expert(x_e_src, ids_d, wts, w13, w2))
+    torch.cuda.synchronize()
+    for k in range(n):
+        ref = oracle_expert(e, ids_e[k])
+        y = outs[k].float().cpu().numpy()
+        err = np.max(np.abs(y - ref["out"]) / np.where(ref["den"] > 0, ref["den"], 1.0))
+        assert err <= TOL, (k, err)
+
+
 def test_more_items_than_resident_ctas():
     """More (expert, row tile) items than resident CTAs (64 experts x 8 tiles
     over 3 CTAs an SM, a partly filled last round), ragged N and K, an invalid
