@@ -525,10 +525,10 @@ def bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind):
     """The other workloads of the layer, each timed as a graph of back-to-back
     calls whose weights (or routed experts) rotate over more than 4x L2:
     the small GEMV M=1 N=512 K=1024 with 1x32 row codes; the decode linear at
-    K=2080 (K % 128 != 0, padded) for M = 1 and 32; the sweep linear N=7168
-    K=8192 at M = 1, 32 and 256; the sweep experts E=256 N=4096 K=7168 top-8
-    at T = 1, 8 and 64 (A16W4), the top-k ids rotating over 16 draws so
-    consecutive calls touch different experts."""
+    K=2080 (K % 128 != 0, padded) for M = 1 and 32; the sweep linears N=24576
+    K=1536 and N=7168 K=8192 at M = 1, 32 and 256; the sweep experts E=256
+    N=4096 K=7168 top-8 at T = 1, 8, 64 and 256 (A16W4), the top-k ids
+    rotating over 16 draws so consecutive calls touch different experts."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     lines = []
 
@@ -563,10 +563,12 @@ def bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind):
     linear_lines("MXFP8 GEMV, 1x32 row codes 120..130", inputs.gemv_small(), (1,), False)
     linear_lines("MXFP8 decode linear, 32x32 codes, K padded to 2176",
                  inputs.decode_linear(K=2080, Ms=(1, 32)), (1, 32), True)
+    linear_lines("MXFP8 sweep linear, 32x32 codes", inputs.decode_linear(K=1536, Ms=(1, 32, 256), N=24576),
+                 (1, 32, 256), True)
     linear_lines("MXFP8 sweep linear, 32x32 codes", inputs.decode_linear(K=8192, Ms=(1, 32, 256), N=7168),
                  (1, 32, 256), True)
 
-    lines += bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, (1, 8, 64))
+    lines += bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, (1, 8, 64, 256))
     torch.cuda.empty_cache()
     return lines
 
