@@ -195,7 +195,13 @@ int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mo
 
 /* Workspace bytes mxfp8_linear needs for M tokens on weight w: the size of the
  * quantized activation and its codes (used by the GEMM for M > 32 and by the
- * MX_LINEAR_CLUSTER_GEMV path; the default decode GEMV uses none of it). */
+ * MX_LINEAR_CLUSTER_GEMV path; the default decode GEMV uses none of it), plus,
+ * for M > 32 when the GEMM's output tiles would leave more than half the SMs
+ * of the current device idle, room for f32 partial sums of up to 8 K ranges
+ * ([ranges, M, N], at most 64 MB; the size depends on the current device's SM
+ * count, 152 assumed when there is no device).  That room is optional: a
+ * workspace holding only the quantized activation and codes is accepted and
+ * the GEMM then splits K into as many ranges as the bytes past them hold. */
 size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
 
 /*
@@ -208,8 +214,11 @@ size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w);
  *   workspace  device scratch of mxfp8_linear_workspace_size(M, w) bytes
  * M <= MX_GEMV_MAX_M runs the split-K decode GEMV on the tensor cores (block
  * scales applied by tcgen05, activation quantized inside the kernel), larger M
- * the block-scaled GEMM.  Within the decode range a token's result does not
- * depend on M.
+ * the block-scaled GEMM (which, when its tiles would leave SMs idle, splits K
+ * into ranges and adds their f32 sums in range order before the bias and the
+ * one rounding).  Within the decode range a token's result does not depend on
+ * M; above it, the K split (and so the f32 summation order) depends on M, the
+ * device's SM count and the workspace's size.
  * The kernels start streaming w's buffers before the previous kernel on the
  * stream has finished (programmatic dependent launch): w must not be written
  * by the kernel launched just before on the same stream (mx_pack_weights
@@ -220,7 +229,9 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
                  unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes mxfp8_linear_q needs for M tokens on weight w (the
- * activation's scale-factor atoms for the GEMM when M > MX_GEMV_MAX_M, else 0). */
+ * activation's scale-factor atoms for the GEMM when M > MX_GEMV_MAX_M, then
+ * the optional room for the GEMM's K-range partial sums as in
+ * mxfp8_linear_workspace_size; 0 for M <= MX_GEMV_MAX_M). */
 size_t mxfp8_linear_q_workspace_size(int M, const mx_packed_weight* w);
 
 /*

@@ -69,18 +69,33 @@ PackRegions pack_regions(int fmt, int E, int N, int K) {
 }
 
 struct LinearWs {
-  size_t xq_off, codes_off, total;
+  size_t xq_off, codes_off, part_off, total;  // part_off: the bytes the call needs
 };
 
+// SM count the GEMM's K split is sized for: the current device's, else the
+// GB300's 152 (a host without a device still gets a size).
+int gemm_sizing_sms() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      v > 0)
+    return v;
+  cudaGetLastError();
+  return 152;
+}
+
 // Workspace of the cluster GEMV (M <= 32) and of the GEMM (M > 32): quantized
-// activation [Mp, Kp] then its codes / scale atoms.  The tensor-core GEMV
-// (M <= 32, the default) quantizes in shared memory and needs none.
-LinearWs linear_ws(int M, int Kp) {
+// activation [Mp, Kp] and its codes / scale atoms (required), then room for
+// the GEMM's K-range partial sums (when its tiles leave SMs idle; a smaller
+// workspace gets fewer ranges).  The tensor-core GEMV (M <= 32, the default)
+// quantizes in shared memory and needs none.
+LinearWs linear_ws(int M, int N, int Kp) {
   LinearWs r;
   const size_t Mp = M <= MX_GEMV_MAX_M ? static_cast<size_t>(M) : (static_cast<size_t>(M) + 127) / 128 * 128;
   r.xq_off = 0;
   r.codes_off = align_up(Mp * Kp, kAlign);
-  r.total = r.codes_off + align_up(Mp * (Kp / 32), kAlign);
+  r.part_off = r.codes_off + align_up(Mp * (Kp / 32), kAlign);
+  const size_t part = M > MX_GEMV_MAX_M ? gemm_part_bytes(M, N, Kp, gemm_sizing_sms()) : 0;
+  r.total = r.part_off + align_up(part, kAlign);
   return r;
 }
 
@@ -377,7 +392,7 @@ int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mo
 
 size_t mxfp8_linear_workspace_size(int M, const mx_packed_weight* w) {
   if (!w || M <= 0) return 0;
-  return linear_ws(M, w->Kp).total;
+  return linear_ws(M, w->N, w->Kp).total;
 }
 
 int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bias, void* out,
@@ -402,7 +417,7 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
   const bool no_fuse = (flags & MX_LINEAR_NO_FUSED_QUANT) != 0;
   const bool legacy = (flags & MX_LINEAR_CLUSTER_GEMV) != 0;
   const int Kp = w->Kp;
-  const LinearWs L = linear_ws(M, Kp);
+  const LinearWs L = linear_ws(M, w->N, Kp);
 
   auto run_chunk = [&](const void* xc, int Mc, void* oc) -> int {
     GemvArgs a = {};
@@ -442,8 +457,8 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     return launch_gemv_tc(g, stream);
   }
   const bool needs_ws = (M > kFusedQuantMaxM && !force_fuse) || no_fuse || M > MX_GEMV_MAX_M;
-  if (needs_ws && (!workspace || workspace_bytes < L.total))
-    return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, L.total);
+  if (needs_ws && (!workspace || workspace_bytes < L.part_off))
+    return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, L.part_off);
   if (needs_ws && !aligned16(workspace)) return set_error(MX_ERR_ALIGN, "workspace needs 16-byte alignment");
   const bool force_gemv = (flags & (1u << 13)) != 0;  // tuning: chunked GEMV for M > 32
   if (M > MX_GEMV_MAX_M && !force_gemv) {
@@ -460,6 +475,10 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     g.bias = bias;
     g.out = out;
     g.M = M;
+    if (workspace_bytes > L.part_off) {
+      g.part = ws + L.part_off;
+      g.part_bytes = workspace_bytes - L.part_off;
+    }
     return launch_gemm(g, stream);
   }
   const size_t xrow = static_cast<size_t>(w->K) * 2, orow = static_cast<size_t>(w->N) * 2;
@@ -471,9 +490,14 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
   return MX_OK;
 }
 
+// the activation's scale atoms, then the GEMM's K-range partial sums (if any)
+static size_t q_atoms_bytes(int M, const mx_packed_weight* w) {
+  return align_up(static_cast<size_t>((M + 127) / 128) * (w->Kp / 128) * 512, kAlign);
+}
+
 size_t mxfp8_linear_q_workspace_size(int M, const mx_packed_weight* w) {
   if (!w || M <= MX_GEMV_MAX_M) return 0;
-  return static_cast<size_t>((M + 127) / 128) * (w->Kp / 128) * 512;
+  return q_atoms_bytes(M, w) + align_up(gemm_part_bytes(M, w->N, w->Kp, gemm_sizing_sms()), kAlign);
 }
 
 int mxfp8_linear_q(const uint8_t* xq, const uint8_t* xcodes, int M, const mx_packed_weight* w, const void* bias,
@@ -499,7 +523,7 @@ int mxfp8_linear_q(const uint8_t* xq, const uint8_t* xcodes, int M, const mx_pac
     g.M = M;
     return launch_gemv_tc(g, stream);
   }
-  const size_t need = mxfp8_linear_q_workspace_size(M, w);
+  const size_t need = q_atoms_bytes(M, w);  // the partial sums take what room is left
   if (!workspace || workspace_bytes < need)
     return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return set_error(MX_ERR_ALIGN, "workspace needs 16-byte alignment");
@@ -516,6 +540,10 @@ int mxfp8_linear_q(const uint8_t* xq, const uint8_t* xcodes, int M, const mx_pac
   g.bias = bias;
   g.out = out;
   g.M = M;
+  if (workspace_bytes > need) {
+    g.part = sfa + need;
+    g.part_bytes = workspace_bytes - need;
+  }
   return launch_gemm(g, stream);
 }
 

@@ -53,6 +53,8 @@ struct GemmParams {
   const __nv_bfloat16* bias;  // [N] or null
   __nv_bfloat16* out;         // [M, N]
   int M, N, KT, RTb, m_tiles, n_tiles;
+  int ksplit;                 // K ranges a tile (gemm_ksplit); > 1: f32 partial sums to part
+  float* part;                // [ksplit, M, N]
 };
 
 constexpr uint32_t kIdesc = mxf8_idesc(BM, BN);
@@ -89,7 +91,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   // only now that this CTA holds its tensor memory: a dependent grid then
   // never takes columns that a CTA of this grid still waits for
   pdl_launch_dependents();
-  const int ntiles = p.m_tiles * p.n_tiles;
+  // work units: (tile, K range), the range fastest
+  const int S = p.ksplit;
+  const int nunits = p.m_tiles * p.n_tiles * S;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -99,10 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     pdl_wait_prior_grid();  // the quantized activation is complete and visible
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
+      const int tile = u / S, ks = u - tile * S;
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
       const int rb0 = min(2 * nt, p.RTb - 1), rb1 = min(2 * nt + 1, p.RTb - 1);
-      for (int kt = 0; kt < p.KT; ++kt) {
+      for (int kt = ks * p.KT / S; kt < (ks + 1) * p.KT / S; ++kt) {
         if (!mbar_wait(&empty[stage], phase ^ 1u)) { *abort_flag = 1u; break; }
         uint8_t* st = smem + stage * kStageBytes;
         mbar_arrive_expect_tx(&full[stage], kTxBytes);
@@ -120,10 +125,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // ------------------------------------------------------------ MMA issuer
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
+      const int ks = u % S, k0 = ks * p.KT / S, k1 = (ks + 1) * p.KT / S;
       if (!mbar_wait(acc_empty, acc_phase ^ 1u)) { *abort_flag = 1u; break; }
       tc_fence_after();
-      for (int kt = 0; kt < p.KT; ++kt) {
+      for (int kt = k0; kt < k1; ++kt) {
         if (!mbar_wait(&full[stage], phase)) { *abort_flag = 1u; break; }
         tc_fence_after();
         const uint32_t st = smem_u32(smem + stage * kStageBytes);
@@ -138,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const uint32_t idesc = kIdesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
           // +32 bytes along K inside the swizzle atom = +2 in the start-address field
           tc_mma_mxf8(tmem + kAccCol, adesc + 2 * k, bdesc + 2 * k, idesc, sf_col, sf_col + 4,
-                      (kt | k) != 0 ? 1u : 0u);
+                      (kt != k0 || k != 0) ? 1u : 0u);
         }
         tc_commit(&empty[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -151,7 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int q = warp & 3;              // tensor-memory lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // columns [128 half, 128 half + 128)
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
+      const int tile = u / S, ks = u - tile * S;
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
       if (!mbar_wait(acc_full, acc_phase)) { *abort_flag = 1u; break; }
       tc_fence_after();
@@ -167,7 +174,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       acc_phase ^= 1u;
       const int row = mt * BM + q * 32 + lane;
       const int nb = nt * BN + half * 128;
-      if (row < p.M) {
+      if (S > 1) {
+        // this K range's f32 sums; the finishing kernel adds the ranges and the bias
+        if (row < p.M) {
+          float* dst = p.part + (static_cast<long long>(ks) * p.M + row) * p.N + nb;
+          if (nb + 128 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < 128; j += 4)
+              *reinterpret_cast<float4*>(dst + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+              if (nb + j < p.N) dst[j] = __uint_as_float(r[j]);
+          }
+        }
+      } else if (row < p.M) {
         __nv_bfloat16* dst = p.out + static_cast<long long>(row) * p.N + nb;
         if (nb + 128 <= p.N && (p.N & 7) == 0) {
 #pragma unroll
@@ -206,9 +228,76 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 }
 
+// Split-K finish: out[m, n] = bf16(sum over the S ranges of part[s, m, n], in
+// range order, + bias[n]); one thread a 4 consecutive columns of a row.
+// Launched as a programmatic dependent of the GEMM.
+__global__ void __launch_bounds__(256) gemm_finish_kernel(const float* __restrict__ part, int S, int M, int N,
+                                                          const __nv_bfloat16* __restrict__ bias,
+                                                          __nv_bfloat16* __restrict__ out) {
+  pdl_wait_prior_grid();
+  const int N4 = (N + 3) >> 2;
+  const long long total = static_cast<long long>(M) * N4;
+  const long long plane = static_cast<long long>(M) * N;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(i / N4), n = static_cast<int>(i - static_cast<long long>(m) * N4) * 4;
+    const float* src = part + static_cast<long long>(m) * N + n;
+    if (n + 4 <= N && (N & 3) == 0) {
+      float4 v = *reinterpret_cast<const float4*>(src);
+      for (int k = 1; k < S; ++k) {
+        const float4 w = *reinterpret_cast<const float4*>(src + k * plane);
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
+      if (bias) {
+        v.x += __bfloat162float(bias[n]);
+        v.y += __bfloat162float(bias[n + 1]);
+        v.z += __bfloat162float(bias[n + 2]);
+        v.w += __bfloat162float(bias[n + 3]);
+      }
+      const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&a);
+      pk.y = *reinterpret_cast<const uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(out + static_cast<long long>(m) * N + n) = pk;
+    } else {
+      for (int c = 0; c < 4 && n + c < N; ++c) {
+        float v = src[c];
+        for (int k = 1; k < S; ++k) v += src[k * plane + c];
+        if (bias) v += __bfloat162float(bias[n + c]);
+        out[static_cast<long long>(m) * N + n + c] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 unsigned int take_error_flags_gemm() { return take_tu_error_flags(); }
+
+// K ranges a tile: only when the 128 x 256 tiles would leave more than half
+// the SMs idle (M up to a few hundred rows on a narrow N); then enough ranges
+// to fill one wave, at most 8, each of at least 4 K steps, with at most 64 MB
+// of partial sums -- and no more than `room` bytes of them.  (N=7168 K=8192:
+// 28 tiles at M = 64 / 128 leave 124 of 152 SMs idle.)
+int gemm_ksplit(int M, int N, int Kp, int sms, size_t room) {
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN), KT = Kp / BKB;
+  if (tiles <= 0 || 2 * tiles > sms) return 1;
+  int S = sms / tiles;
+  if (S > 8) S = 8;
+  if (S > KT / 4) S = KT / 4;
+  const size_t plane = static_cast<size_t>(M) * static_cast<size_t>(N) * 4;
+  const size_t cap = room < (static_cast<size_t>(64) << 20) ? room : (static_cast<size_t>(64) << 20);
+  while (S > 1 && S * plane > cap) --S;
+  return S > 1 ? S : 1;
+}
+
+size_t gemm_part_bytes(int M, int N, int Kp, int sms) {
+  const int S = gemm_ksplit(M, N, Kp, sms, ~static_cast<size_t>(0));
+  return S > 1 ? static_cast<size_t>(S) * M * static_cast<size_t>(N) * 4 : 0;
+}
 
 int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   const mx_packed_weight* w = a.w;
@@ -226,6 +315,8 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.m_tiles = (a.M + BM - 1) / BM;
   p.n_tiles = (w->N + BN - 1) / BN;
   const int Mp = p.m_tiles * BM;
+  p.ksplit = a.part ? gemm_ksplit(a.M, w->N, w->Kp, di.sm_count, a.part_bytes) : 1;
+  p.part = static_cast<float*>(a.part);
   CUtensorMap amap, bmap;
   const uint64_t a_cols = a.xq_cols ? a.xq_cols : w->Kp, a_rows = a.xq_rows ? a.xq_rows : Mp;
   const uint64_t a_ld = a.xq_ld ? a.xq_ld : w->Kp;
@@ -239,8 +330,8 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (raise_smem_limit(reinterpret_cast<const void*>(gemm_kernel), kSmemBytes, di, smem_set) != MX_OK)
     return MX_ERR_CUDA;
   cudaError_t e;
-  const int ntiles = p.m_tiles * p.n_tiles;
-  const int grid = ntiles < di.sm_count ? ntiles : di.sm_count;
+  const int nunits = p.m_tiles * p.n_tiles * p.ksplit;
+  const int grid = nunits < di.sm_count ? nunits : di.sm_count;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -253,6 +344,15 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, gemm_kernel, amap, bmap, p);
   if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+  if (p.ksplit > 1) {
+    const long long items = static_cast<long long>(a.M) * ((w->N + 3) / 4);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(items, 256)), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, gemm_finish_kernel, static_cast<const float*>(p.part), p.ksplit, a.M, w->N,
+                           p.bias, p.out);
+    if (e != cudaSuccess) return set_error(MX_ERR_CUDA, "gemm finish launch: %s", cudaGetErrorString(e));
+  }
   return MX_OK;
 }
 

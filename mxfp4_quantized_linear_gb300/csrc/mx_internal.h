@@ -115,8 +115,14 @@ struct GemmArgs {
   void* out;            // bf16 [M, N]
   int M;
   int xq_rows, xq_cols, xq_ld;  // 0: the workspace layout [roundup(M,128), Kp]
+  void* part;           // room for split-K partial sums (up to gemm_part_bytes), or null: no split
+  size_t part_bytes;
 };
 int launch_gemm(const GemmArgs& a, cudaStream_t stream);
+// K ranges the GEMM splits each tile into on a device of `sms` SMs with `room`
+// bytes for partial sums, and the bytes the unconstrained split takes (0: none)
+int gemm_ksplit(int M, int N, int Kp, int sms, size_t room);
+size_t gemm_part_bytes(int M, int N, int Kp, int sms);
 unsigned int take_error_flags_gemm();
 
 // ---- routing + MoE (moe.cu)

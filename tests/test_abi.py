@@ -73,6 +73,15 @@ def test_host_side_checks_of_the_newer_entry_points():
     assert lib.mxfp8_linear_q(None, None, 0, ctypes.byref(e4), None, None, 0, None, 0, None) == b.MX_OK
     assert lib.mxfp8_linear_q_workspace_size(32, ctypes.byref(e4)) == 0
     assert lib.mxfp8_linear_q_workspace_size(33, ctypes.byref(e4)) == 512
+    # the GEMM's K split on a host without a device is sized for 152 SMs:
+    # N=7168 K=8192 M=64 is 28 tiles of 128 x 256 -> 5 K ranges of f32 sums
+    # [5, 64, 7168]; N=24576 K=1536 is 96 tiles -> no split
+    w1 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=7168, K=8192, Kp=8192)
+    base = 128 * 8192 + 128 * 256
+    assert lib.mxfp8_linear_workspace_size(64, ctypes.byref(w1)) == base + 5 * 64 * 7168 * 4
+    assert lib.mxfp8_linear_q_workspace_size(64, ctypes.byref(w1)) == 64 * 512 + 5 * 64 * 7168 * 4
+    w2 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=24576, K=1536, Kp=1536)
+    assert lib.mxfp8_linear_workspace_size(64, ctypes.byref(w2)) == 128 * 1536 + 128 * 48
     # expert: w13 must carry the gate/up layout, w2 must fit it
     assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2p), ctypes.byref(e2p), None, None, 0, None,
                                 None) == b.MX_ERR_ARG

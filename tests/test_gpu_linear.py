@@ -237,3 +237,35 @@ def test_large_m_padded_rows_and_k():
     c = inputs.e8m0_codes((N, K // 32), 118, 132, g)
     b = inputs.bf16_normal((N,), g)
     check(pack(w, c), w, c, inputs.bf16_normal((M, K), g), bias=b)
+
+
+@pytest.mark.parametrize("M,N", [(45, 203), (130, 1000)])
+def test_gemm_k_split_ragged_n_with_bias(M, N):
+    """Few output tiles on a long K: the GEMM splits K into ranges (f32 partial
+    sums, then the ranges added in order, the bias, one rounding).  N = 203
+    takes the element-wise partial and finishing stores, N = 1000 the vector
+    ones; every output against the oracle."""
+    K = 4128
+    g = inputs.generator(M + N)
+    w = inputs.e4m3_bytes((N, K), g)
+    c = inputs.e8m0_codes((N, K // 32), 118, 132, g)
+    b = inputs.bf16_normal((N,), g)
+    p = pack(w, c)
+    Mp, Kp = (M + 127) // 128 * 128, p.desc.Kp
+    no_split = -(-Mp * Kp // 256) * 256 + -(-Mp * Kp // 32 // 256) * 256
+    full = mx.mxfp8_linear_workspace_size(M, p)
+    assert full >= no_split + 2 * M * N * 4   # room for two or more K ranges
+    x = inputs.bf16_normal((M, K), g)
+    check(p, w, c, x, bias=b)
+    dev = cuda_device()
+    # the required bytes only (no split), then room for two ranges: both
+    # against the oracle too
+    for nbytes in (no_split, no_split + 2 * M * N * 4):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        y2 = mx.mxfp8_linear(x.to(dev), p, b.to(dev), workspace=ws)
+        torch.cuda.synchronize()
+        wn, cn = u8(w), row_codes(u8(c), N)
+        ref = ref_linear(bf16_np(x), wn, cn, bf16_np(b))
+        y2n = y2.float().cpu().numpy()
+        assert normalized_error(y2n, ref["y"], ref["A"], ref["B"]) <= TOL
+        assert elementwise_excess(y2n, ref) <= 0.0
