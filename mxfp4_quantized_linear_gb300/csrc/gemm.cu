@@ -175,18 +175,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int row = mt * BM + q * 32 + lane;
       const int nb = nt * BN + half * 128;
       if (S > 1) {
-        // this K range's f32 sums; the finishing kernel adds the ranges and the bias
-        if (row < p.M) {
-          float* dst = p.part + (static_cast<long long>(ks) * p.M + row) * p.N + nb;
-          if (nb + 128 <= p.N && (p.N & 3) == 0) {
+        // this K range's f32 sums; the finishing kernel adds the ranges and the
+        // bias.  A split grid runs one unit a CTA, so the operand ring is idle
+        // once the accumulator is full: each warp transposes its 32 rows x 128
+        // columns through 16.5 KB of it (rows padded to 132 words) and stores
+        // whole rows, a warp 512 contiguous bytes an instruction.
+        float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 32 * 132;
 #pragma unroll
-            for (int j = 0; j < 128; j += 4)
-              *reinterpret_cast<float4*>(dst + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        for (int j = 0; j < 128; j += 4)
+          *reinterpret_cast<float4*>(stg + lane * 132 + j) =
+              make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                          __uint_as_float(r[j + 3]));
+        __syncwarp();
+        const int row0 = mt * BM + q * 32;
+        const int rows = min(32, p.M - row0);
+        const bool vec = (p.N & 3) == 0 && nb + lane * 4 + 4 <= p.N;
+        for (int rr = 0; rr < rows; ++rr) {
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 132 + lane * 4);
+          float* dst = p.part + (static_cast<long long>(ks) * p.M + row0 + rr) * p.N + nb + lane * 4;
+          if (vec) {
+            *reinterpret_cast<float4*>(dst) = v;
           } else {
-#pragma unroll
-            for (int j = 0; j < 128; ++j)
-              if (nb + j < p.N) dst[j] = __uint_as_float(r[j]);
+            const float e[4] = {v.x, v.y, v.z, v.w};
+            for (int c = 0; c < 4; ++c)
+              if (nb + lane * 4 + c < p.N) dst[c] = e[c];
           }
         }
       } else if (row < p.M) {
@@ -332,6 +344,8 @@ int launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   cudaError_t e;
   const int nunits = p.m_tiles * p.n_tiles * p.ksplit;
   const int grid = nunits < di.sm_count ? nunits : di.sm_count;
+  // the split epilogue stages its stores in the operand ring: one unit a CTA
+  if (p.ksplit > 1 && nunits > grid) return set_error(MX_ERR_UNSUPPORTED, "K split of %d units on %d CTAs", nunits, grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
