@@ -852,7 +852,12 @@ MX_DEV int moe_split_for(unsigned items, unsigned slots, unsigned KT, int kmax, 
 // added in range order (deterministic), in the pass's output form.  Launched
 // as a programmatic dependent of the expert GEMM; it does not release its own
 // dependents early (measured on GB300: letting the next call's activation
-// kernel launch at once was no faster, T=1 28.1 -> 28.4 us).
+// kernel launch at once was no faster, T=1 28.1 -> 28.4 us).  One thread 4
+// consecutive output columns of a pair.  It sits on the decode call's critical
+// path, so its dependent loads are few: the range count, the valid count and
+// the pair's row in one round trip, then every range's partial sums at once.
+constexpr int kFinishMaxSplit = 8;  // ranges the finishing kernel unrolls (>= kMaxKSplit)
+
 __global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict__ part,
                                                          const int32_t* __restrict__ split, int P, int N,
                                                          const int32_t* __restrict__ pairs,
@@ -860,30 +865,83 @@ __global__ void __launch_bounds__(256) moe_finish_kernel(const float* __restrict
                                                          int gate_up, __nv_bfloat16* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   pdl_wait_prior_grid();
-  const int S = *split;  // the count the GEMM chose (its CTA 0 wrote it)
-  if (S == 1) return;  // the GEMM did not split K and wrote the outputs itself
   const int cols = out_mode == kMoeOutSwiglu ? N / 2 : N;
-  const long long total = static_cast<long long>(*n_valid) * cols;
+  const int cols4 = (cols + 3) >> 2;
+  const long long total = static_cast<long long>(P) * cols4;
   const long long PN = static_cast<long long>(P) * N;
+  const bool vec = (N & 7) == 0;  // 16-byte partial rows, 8-byte bf16 / 16-byte f32 stores
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int j = static_cast<int>(idx / cols), c = static_cast<int>(idx - static_cast<long long>(j) * cols);
-    const int pt = pairs[j];
+    const int j = static_cast<int>(idx / cols4), c = static_cast<int>(idx - static_cast<long long>(j) * cols4) * 4;
+    // independent loads (pairs holds P entries; j < P)
+    const int S = *split, nv = *n_valid, pt = pairs[j];
+    if (S == 1) return;  // the GEMM did not split K and wrote the outputs itself
+    if (j >= nv) continue;
     const float* src = part + static_cast<long long>(pt) * N;
     if (out_mode == kMoeOutSwiglu) {
-      // packed rows 16 (c / 8) + c % 8 (gate) and 8 further on (up)
+      // packed rows 16 (c / 8) + c % 8 (gate) and 8 further on (up); 4
+      // consecutive c stay inside one group of 8
       const int ng = (c >> 3) * 16 + (c & 7);
-      float g = 0.0f, u = 0.0f;
-      for (int k = 0; k < S; ++k) {
-        g += src[k * PN + ng];
-        u += src[k * PN + ng + 8];
+      float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+      if (vec) {
+        float4 pg[kFinishMaxSplit], pu[kFinishMaxSplit];
+#pragma unroll
+        for (int k = 0; k < kFinishMaxSplit; ++k)
+          if (k < S) {
+            pg[k] = *reinterpret_cast<const float4*>(src + k * PN + ng);
+            pu[k] = *reinterpret_cast<const float4*>(src + k * PN + ng + 8);
+          }
+#pragma unroll
+        for (int k = 0; k < kFinishMaxSplit; ++k)
+          if (k < S) {
+            g[0] += pg[k].x; g[1] += pg[k].y; g[2] += pg[k].z; g[3] += pg[k].w;
+            u[0] += pu[k].x; u[1] += pu[k].y; u[2] += pu[k].z; u[3] += pu[k].w;
+          }
+        const __nv_bfloat162 a = __floats2bfloat162_rn(silu_f32(g[0]) * u[0], silu_f32(g[1]) * u[1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(silu_f32(g[2]) * u[2], silu_f32(g[3]) * u[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&a);
+        pk.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(out + static_cast<long long>(pt) * cols + c) = pk;
+      } else {
+        for (int e = 0; e < 4 && c + e < cols; ++e) {
+          for (int k = 0; k < S; ++k) {
+            g[e] += src[k * PN + ng + e];
+            u[e] += src[k * PN + ng + e + 8];
+          }
+          out[static_cast<long long>(pt) * cols + c + e] = __float2bfloat16_rn(silu_f32(g[e]) * u[e]);
+        }
       }
-      out[static_cast<long long>(pt) * cols + c] = __float2bfloat16_rn(silu_f32(g) * u);
     } else {
-      float y = 0.0f;
-      for (int k = 0; k < S; ++k) y += src[k * PN + c];
-      if (out_mode == kMoeOutF32) out_f32[static_cast<long long>(pt) * N + c] = y;
-      else out[static_cast<long long>(pt) * N + (gate_up ? gate_up_row(c, N) : c)] = __float2bfloat16_rn(y);
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+      if (vec) {
+        float4 pv[kFinishMaxSplit];
+#pragma unroll
+        for (int k = 0; k < kFinishMaxSplit; ++k)
+          if (k < S) pv[k] = *reinterpret_cast<const float4*>(src + k * PN + c);
+#pragma unroll
+        for (int k = 0; k < kFinishMaxSplit; ++k)
+          if (k < S) {
+            y[0] += pv[k].x; y[1] += pv[k].y; y[2] += pv[k].z; y[3] += pv[k].w;
+          }
+        if (out_mode == kMoeOutF32) {
+          *reinterpret_cast<float4*>(out_f32 + static_cast<long long>(pt) * N + c) = make_float4(y[0], y[1], y[2], y[3]);
+        } else {
+          // a gate / up interleaved weight's rows c..c+3 stay consecutive in gate-then-up order
+          const int oc = gate_up ? gate_up_row(c, N) : c;
+          const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]), b = __floats2bfloat162_rn(y[2], y[3]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&a);
+          pk.y = *reinterpret_cast<const uint32_t*>(&b);
+          *reinterpret_cast<uint2*>(out + static_cast<long long>(pt) * N + oc) = pk;
+        }
+      } else {
+        for (int e = 0; e < 4 && c + e < cols; ++e) {
+          for (int k = 0; k < S; ++k) y[e] += src[k * PN + c + e];
+          if (out_mode == kMoeOutF32) out_f32[static_cast<long long>(pt) * N + c + e] = y[e];
+          else out[static_cast<long long>(pt) * N + (gate_up ? gate_up_row(c + e, N) : c + e)] = __float2bfloat16_rn(y[e]);
+        }
+      }
     }
   }
 }
@@ -1339,6 +1397,7 @@ size_t moe_act_bytes(long long P, int Kp, int E) { return 2 * act_region(P, Kp) 
 // kSplitMaxPairs pairs (the decode sizes whose few experts leave SM slots idle).
 constexpr int kMaxKSplit = 8, kSplitMaxPairs = 64;
 static_assert(kMaxKSplit <= 32, "the split choice costs one count a lane");
+static_assert(kMaxKSplit <= kFinishMaxSplit, "the finishing kernel unrolls every range");
 static_assert(kEarlyPairs >= kSplitMaxPairs && kEarlyPairs == 64, "the 16-row form routes its pairs with two ballots");
 size_t moe_part_bytes(long long P, int N) {
   return P <= kSplitMaxPairs ? static_cast<size_t>(kMaxKSplit) * P * N * sizeof(float) : 0;
@@ -1498,7 +1557,8 @@ int launch_moe(const MoeLaunch& a, cudaStream_t stream) {
     int rc = n16 ? launch_moe_gemm<kMoeNarrow16>(a, p, xh, xl, cs, cfg) : launch_moe_gemm<kMoeNarrow>(a, p, xh, xl, cs, cfg);
     if (rc != MX_OK || p.ksplit == 1) return rc;
     // add the K ranges' partial sums (programmatic dependent of the GEMM)
-    const long long total = P * static_cast<long long>(w->N);
+    const int cols = a.out_mode == kMoeOutSwiglu ? w->N / 2 : w->N;
+    const long long total = P * static_cast<long long>((cols + 3) / 4);
     cfg.gridDim = dim3(static_cast<unsigned>(blocks_for(total, 256)), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
