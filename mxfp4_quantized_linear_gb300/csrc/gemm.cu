@@ -100,24 +100,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tma_prefetch_desc(&amap);
     tma_prefetch_desc(&bmap);
     const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_last();
+    // a stage's weight half: B and its two scale atoms
+    auto load_b = [&](int stage, int kt, int nt) {
+      uint8_t* st = smem + stage * kStageBytes;
+      const int rb0 = min(2 * nt, p.RTb - 1), rb1 = min(2 * nt + 1, p.RTb - 1);
+      tma_load_2d(st + kABytes, &bmap, &full[stage], kt * BKB, nt * BN, pol_b);
+      bulk_load(st + kABytes + kBBytes + kSfaBytes, p.sfb + (static_cast<long long>(rb0) * p.KT + kt) * 512, 512,
+                &full[stage]);
+      bulk_load(st + kABytes + kBBytes + kSfaBytes + 512, p.sfb + (static_cast<long long>(rb1) * p.KT + kt) * 512,
+                512, &full[stage]);
+    };
+    // the weights do not depend on the kernel before (the activation
+    // quantizer): the first unit's first stages start loading them before the
+    // dependency wait, so they stream while the quantizer finishes (each
+    // stage's barrier expects its activation half too)
+    int pre = 0;
+    if (static_cast<int>(blockIdx.x) < nunits) {
+      const int tile = blockIdx.x / S, ks = blockIdx.x - tile * S;
+      const int k0 = ks * p.KT / S, k1 = (ks + 1) * p.KT / S;
+      pre = min(kStages, k1 - k0);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], kTxBytes);  // stage i is free: nothing has used it yet
+        load_b(i, k0 + i, tile / p.m_tiles);
+      }
+    }
     pdl_wait_prior_grid();  // the quantized activation is complete and visible
     int stage = 0;
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
       const int tile = u / S, ks = u - tile * S;
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-      const int rb0 = min(2 * nt, p.RTb - 1), rb1 = min(2 * nt + 1, p.RTb - 1);
-      for (int kt = ks * p.KT / S; kt < (ks + 1) * p.KT / S; ++kt) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u)) { *abort_flag = 1u; break; }
+      const int k0 = ks * p.KT / S;
+      for (int kt = k0; kt < (ks + 1) * p.KT / S; ++kt) {
+        const bool early = u == static_cast<int>(blockIdx.x) && kt - k0 < pre;  // weight half already loading
+        if (!early) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u)) { *abort_flag = 1u; break; }
+          mbar_arrive_expect_tx(&full[stage], kTxBytes);
+          load_b(stage, kt, nt);
+        }
         uint8_t* st = smem + stage * kStageBytes;
-        mbar_arrive_expect_tx(&full[stage], kTxBytes);
         tma_load_2d(st, &amap, &full[stage], kt * BKB, mt * BM, pol_a);
-        tma_load_2d(st + kABytes, &bmap, &full[stage], kt * BKB, nt * BN, pol_b);
         bulk_load(st + kABytes + kBBytes, p.sfa + (static_cast<long long>(mt) * p.KT + kt) * 512, 512, &full[stage]);
-        bulk_load(st + kABytes + kBBytes + kSfaBytes, p.sfb + (static_cast<long long>(rb0) * p.KT + kt) * 512, 512,
-                  &full[stage]);
-        bulk_load(st + kABytes + kBBytes + kSfaBytes + 512, p.sfb + (static_cast<long long>(rb1) * p.KT + kt) * 512,
-                  512, &full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
