@@ -395,6 +395,26 @@ def bench_prefill(mx, inputs, dev, stream, bf16_peak, peak_kind, mx8_peak=None):
             "note": f"frac_2x_bf16: against 2 x the {peak_kind} bf16 dense peak (nominal 8-bit ratio)"}
 
 
+def bench_linear_shape(mx, inputs, dev, stream, hbm_peak, N, K, M):
+    """One MXFP8 linear shape, graph-timed: calls back to back over packed
+    weight copies rotated past 4x L2 (us a call, GB/s of algorithmic bytes)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    c = inputs.decode_linear(K=K, Ms=(M,), N=N)
+    wd, cd = c["w"].to(dev), c["codes"].to(dev)
+    ncopies = max(4, -(-4 * l2 // mx.mx_pack_size("e4m3", 1, N, K)))
+    with torch.cuda.stream(stream):
+        packed = [mx.mx_pack_weights(wd, cd, "e4m3") for _ in range(ncopies)]
+    x = c["xs"][M].to(dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    work = torch.empty(max(256, mx.mxfp8_linear_workspace_size(M, packed[0])), dtype=torch.uint8, device=dev)
+    fns = [lambda i=i: mx.mxfp8_linear(x, packed[i % ncopies], out=out, workspace=work) for i in range(2 * ncopies)]
+    ms = graph_ms(stream, fns)
+    b = linear_bytes(M, N, K, True)
+    return {"workload": f"MXFP8 linear N={N} K={K} M={M}, 32x32 codes", "us": round(ms * 1e3, 3),
+            "GB/s": round(b / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "TFLOP/s": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}
+
+
 def bench_moe(mx, inputs, dev, stream, hbm_peak):
     m = inputs.moe_gate_up()
     with torch.cuda.stream(stream):
@@ -829,7 +849,7 @@ def main():
                     help="print one JSON line per shape of the linear / MoE sweep instead of the step")
     ap.add_argument("--case", default=None,
                     choices=["mxf8_peak", "gemm_m4096", "moe_gate_up", "moe_expert", "moe_w4a8_prefill", "configs",
-                             "moe_decode"],
+                             "moe_decode", "linear_n7168_k8192_m64"],
                     help="run only this secondary workload and print its JSON (e.g. to profile one kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -855,7 +875,9 @@ def main():
                    "moe_expert": lambda: bench_expert(mx, inputs, dev, stream, hbm_peak),
                    "moe_w4a8_prefill": lambda: bench_w4a8(mx, inputs, dev, stream, bf16_peak, peak_kind),
                    "configs": lambda: bench_configs(mx, inputs, dev, stream, hbm_peak, bf16_peak, peak_kind),
-                   "moe_decode": lambda: bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, (1,))}
+                   "moe_decode": lambda: bench_sweep_experts(mx, inputs, dev, stream, hbm_peak, (1,)),
+                   "linear_n7168_k8192_m64": lambda: bench_linear_shape(mx, inputs, dev, stream, hbm_peak, 7168,
+                                                                        8192, 64)}
             print(json.dumps({args.case: fns[args.case]()}), flush=True)
         return
     if args.sweep:
