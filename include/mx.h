@@ -69,9 +69,9 @@ enum { MX_SCALE_BLOCK32X32 = 0, MX_SCALE_ROW1X32 = 1 };
                                     up row 8 q + i - 8; codes alike                         */
 
 /* mxfp8_linear flags */
-#define MX_LINEAR_NO_FUSED_QUANT 1u /* cluster GEMV: always quantize x in a separate launch
-                                       (the pages' kill switch of the fused quant,
-                                       rocm_native, apply_weights)                         */
+#define MX_LINEAR_NO_FUSED_QUANT 1u /* M <= 32: always quantize x in a separate launch into
+                                       the workspace (the pages' kill switch of the fused
+                                       quant, rocm_native, apply_weights); same bits      */
 #define MX_LINEAR_CLUSTER_GEMV (1u << 14) /* M <= 32: run the CUDA-core-scaled mma.sync GEMV
                                        with cluster split-K (fused quant for M <= 8)
                                        instead of the tensor-core GEMV                      */
@@ -194,8 +194,9 @@ int mx_dequant(const uint8_t* bytes, const uint8_t* codes, int fmt, int scale_mo
 /* ------------------------------------------------------------- MXFP8 linear */
 
 /* Workspace bytes mxfp8_linear needs for M tokens on weight w: the size of the
- * quantized activation and its codes (used by the GEMM for M > 32 and by the
- * MX_LINEAR_CLUSTER_GEMV path; the default decode GEMV uses none of it), plus,
+ * quantized activation and its codes (used by the GEMM for M > 32, by the
+ * MX_LINEAR_CLUSTER_GEMV path and with MX_LINEAR_NO_FUSED_QUANT; the default
+ * decode GEMV uses none of it), plus,
  * for M > 32 when the GEMM's output tiles would leave more than half the SMs
  * of the current device idle, room for f32 partial sums of up to 8 K ranges
  * ([ranges, M, N], at most 64 MB; the size depends on the current device's SM

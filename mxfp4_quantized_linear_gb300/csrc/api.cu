@@ -454,6 +454,21 @@ int mxfp8_linear(const void* x, int M, const mx_packed_weight* w, const void* bi
     g.force_bulk = (flags >> 23) & 1u;                          // tuning: bulk-copy reduction
     g.force_cap = static_cast<int>((flags >> 24) & 0x7u);       // tuning: CTAs per SM
     g.force_recv = static_cast<int>((flags >> 27) & 0x3u);      // tuning: receive-buffer placement
+    if (no_fuse) {
+      // the fused quant switched off: x quantized by its own launch (the same
+      // block rule, so the same bits) into the workspace, which the GEMV reads
+      // after its dependency wait
+      if (!workspace || workspace_bytes < L.total)
+        return set_error(MX_ERR_WORKSPACE, "workspace of %zu bytes, needs %zu", workspace_bytes, L.total);
+      if (!aligned16(workspace)) return set_error(MX_ERR_ALIGN, "workspace needs 16-byte alignment");
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      cudaError_t e = launch_quant_act(x, M, w->K, w->K, ws + L.xq_off, w->K, ws + L.codes_off, w->K / 32, 128,
+                                       nullptr, true, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+      g.x = nullptr;
+      g.xq = ws + L.xq_off;
+      g.xcodes = ws + L.codes_off;
+    }
     return launch_gemv_tc(g, stream);
   }
   const bool needs_ws = (M > kFusedQuantMaxM && !force_fuse) || no_fuse || M > MX_GEMV_MAX_M;

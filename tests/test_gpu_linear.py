@@ -141,6 +141,19 @@ def test_prefill_full_size_sampled():
     assert elementwise_excess(y[np.ix_(ms, ns)], ref) <= 0.0
 
 
+@pytest.mark.parametrize("M,K", [(1, 2048), (5, 2080), (17, 2080), (32, 2048)])
+def test_tensor_core_gemv_separate_quantizer_is_bit_identical(M, K):
+    """MX_LINEAR_NO_FUSED_QUANT on the tensor-core GEMV: x quantized by its own
+    launch into the workspace gives the fused path's bits (and the oracle's)."""
+    c = inputs.decode_linear(K=K, Ms=(M,), N=704, seed=M)
+    p = pack(c["w"], c["codes"])
+    x = c["xs"][M]
+    y = gpu_linear(p, x)
+    yu = gpu_linear(p, x, flags=mx.MX_LINEAR_NO_FUSED_QUANT)
+    assert torch.equal(y.view(torch.int16), yu.view(torch.int16))
+    check(p, c["w"], c["codes"], x, flags=mx.MX_LINEAR_NO_FUSED_QUANT)
+
+
 @pytest.mark.parametrize("M", [1, 5, 9, 32])
 def test_cluster_gemv_path(M):
     """The mma.sync GEMV with cluster split-K (MX_LINEAR_CLUSTER_GEMV)."""
