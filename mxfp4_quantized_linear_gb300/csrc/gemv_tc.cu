@@ -147,7 +147,7 @@ __host__ __device__ inline Layout layout_for(int ring, int steps, int splits, in
 // of weight requests in flight on every SM.
 constexpr int kDefaultRing = 2;
 constexpr int kMaxAutoRing = 4;
-constexpr int kLongSlice = 8;             // K steps a CTA from which the ring is kMaxAutoRing deep
+constexpr int kWholeSlice = 5;            // K steps a CTA up to which a whole slice may sit in the ring
 
 __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const TcGemvParams p) {
@@ -491,13 +491,28 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
 
 unsigned int take_error_flags_gemv_tc() { return take_tu_error_flags(); }
 
-// Splits along K: the largest power of two (<= 8) giving at most three CTAs per
-// SM, so the grid runs as one wave with short slices requested at once; more
-// splits only when a slice would exceed kMaxSteps.  Depends on (N, K) and the
-// SM count, never on M.
+// Splits along K.  First choice: the largest power of two (<= 8) giving at
+// most 1.5 CTAs per SM with at most kWholeSlice K steps a CTA, whose whole
+// slice then sits in the weight ring: two consecutive calls' grids stay
+// resident together (measured on GB300, N=7168, us a call at M = 1 / 4 / 16
+// / 32: K=2048 4.87 / 4.93 / 6.07 / 8.31 -> 4.99 / 5.08 / 5.93 / 7.68 with 4
+// splits instead of 8, K=2080 5.73 / 6.01 / 7.64 / 10.01 -> 5.32 / 5.60 /
+// 6.94 / 9.09).  Else the largest power of two giving at most three
+// CTAs per SM, so the grid runs as one wave with short slices requested at
+// once; more splits only when a slice would exceed kMaxSteps.  Depends on
+// (N, K) and the SM count, never on M.
+static int gemv_tc_whole_splits(int RT, int KT, int sms) {
+  int best = 0;
+  for (int S = 1; S <= 8 && S <= KT; S *= 2)  // every slice at least one K step
+    if (2 * RT * S <= 3 * sms && (KT + S - 1) / S <= kWholeSlice) best = S;
+  return best;
+}
+
 int gemv_tc_splits(int N, int Kp, int sms, int force) {
   const int RT = (N + kRows - 1) / kRows, KT = Kp / kStepB;
   if (force > 0) return force;
+  const int whole = gemv_tc_whole_splits(RT, KT, sms);
+  if (whole > 0) return whole;
   int S = 1;
   while (S < 8 && 2 * S <= KT && RT * 2 * S <= 3 * sms) S *= 2;
   while ((KT + S - 1) / S > kMaxSteps && S < 8) ++S;
@@ -548,15 +563,20 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
     return t > floor_bytes ? t : floor_bytes;
   };
   static int smem_set[64];
-  // Weight ring depth: two stages keep 3-4 CTAs per SM resident; a long K
-  // slice (8 steps and more, where the grid needs a second wave anyway)
-  // streams better with four (measured on GB300).  The depth never changes a
-  // result.
+  // Weight ring depth: the whole slice when the split was chosen for that;
+  // else two stages while the grid has more CTAs than SMs (3-5 CTAs an SM
+  // stay resident; N=7168 K=8192 at M = 1 / 16: 16.7 / 20.4 -> 12.9 / 15.3
+  // us with two instead of four, M = 32 24.5 -> 26.7), four when every CTA
+  // has an SM of its own (N=2048 K=7168 at M = 1 / 32: 7.45 / 12.25 -> 5.96 /
+  // 10.90 us).  Measured on GB300; the depth never changes a result.
+  const int RTn = (w->N + kRows - 1) / kRows;
   if (a.force_ring > 0) {
     const int r = a.force_ring < kMaxRing ? a.force_ring : kMaxRing;
     p.ring = steps < r ? steps : r;
+  } else if (!a.force_splits && p.splits == gemv_tc_whole_splits(RTn, p.KT, di.sm_count)) {
+    p.ring = steps;
   } else {
-    const int r = steps >= kLongSlice ? kMaxAutoRing : kDefaultRing;
+    const int r = RTn * p.splits <= di.sm_count ? kMaxAutoRing : kDefaultRing;
     p.ring = steps < r ? steps : r;
   }
   const int smem = smem_for(p.ring, &p.own_recv);
