@@ -148,6 +148,7 @@ __host__ __device__ inline Layout layout_for(int ring, int steps, int splits, in
 constexpr int kDefaultRing = 2;
 constexpr int kMaxAutoRing = 4;
 constexpr int kWholeSlice = 5;            // K steps a CTA up to which a whole slice may sit in the ring
+constexpr int kLongSlice = 8;             // K steps a CTA from which M > 16 takes kMaxAutoRing stages
 
 __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const TcGemvParams p) {
@@ -566,9 +567,11 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   // Weight ring depth: the whole slice when the split was chosen for that;
   // else two stages while the grid has more CTAs than SMs (3-5 CTAs an SM
   // stay resident; N=7168 K=8192 at M = 1 / 16: 16.7 / 20.4 -> 12.9 / 15.3
-  // us with two instead of four, M = 32 24.5 -> 26.7), four when every CTA
-  // has an SM of its own (N=2048 K=7168 at M = 1 / 32: 7.45 / 12.25 -> 5.96 /
-  // 10.90 us).  Measured on GB300; the depth never changes a result.
+  // us with two instead of four), four when every CTA has an SM of its own
+  // (N=2048 K=7168 at M = 1 / 32: 7.45 / 12.25 -> 5.96 / 10.90 us) or, above
+  // 16 tokens (four CTAs an SM at most), for slices of kLongSlice steps and
+  // more (N=7168 K=8192 M = 32: 26.7 with two, 24.5 us with four).  Measured
+  // on GB300; the depth never changes a result, so it may follow M.
   const int RTn = (w->N + kRows - 1) / kRows;
   if (a.force_ring > 0) {
     const int r = a.force_ring < kMaxRing ? a.force_ring : kMaxRing;
@@ -576,7 +579,8 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   } else if (!a.force_splits && p.splits == gemv_tc_whole_splits(RTn, p.KT, di.sm_count)) {
     p.ring = steps;
   } else {
-    const int r = RTn * p.splits <= di.sm_count ? kMaxAutoRing : kDefaultRing;
+    const bool deep = RTn * p.splits <= di.sm_count || (a.M > 16 && steps >= kLongSlice);
+    const int r = deep ? kMaxAutoRing : kDefaultRing;
     p.ring = steps < r ? steps : r;
   }
   const int smem = smem_for(p.ring, &p.own_recv);
