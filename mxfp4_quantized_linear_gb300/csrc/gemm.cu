@@ -23,6 +23,12 @@
 //                    columns into registers, release of the accumulator (the
 //                    next tile's MMAs start), then bias in f32, bf16 round and
 //                    store from registers, overlapping those MMAs.
+// The producer requests its first unit's weight stages before the grid
+// dependency wait (the weight does not depend on the quantizer before it).
+// When the tiles would leave more than half the SMs idle (M of a few hundred
+// rows on a narrow N), K is split into ranges: one (tile, range) unit a CTA,
+// its f32 sums staged through the idle operand ring into the workspace, and
+// gemm_finish_kernel adds a tile's ranges in order, the bias, and rounds once.
 // Every mbarrier wait is bounded; on a timeout the CTA flags the error, stops
 // issuing, and still frees its tensor memory.
 
