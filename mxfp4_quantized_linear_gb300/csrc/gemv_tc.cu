@@ -565,10 +565,11 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   };
   static int smem_set[64];
   // Weight ring depth: the whole slice when the split was chosen for that;
-  // else two stages while the grid has more CTAs than SMs (3-5 CTAs an SM
-  // stay resident; N=7168 K=8192 at M = 1 / 16: 16.7 / 20.4 -> 12.9 / 15.3
-  // us with two instead of four), four when every CTA has an SM of its own
-  // (N=2048 K=7168 at M = 1 / 32: 7.45 / 12.25 -> 5.96 / 10.90 us) or, above
+  // else two stages while the grid has more than two CTAs an SM (3-5 stay
+  // resident; N=7168 K=8192 at M = 1 / 16: 16.7 / 20.4 -> 12.9 / 15.3 us with
+  // two instead of four), four with at most two (N=2048 K=7168 at M = 1 / 32:
+  // 7.45 / 12.25 -> 5.96 / 10.90 us; N=4096 K=7168, 224 CTAs: 8.99 / 14.13 ->
+  // 7.74 / 11.83 us with 8 slices) or, above
   // 16 tokens (four CTAs an SM at most), for slices of kLongSlice steps and
   // more (N=7168 K=8192 M = 32: 26.7 with two, 24.5 us with four).  Measured
   // on GB300; the depth never changes a result, so it may follow M.
@@ -579,7 +580,7 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   } else if (!a.force_splits && p.splits == gemv_tc_whole_splits(RTn, p.KT, di.sm_count)) {
     p.ring = steps;
   } else {
-    const bool deep = RTn * p.splits <= di.sm_count || (a.M > 16 && steps >= kLongSlice);
+    const bool deep = RTn * p.splits <= 2 * di.sm_count || (a.M > 16 && steps >= kLongSlice);
     const int r = deep ? kMaxAutoRing : kDefaultRing;
     p.ring = steps < r ? steps : r;
   }
