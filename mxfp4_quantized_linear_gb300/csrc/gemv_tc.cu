@@ -580,8 +580,16 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   } else if (!a.force_splits && p.splits == gemv_tc_whole_splits(RTn, p.KT, di.sm_count)) {
     p.ring = steps;
   } else {
-    const bool deep = RTn * p.splits <= 2 * di.sm_count || (a.M > 16 && steps >= kLongSlice);
-    const int r = deep ? kMaxAutoRing : kDefaultRing;
+    const int grid = RTn * p.splits;
+    int r = grid <= 2 * di.sm_count || (a.M > 16 && steps >= kLongSlice) ? kMaxAutoRing : kDefaultRing;
+    if (r == kDefaultRing && a.M <= 16 && steps > 2) {
+      // a third stage while the grid keeps at least 15 % of the CTA slots
+      // spare for the next call (N=24576 K=1536, 384 CTAs, at M = 1 / 16:
+      // 9.48 / 13.77 -> 8.42 / 11.17 us; N=7168 K=8192, 448 CTAs: slower)
+      p.ring = 3;
+      int own3 = 0;
+      if (per_sm(smem_for(3, &own3)) * di.sm_count * 20 >= grid * 23) r = 3;
+    }
     p.ring = steps < r ? steps : r;
   }
   const int smem = smem_for(p.ring, &p.own_recv);
