@@ -1,7 +1,7 @@
 """mx_measure_mxf8_peak: the dense MXFP8 tensor throughput measured by an
 MMA-only tcgen05 loop (the roofline denominator of the block-scaled GEMM).
 The loop checks its own accumulators; here the figure must also be physical:
-above the best this build's GEMM has reached on a GB300 (2.8 PFLOP/s) and below
+above the best the library's GEMM kernel reaches on a GB300 (2.8 PFLOP/s) and below
 twice the nominal dense fp8 rate (4.5 PFLOP/s)."""
 import pytest
 
