@@ -582,10 +582,13 @@ int launch_gemv_tc(const TcGemvArgs& a, cudaStream_t stream) {
   } else {
     const int grid = RTn * p.splits;
     int r = grid <= 2 * di.sm_count || (a.M > 16 && steps >= kLongSlice) ? kMaxAutoRing : kDefaultRing;
-    if (r == kDefaultRing && a.M <= 16 && steps > 2) {
+    if (r == kDefaultRing && a.M <= 16 && p.KT / p.splits > 3) {
       // a third stage while the grid keeps at least 15 % of the CTA slots
       // spare for the next call (N=24576 K=1536, 384 CTAs, at M = 1 / 16:
-      // 9.48 / 13.77 -> 8.42 / 11.17 us; N=7168 K=8192, 448 CTAs: slower)
+      // 9.48 / 13.77 -> 8.42 / 11.17 us; N=7168 K=8192, 448 CTAs: slower).
+      // Only when every slice is longer than 3 steps: a slice that fits the
+      // ring whole takes a second MMA issuer and accumulator (issuers_for),
+      // which would change the summation order between M = 16 and 17.
       p.ring = 3;
       int own3 = 0;
       if (per_sm(smem_for(3, &own3)) * di.sm_count * 20 >= grid * 23) r = 3;

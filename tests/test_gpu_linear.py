@@ -115,6 +115,23 @@ def test_batch_invariance_and_fused_equals_unfused():
     assert torch.equal(y4.view(torch.int16), y32[:4].view(torch.int16))
 
 
+@pytest.mark.parametrize("N,K", [(24576, 1536), (24576, 896), (4096, 7168), (7168, 8192)])
+def test_batch_invariance_where_the_ring_depth_follows_m(N, K):
+    """Shapes whose weight ring depth differs between M <= 16 and M > 16 (a
+    third stage, or a fourth on long slices), or whose slices are 3 and 4
+    steps long (K=896: 7 steps over 2 slices): each token's output is the same
+    bits at M = 1, 16, 17 and 32."""
+    g = inputs.generator(N + K + 1)
+    w = inputs.e4m3_bytes((N, K), g)
+    c = inputs.e8m0_codes((N // 32, K // 32), 118, 132, g)
+    p = pack(w, c)
+    x = inputs.bf16_normal((32, K), g)
+    y32 = gpu_linear(p, x).cpu()
+    for M in (1, 16, 17):
+        yM = gpu_linear(p, x[:M]).cpu()
+        assert torch.equal(yM.view(torch.int16), y32[:M].view(torch.int16)), M
+
+
 @pytest.mark.parametrize("N,K", [(24576, 1536), (7168, 8192)])
 def test_layer_sweep_linears_sampled_rows(N, K):
     g = inputs.generator(N + K)
