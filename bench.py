@@ -791,14 +791,27 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_step(c):
-    """One step of the workload on the oracle: the four calls, fp64."""
+def oracle_step(c, rows=None):
+    """One step of the workload on the oracle: the four calls, fp64 (on the
+    first ``rows`` weight rows only, a multiple of 32, when given)."""
     from oracle.linear import mxfp8_linear as ref_linear
     w = c["w"].numpy()
     codes = c["codes"].numpy()
+    if rows is not None:
+        w, codes = w[:rows], codes[:rows // 32]
     for M in MS:
         x = c["xs"][M].float().numpy().astype(np.float64)
         ref_linear(x, w, codes)
+
+
+def reference_rows(N, sec_full, steps, warmup, budget_s=150.0):
+    """Weight rows a reference-arm step samples so that warmup + steps of them
+    take about budget_s at most: all N when that fits, else the largest
+    multiple of 32 that does (at least 32)."""
+    total = max(1, steps + warmup) * sec_full
+    if total <= budget_s:
+        return N
+    return max(32, int(N * budget_s / total) // 32 * 32)
 
 
 def cpu_baseline(steps=1):
@@ -820,20 +833,25 @@ def run_reference(args, ws, rank):
         return None
     from mxfp4_quantized_linear_gb300 import inputs
     c = inputs.decode_linear(K=K_DEC, Ms=MS, N=N_DEC)
-    for _ in range(args.warmup):
-        oracle_step(c)
+    # one full step (the first warm-up) sizes the sample of every later step
+    t0 = time.perf_counter()
+    oracle_step(c)
+    rows = reference_rows(N_DEC, time.perf_counter() - t0, args.steps, args.warmup)
+    for _ in range(args.warmup - 1):
+        oracle_step(c, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(c)
+        oracle_step(c, rows)
     sec = (time.perf_counter() - t0) / args.steps
-    step_bytes = sum(linear_bytes(M, N_DEC, K_DEC, True) for M in MS)
+    step_bytes = sum(linear_bytes(M, rows, K_DEC, True) for M in MS)
     v = step_bytes / sec / 1e9
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "N": N_DEC, "K": K_DEC, "Ms": list(MS)},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"{args.steps} full steps of the workload on the CPU oracle"},
+                             "sample": f"{args.steps} steps of the workload on the CPU oracle, each on "
+                                       f"{rows} of the {N_DEC} weight rows"},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -33,3 +33,14 @@ def test_sampler_context_is_safe_without_gpu():
         pass
     s = cs.summary()
     assert s["samples"] >= 0 and isinstance(s["reasons"], list)
+
+
+def test_reference_arm_sample_keeps_the_run_bounded():
+    """The reference arm samples fewer weight rows a step when warmup + steps
+    full oracle steps would run past its budget: the driver's short run keeps
+    every row, a 20,000-step run a 32-row-aligned slice."""
+    assert bench.reference_rows(7168, 0.9, 20, 5) == 7168
+    rows = bench.reference_rows(7168, 0.9, 20000, 200)
+    assert rows % 32 == 0 and 32 <= rows < 7168
+    assert (20000 + 200) * 0.9 * rows / 7168 <= 150.0 + 0.9 * 32 / 7168 * 20200
+    assert bench.reference_rows(7168, 100.0, 1000, 3) == 32
