@@ -82,6 +82,24 @@ def test_host_side_checks_of_the_newer_entry_points():
     assert lib.mxfp8_linear_q_workspace_size(64, ctypes.byref(w1)) == 64 * 512 + 5 * 64 * 7168 * 4
     w2 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=24576, K=1536, Kp=1536)
     assert lib.mxfp8_linear_workspace_size(64, ctypes.byref(w2)) == 128 * 1536 + 128 * 48
+
+    def split_room(M, w):
+        """bytes past the required quantized activation and codes"""
+        Mp = -(-M // 128) * 128
+        need = -(-Mp * w.Kp // 256) * 256 + -(-Mp * (w.Kp // 32) // 256) * 256
+        return lib.mxfp8_linear_workspace_size(M, ctypes.byref(w)) - need
+
+    # 152 SMs: S = min(8, SMs / tiles, K steps / 4), ranges [S, M, N] f32
+    assert split_room(33, w1) == 5 * 33 * 7168 * 4      # 28 tiles
+    assert split_room(256, w1) == 2 * 256 * 7168 * 4    # 56 tiles
+    assert split_room(384, w1) == 0                     # 84 tiles > 152 / 2
+    w5 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=320, K=4160, Kp=4224)
+    assert split_room(1000, w5) == 8 * 1000 * 320 * 4   # 16 tiles, 33 K steps
+    w6 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=192, K=512, Kp=512)
+    assert split_room(130, w6) == 0                     # 4 K steps: ranges would be shorter than 4
+    w7 = b.MxPackedWeightC(fmt=b.MX_FMT_E4M3, E=1, N=7168, K=65536, Kp=65536)
+    assert split_room(256, w7) == 2 * 256 * 7168 * 4    # 14.7 MB a range: under the 64 MB cap
+    assert split_room(64 * 128, w7) == 0                # 1792 tiles
     # expert: w13 must carry the gate/up layout, w2 must fit it
     assert lib.mxfp4_moe_expert(None, None, None, 1, 1, ctypes.byref(e2p), ctypes.byref(e2p), None, None, 0, None,
                                 None) == b.MX_ERR_ARG
