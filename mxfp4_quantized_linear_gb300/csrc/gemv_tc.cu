@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
   const int own_rows = own_hi > own_lo ? own_hi - own_lo : 0;
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* wempty = wfull + kMaxRing;
-  uint64_t* xready = wempty + kMaxRing;  // quantized activation written (128 arrivals)
-  uint64_t* accfull = xready + 1;
+  uint64_t* xready = wempty + kMaxRing;  // [kMaxSteps]: step i's quantized activation written (128 arrivals)
+  uint64_t* accfull = xready + kMaxSteps;
   uint64_t* redbar = accfull + 1;        // this CTA's rows: all S partials received
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(redbar + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 1);
     }
-    mbar_init(xready, 128);
+    for (int s = 0; s < kMaxSteps; ++s) mbar_init(&xready[s], 128);
     mbar_init(accfull, static_cast<uint32_t>(n_iss));  // one commit a issuer
     mbar_init(redbar, 1);
     *abort_flag = 0u;
@@ -241,10 +241,13 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
         tc_fence_after();
         tc_cp_sf(tmem + sf_base + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
       }
-      if (ok && !mbar_wait(xready, 0)) { *abort_flag = 1u; ok = false; }
-      tc_fence_after();
       const uint32_t idesc_n = p.M <= 16 ? kIdesc16 : kIdesc32;
+      // up to 8 tokens every step is signalled at once: one wait, on the last
+      const bool per_step = p.M > 8;
+      if (ok && !per_step && !mbar_wait(&xready[ns - 1], 0)) { *abort_flag = 1u; ok = false; }
       for (int i = 1; i < ns && ok; i += 2) {
+        if (per_step && !mbar_wait(&xready[i], 0)) { *abort_flag = 1u; ok = false; break; }
+        tc_fence_after();
         const uint32_t sf = tmem + sf_base + static_cast<uint32_t>(i * 8);
         tc_cp_sf(sf + 4, sf_desc(smem_u32(smem + L.sfx + i * 512)));
         const uint64_t adesc = sw128_desc(smem_u32(smem + L.w + i * kWBox));
@@ -267,13 +270,12 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
     bool ok = true;
     const int pre = ns < ring ? ns : ring;
     const uint32_t idesc_n = p.M <= 16 ? kIdesc16 : kIdesc32;
+    const bool per_step = p.M > 8;  // else every step is signalled at once: one wait, on the last
     for (int i = 0; i < pre && ok; i += n_iss) {
       if (!mbar_wait(&wfull[i], 0u)) { *abort_flag = 1u; ok = false; break; }
       tc_fence_after();
       tc_cp_sf(tmem + sf_base + static_cast<uint32_t>(i * 8), sf_desc(smem_u32(smem + L.sfw + i * 512)));
     }
-    if (ok && !mbar_wait(xready, 0)) { *abort_flag = 1u; ok = false; }
-    tc_fence_after();
     for (int i = 0; i < ns && ok; i += n_iss) {
       const int stage = i % ring;
       const uint32_t sf = tmem + sf_base + static_cast<uint32_t>(i * 8);
@@ -282,6 +284,15 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
         tc_fence_after();
         tc_cp_sf(sf, sf_desc(smem_u32(smem + L.sfw + stage * 512)));
       }
+      // step i's activation (above 8 tokens the quantizing warps signal each
+      // step as it is written, so the MMAs of the first steps overlap the
+      // quantization of the later ones)
+      if ((per_step || i == 0) && !mbar_wait(&xready[per_step ? i : ns - 1], 0)) {
+        *abort_flag = 1u;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       tc_cp_sf(sf + 4, sf_desc(smem_u32(smem + L.sfx + i * 512)));
       const uint64_t adesc = sw128_desc(smem_u32(smem + L.w + stage * kWBox));
       const uint64_t bdesc = sw128_desc(smem_u32(smem + L.xq + i * xqb));
@@ -322,8 +333,16 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
       }
     }
     // bf16 activation: one whole 32-element MX block a thread (item = (step,
-    // token, block)), kXBlocks blocks in flight a thread
+    // token, block)), kXBlocks blocks in flight a thread.  Items are
+    // step-major, so above 8 tokens, once a thread moves past a step it
+    // arrives on that step's barrier: the MMAs of a step start as soon as its
+    // 128 threads are past it (measured on GB300, us a call at M = 16 / 32:
+    // N=7168 K=8192 15.31 / 24.64 -> 14.29 / 21.80, N=7168 K=2048 6.10 / 7.71
+    // -> 6.04 / 7.40).  Up to 8 tokens there is too little to overlap and
+    // every step is signalled at the end (signalling as it goes cost 1-3 %).
     const int blocks = ns * mrows * 4;
+    const bool per_step = mrows > 8;
+    int arrived = 0;  // steps below this one are signalled by this thread
     for (int b0 = et; b0 < blocks && p.xq == nullptr; b0 += 128 * kXBlocks) {
       uint4 u[kXBlocks][4];
 #pragma unroll
@@ -355,9 +374,18 @@ __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm) gemv_tc_kernel(const 
         *reinterpret_cast<uint4*>(rowp + (((2 * kb + 1) ^ (t & 7)) << 4)) = q8[1];
         smem[L.sfx + step * 512 + t * 16 + kb] = static_cast<uint8_t>(code);
       }
+      // this thread's later items are all in step `upto` or later
+      const int nb = b0 + 128 * kXBlocks;
+      const int upto = nb < blocks ? (((nb >> 2) * mmul) >> 16) : ns;
+      if (per_step && upto > arrived) {
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        for (; arrived < upto; ++arrived) mbar_arrive(&xready[arrived]);
+      }
     }
-    fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-    mbar_arrive(xready);
+    if (arrived < ns) {
+      fence_proxy_async_smem();
+      for (; arrived < ns; ++arrived) mbar_arrive(&xready[arrived]);
+    }
 
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, r = q * 32 + lane;
